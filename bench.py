@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Muon-step benchmark: ms per step and achieved TFLOP/s on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2|c1|c3|c4|c5]
+                    [--impl ours|reference]
+
+One step = momentum -> Newton-Schulz (5 steps) -> decoupled-decay update over
+the whole workload, through the C ABI (libmuon).  ``value`` is the achieved
+nominal TFLOP/s (sum over matrices of 5*(4 m^2 n + 2 m^3), m <= n) divided by
+the device time of a step, inputs resident in HBM; ``e2e`` is the same metric
+with the step's inputs copied from pinned host memory and its results (W',
+Mom') copied back inside the timed region.  Between timed steps a 512 MiB
+buffer is written to flush the 129 MB L2 (outside the timed events).
+
+``--impl reference`` times the float64 CPU oracle (the deliberately slow
+reference) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon step ms & achieved TFLOP/s vs GB300 bf16 peak (per config, 1 GPU)"
+HP = dict(mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
+STEPS_NS = 5
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _shapes(groups):
+    out = []
+    for g in groups:
+        w = g["W"]
+        b, r, c = (1, *w.shape) if w.dim() == 2 else tuple(w.shape)
+        out.append((b, r, c, w.element_size(), g["G"].element_size()))
+    return out
+
+
+def nominal_flops(shapes, steps=STEPS_NS):
+    f = 0
+    for b, r, c, _, _ in shapes:
+        m, n = min(r, c), max(r, c)
+        f += b * steps * (4 * m * m * n + 2 * m ** 3)
+    return f
+
+
+def algorithmic_bytes(shapes):
+    """Per kernel kind: prep reads G, Mom and writes Mom, X, X^T (bf16);
+    update reads W, the bf16 result and writes W."""
+    prep = upd = 0
+    for b, r, c, we, ge in shapes:
+        e = b * r * c
+        prep += e * (ge + 4 + 4 + 2 + 2)
+        upd += e * (we + we + 2)
+    return {"prep": prep, "update": upd}
+
+
+def gemm_flops_per_kind(shapes, steps=STEPS_NS):
+    """Algorithmic (symmetry-aware) flops of one step for each GEMM kind."""
+    gram = poly = apply = 0
+    for b, r, c, _, _ in shapes:
+        m, n = min(r, c), max(r, c)
+        gram += b * steps * m * (m + 1) * n
+        poly += b * steps * m * m * (m + 1)
+        apply += b * steps * 2 * m * m * n
+    return {"gram": gram, "poly": poly, "apply": apply}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(",") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for k, name in enumerate(names):
+                    if r[5 + k].strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The float64 oracle on the host cores, on a bounded sample per step."""
+    import numpy as np
+    import torch
+    from newton_schulz_gb300 import synth
+    from oracle import muon_ref as R
+
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    # bounded sample: a few matrices of each group of the workload
+    groups = synth.CONFIGS[args.config]("cpu") if args.config in ("c1", "c2") else None
+    if groups is None:
+        groups = _sample_groups_cpu(args.config)
+    shapes = _shapes(groups)
+    sample = []
+    budget = {"c1": 5, "c2": 8, "c3": 2, "c4": 1, "c5": 1}[args.config]
+    for g, (b, r, c, _, _) in zip(groups, shapes):
+        k = min(b, budget)
+        sample.append({k2: g[k2][:k].double().numpy() for k2 in ("W", "G", "Mom")})
+    s_shapes = [(x["W"].shape[0], x["W"].shape[1], x["W"].shape[2], 4, 4) for x in sample]
+    flops = nominal_flops(s_shapes)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for x in sample:
+            R.muon_step_ref(x["W"], x["G"], x["Mom"], **HP)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    t = statistics.median(times)
+    tf = flops / t / 1e12
+    sample_desc = "; ".join(f"{x['W'].shape[0]}x[{x['W'].shape[1]},{x['W'].shape[2]}]"
+                            for x in sample)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.WORKLOAD_NAMES[args.config], "sample": sample_desc},
+        "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _sample_groups_cpu(config):
+    """Small CPU stand-ins with the workload's shapes (for the oracle only)."""
+    import torch
+    from newton_schulz_gb300 import synth
+    if config == "c3":
+        out = []
+        for r, c in ((2048, 768), (768, 2048)):
+            out.append(synth.random_group((2, r, c), torch.bfloat16, torch.float32, "cpu", r, 1e-3))
+        return out
+    if config == "c4":
+        return [synth.random_group((1, r, c), torch.bfloat16, torch.bfloat16, "cpu", i, 1e-3)
+                for i, (r, c) in enumerate(((4096, 4096), (1024, 4096), (14336, 4096)))]
+    return [synth.random_group((1, 8192, 8192), torch.bfloat16, torch.float32, "cpu", 5, 1.0)]
+
+
+def cpu_baseline_sample(config, budget_s=12.0):
+    """Oracle seconds per step on a bounded sample, scaled to the whole workload."""
+    import torch
+    from newton_schulz_gb300 import synth
+    from oracle import muon_ref as R
+    cores = len(os.sched_getaffinity(0))
+    if config in ("c1", "c2"):
+        groups = synth.CONFIGS[config]("cpu")
+    else:
+        groups = _sample_groups_cpu(config)
+    done_flops, t_total, n_mats, desc = 0, 0.0, 0, []
+    for g in groups:
+        b = g["W"].shape[0] if g["W"].dim() == 3 else 1
+        for i in range(b):
+            x = {k: g[k][i].double().numpy() for k in ("W", "G", "Mom")}
+            t0 = time.perf_counter()
+            R.muon_step_ref(x["W"], x["G"], x["Mom"], **HP)
+            t_total += time.perf_counter() - t0
+            r, c = x["W"].shape
+            m, n = min(r, c), max(r, c)
+            done_flops += STEPS_NS * (4 * m * m * n + 2 * m ** 3)
+            n_mats += 1
+            if t_total > budget_s:
+                break
+        desc.append(f"{g['W'].shape}")
+        if t_total > budget_s:
+            break
+    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n_mats} matrices of {config} ({t_total:.1f} s, float64 NumPy)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = _dist_env()
+
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, world, rank)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    import torch
+    from newton_schulz_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    binding.load()
+
+    groups = synth.CONFIGS[args.config](dev)
+    shapes = _shapes(groups)
+    flops = nominal_flops(shapes)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    arr = binding.make_groups(groups)
+
+    def step():
+        binding.muon_step_grouped(arr, stream=stream, **HP)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = binding.muon_query_status()
+    if st != 0:
+        raise SystemExit(f"device status {binding.muon_status_string(st)} after warm-up")
+    launches_per_step = binding.muon_last_launch_count()
+
+    # ---- device-resident timed region ------------------------------------------------
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    binding.muon_profile_enable(True)
+    binding.muon_profile_read()      # reset
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    prof = binding.muon_profile_read()
+    binding.muon_profile_enable(False)
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t_ms = statistics.median(step_ms)
+    if world > 1:
+        t = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+
+    # ---- end to end: pinned host inputs in, results out, through the C ABI ------------
+    host_in = [{k: g[k].to("cpu").pin_memory() for k in ("W", "G", "Mom")} for g in groups]
+    host_out = [{k: torch.empty_like(h[k]).pin_memory() for k in ("W", "Mom")} for h in host_in]
+    h2d = sum(h[k].numel() * h[k].element_size() for h in host_in for k in h)
+    d2h = sum(h[k].numel() * h[k].element_size() for h in host_out for k in h)
+    e2e_ms = []
+    for i in range(args.warmup + max(3, args.steps // 2)):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for g, h in zip(groups, host_in):
+            for k in ("W", "G", "Mom"):
+                g[k].copy_(h[k], non_blocking=True)
+        step()
+        for g, h in zip(groups, host_out):
+            for k in ("W", "Mom"):
+                h[k].copy_(g[k], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_t = statistics.median(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_t], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_t = float(t.item())
+
+    st = binding.muon_query_status()
+    if st != 0:
+        raise SystemExit(f"device status {binding.muon_status_string(st)} after timing")
+
+    # ---- roofline of the dominant kernel ------------------------------------------------
+    peaks = _peaks()
+    kinds = {k: (ms / max(1, n), n) for k, (ms, n) in prof.items() if n}
+    per_step_ms = {k: prof[k][0] / args.steps for k in prof}
+    dom = max(per_step_ms, key=per_step_ms.get)
+    avg_ms, n_launch = kinds[dom]
+    byt = algorithmic_bytes(shapes)
+    fl = gemm_flops_per_kind(shapes)
+    launches_kind = n_launch / args.steps
+    if dom in ("prep", "update"):
+        per_launch = byt[dom] / launches_kind
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "kernel": dom, "peak_source": peaks["source"]}
+    else:
+        per_launch = fl[dom] / launches_kind
+        achieved = per_launch / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "kernel": dom, "peak_source": peaks["source"]}
+
+    value = world * flops / (t_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": synth.WORKLOAD_NAMES[args.config], "config": args.config,
+                   "matrices": sum(s[0] for s in shapes), "nominal_gflop_per_step": flops / 1e9,
+                   "l2": "512 MiB L2 flush between timed steps (outside events)",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": world * flops / (e2e_t * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_t, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+        "kernel_ms_per_step": {k: round(v, 5) for k, v in per_step_ms.items()},
+        "roofline": roof,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(args.config)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

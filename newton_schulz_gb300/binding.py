@@ -1,0 +1,225 @@
+"""Thin ctypes binding of libmuon (include/muon.h): argument marshalling only.
+
+Every step of the Muon path runs in the library's CUDA kernels; this module
+only turns tensors into pointers, shapes and a stream handle.  Loading fails
+loudly when the library has not been built (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmuon.so")
+
+MUON_OK = 0
+STATUS_NAMES = {
+    0: "MUON_OK", 1: "MUON_ERR_INVALID_ARGUMENT", 2: "MUON_ERR_UNSUPPORTED",
+    3: "MUON_ERR_ALIAS", 4: "MUON_ERR_OUT_OF_MEMORY", 5: "MUON_ERR_CUDA",
+    6: "MUON_ERR_TIMEOUT", 7: "MUON_ERR_NONFINITE",
+}
+MUON_F32, MUON_BF16 = 0, 1
+SCALE_SQRT_MAX1_R_OVER_C, SCALE_RMS_0P2_SQRT_MAXDIM, SCALE_ONE = 0, 1, 2
+NS_BF16, NS_TF32 = 0, 1
+PROFILE_KINDS = ("prep", "gram", "poly", "apply", "update")
+
+EXPORTED = (
+    "muon_ns_default_config", "muon_ns_batched", "muon_ns_batched_ex", "muon_step_grouped",
+    "muon_step_grouped_ex", "muon_query_status", "muon_status_string",
+    "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
+    "muon_profile_read",
+)
+
+
+class MuonError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class NsConfig(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int32), ("coeffs", ctypes.POINTER(ctypes.c_float)),
+                ("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
+                ("eps", ctypes.c_float), ("precision", ctypes.c_int32)]
+
+
+class Group(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("w_dtype", ctypes.c_int32),
+                ("G", ctypes.c_void_p), ("g_dtype", ctypes.c_int32),
+                ("Mom", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("M", ctypes.c_int64), ("N", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmuon.so (raises OSError when it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"{path} not found: build it with `python -m newton_schulz_gb300.build`")
+    lib = ctypes.CDLL(path)
+    i32, i64, vp, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+    lib.muon_ns_default_config.argtypes = [ctypes.POINTER(NsConfig)]
+    lib.muon_ns_default_config.restype = i32
+    lib.muon_ns_batched.argtypes = [vp, i64, i64, i64, ctypes.c_int, f32, f32, f32, vp]
+    lib.muon_ns_batched.restype = i32
+    lib.muon_ns_batched_ex.argtypes = [vp, i32, i64, i64, i64, ctypes.POINTER(NsConfig), vp, vp]
+    lib.muon_ns_batched_ex.restype = i32
+    lib.muon_step_grouped.argtypes = [ctypes.POINTER(Group), ctypes.c_int, f32, ctypes.c_int,
+                                      f32, f32, ctypes.c_int, vp]
+    lib.muon_step_grouped.restype = i32
+    lib.muon_step_grouped_ex.argtypes = [ctypes.POINTER(Group), ctypes.c_int, f32, ctypes.c_int,
+                                         f32, f32, ctypes.c_int, ctypes.POINTER(NsConfig), vp]
+    lib.muon_step_grouped_ex.restype = i32
+    lib.muon_query_status.argtypes = [vp]
+    lib.muon_query_status.restype = i32
+    lib.muon_status_string.argtypes = [i32]
+    lib.muon_status_string.restype = ctypes.c_char_p
+    lib.muon_release_workspace.argtypes = []
+    lib.muon_release_workspace.restype = None
+    lib.muon_last_launch_count.argtypes = []
+    lib.muon_last_launch_count.restype = ctypes.c_int
+    lib.muon_profile_enable.argtypes = [ctypes.c_int]
+    lib.muon_profile_enable.restype = ctypes.c_int
+    lib.muon_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
+    lib.muon_profile_read.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+# ---- marshalling helpers ----------------------------------------------------------
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return MUON_F32
+    if t.dtype == torch.bfloat16:
+        return MUON_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _shape3(t):
+    if t.dim() == 2:
+        return 1, t.shape[0], t.shape[1]
+    if t.dim() == 3:
+        return t.shape[0], t.shape[1], t.shape[2]
+    raise ValueError("tensors must be [M,N] or [B,M,N]")
+
+
+def _check_contig(*ts):
+    for t in ts:
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous row-major")
+
+
+def check(code: int, where: str) -> None:
+    if code != MUON_OK:
+        raise MuonError(code, where)
+
+
+def make_config(steps: int = 5, coeffs: Optional[Sequence[Sequence[float]]] = None,
+                a: float = 3.4445, b: float = -4.7750, c: float = 2.0315,
+                eps: float = 1e-7, precision: int = NS_BF16):
+    """Build an NsConfig; keeps the coefficient array alive on the object."""
+    cfg = NsConfig()
+    cfg.steps, cfg.a, cfg.b, cfg.c, cfg.eps, cfg.precision = steps, a, b, c, eps, precision
+    if coeffs is not None:
+        flat = [float(v) for row in coeffs for v in row]
+        arr = (ctypes.c_float * max(1, len(flat)))(*flat)
+        cfg.coeffs = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+        cfg._keep = arr
+    return cfg
+
+
+# ---- entry points (same names as the C ABI) -------------------------------------------
+def muon_ns_batched(X, steps: int = 5, a: float = 3.4445, b: float = -4.7750,
+                    c: float = 2.0315, stream=None) -> None:
+    """In-place NS of every [M,N] slice of a contiguous bf16 CUDA tensor."""
+    _check_contig(X)
+    B, M, N = _shape3(X)
+    check(load().muon_ns_batched(X.data_ptr(), B, M, N, steps, a, b, c, _stream_ptr(stream)),
+          "muon_ns_batched")
+
+
+def muon_ns_batched_ex(X, cfg=None, out=None, stream=None) -> None:
+    _check_contig(X)
+    B, M, N = _shape3(X)
+    if out is not None:
+        _check_contig(out)
+    check(load().muon_ns_batched_ex(X.data_ptr(), _dtype_code(X), B, M, N,
+                                    ctypes.byref(cfg) if cfg is not None else None,
+                                    out.data_ptr() if out is not None else None,
+                                    _stream_ptr(stream)), "muon_ns_batched_ex")
+
+
+def make_groups(groups: Iterable[dict]):
+    """[{"W","G","Mom"}] of contiguous CUDA tensors -> ctypes array."""
+    groups = list(groups)
+    arr = (Group * max(1, len(groups)))()
+    for i, g in enumerate(groups):
+        W, G, Mom = g["W"], g["G"], g["Mom"]
+        _check_contig(W, G, Mom)
+        B, M, N = _shape3(W)
+        arr[i] = Group(W.data_ptr(), _dtype_code(W), G.data_ptr(), _dtype_code(G),
+                       Mom.data_ptr(), B, M, N)
+    return arr, len(groups)
+
+
+def muon_step_grouped(groups, mu: float = 0.95, nesterov: bool = True, lr: float = 0.02,
+                      wd: float = 0.01, scale_rule: int = SCALE_SQRT_MAX1_R_OVER_C,
+                      ns_cfg=None, stream=None) -> None:
+    """One fused Muon step over groups of [B,M,N] tensors (W, G, Mom)."""
+    arr, n = groups if isinstance(groups, tuple) else make_groups(groups)
+    lib = load()
+    if ns_cfg is None:
+        code = lib.muon_step_grouped(arr, n, mu, int(nesterov), lr, wd, scale_rule,
+                                     _stream_ptr(stream))
+    else:
+        code = lib.muon_step_grouped_ex(arr, n, mu, int(nesterov), lr, wd, scale_rule,
+                                        ctypes.byref(ns_cfg), _stream_ptr(stream))
+    check(code, "muon_step_grouped")
+
+
+muon_step_grouped_ex = muon_step_grouped
+
+
+def muon_query_status(stream=None) -> int:
+    return load().muon_query_status(_stream_ptr(stream))
+
+
+def muon_status_string(code: int) -> str:
+    return load().muon_status_string(code).decode()
+
+
+def muon_release_workspace() -> None:
+    load().muon_release_workspace()
+
+
+def muon_last_launch_count() -> int:
+    return load().muon_last_launch_count()
+
+
+def muon_profile_enable(enable: bool = True) -> int:
+    return load().muon_profile_enable(int(enable))
+
+
+def muon_profile_read():
+    """{kind: (ms_total, launches)} since the last read (stream synchronised first)."""
+    n = len(PROFILE_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    load().muon_profile_read(ms, cnt, n)
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(PROFILE_KINDS)}

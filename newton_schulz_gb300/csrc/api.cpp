@@ -1,0 +1,865 @@
+// C ABI of libmuon: argument validation, the core-shape planner, the
+// workspace cache, tensor-map construction and kernel launches.
+//
+// Planner (HyperParallel-FSDP section 6.6, Fig. 10(a)): every slice of every
+// group becomes one NS problem with m = min(rows, cols), n = max(rows, cols)
+// (transpose-first when rows > cols); problems with the same core shape
+// (m, n) share one workspace region and one set of tensor maps, so a single
+// launch per phase covers all of them.  Work is cut into chunks whose X
+// operands hold at most `cap` elements (2^29 by default, the page's
+// memory-safe batch cap; MUON_WS_CAP overrides); one workspace, sized for the
+// largest chunk, is allocated once per (device, stream) and reused.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "muon_internal.h"
+
+using namespace muon;
+
+namespace {
+
+constexpr float kDefA = 3.4445f, kDefB = -4.7750f, kDefC = 2.0315f, kDefEps = 1e-7f;
+constexpr int kDefSteps = 5;
+constexpr float kShiftFrac = 0.58f;   // alpha_k = 0.58 a_k (about 2 for the default quintic)
+
+// ---- driver entry point for tensor maps (no link-time libcuda dependency) ----
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// ---- global state ---------------------------------------------------------------
+// Data workspace (operands, Gram/polynomial buffers, partials) plus a
+// separate counter buffer.  Every kernel leaves the counters it uses at zero,
+// and counters never share memory with data, so a new plan (other offsets)
+// always starts from zeroed counters.
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  unsigned* ctr = nullptr;
+  size_t ctr_bytes = 0;
+  bool dirty = false;  // a kernel gave up mid-way: counters must be re-zeroed
+};
+
+struct DevState {
+  unsigned* status = nullptr;
+  int sms = 0;
+};
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t e0, e1;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+std::map<int, DevState> g_dev;
+bool g_prof = false;
+std::vector<ProfRec> g_prof_recs;
+thread_local int t_last_launches = 0;
+
+size_t env_size(const char* name, size_t dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  unsigned long long x = std::strtoull(v, &end, 10);
+  return (end && *end == 0 && x > 0) ? static_cast<size_t>(x) : dflt;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+muon_status_t dev_state(DevState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  DevState& d = g_dev[dev];
+  if (!d.status) {
+    if (cudaMalloc(&d.status, 256) != cudaSuccess) {
+      d.status = nullptr;
+      return MUON_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemset(d.status, 0, 256) != cudaSuccess) return MUON_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MUON_ERR_CUDA;
+  }
+  *out = &d;
+  return MUON_OK;
+}
+
+// ---- plan --------------------------------------------------------------------------
+struct Req {            // one user group
+  void* W;
+  int w_dtype;
+  const void* G;
+  int g_dtype;
+  float* Mom;
+  int64_t B, r, c, m, n;
+  bool trans;
+};
+
+struct SliceP {
+  int req;
+  int64_t b0, cnt;
+  int ng;
+  int64_t idx0;
+};
+
+struct NsGroupP {
+  int64_t m, n, cnt = 0;
+  int64_t m_pad, n_pad;
+  int ksplit = 1, kb_per_split = 1, num_kb_gram = 1;
+  int64_t tri = 1, prep_tiles = 1;
+  size_t off_X, off_Xt0, off_Xt1, off_A, off_B, off_inv, off_ssq, off_part;
+  size_t ctr_prep, ctr_tile;   // element offsets in the counter buffer
+};
+
+struct ChunkP {
+  std::vector<SliceP> slices;
+  std::vector<NsGroupP> groups;
+  size_t bytes = 0;
+  size_t ctrs = 0;             // counters used (elements)
+};
+
+void layout_chunk(ChunkP& ch, int sms) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 16), 1024);
+    return o;
+  };
+  const int bm = gemm_block_m(), bk = gemm_block_k();
+  size_t ctr = 0;
+  for (auto& g : ch.groups) {
+    g.m_pad = rup(g.m, 8);
+    g.n_pad = rup(g.n, 8);
+    const int64_t nt = cdiv(g.m, bm);
+    g.tri = nt * (nt + 1) / 2;
+    g.num_kb_gram = static_cast<int>(cdiv(g.n, bk));
+    // split-K for the Gram when the symmetric tiles alone cannot fill the GPU
+    const int64_t tiles = g.cnt * g.tri;
+    const int64_t target = 2LL * sms;
+    int ks = 1;
+    if (tiles < target && g.num_kb_gram >= 8) {
+      ks = static_cast<int>(std::min<int64_t>(cdiv(target, tiles), g.num_kb_gram / 4));
+      ks = std::max(ks, 1);
+    }
+    g.kb_per_split = static_cast<int>(cdiv(g.num_kb_gram, ks));
+    g.ksplit = static_cast<int>(cdiv(g.num_kb_gram, g.kb_per_split));
+    g.prep_tiles = cdiv(g.m, kPrepTile) * cdiv(g.n, kPrepTile);
+    const size_t e2 = 2;
+    g.off_X = take(static_cast<size_t>(g.cnt * g.m * g.n_pad) * e2);
+    g.off_Xt0 = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
+    g.off_Xt1 = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
+    g.off_A = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+    g.off_B = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+    g.off_inv = take(static_cast<size_t>(g.cnt) * 4);
+    g.off_ssq = take(static_cast<size_t>(g.cnt * g.prep_tiles) * 4);
+    g.off_part = take(g.ksplit > 1 ? static_cast<size_t>(g.cnt * g.tri * g.ksplit) * bm * bm * 4
+                                   : 16);
+    g.ctr_prep = ctr;
+    ctr += static_cast<size_t>(g.cnt);
+    g.ctr_tile = ctr;
+    ctr += static_cast<size_t>(g.cnt * g.tri);
+  }
+  ch.bytes = off;
+  ch.ctrs = ctr;
+}
+
+std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms) {
+  const int64_t cap = static_cast<int64_t>(env_size("MUON_WS_CAP", size_t(1) << 29));
+  std::vector<int> order;
+  for (int i = 0; i < static_cast<int>(reqs.size()); ++i)
+    if (reqs[i].B > 0 && reqs[i].m > 0) order.push_back(i);
+  // largest matrices first; same core shapes adjacent
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    const Req &a = reqs[x], &b = reqs[y];
+    if (a.m * a.n != b.m * b.n) return a.m * a.n > b.m * b.n;
+    if (a.m != b.m) return a.m > b.m;
+    return false;
+  });
+  std::vector<ChunkP> chunks;
+  ChunkP cur;
+  int64_t cur_elems = 0;
+  auto close = [&] {
+    if (!cur.slices.empty()) chunks.push_back(std::move(cur));
+    cur = ChunkP();
+    cur_elems = 0;
+  };
+  for (int ri : order) {
+    const Req& q = reqs[ri];
+    const int64_t per = q.m * q.n;
+    int64_t b = 0;
+    while (b < q.B) {
+      int ng = -1;
+      for (int k = 0; k < static_cast<int>(cur.groups.size()); ++k)
+        if (cur.groups[k].m == q.m && cur.groups[k].n == q.n) ng = k;
+      const bool need_group = ng < 0;
+      const bool full_tables = static_cast<int>(cur.slices.size()) >= kMaxSlices ||
+                               (need_group && static_cast<int>(cur.groups.size()) >= kMaxNsGroups);
+      int64_t fit = (cap - cur_elems) / per;
+      if (!cur.slices.empty() && (fit <= 0 || full_tables)) {
+        close();
+        continue;
+      }
+      if (fit <= 0) fit = 1;   // one matrix larger than the cap runs alone
+      const int64_t take = std::min(q.B - b, fit);
+      if (need_group) {
+        NsGroupP g;
+        g.m = q.m;
+        g.n = q.n;
+        cur.groups.push_back(g);
+        ng = static_cast<int>(cur.groups.size()) - 1;
+      }
+      SliceP s;
+      s.req = ri;
+      s.b0 = b;
+      s.cnt = take;
+      s.ng = ng;
+      s.idx0 = cur.groups[ng].cnt;
+      cur.groups[ng].cnt += take;
+      cur.slices.push_back(s);
+      cur_elems += take * per;
+      b += take;
+    }
+  }
+  close();
+  for (auto& ch : chunks) layout_chunk(ch, sms);
+  return chunks;
+}
+
+// ---- workspace ---------------------------------------------------------------------
+muon_status_t get_workspace(cudaStream_t stream, size_t bytes, size_t ctrs, char** out,
+                            unsigned** ctr_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  Workspace& w = g_ws[{dev, stream}];
+  const size_t ctr_bytes = std::max<size_t>(ctrs, 1) * sizeof(unsigned);
+  if (w.bytes < bytes || w.ctr_bytes < ctr_bytes) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+  }
+  if (w.bytes < bytes) {
+    if (w.ptr) cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+    const size_t want = align_up(bytes, size_t(1) << 21);
+    if (cudaMalloc(&w.ptr, want) != cudaSuccess) {
+      cudaGetLastError();
+      w.ptr = nullptr;
+      return MUON_ERR_OUT_OF_MEMORY;
+    }
+    w.bytes = want;
+  }
+  if (w.ctr_bytes < ctr_bytes) {
+    if (w.ctr) cudaFree(w.ctr);
+    w.ctr = nullptr;
+    w.ctr_bytes = 0;
+    const size_t want = align_up(ctr_bytes, size_t(1) << 16);
+    if (cudaMalloc(&w.ctr, want) != cudaSuccess) {
+      cudaGetLastError();
+      w.ctr = nullptr;
+      return MUON_ERR_OUT_OF_MEMORY;
+    }
+    w.ctr_bytes = want;
+    w.dirty = true;
+  }
+  if (w.dirty) {
+    if (cudaMemsetAsync(w.ctr, 0, w.ctr_bytes, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    w.dirty = false;
+  }
+  *out = static_cast<char*>(w.ptr);
+  *ctr_out = w.ctr;
+  return MUON_OK;
+}
+
+// ---- tensor maps ---------------------------------------------------------------------
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t cnt,
+              int64_t pitch, int64_t mstride, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(cnt)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch * 2),
+                           static_cast<cuuint64_t>(mstride * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(gemm_block_k()),
+                       static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---- launches ----------------------------------------------------------------------
+struct Launcher {
+  cudaStream_t stream;
+  int count = 0;
+  template <typename F>
+  muon_status_t run(int kind, F&& f) {
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (g_prof) {
+      cudaEventCreate(&e0);
+      cudaEventCreate(&e1);
+      cudaEventRecord(e0, stream);
+    }
+    cudaError_t e = f();
+    if (e != cudaSuccess) {
+      if (e0) cudaEventDestroy(e0);
+      if (e1) cudaEventDestroy(e1);
+      return MUON_ERR_CUDA;
+    }
+    if (g_prof) {
+      cudaEventRecord(e1, stream);
+      g_prof_recs.push_back({kind, e0, e1});
+    }
+    ++count;
+    return MUON_OK;
+  }
+};
+
+struct NsCfg {
+  int steps;
+  std::vector<float> coeffs;   // [steps][3]
+  float eps;
+};
+
+muon_status_t check_ns_cfg(const muon_ns_config_t* cfg, NsCfg* out) {
+  if (!cfg) {
+    out->steps = kDefSteps;
+    out->coeffs.clear();
+    for (int i = 0; i < kDefSteps; ++i) out->coeffs.insert(out->coeffs.end(), {kDefA, kDefB, kDefC});
+    out->eps = kDefEps;
+    return MUON_OK;
+  }
+  if (cfg->steps < 0 || cfg->steps > kMaxSteps) return MUON_ERR_INVALID_ARGUMENT;
+  if (cfg->precision != MUON_NS_BF16) {
+    if (cfg->precision == MUON_NS_TF32) return MUON_ERR_UNSUPPORTED;
+    return MUON_ERR_INVALID_ARGUMENT;
+  }
+  if (!std::isfinite(cfg->eps) || cfg->eps < 0.f) return MUON_ERR_INVALID_ARGUMENT;
+  out->steps = cfg->steps;
+  out->eps = cfg->eps;
+  out->coeffs.clear();
+  for (int i = 0; i < cfg->steps; ++i) {
+    float a = cfg->a, b = cfg->b, c = cfg->c;
+    if (cfg->coeffs) {
+      a = cfg->coeffs[3 * i];
+      b = cfg->coeffs[3 * i + 1];
+      c = cfg->coeffs[3 * i + 2];
+    }
+    if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c))
+      return MUON_ERR_INVALID_ARGUMENT;
+    out->coeffs.insert(out->coeffs.end(), {a, b, c});
+  }
+  return MUON_OK;
+}
+
+float scale_value(int64_t r, int64_t c, int rule) {
+  switch (rule) {
+    case MUON_SCALE_SQRT_MAX1_R_OVER_C:
+      return static_cast<float>(std::sqrt(std::max(1.0, double(r) / double(c))));
+    case MUON_SCALE_RMS_0P2_SQRT_MAXDIM:
+      return static_cast<float>(0.2 * std::sqrt(double(std::max(r, c))));
+    default:
+      return 1.f;
+  }
+}
+
+size_t esize(int dt) { return dt == MUON_F32 ? 4 : 2; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Run the whole step (step_mode) or an NS-only pass over `reqs`.
+// NS-only: reqs[i].G is the input, reqs[i].W the output (dtype w_dtype).
+muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int nesterov, float lr,
+                  float wd, int scale_rule, const NsCfg& ns, cudaStream_t stream) {
+  DevState* dev = nullptr;
+  muon_status_t st = dev_state(&dev);
+  if (st != MUON_OK) return st;
+  std::vector<ChunkP> plan = make_plan(reqs, dev->sms);
+  if (plan.empty()) {
+    t_last_launches = 0;
+    return MUON_OK;
+  }
+  size_t need = 0, need_ctr = 0;
+  for (auto& ch : plan) {
+    need = std::max(need, ch.bytes);
+    need_ctr = std::max(need_ctr, ch.ctrs);
+  }
+  char* ws = nullptr;
+  unsigned* ctr = nullptr;
+  st = get_workspace(stream, need, need_ctr, &ws, &ctr);
+  if (st != MUON_OK) return st;
+  const unsigned long long timeout_ns =
+      static_cast<unsigned long long>(env_size("MUON_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
+
+  Launcher L{stream};
+  for (const ChunkP& ch : plan) {
+    // ---- K1 -------------------------------------------------------------------
+    {
+      PrepParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      int64_t blocks = 0;
+      for (size_t i = 0; i < ch.slices.size(); ++i) {
+        const SliceP& s = ch.slices[i];
+        const Req& q = reqs[s.req];
+        const NsGroupP& g = ch.groups[s.ng];
+        PrepSlice& ps = pp.s[i];
+        const int64_t per = q.r * q.c;
+        ps.G = static_cast<const char*>(q.G) + s.b0 * per * esize(q.g_dtype);
+        ps.Mom = step_mode ? q.Mom + s.b0 * per : nullptr;
+        auto* X = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X) + s.idx0 * g.m * g.n_pad;
+        auto* Xt = reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt0) + s.idx0 * g.n * g.m_pad;
+        ps.direct = q.trans ? Xt : X;
+        ps.transp = q.trans ? X : Xt;
+        ps.pitch_d = q.trans ? g.m_pad : g.n_pad;
+        ps.pitch_t = q.trans ? g.n_pad : g.m_pad;
+        ps.mstride_d = q.trans ? g.n * g.m_pad : g.m * g.n_pad;
+        ps.mstride_t = q.trans ? g.m * g.n_pad : g.n * g.m_pad;
+        ps.ssq_part = reinterpret_cast<float*>(ws + g.off_ssq) + s.idx0 * g.prep_tiles;
+        ps.inv = reinterpret_cast<float*>(ws + g.off_inv) + s.idx0;
+        ps.cnt = ctr + g.ctr_prep + s.idx0;
+        ps.r = q.r;
+        ps.c = q.c;
+        ps.count = static_cast<int>(s.cnt);
+        ps.g_dtype = q.g_dtype;
+        ps.tiles_r = static_cast<int>(cdiv(q.r, kPrepTile));
+        ps.tiles_c = static_cast<int>(cdiv(q.c, kPrepTile));
+        ps.tile_base = static_cast<int>(blocks);
+        const bool gvec = q.g_dtype == MUON_F32 ? (q.c % 4 == 0) : (q.c % 8 == 0);
+        ps.vec = gvec && aligned(ps.G, 16) && (!step_mode || aligned(ps.Mom, 16));
+        ps.trans = q.trans ? 1 : 0;
+        blocks += s.cnt * ps.tiles_r * ps.tiles_c;
+      }
+      if (blocks >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+      pp.n_slices = static_cast<int>(ch.slices.size());
+      pp.total_blocks = static_cast<int>(blocks);
+      pp.step_mode = step_mode ? 1 : 0;
+      pp.mu = mu;
+      pp.nesterov = nesterov ? 1 : 0;
+      pp.eps = ns.eps;
+      pp.status = dev->status;
+      st = L.run(0, [&] { return launch_prep(pp, stream); });
+      if (st != MUON_OK) return st;
+    }
+    // ---- tensor maps -------------------------------------------------------------
+    struct Maps {
+      CUtensorMap X, A, B, Xt[2];
+    };
+    std::vector<Maps> maps(ch.groups.size());
+    for (size_t k = 0; k < ch.groups.size(); ++k) {
+      const NsGroupP& g = ch.groups[k];
+      const int bm = gemm_block_m(), bn = gemm_block_n();
+      bool ok = make_map(&maps[k].X, ws + g.off_X, g.n, g.m, g.cnt, g.n_pad, g.m * g.n_pad, bm) &&
+                make_map(&maps[k].A, ws + g.off_A, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bm) &&
+                make_map(&maps[k].B, ws + g.off_B, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bn) &&
+                make_map(&maps[k].Xt[0], ws + g.off_Xt0, g.m, g.n, g.cnt, g.m_pad, g.n * g.m_pad,
+                         bm) &&
+                make_map(&maps[k].Xt[1], ws + g.off_Xt1, g.m, g.n, g.cnt, g.m_pad, g.n * g.m_pad,
+                         bm);
+      if (!ok) return MUON_ERR_CUDA;
+    }
+    // ---- NS iterations -----------------------------------------------------------
+    const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
+    for (int it = 0; it < ns.steps; ++it) {
+      const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
+      for (int phase = 0; phase < 3; ++phase) {
+        GemmParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        int64_t tiles = 0;
+        for (size_t k = 0; k < ch.groups.size(); ++k) {
+          const NsGroupP& g = ch.groups[k];
+          GemmGroup& G = gp.g[k];
+          const int64_t nt = cdiv(g.m, bm);
+          auto* Xb = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X);
+          auto* Ab = reinterpret_cast<__nv_bfloat16*>(ws + g.off_A);
+          auto* Bb = reinterpret_cast<__nv_bfloat16*>(ws + g.off_B);
+          __nv_bfloat16* Xt[2] = {reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt0),
+                                  reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt1)};
+          G.m = static_cast<int>(g.m);
+          G.n = static_cast<int>(g.n);
+          G.count = static_cast<int>(g.cnt);
+          G.inv = reinterpret_cast<const float*>(ws + g.off_inv);
+          G.tile_base = static_cast<int>(tiles);
+          if (phase == kEpiGram) {
+            G.mapA = maps[k].X;
+            G.mapB = maps[k].X;
+            G.out0 = Ab;
+            G.pitch0 = g.m_pad;
+            G.mstride0 = g.m * g.m_pad;
+            G.partial = reinterpret_cast<float*>(ws + g.off_part);
+            G.tile_cnt = ctr + g.ctr_tile;
+            G.nt = static_cast<int>(nt);
+            G.ksplit = g.ksplit;
+            G.kb_per_split = g.kb_per_split;
+            G.num_kb = g.num_kb_gram;
+            G.tiles_per_mat = static_cast<int>(g.tri * g.ksplit);
+          } else if (phase == kEpiPoly) {
+            G.mapA = maps[k].A;
+            G.mapB = maps[k].A;
+            G.epi_in = Ab;
+            G.pitch_in = g.m_pad;
+            G.mstride_in = g.m * g.m_pad;
+            G.out0 = Bb;
+            G.pitch0 = g.m_pad;
+            G.mstride0 = g.m * g.m_pad;
+            G.nt = static_cast<int>(nt);
+            G.ksplit = 1;
+            G.num_kb = static_cast<int>(cdiv(g.m, bk));
+            G.kb_per_split = G.num_kb;
+            G.tiles_per_mat = static_cast<int>(g.tri);
+          } else {
+            G.mapA = maps[k].Xt[it & 1];
+            G.mapB = maps[k].B;
+            G.epi_in = Xt[it & 1];
+            G.pitch_in = g.m_pad;
+            G.mstride_in = g.n * g.m_pad;
+            G.out0 = Xt[(it + 1) & 1];
+            G.pitch0 = g.m_pad;
+            G.mstride0 = g.n * g.m_pad;
+            G.out1 = Xb;
+            G.pitch1 = g.n_pad;
+            G.mstride1 = g.m * g.n_pad;
+            G.nt = static_cast<int>(cdiv(g.m, bn));
+            G.mt = static_cast<int>(cdiv(g.n, bm));
+            G.ksplit = 1;
+            G.num_kb = static_cast<int>(cdiv(g.m, bk));
+            G.kb_per_split = G.num_kb;
+            G.tiles_per_mat = G.nt * G.mt;
+          }
+          tiles += static_cast<int64_t>(G.tiles_per_mat) * g.cnt;
+        }
+        if (tiles >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+        gp.n_groups = static_cast<int>(ch.groups.size());
+        gp.total_tiles = static_cast<int>(tiles);
+        // X' = a X + (b A + c A^2) X is evaluated as (a - alpha) X + (B + alpha I) X:
+        // identical in exact arithmetic, but the bf16 operand B + alpha I is
+        // smaller where a X and B X cancel, which lowers the rounding error.
+        const float alpha = kShiftFrac * ca;
+        gp.a = ca - alpha;
+        gp.b = cb;
+        gp.c = cc;
+        gp.alpha = alpha;
+        gp.first = it == 0 ? 1 : 0;
+        gp.status = dev->status;
+        gp.timeout_ns = timeout_ns;
+        st = L.run(1 + phase, [&] { return launch_gemm(phase, gp, stream); });
+        if (st != MUON_OK) return st;
+      }
+    }
+    // ---- K6 -------------------------------------------------------------------
+    {
+      FinParams fp;
+      std::memset(&fp, 0, sizeof(fp));
+      int64_t blocks = 0;
+      for (size_t i = 0; i < ch.slices.size(); ++i) {
+        const SliceP& s = ch.slices[i];
+        const Req& q = reqs[s.req];
+        const NsGroupP& g = ch.groups[s.ng];
+        FinSlice& fs = fp.s[i];
+        const int64_t per = q.r * q.c;
+        fs.W = static_cast<char*>(q.W) + s.b0 * per * esize(q.w_dtype);
+        const int fin = ns.steps & 1;
+        auto* X = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X) + s.idx0 * g.m * g.n_pad;
+        auto* Xt = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
+                   s.idx0 * g.n * g.m_pad;
+        fs.O = q.trans ? Xt : X;
+        fs.pitch_o = q.trans ? g.m_pad : g.n_pad;
+        fs.mstride_o = q.trans ? g.n * g.m_pad : g.m * g.n_pad;
+        fs.inv = ns.steps == 0 ? reinterpret_cast<const float*>(ws + g.off_inv) + s.idx0
+                               : nullptr;
+        fs.r = q.r;
+        fs.c = q.c;
+        fs.count = static_cast<int>(s.cnt);
+        fs.w_dtype = q.w_dtype;
+        fs.tiles_r = static_cast<int>(cdiv(q.r, kFinRows));
+        fs.tiles_c = static_cast<int>(cdiv(q.c, kFinCols));
+        fs.tile_base = static_cast<int>(blocks);
+        fs.vec = (q.w_dtype == MUON_F32 ? (q.c % 4 == 0) : (q.c % 8 == 0)) && aligned(fs.W, 16);
+        fs.scale = scale_value(q.r, q.c, scale_rule);
+        blocks += s.cnt * fs.tiles_r * fs.tiles_c;
+      }
+      if (blocks >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+      fp.n_slices = static_cast<int>(ch.slices.size());
+      fp.total_blocks = static_cast<int>(blocks);
+      fp.step_mode = step_mode ? 1 : 0;
+      fp.lr = lr;
+      fp.wd = wd;
+      st = L.run(4, [&] { return launch_finish(fp, stream); });
+      if (st != MUON_OK) return st;
+    }
+  }
+  t_last_launches = L.count;
+  return MUON_OK;
+}
+
+bool ranges_overlap(const std::vector<std::pair<uintptr_t, uintptr_t>>& r) {
+  std::vector<std::pair<uintptr_t, uintptr_t>> v;
+  for (auto& x : r)
+    if (x.second > x.first) v.push_back(x);
+  std::sort(v.begin(), v.end());
+  for (size_t i = 1; i < v.size(); ++i)
+    if (v[i].first < v[i - 1].second) return true;
+  return false;
+}
+
+muon_status_t step_impl(const muon_group_t* groups, int n_groups, float mu, int nesterov,
+                        float lr, float wd, int scale_rule, const muon_ns_config_t* nscfg,
+                        cudaStream_t stream) {
+  if (n_groups < 0 || (n_groups > 0 && !groups)) return MUON_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(mu) || !std::isfinite(lr) || !std::isfinite(wd))
+    return MUON_ERR_INVALID_ARGUMENT;
+  if (scale_rule < 0 || scale_rule > MUON_SCALE_ONE) return MUON_ERR_INVALID_ARGUMENT;
+  NsCfg ns;
+  muon_status_t st = check_ns_cfg(nscfg, &ns);
+  if (st != MUON_OK) return st;
+  std::vector<Req> reqs;
+  std::vector<std::pair<uintptr_t, uintptr_t>> written, all;
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_group_t& g = groups[i];
+    if (g.B < 0 || g.M < 0 || g.N < 0) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.w_dtype != MUON_F32 && g.w_dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.g_dtype != MUON_F32 && g.g_dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.B == 0 || g.M == 0 || g.N == 0) continue;
+    if (!g.W || !g.G || !g.Mom) return MUON_ERR_INVALID_ARGUMENT;
+    if (!aligned(g.W, esize(g.w_dtype)) || !aligned(g.G, esize(g.g_dtype)) || !aligned(g.Mom, 4))
+      return MUON_ERR_INVALID_ARGUMENT;
+    if (g.M > (1LL << 30) || g.N > (1LL << 30) || g.B > (1LL << 30))
+      return MUON_ERR_UNSUPPORTED;
+    const int64_t per = g.M * g.N;
+    const auto w0 = reinterpret_cast<uintptr_t>(g.W);
+    const auto g0 = reinterpret_cast<uintptr_t>(g.G);
+    const auto m0 = reinterpret_cast<uintptr_t>(g.Mom);
+    const uintptr_t wl = static_cast<uintptr_t>(g.B * per) * esize(g.w_dtype);
+    const uintptr_t gl = static_cast<uintptr_t>(g.B * per) * esize(g.g_dtype);
+    const uintptr_t ml = static_cast<uintptr_t>(g.B * per) * 4;
+    written.push_back({w0, w0 + wl});
+    written.push_back({m0, m0 + ml});
+    // a G range may be shared by two groups, but never with a written range
+    for (auto& x : std::vector<std::pair<uintptr_t, uintptr_t>>{{w0, w0 + wl}, {m0, m0 + ml}})
+      if (g0 < x.second && x.first < g0 + gl) return MUON_ERR_ALIAS;
+    all.push_back({g0, g0 + gl});
+    Req q;
+    q.W = g.W;
+    q.w_dtype = g.w_dtype;
+    q.G = g.G;
+    q.g_dtype = g.g_dtype;
+    q.Mom = g.Mom;
+    q.B = g.B;
+    q.r = g.M;
+    q.c = g.N;
+    q.trans = g.M > g.N;
+    q.m = std::min(g.M, g.N);
+    q.n = std::max(g.M, g.N);
+    reqs.push_back(q);
+  }
+  if (ranges_overlap(written)) return MUON_ERR_ALIAS;
+  for (auto& gr : all)
+    for (auto& w : written)
+      if (gr.first < w.second && w.first < gr.second) return MUON_ERR_ALIAS;
+  if (reqs.empty()) {
+    t_last_launches = 0;
+    return MUON_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  return run(reqs, true, mu, nesterov, lr, wd, scale_rule, ns, stream);
+}
+
+muon_status_t ns_impl(void* X, int dtype, int64_t B, int64_t M, int64_t N,
+                      const muon_ns_config_t* cfg, void* out, cudaStream_t stream) {
+  if (B < 0 || M < 0 || N < 0) return MUON_ERR_INVALID_ARGUMENT;
+  if (dtype != MUON_F32 && dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+  NsCfg ns;
+  muon_status_t st = check_ns_cfg(cfg, &ns);
+  if (st != MUON_OK) return st;
+  if (B == 0 || M == 0 || N == 0) {
+    t_last_launches = 0;
+    return MUON_OK;
+  }
+  if (!X) return MUON_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, esize(dtype)) || (out && !aligned(out, esize(dtype))))
+    return MUON_ERR_INVALID_ARGUMENT;
+  if (M > (1LL << 30) || N > (1LL << 30) || B > (1LL << 30)) return MUON_ERR_UNSUPPORTED;
+  const uintptr_t len = static_cast<uintptr_t>(B * M * N) * esize(dtype);
+  if (out && out != X) {
+    const auto x0 = reinterpret_cast<uintptr_t>(X), o0 = reinterpret_cast<uintptr_t>(out);
+    if (x0 < o0 + len && o0 < x0 + len) return MUON_ERR_ALIAS;
+  }
+  Req q;
+  q.W = out ? out : X;
+  q.w_dtype = dtype;
+  q.G = X;
+  q.g_dtype = dtype;
+  q.Mom = nullptr;
+  q.B = B;
+  q.r = M;
+  q.c = N;
+  q.trans = M > N;
+  q.m = std::min(M, N);
+  q.n = std::max(M, N);
+  std::lock_guard<std::mutex> lock(g_mu);
+  return run({q}, false, 0.f, 0, 0.f, 0.f, MUON_SCALE_ONE, ns, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status_t muon_ns_default_config(muon_ns_config_t* cfg) {
+  if (!cfg) return MUON_ERR_INVALID_ARGUMENT;
+  cfg->steps = kDefSteps;
+  cfg->coeffs = nullptr;
+  cfg->a = kDefA;
+  cfg->b = kDefB;
+  cfg->c = kDefC;
+  cfg->eps = kDefEps;
+  cfg->precision = MUON_NS_BF16;
+  return MUON_OK;
+}
+
+muon_status_t muon_ns_batched(void* X, int64_t B, int64_t M, int64_t N, int steps, float a,
+                              float b, float c, cudaStream_t stream) {
+  muon_ns_config_t cfg;
+  muon_ns_default_config(&cfg);
+  cfg.steps = steps;
+  cfg.a = a;
+  cfg.b = b;
+  cfg.c = c;
+  try {
+    return ns_impl(X, MUON_BF16, B, M, N, &cfg, nullptr, stream);
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
+muon_status_t muon_ns_batched_ex(void* X, int32_t dtype, int64_t B, int64_t M, int64_t N,
+                                 const muon_ns_config_t* cfg, void* out, cudaStream_t stream) {
+  try {
+    return ns_impl(X, dtype, B, M, N, cfg, out, stream);
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
+muon_status_t muon_step_grouped(const muon_group_t* groups, int n_groups, float mu, int nesterov,
+                                float lr, float wd, int scale_rule, cudaStream_t stream) {
+  try {
+    return step_impl(groups, n_groups, mu, nesterov, lr, wd, scale_rule, nullptr, stream);
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
+muon_status_t muon_step_grouped_ex(const muon_group_t* groups, int n_groups, float mu,
+                                   int nesterov, float lr, float wd, int scale_rule,
+                                   const muon_ns_config_t* ns, cudaStream_t stream) {
+  try {
+    return step_impl(groups, n_groups, mu, nesterov, lr, wd, scale_rule, ns, stream);
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
+muon_status_t muon_query_status(cudaStream_t stream) {
+  try {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevState* dev = nullptr;
+    muon_status_t st = dev_state(&dev);
+    if (st != MUON_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, dev->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    if (v) {
+      if (cudaMemset(dev->status, 0, sizeof(v)) != cudaSuccess) return MUON_ERR_CUDA;
+      for (auto& kv : g_ws) kv.second.dirty = true;
+    }
+    if (v & kDevTimeout) return MUON_ERR_TIMEOUT;
+    if (v & kDevNonfinite) return MUON_ERR_NONFINITE;
+    return MUON_OK;
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
+
+const char* muon_status_string(muon_status_t s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARGUMENT: return "MUON_ERR_INVALID_ARGUMENT";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_ALIAS: return "MUON_ERR_ALIAS";
+    case MUON_ERR_OUT_OF_MEMORY: return "MUON_ERR_OUT_OF_MEMORY";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+    case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
+    default: return "MUON_ERR_UNKNOWN";
+  }
+}
+
+void muon_release_workspace(void) {
+  try {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+      if (kv.second.ptr || kv.second.ctr) {
+        cudaSetDevice(kv.first.first);
+        cudaStreamSynchronize(kv.first.second);
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+        if (kv.second.ctr) cudaFree(kv.second.ctr);
+      }
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+  } catch (...) {
+  }
+}
+
+int muon_last_launch_count(void) { return t_last_launches; }
+
+int muon_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_prof = enable != 0;
+  return 5;
+}
+
+int muon_profile_read(double* ms, int64_t* launches, int n) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& r : g_prof_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.e1) == cudaSuccess && cudaEventElapsedTime(&t, r.e0, r.e1) ==
+                                                         cudaSuccess) {
+      if (r.kind < n) {
+        if (ms) ms[r.kind] += t;
+        if (launches) launches[r.kind] += 1;
+      }
+    }
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  g_prof_recs.clear();
+  return 5;
+}
+
+}  // extern "C"

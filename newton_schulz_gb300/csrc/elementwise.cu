@@ -1,0 +1,286 @@
+// Memory-bound kernels of the Muon step.
+//
+//  prep_kernel   (K1)  momentum + Nesterov, per-matrix ||D||_F^2 partials,
+//                      bf16 cast, and both layouts ([r][c] and [c][r]) of the
+//                      Newton-Schulz operand, in one pass over G and Mom.
+//                      DMuon-2 section 2.1 (M_t = mu*M_{t-1} + G, Nesterov);
+//                      HyperParallel-FSDP section 2.3 Eq. (1) (X0 = G/(||G||+eps))
+//                      and section 6.6 (transpose-first, bf16 NS path).
+//  finish_kernel (K6)  W <- (1 - lr*wd)*W - lr*s*O (RFC issue 204 item 6,
+//                      DMuon-2 section 2.1), or the copy-back of an NS-only call.
+//
+// Both are HBM-bound streaming kernels: 16-byte vector loads and stores,
+// warp-shuffle reductions, deterministic two-stage norm (per-tile partials,
+// then the last-arriving block of each matrix sums them in a fixed order).
+#include "muon_internal.h"
+
+namespace muon {
+
+namespace {
+
+__device__ __forceinline__ float bf16_to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ void load8_f32_stream(const float* p, float* d) {
+  float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  float4 b = __ldcs(reinterpret_cast<const float4*>(p + 4));
+  d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
+  d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
+}
+
+__device__ __forceinline__ void store8_f32(float* p, const float* d) {
+  *reinterpret_cast<float4*>(p) = make_float4(d[0], d[1], d[2], d[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(d[4], d[5], d[6], d[7]);
+}
+
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* d) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float2 f = __bfloat1622float2(h[j]);
+    d[2 * j] = f.x;
+    d[2 * j + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* d) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
+  return u;
+}
+
+template <typename Slice>
+__device__ __forceinline__ int find_slice(const Slice* s, int n, int blk) {
+  int i = 0;
+  while (i + 1 < n && blk >= s[i + 1].tile_base) ++i;
+  return i;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// K1
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepParams p) {
+  // fp32 tile of D in the stored [r][c] layout (+1 pad against bank conflicts)
+  __shared__ float sD[kPrepTile][kPrepTile + 1];
+  __shared__ float red[8];
+  __shared__ double dred[256];
+  __shared__ int s_last;
+
+  const int si = find_slice(p.s, p.n_slices, blockIdx.x);
+  const PrepSlice& s = p.s[si];
+  const int local = blockIdx.x - s.tile_base;
+  const int tiles = s.tiles_r * s.tiles_c;
+  const int mat = local / tiles;
+  const int t = local - mat * tiles;
+  const int ti = t / s.tiles_c, tj = t - ti * s.tiles_c;
+  const int64_t r0 = (int64_t)ti * kPrepTile, c0 = (int64_t)tj * kPrepTile;
+  const int tx = threadIdx.x & 7, ty = threadIdx.x >> 3;
+  const int64_t moff = (int64_t)mat * s.r * s.c;
+
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int lr = ty + 32 * pass;
+    const int64_t gr = r0 + lr;
+    const int lc = tx * 8;
+    const int64_t gc = c0 + lc;
+    float d[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j] = 0.f;
+    int nvalid = 0;
+    if (gr < s.r && gc < s.c) nvalid = (int)min((int64_t)8, s.c - gc);
+    if (nvalid > 0) {
+      const int64_t e = moff + gr * s.c + gc;
+      float g[8];
+      if (nvalid == 8 && s.vec) {
+        if (s.g_dtype == 0) load8_f32_stream(reinterpret_cast<const float*>(s.G) + e, g);
+        else load8_bf16(reinterpret_cast<const __nv_bfloat16*>(s.G) + e, g);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          g[j] = 0.f;
+          if (j < nvalid)
+            g[j] = s.g_dtype == 0 ? reinterpret_cast<const float*>(s.G)[e + j]
+                                  : bf16_to_f(reinterpret_cast<const __nv_bfloat16*>(s.G)[e + j]);
+        }
+      }
+      if (p.step_mode) {
+        float m[8];
+        if (nvalid == 8 && s.vec) {
+          load8_f32_stream(s.Mom + e, m);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m[j] = j < nvalid ? s.Mom[e + j] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float mn = fmaf(p.mu, m[j], g[j]);          // M_t = mu*M_{t-1} + G
+          m[j] = mn;
+          d[j] = p.nesterov ? fmaf(p.mu, mn, g[j]) : mn;    // D = G + mu*M_t
+        }
+        if (nvalid == 8 && s.vec) {
+          store8_f32(s.Mom + e, m);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < nvalid) s.Mom[e + j] = m[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j] = g[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j >= nvalid) d[j] = 0.f;
+      // [r][c] copy: the padded workspace row always has room for 8 elements.
+      *reinterpret_cast<uint4*>(s.direct + (int64_t)mat * s.mstride_d + gr * s.pitch_d + gc) =
+          pack8_bf16(d);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sD[lr][lc + j] = d[j];
+  }
+  __syncthreads();
+  // [c][r] copy from the shared-memory tile.
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int lcc = ty + 32 * pass;
+    const int64_t gcc = c0 + lcc;
+    const int lrr = tx * 8;
+    const int64_t grr = r0 + lrr;
+    if (gcc < s.c && grr < s.r) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = sD[lrr + j][lcc];
+      *reinterpret_cast<uint4*>(s.transp + (int64_t)mat * s.mstride_t + gcc * s.pitch_t + grr) =
+          pack8_bf16(v);
+    }
+  }
+
+  // Tile partial of ||D||_F^2, summed in an order fixed by the coordinates of
+  // the NS operand X (X = D, or D^T when transposed), so that a matrix and its
+  // transpose give bit-identical norms.  Thread t sums 16 consecutive X
+  // columns of X row t/4; then a fixed shuffle tree and the 8 warps in order.
+  float ssq = 0.f;
+  {
+    const int xi = threadIdx.x >> 2, xj0 = (threadIdx.x & 3) * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float v = s.trans ? sD[xj0 + j][xi] : sD[xi][xj0 + j];
+      ssq = fmaf(v, v, ssq);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ssq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.f;
+    for (int w = 0; w < 8; ++w) b += red[w];
+    // partial slot indexed by the X tile coordinates
+    const int xt = s.trans ? tj * s.tiles_r + ti : ti * s.tiles_c + tj;
+    s.ssq_part[(int64_t)mat * tiles + xt] = b;
+    __threadfence();
+    const unsigned prev = atomicAdd(&s.cnt[mat], 1u);
+    s_last = (prev == (unsigned)(tiles - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // Last block of this matrix: sum the partials in a fixed order.
+  __threadfence();
+  double acc = 0.0;
+  const float* part = s.ssq_part + (int64_t)mat * tiles;
+  for (int i = threadIdx.x; i < tiles; i += 256) acc += (double)__ldcg(part + i);
+  dred[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) dred[threadIdx.x] += dred[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double tot = dred[0];
+    const double nrm = sqrt(tot);
+    if (!isfinite(tot)) atomicOr(p.status, kDevNonfinite);
+    s.inv[mat] = (float)(1.0 / (nrm + (double)p.eps));
+    s.cnt[mat] = 0u;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K6
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinParams p) {
+  const int si = find_slice(p.s, p.n_slices, blockIdx.x);
+  const FinSlice& s = p.s[si];
+  const int local = blockIdx.x - s.tile_base;
+  const int tiles = s.tiles_r * s.tiles_c;
+  const int mat = local / tiles;
+  const int t = local - mat * tiles;
+  const int ti = t / s.tiles_c, tj = t - ti * s.tiles_c;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t gr = (int64_t)ti * kFinRows + ty;
+  const int64_t gc = (int64_t)tj * kFinCols + tx * 8;
+  if (gr >= s.r || gc >= s.c) return;
+  const int nvalid = (int)min((int64_t)8, s.c - gc);
+
+  float o[8];
+  load8_bf16(s.O + (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc, o);
+  const float os = s.inv ? s.inv[mat] : 1.f;
+  const int64_t e = (int64_t)mat * s.r * s.c + gr * s.c + gc;
+
+  if (p.step_mode) {
+    const float decay = 1.f - p.lr * p.wd;
+    const float step = p.lr * s.scale * os;
+    float w[8];
+    if (s.w_dtype == 0) {
+      float* W = reinterpret_cast<float*>(s.W);
+      if (nvalid == 8 && s.vec) {
+        load8_f32_stream(W + e, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = fmaf(decay, w[j], -step * o[j]);
+        store8_f32(W + e, w);
+      } else {
+        for (int j = 0; j < nvalid; ++j) W[e + j] = fmaf(decay, W[e + j], -step * o[j]);
+      }
+    } else {
+      __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(s.W);
+      if (nvalid == 8 && s.vec) {
+        load8_bf16(W + e, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = fmaf(decay, w[j], -step * o[j]);
+        *reinterpret_cast<uint4*>(W + e) = pack8_bf16(w);
+      } else {
+        for (int j = 0; j < nvalid; ++j)
+          W[e + j] = __float2bfloat16_rn(fmaf(decay, bf16_to_f(W[e + j]), -step * o[j]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] *= os;
+    if (s.w_dtype == 0) {
+      float* W = reinterpret_cast<float*>(s.W);
+      if (nvalid == 8 && s.vec) store8_f32(W + e, o);
+      else for (int j = 0; j < nvalid; ++j) W[e + j] = o[j];
+    } else {
+      __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(s.W);
+      if (nvalid == 8 && s.vec) *reinterpret_cast<uint4*>(W + e) = pack8_bf16(o);
+      else for (int j = 0; j < nvalid; ++j) W[e + j] = __float2bfloat16_rn(o[j]);
+    }
+  }
+}
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
+  if (p.total_blocks <= 0) return cudaSuccess;
+  prep_kernel<<<p.total_blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finish(const FinParams& p, cudaStream_t s) {
+  if (p.total_blocks <= 0) return cudaSuccess;
+  finish_kernel<<<p.total_blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace muon

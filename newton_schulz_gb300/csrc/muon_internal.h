@@ -1,0 +1,120 @@
+// Internal interface between the host planner (api.cpp) and the CUDA
+// kernels.  Every kernel takes one __grid_constant__ parameter struct, so a
+// launch needs no host-to-device descriptor copy.
+#pragma once
+
+#include <cuda.h>           // CUtensorMap (type only; the driver is reached at run time)
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace muon {
+
+// ---- device status word bits ------------------------------------------------
+constexpr unsigned kDevTimeout = 1u;
+constexpr unsigned kDevNonfinite = 2u;
+
+// ---- limits ------------------------------------------------------------------
+constexpr int kMaxSlices = 64;    // user (group, batch-range) pieces per launch
+constexpr int kMaxNsGroups = 12;  // core shapes per NS launch
+constexpr int kMaxSteps = 64;
+
+// ---- K1: momentum / norm / cast / transpose ---------------------------------
+constexpr int kPrepTile = 64;     // 64 x 64 tile of the stored [r][c] matrix
+
+struct PrepSlice {
+  const void* G;          // [count][r][c] (gradient, or the NS input)
+  float* Mom;             // [count][r][c] fp32 (step mode), else null
+  __nv_bfloat16* direct;  // workspace copy in [r][c] layout
+  __nv_bfloat16* transp;  // workspace copy in [c][r] layout
+  float* ssq_part;        // [count][tiles] per-tile partial sum of squares
+  float* inv;             // [count] 1/(||D||_F + eps)
+  unsigned* cnt;          // [count] arrival counters (left at zero)
+  int64_t r, c;
+  int64_t pitch_d, pitch_t;   // row pitches (elements)
+  int64_t mstride_d, mstride_t;
+  int count;
+  int g_dtype;            // 0 f32, 1 bf16
+  int tiles_r, tiles_c;
+  int tile_base;          // first block of this slice
+  int vec;                // 1: 16-byte vector path is legal
+  int trans;              // 1: X = D^T (rows > cols)
+};
+
+struct PrepParams {
+  PrepSlice s[kMaxSlices];
+  int n_slices;
+  int total_blocks;
+  int step_mode;          // 1: momentum step, 0: NS-only input
+  float mu;
+  int nesterov;
+  float eps;
+  unsigned* status;
+};
+
+// ---- K6: update / copy-back --------------------------------------------------
+constexpr int kFinRows = 8, kFinCols = 256;
+
+struct FinSlice {
+  void* W;                     // step: weights [count][r][c]; ns: output
+  const __nv_bfloat16* O;      // NS result in [r][c] layout (workspace)
+  const float* inv;            // [count] extra factor when steps == 0, else null
+  int64_t r, c, pitch_o, mstride_o;
+  int count;
+  int w_dtype;
+  int tiles_r, tiles_c, tile_base;
+  int vec;
+  float scale;                 // update scale s(r, c)
+};
+
+struct FinParams {
+  FinSlice s[kMaxSlices];
+  int n_slices;
+  int total_blocks;
+  int step_mode;
+  float lr, wd;
+};
+
+// ---- NS GEMM phases -----------------------------------------------------------
+enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiApply = 2 };
+
+struct alignas(128) GemmGroup {
+  CUtensorMap mapA;       // operand A (rows = tile M dim, inner = K)
+  CUtensorMap mapB;       // operand B (rows = tile N dim, inner = K)
+  const __nv_bfloat16* epi_in;   // poly: A; apply: Xt_old
+  __nv_bfloat16* out0;           // gram: A; poly: B; apply: Xt_new
+  __nv_bfloat16* out1;           // apply: X
+  const float* inv;              // first iteration scale (per matrix) or null
+  float* partial;                // gram split-K partials
+  unsigned* tile_cnt;            // gram split-K arrival counters
+  int64_t pitch_in, pitch0, pitch1;
+  int64_t mstride_in, mstride0, mstride1;
+  int m, n;
+  int count;
+  int tiles_per_mat;
+  int tile_base;
+  int nt;          // symmetric: tiles per side; apply: tiles along m (N dim)
+  int mt;          // apply: tiles along n (M dim)
+  int ksplit, kb_per_split, num_kb;
+};
+
+struct GemmParams {
+  GemmGroup g[kMaxNsGroups];
+  int n_groups;
+  int total_tiles;
+  float a, b, c;           // apply uses a - alpha; poly adds alpha on the diagonal
+  float alpha;             // shift: X' = (a - alpha) X + (b A + c A^2 + alpha I) X
+  int first;              // 1: operands are unnormalised, apply inv scale
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+// ---- launchers (return cudaGetLastError()) ----------------------------------
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
+cudaError_t launch_finish(const FinParams& p, cudaStream_t s);
+cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s);
+int gemm_block_n();      // N tile of the NS GEMMs
+int gemm_block_m();      // M tile (TMEM lanes)
+int gemm_block_k();      // K per pipeline stage
+
+}  // namespace muon

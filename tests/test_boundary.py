@@ -1,0 +1,117 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports
+every entry point declared in include/muon.h, and rejects bad arguments before
+touching CUDA (nothing is enqueued, so no device is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from newton_schulz_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "muon.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(muon_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ("muon_ns_batched", "muon_step_grouped", "muon_ns_batched_ex",
+              "muon_step_grouped_ex", "muon_query_status", "muon_status_string",
+              "muon_release_workspace"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    for name in binding.EXPORTED:
+        assert name in _declared_functions()
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        assert lib.muon_status_string(code).decode() == name
+    assert lib.muon_status_string(99).decode() == "MUON_ERR_UNKNOWN"
+
+
+def test_default_config(lib):
+    cfg = binding.NsConfig()
+    assert lib.muon_ns_default_config(ctypes.byref(cfg)) == 0
+    assert cfg.steps == 5 and cfg.precision == 0
+    assert abs(cfg.a - 3.4445) < 1e-6 and abs(cfg.b + 4.775) < 1e-6 and abs(cfg.c - 2.0315) < 1e-6
+    assert abs(cfg.eps - 1e-7) < 1e-12
+    assert lib.muon_ns_default_config(None) == 1
+
+
+E_INV, E_UNS, E_ALIAS = 1, 2, 3
+
+
+def _grp(W=0x1000, G=0x100000, M_=0x200000, B=1, M=4, N=8, wdt=0, gdt=0):
+    return binding.Group(W, wdt, G, gdt, M_, B, M, N)
+
+
+def _step(lib, groups, n=None, mu=0.95, lr=0.02, wd=0.01, rule=0, cfg=None):
+    arr = (binding.Group * max(1, len(groups)))(*groups)
+    n = len(groups) if n is None else n
+    if cfg is None:
+        return lib.muon_step_grouped(arr, n, mu, 1, lr, wd, rule, None)
+    return lib.muon_step_grouped_ex(arr, n, mu, 1, lr, wd, rule, ctypes.byref(cfg), None)
+
+
+def test_step_argument_errors(lib):
+    assert lib.muon_step_grouped(None, 1, 0.95, 1, 0.02, 0.01, 0, None) == E_INV
+    assert lib.muon_step_grouped(None, -1, 0.95, 1, 0.02, 0.01, 0, None) == E_INV
+    assert _step(lib, [_grp(B=-1)]) == E_INV
+    assert _step(lib, [_grp(M=-2)]) == E_INV
+    assert _step(lib, [_grp(W=0)]) == E_INV
+    assert _step(lib, [_grp(G=0)]) == E_INV
+    assert _step(lib, [_grp(M_=0)]) == E_INV
+    assert _step(lib, [_grp(wdt=7)]) == E_INV
+    assert _step(lib, [_grp(gdt=-1)]) == E_INV
+    assert _step(lib, [_grp(W=0x1001)]) == E_INV          # misaligned f32
+    assert _step(lib, [_grp()], rule=9) == E_INV
+    assert _step(lib, [_grp()], mu=float("nan")) == E_INV
+    assert _step(lib, [_grp()], lr=float("inf")) == E_INV
+
+
+def test_step_alias_errors(lib):
+    # W overlaps Mom
+    assert _step(lib, [_grp(W=0x1000, M_=0x1040)]) == E_ALIAS
+    # G overlaps W
+    assert _step(lib, [_grp(W=0x1000, G=0x1010)]) == E_ALIAS
+    # W of one group overlaps Mom of another
+    assert _step(lib, [_grp(W=0x1000, G=0x100000, M_=0x200000),
+                       _grp(W=0x300000, G=0x400000, M_=0x1000)]) == E_ALIAS
+
+
+def test_ns_config_errors(lib):
+    assert _step(lib, [_grp()], cfg=binding.make_config(steps=-1)) == E_INV
+    assert _step(lib, [_grp()], cfg=binding.make_config(steps=65)) == E_INV
+    assert _step(lib, [_grp()], cfg=binding.make_config(eps=-1.0)) == E_INV
+    assert _step(lib, [_grp()], cfg=binding.make_config(precision=1)) == E_UNS
+    assert _step(lib, [_grp()], cfg=binding.make_config(precision=5)) == E_INV
+    bad = binding.make_config(steps=2, coeffs=[[1, 2, 3], [float("nan"), 0, 0]])
+    assert _step(lib, [_grp()], cfg=bad) == E_INV
+
+
+def test_empty_inputs_are_noops(lib):
+    assert lib.muon_step_grouped(None, 0, 0.95, 1, 0.02, 0.01, 0, None) == 0
+    assert _step(lib, [_grp(B=0, W=0, G=0, M_=0)]) == 0
+    assert lib.muon_ns_batched(None, 0, 3, 4, 5, 1.0, 0.0, 0.0, None) == 0
+    assert lib.muon_ns_batched(0x1000, 2, 0, 4, 5, 1.0, 0.0, 0.0, None) == 0
+
+
+def test_ns_argument_errors(lib):
+    assert lib.muon_ns_batched(None, 1, 3, 4, 5, 1.0, 0.0, 0.0, None) == E_INV
+    assert lib.muon_ns_batched(0x1001, 1, 3, 4, 5, 1.0, 0.0, 0.0, None) == E_INV
+    assert lib.muon_ns_batched(0x1000, -1, 3, 4, 5, 1.0, 0.0, 0.0, None) == E_INV
+    assert lib.muon_ns_batched(0x1000, 1, 3, 4, -1, 1.0, 0.0, 0.0, None) == E_INV
+    assert lib.muon_ns_batched(0x1000, 1, 3, 4, 5, float("nan"), 0.0, 0.0, None) == E_INV
+    assert lib.muon_ns_batched_ex(0x1000, 3, 1, 3, 4, None, None, None) == E_INV
+    # out overlapping X
+    assert lib.muon_ns_batched_ex(0x1000, 0, 1, 3, 4, None, 0x1008, None) == E_ALIAS
