@@ -134,6 +134,27 @@ muon_status_t muon_step_grouped(const muon_group_t *groups, int n_groups, float 
                                 int nesterov, float lr, float wd, int scale_rule,
                                 cudaStream_t stream);
 
+/* Allocation-free variant of muon_ns_batched (no counterpart on the pages:
+ * it exists for deployment, not for the method).  For callers that must not
+ * allocate device memory -- code running inside a framework whose caching
+ * allocator has to own every device allocation, or a process whose memory
+ * budget is carved up before it starts -- this call keeps its whole
+ * workspace in one fixed 64 MiB device array inside the library, so it calls
+ * no cudaMalloc, cudaFree or allocating library routine.  Every GPU that
+ * loads the library holds those 64 MiB until the process exits.
+ *   Same arguments and result as muon_ns_batched (bf16 X [B,M,N], in place,
+ *   eps = 1e-7).  A problem whose workspace does not fit in the array
+ *   (roughly 3*B*M*N + 2*B*min(M,N)^2 bf16 values plus split-K partials) is
+ *   rejected with MUON_ERR_UNSUPPORTED before anything is enqueued.
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls share the one array: calls that can overlap on the GPU (other
+ *   streams, other host threads) race and must be serialised by the caller.
+ *   Device-side conditions (a non-finite norm) are not reported through
+ *   muon_query_status for this entry point. */
+muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, int steps,
+                                      float a, float b, float c, cudaStream_t stream);
+
 /* As muon_step_grouped with an explicit NS configuration (NULL = defaults). */
 muon_status_t muon_step_grouped_ex(const muon_group_t *groups, int n_groups, float mu,
                                    int nesterov, float lr, float wd, int scale_rule,
