@@ -66,13 +66,15 @@ def nominal_flops(shapes, steps=STEPS_NS):
 
 def algorithmic_bytes(shapes):
     """Per kernel kind: prep reads G, Mom and writes Mom, X, X^T (bf16);
-    update reads W, the bf16 result and writes W."""
-    prep = upd = 0
+    update reads W, the bf16 result and writes W; the fused small-m kernel
+    moves only the compulsory bytes (G read, Mom and W read and written)."""
+    prep = upd = fused = 0
     for b, r, c, we, ge in shapes:
         e = b * r * c
         prep += e * (ge + 4 + 4 + 2 + 2)
         upd += e * (we + we + 2)
-    return {"prep": prep, "update": upd}
+        fused += e * (ge + 4 + 4 + we + we)
+    return {"prep": prep, "update": upd, "fused_small": fused}
 
 
 def gemm_flops_per_kind(shapes, steps=STEPS_NS):
@@ -355,7 +357,7 @@ def main():
     byt = algorithmic_bytes(shapes)
     fl = gemm_flops_per_kind(shapes)
     launches_kind = n_launch / args.steps
-    if dom in ("prep", "update"):
+    if dom in ("prep", "update", "fused_small"):
         per_launch = byt[dom] / launches_kind
         achieved = per_launch / (avg_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

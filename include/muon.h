@@ -179,7 +179,8 @@ int muon_last_launch_count(void);
  * stream is synchronised) adds the elapsed milliseconds per kernel kind into
  * ms[0..n) and launch counts into launches[0..n) and resets the record.
  * Kinds: 0 prep (momentum/norm/cast/transpose), 1 Gram, 2 polynomial,
- * 3 apply, 4 update/copy-back.  Returns the number of kinds (5). */
+ * 3 apply, 4 update/copy-back, 5 fused small-m step.  Returns the number of
+ * kinds (6). */
 int muon_profile_enable(int enable);
 int muon_profile_read(double *ms, int64_t *launches, int n);
 

@@ -22,7 +22,7 @@ STATUS_NAMES = {
 MUON_F32, MUON_BF16 = 0, 1
 SCALE_SQRT_MAX1_R_OVER_C, SCALE_RMS_0P2_SQRT_MAXDIM, SCALE_ONE = 0, 1, 2
 NS_BF16, NS_TF32 = 0, 1
-PROFILE_KINDS = ("prep", "gram", "poly", "apply", "update")
+PROFILE_KINDS = ("prep", "gram", "poly", "apply", "update", "fused_small")
 
 EXPORTED = (
     "muon_ns_default_config", "muon_ns_batched", "muon_ns_batched_ex", "muon_step_grouped",

@@ -187,6 +187,56 @@ void layout_chunk(ChunkP& ch, int sms) {
   ch.ctrs = ctr;
 }
 
+// Shared-memory carve-up of the fused small-m kernel for cluster size cs.
+void small_layout(int64_t m, int64_t n, int cs, SmallParams* sp) {
+  sp->cs = cs;
+  sp->w = static_cast<int>(rup(cdiv(n, cs), 128));
+  sp->mr = static_cast<int>(rup(m, 8));
+  sp->nmm = static_cast<int>(rup(m, 16));
+  const size_t xbytes = static_cast<size_t>(sp->w / 64) * sp->mr * 128;
+  sp->off_bt = static_cast<int>(align_up(xbytes, 1024));
+  sp->off_part = sp->off_bt + 2 * kSmallBTile;
+  sp->off_a = sp->off_part + static_cast<int>(align_up(2 * m * m * 4, 16));
+  sp->off_misc = sp->off_a + static_cast<int>(align_up(m * (m + 1) * 4, 16));
+  // at least 80 KB: at most two CTAs per SM, so two TMEM allocations always fit
+  sp->smem_bytes = std::max(sp->off_misc + 128 + 1024, 80 * 1024);
+}
+
+// Cluster size of the fused small-m kernel for a core shape (m, n) with
+// `count` matrices, or false when the shape goes to the grouped GEMM path.
+// Among the cluster sizes whose share of X fits in shared memory, pick the
+// one with the least (waves x per-CTA work), waves = count / (clusters the
+// device can hold at once).  MUON_SMALL_CS forces a size when it fits.
+bool small_shape(int64_t m, int64_t n, int64_t count, int* cs_out) {
+  const char* env = std::getenv("MUON_SMALL_PATH");
+  if (env && env[0] == '0') return false;
+  if (m > kSmallMaxM) return false;
+  const int forced = static_cast<int>(env_size("MUON_SMALL_CS", 0));
+  static std::map<std::pair<int, int>, int> occ;   // (cs, smem) -> max active clusters
+  int best = 0;
+  double best_cost = 0;
+  for (int cs = 1; cs <= kSmallMaxCluster; cs *= 2) {
+    if (forced && cs != forced) continue;
+    SmallParams sp;
+    small_layout(m, n, cs, &sp);
+    if (static_cast<int64_t>(sp.w / 64) * sp.mr * 128 > kSmallMaxXBytes) continue;
+    if (sp.smem_bytes > 227 * 1024) continue;
+    if (cs > 1 && (static_cast<int64_t>(cs - 1) * sp.w >= n)) continue;   // an idle CTA
+    int& mc = occ[{cs, sp.smem_bytes}];
+    if (mc == 0) mc = small_max_active_clusters(cs, sp.smem_bytes);
+    if (mc <= 0) continue;
+    const double waves = static_cast<double>(cdiv(count, mc));
+    const double cost = waves * (static_cast<double>(sp.w) * sp.mr + 20000.0);
+    if (!best || cost < best_cost) {
+      best = cs;
+      best_cost = cost;
+    }
+  }
+  if (!best) return false;
+  *cs_out = best;
+  return true;
+}
+
 std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms) {
   const int64_t cap = static_cast<int64_t>(env_size("MUON_WS_CAP", size_t(1) << 29));
   std::vector<int> order;
@@ -397,9 +447,80 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
   DevState* dev = nullptr;
   muon_status_t st = dev_state(&dev);
   if (st != MUON_OK) return st;
-  std::vector<ChunkP> plan = make_plan(reqs, dev->sms);
+  const unsigned long long timeout_ns0 =
+      static_cast<unsigned long long>(env_size("MUON_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
+  Launcher L0{stream};
+
+  // ---- small core shapes: one fused cluster kernel per core shape -------------------
+  std::vector<Req> large;
+  {
+    std::map<std::pair<int64_t, int64_t>, std::vector<int>> shapes;
+    for (int i = 0; i < static_cast<int>(reqs.size()); ++i) {
+      const Req& q = reqs[i];
+      if (q.B <= 0 || q.m <= 0) continue;
+      shapes[{q.m, q.n}].push_back(i);
+    }
+    for (auto& kv : shapes) {
+      const int64_t m = kv.first.first, n = kv.first.second;
+      int64_t count = 0;
+      for (int i : kv.second) count += reqs[i].B;
+      int cs = 0;
+      if (!small_shape(m, n, count, &cs)) {
+        for (int i : kv.second) large.push_back(reqs[i]);
+        continue;
+      }
+      for (size_t b = 0; b < kv.second.size(); b += kMaxSlices) {
+        SmallParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        int64_t mats = 0;
+        const size_t e = std::min(kv.second.size(), b + kMaxSlices);
+        for (size_t k = b; k < e; ++k) {
+          const Req& q = reqs[kv.second[k]];
+          SmallSlice& ss = sp.s[k - b];
+          ss.G = q.G;
+          ss.Mom = step_mode ? q.Mom : nullptr;
+          ss.W = q.W;
+          ss.count = static_cast<int>(q.B);
+          ss.mat_base = static_cast<int>(mats);
+          ss.trans = q.trans ? 1 : 0;
+          ss.g_dtype = q.g_dtype;
+          ss.w_dtype = q.w_dtype;
+          const int64_t inner = q.c;   // contiguous extent of a stored row
+          ss.gvec = (q.g_dtype == MUON_F32 ? inner % 4 == 0 : inner % 8 == 0) &&
+                    aligned(q.G, 16) && inner % 4 == 0 && (!step_mode || aligned(q.Mom, 16));
+          ss.wvec = (q.w_dtype == MUON_F32 ? inner % 4 == 0 : inner % 8 == 0) && aligned(q.W, 16);
+          ss.scale = scale_value(q.r, q.c, scale_rule);
+          mats += q.B;
+        }
+        if (mats * cs >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+        sp.n_slices = static_cast<int>(e - b);
+        sp.m = static_cast<int>(m);
+        sp.n = static_cast<int>(n);
+        small_layout(m, n, cs, &sp);
+        sp.steps = ns.steps;
+        for (int it = 0; it < ns.steps; ++it) {
+          const float ca = ns.coeffs[3 * it], alpha = kShiftFrac * ca;
+          sp.coef[it][0] = ca - alpha;
+          sp.coef[it][1] = ns.coeffs[3 * it + 1];
+          sp.coef[it][2] = ns.coeffs[3 * it + 2];
+          sp.coef[it][3] = alpha;
+        }
+        sp.step_mode = step_mode ? 1 : 0;
+        sp.nesterov = nesterov ? 1 : 0;
+        sp.mu = mu;
+        sp.lr = lr;
+        sp.wd = wd;
+        sp.eps = ns.eps;
+        sp.status = dev->status;
+        sp.timeout_ns = timeout_ns0;
+        st = L0.run(5, [&] { return launch_small(sp, static_cast<int>(mats), stream); });
+        if (st != MUON_OK) return st;
+      }
+    }
+  }
+  std::vector<ChunkP> plan = make_plan(large, dev->sms);
   if (plan.empty()) {
-    t_last_launches = 0;
+    t_last_launches = L0.count;
     return MUON_OK;
   }
   size_t need = 0, need_ctr = 0;
@@ -423,7 +544,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       int64_t blocks = 0;
       for (size_t i = 0; i < ch.slices.size(); ++i) {
         const SliceP& s = ch.slices[i];
-        const Req& q = reqs[s.req];
+        const Req& q = large[s.req];
         const NsGroupP& g = ch.groups[s.ng];
         PrepSlice& ps = pp.s[i];
         const int64_t per = q.r * q.c;
@@ -575,7 +696,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       int64_t blocks = 0;
       for (size_t i = 0; i < ch.slices.size(); ++i) {
         const SliceP& s = ch.slices[i];
-        const Req& q = reqs[s.req];
+        const Req& q = large[s.req];
         const NsGroupP& g = ch.groups[s.ng];
         FinSlice& fs = fp.s[i];
         const int64_t per = q.r * q.c;
@@ -610,7 +731,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       if (st != MUON_OK) return st;
     }
   }
-  t_last_launches = L.count;
+  t_last_launches = L.count + L0.count;
   return MUON_OK;
 }
 
@@ -841,7 +962,7 @@ int muon_last_launch_count(void) { return t_last_launches; }
 int muon_profile_enable(int enable) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_prof = enable != 0;
-  return 5;
+  return 6;
 }
 
 int muon_profile_read(double* ms, int64_t* launches, int n) {
@@ -859,7 +980,7 @@ int muon_profile_read(double* ms, int64_t* launches, int n) {
     cudaEventDestroy(r.e1);
   }
   g_prof_recs.clear();
-  return 5;
+  return 6;
 }
 
 }  // extern "C"

@@ -109,6 +109,45 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
+// ---- fused small-m path (one thread-block cluster per matrix) ---------------
+constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
+constexpr int kSmallMaxXBytes = 176 * 1024; // X columns held per CTA (bf16, swizzled)
+constexpr int kSmallMaxCluster = 8;        // portable cluster sizes 1..8
+constexpr int kSmallUnroll = 4;            // streaming items in flight per thread
+constexpr int kSmallThreads = 256;
+constexpr int kSmallTmemCols = 256;
+constexpr int kSmallBTile = 8192;          // one B' operand tile: 64 rows x 128 bytes
+
+struct SmallSlice {
+  const void* G;     // step: gradient; NS only: the input
+  float* Mom;        // step mode only
+  void* W;           // step: weights; NS only: the output
+  int count;         // matrices in this slice
+  int mat_base;      // index of its first matrix within the launch
+  int trans;         // stored rows > cols
+  int g_dtype, w_dtype;
+  int gvec, wvec;    // 16-byte vector paths legal for G/Mom and W
+  float scale;       // update scale s(rows, cols)
+};
+
+struct SmallParams {
+  SmallSlice s[kMaxSlices];
+  int n_slices;
+  int m, n;          // core shape, m <= n
+  int cs;            // CTAs per matrix (cluster size)
+  int w;             // X columns per CTA (multiple of 128)
+  int mr;            // X rows held: m rounded up to 8
+  int nmm;           // MMA N (and apply K): m rounded up to 16
+  int steps;
+  float coef[kMaxSteps][4];   // per step: a - alpha, b, c, alpha
+  int step_mode, nesterov;
+  float mu, lr, wd, eps;
+  unsigned* status;
+  unsigned long long timeout_ns;
+  int off_bt, off_part, off_a, off_misc;   // shared-memory carve-up (bytes)
+  int smem_bytes;
+};
+
 // ---- launchers (return cudaGetLastError()) ----------------------------------
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
 cudaError_t launch_finish(const FinParams& p, cudaStream_t s);
@@ -116,5 +155,7 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s);
 int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage
+cudaError_t launch_small(const SmallParams& p, int total_mats, cudaStream_t s);
+int small_max_active_clusters(int cs, int smem_bytes);   // 0 when the query fails
 
 }  // namespace muon

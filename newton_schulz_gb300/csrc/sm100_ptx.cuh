@@ -149,3 +149,59 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 
 }  // namespace ptx
 }  // namespace muon
+
+namespace muon {
+namespace ptx {
+
+// Shared-memory matrix descriptor for an MN-major operand with 128-byte
+// swizzle: 8-row K groups (one 1024-byte swizzle atom each) `kgroup_stride`
+// bytes apart (SBO), 64-element MN chunks `mn_stride` bytes apart (LBO).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride,
+                                                        uint32_t kgroup_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((kgroup_stride >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Byte offset of (row, byte-in-row) in a tile of 128-byte rows written with
+// the 128-byte swizzle (16-byte chunk index XOR row % 8), as TMA lays it out.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row) {
+  return (row >> 3) * 1024u + (row & 7u) * 128u +
+         ((((byte_in_row >> 4) ^ row) & 7u) << 4) + (byte_in_row & 15u);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Full-cluster barrier (every thread of every CTA arrives; release/acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+}  // namespace ptx
+}  // namespace muon

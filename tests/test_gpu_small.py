@@ -1,0 +1,111 @@
+"""GPU parity of the fused small-m cluster kernel (m <= 64), and of the grouped
+GEMM path on the same shapes (MUON_SMALL_PATH=0), against the float64 oracle."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from newton_schulz_gb300 import binding, synth
+from oracle import muon_ref as R
+
+pytestmark = pytest.mark.gpu
+NS_TOL, MOM_TOL, DW_TOL = 3e-2, 1e-6, 1e-2
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+@pytest.fixture(autouse=True)
+def _dev(lib, cuda_ok):
+    yield
+    os.environ.pop("MUON_SMALL_PATH", None)
+
+
+SHAPES = [
+    (3, 8, 300),        # m = 8
+    (2, 33, 1000),      # m = 33: 48-wide MMA N, ragged n
+    (2, 1000, 48),      # transposed, m = 48
+    (6, 64, 4097),      # m = 64, several CTAs per matrix, ragged tail
+    (20, 24, 2048),     # many matrices
+    (1, 24, 10240),     # the tall-skinny shape, eight CTAs
+    (3, 5000, 17),      # transposed, odd m
+]
+
+
+@pytest.mark.parametrize("generic", [False, True])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_small_ns_parity(shape, generic):
+    if generic:
+        os.environ["MUON_SMALL_PATH"] = "0"
+    x = torch.randn(shape, generator=torch.Generator().manual_seed(sum(shape)))
+    X = x.cuda()
+    out = torch.empty_like(X)
+    binding.muon_ns_batched_ex(X, binding.make_config(), out)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    ref = R.ns_batched_ref(_np(x))
+    got = _np(out)
+    for i in range(shape[0]):
+        assert _rel(got[i], ref[i]) <= NS_TOL, (shape, i, _rel(got[i], ref[i]))
+    # one fused launch per core shape on the small path
+    assert binding.muon_last_launch_count() == (17 if generic else 1)
+
+
+@pytest.mark.parametrize("shape", [(4, 24, 3000), (3, 3000, 24), (2, 64, 256)])
+def test_small_step_parity_bf16_grad(shape):
+    g = synth.random_group(shape, torch.bfloat16, torch.float32, "cuda", 31, 1e-3, 1e-3)
+    host = {k: _np(g[k]) for k in ("W", "G", "Mom")}
+    binding.muon_step_grouped([g], mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    w2, m2, _ = R.muon_step_ref(host["W"], host["G"], host["Mom"])
+    assert _rel(_np(g["Mom"]), m2) <= MOM_TOL
+    w = _np(g["W"])
+    for i in range(shape[0]):
+        assert np.linalg.norm(w[i] - w2[i]) <= DW_TOL * np.linalg.norm(w2[i] - host["W"][i])
+
+
+def test_small_transpose_bitwise():
+    x = torch.randn((3, 40, 700), generator=torch.Generator().manual_seed(4)).cuda()
+    o1 = torch.empty_like(x)
+    o2 = torch.empty((3, 700, 40), device="cuda")
+    binding.muon_ns_batched_ex(x, binding.make_config(), o1)
+    binding.muon_ns_batched_ex(x.transpose(1, 2).contiguous(), binding.make_config(), o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.transpose(1, 2), o2)
+
+
+def test_small_steps_zero_and_table():
+    x = torch.randn((2, 20, 500), generator=torch.Generator().manual_seed(8))
+    X = x.cuda()
+    for steps, table in ((0, None), (3, [(3.0, -3.2, 1.2), (2.5, -2.0, 0.6), (1.9, -1.2, 0.3)])):
+        out = torch.empty_like(X)
+        binding.muon_ns_batched_ex(X, binding.make_config(steps=steps, coeffs=table), out)
+        torch.cuda.synchronize()
+        ref = R.ns_batched_ref(_np(x), steps=steps, coeffs=table)
+        tol = 5e-3 if steps == 0 else NS_TOL
+        for i in range(2):
+            assert _rel(_np(out)[i], ref[i]) <= tol
+
+
+def test_small_and_large_groups_in_one_call():
+    groups = [
+        synth.random_group((3, 24, 2048), torch.bfloat16, torch.float32, "cuda", 41, 1e-3),
+        synth.random_group((2, 300, 700), torch.bfloat16, torch.float32, "cuda", 42, 1e-3),
+        synth.random_group((2, 2048, 24), torch.float32, torch.float32, "cuda", 43, 1.0),
+    ]
+    host = [{k: _np(g[k]) for k in ("W", "G", "Mom")} for g in groups]
+    binding.muon_step_grouped(groups)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    for g, h in zip(groups, host):
+        w2, m2, _ = R.muon_step_ref(h["W"], h["G"], h["Mom"])
+        w = _np(g["W"])
+        for i in range(w.shape[0]):
+            assert np.linalg.norm(w[i] - w2[i]) <= DW_TOL * np.linalg.norm(w2[i] - h["W"][i])
