@@ -249,6 +249,8 @@ def main():
     ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end pass (large workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -291,6 +293,17 @@ def main():
         raise SystemExit(f"device status {binding.muon_status_string(st)} after warm-up")
     launches_per_step = binding.muon_last_launch_count()
 
+    line = _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,
+                  launches_per_step)
+    _finish(line, world, rank)
+
+
+def _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,
+           launches_per_step):
+    import torch
+    from newton_schulz_gb300 import binding
+    if world > 1:
+        import torch.distributed as dist
     # ---- device-resident timed region ------------------------------------------------
     sampler = ClockSampler(local)
     if world > 1:
@@ -318,6 +331,19 @@ def main():
         t_ms = float(t.item())
 
     # ---- end to end: pinned host inputs in, results out, through the C ABI ------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = _end_to_end(args, groups, step, stream, flush, world, dev)
+
+    st = binding.muon_query_status()
+    if st != 0:
+        raise SystemExit(f"device status {binding.muon_status_string(st)} after timing")
+    return _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
+                   launches_per_step)
+
+
+def _end_to_end(args, groups, step, stream, flush, world, dev):
+    import torch
     host_in = [{k: g[k].to("cpu").pin_memory() for k in ("W", "G", "Mom")} for g in groups]
     host_out = [{k: torch.empty_like(h[k]).pin_memory() for k in ("W", "Mom")} for h in host_in]
     h2d = sum(h[k].numel() * h[k].element_size() for h in host_in for k in h)
@@ -340,14 +366,16 @@ def main():
             e2e_ms.append(a.elapsed_time(b))
     e2e_t = statistics.median(e2e_ms)
     if world > 1:
+        import torch.distributed as dist
         t = torch.tensor([e2e_t], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_t = float(t.item())
+    return {"ms": e2e_t, "h2d": h2d, "d2h": d2h}
 
-    st = binding.muon_query_status()
-    if st != 0:
-        raise SystemExit(f"device status {binding.muon_status_string(st)} after timing")
 
+def _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
+            launches_per_step):
+    from newton_schulz_gb300 import synth
     # ---- roofline of the dominant kernel ------------------------------------------------
     peaks = _peaks()
     kinds = {k: (ms / max(1, n), n) for k, (ms, n) in prof.items() if n}
@@ -370,6 +398,16 @@ def main():
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
                 "kernel": dom, "peak_source": peaks["source"]}
 
+    per_kind = {}
+    for k, (avg, n) in kinds.items():
+        lk = n / args.steps
+        if k in byt:
+            a = byt[k] / lk / (avg * 1e-3) / 1e9
+            per_kind[k] = {"avg_ms": avg, "GB/s": round(a, 1), "frac": round(a / peaks["hbm_gbs"], 4)}
+        else:
+            a = fl[k] / lk / (avg * 1e-3) / 1e12
+            per_kind[k] = {"avg_ms": avg, "TFLOP/s": round(a, 1),
+                           "frac": round(a / peaks["bf16_tflops"], 4)}
     value = world * flops / (t_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -380,19 +418,27 @@ def main():
                    "matrices": sum(s[0] for s in shapes), "nominal_gflop_per_step": flops / 1e9,
                    "l2": "512 MiB L2 flush between timed steps (outside events)",
                    "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
-        "e2e": {"value": world * flops / (e2e_t * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_t, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e is None else {
+            "value": world * flops / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": e2e["ms"], "h2d_bytes_per_step": e2e["h2d"],
+            "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
         "kernel_ms_per_step": {k: round(v, 5) for k, v in per_step_ms.items()},
         "roofline": roof,
+        "kernels": per_kind,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(args.config)
+    return line
+
+
+def _finish(line, world, rank):
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
 

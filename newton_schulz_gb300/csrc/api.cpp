@@ -149,13 +149,12 @@ void layout_chunk(ChunkP& ch, int sms) {
     off = align_up(off + std::max<size_t>(bytes, 16), 1024);
     return o;
   };
-  const int bm = gemm_block_m(), bk = gemm_block_k();
+  const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
   size_t ctr = 0;
   for (auto& g : ch.groups) {
     g.m_pad = rup(g.m, 8);
     g.n_pad = rup(g.n, 8);
-    const int64_t nt = cdiv(g.m, bm);
-    g.tri = nt * (nt + 1) / 2;
+    g.tri = gemm_sym_tiles(static_cast<int>(g.m));
     g.num_kb_gram = static_cast<int>(cdiv(g.n, bk));
     // split-K for the Gram when the symmetric tiles alone cannot fill the GPU
     const int64_t tiles = g.cnt * g.tri;
@@ -176,7 +175,7 @@ void layout_chunk(ChunkP& ch, int sms) {
     g.off_B = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
     g.off_inv = take(static_cast<size_t>(g.cnt) * 4);
     g.off_ssq = take(static_cast<size_t>(g.cnt * g.prep_tiles) * 4);
-    g.off_part = take(g.ksplit > 1 ? static_cast<size_t>(g.cnt * g.tri * g.ksplit) * bm * bm * 4
+    g.off_part = take(g.ksplit > 1 ? static_cast<size_t>(g.cnt * g.tri * g.ksplit) * bm * bn * 4
                                    : 16);
     g.ctr_prep = ctr;
     ctr += static_cast<size_t>(g.cnt);
@@ -575,15 +574,18 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       if (st != MUON_OK) return st;
     }
     // ---- tensor maps -------------------------------------------------------------
+    // operand P tiles are 128 rows (box bm), operand Q tiles 256 rows (box bn)
     struct Maps {
-      CUtensorMap X, A, B, Xt[2];
+      CUtensorMap Xp, Xq, Ap, Aq, B, Xt[2];
     };
     std::vector<Maps> maps(ch.groups.size());
     for (size_t k = 0; k < ch.groups.size(); ++k) {
       const NsGroupP& g = ch.groups[k];
       const int bm = gemm_block_m(), bn = gemm_block_n();
-      bool ok = make_map(&maps[k].X, ws + g.off_X, g.n, g.m, g.cnt, g.n_pad, g.m * g.n_pad, bm) &&
-                make_map(&maps[k].A, ws + g.off_A, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bm) &&
+      bool ok = make_map(&maps[k].Xp, ws + g.off_X, g.n, g.m, g.cnt, g.n_pad, g.m * g.n_pad, bm) &&
+                make_map(&maps[k].Xq, ws + g.off_X, g.n, g.m, g.cnt, g.n_pad, g.m * g.n_pad, bn) &&
+                make_map(&maps[k].Ap, ws + g.off_A, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bm) &&
+                make_map(&maps[k].Aq, ws + g.off_A, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bn) &&
                 make_map(&maps[k].B, ws + g.off_B, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bn) &&
                 make_map(&maps[k].Xt[0], ws + g.off_Xt0, g.m, g.n, g.cnt, g.m_pad, g.n * g.m_pad,
                          bm) &&
@@ -602,7 +604,6 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         for (size_t k = 0; k < ch.groups.size(); ++k) {
           const NsGroupP& g = ch.groups[k];
           GemmGroup& G = gp.g[k];
-          const int64_t nt = cdiv(g.m, bm);
           auto* Xb = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X);
           auto* Ab = reinterpret_cast<__nv_bfloat16*>(ws + g.off_A);
           auto* Bb = reinterpret_cast<__nv_bfloat16*>(ws + g.off_B);
@@ -614,28 +615,30 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           G.inv = reinterpret_cast<const float*>(ws + g.off_inv);
           G.tile_base = static_cast<int>(tiles);
           if (phase == kEpiGram) {
-            G.mapA = maps[k].X;
-            G.mapB = maps[k].X;
+            G.mapA = maps[k].Xp;
+            G.mapB = maps[k].Xq;
             G.out0 = Ab;
             G.pitch0 = g.m_pad;
             G.mstride0 = g.m * g.m_pad;
             G.partial = reinterpret_cast<float*>(ws + g.off_part);
             G.tile_cnt = ctr + g.ctr_tile;
-            G.nt = static_cast<int>(nt);
+            G.nt = static_cast<int>(cdiv(g.m, bn));
+            G.mt = static_cast<int>(cdiv(g.m, bm));
             G.ksplit = g.ksplit;
             G.kb_per_split = g.kb_per_split;
             G.num_kb = g.num_kb_gram;
             G.tiles_per_mat = static_cast<int>(g.tri * g.ksplit);
           } else if (phase == kEpiPoly) {
-            G.mapA = maps[k].A;
-            G.mapB = maps[k].A;
+            G.mapA = maps[k].Ap;
+            G.mapB = maps[k].Aq;
             G.epi_in = Ab;
             G.pitch_in = g.m_pad;
             G.mstride_in = g.m * g.m_pad;
             G.out0 = Bb;
             G.pitch0 = g.m_pad;
             G.mstride0 = g.m * g.m_pad;
-            G.nt = static_cast<int>(nt);
+            G.nt = static_cast<int>(cdiv(g.m, bn));
+            G.mt = static_cast<int>(cdiv(g.m, bm));
             G.ksplit = 1;
             G.num_kb = static_cast<int>(cdiv(g.m, bk));
             G.kb_per_split = G.num_kb;

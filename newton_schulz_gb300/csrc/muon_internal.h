@@ -93,8 +93,8 @@ struct alignas(128) GemmGroup {
   int count;
   int tiles_per_mat;
   int tile_base;
-  int nt;          // symmetric: tiles per side; apply: tiles along m (N dim)
-  int mt;          // apply: tiles along n (M dim)
+  int nt;          // apply: tiles along m (N dim); symmetric: column tiles
+  int mt;          // apply: tiles along n (M dim); symmetric: row tiles
   int ksplit, kb_per_split, num_kb;
 };
 
@@ -155,6 +155,7 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s);
 int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage
+int gemm_sym_tiles(int m);   // tiles of a symmetric m x m product (holding some col >= row)
 cudaError_t launch_small(const SmallParams& p, int total_mats, cudaStream_t s);
 int small_max_active_clusters(int cs, int smem_bytes);   // 0 when the query fails
 

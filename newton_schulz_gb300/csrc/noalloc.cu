@@ -116,7 +116,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   const int64_t m = trans ? N : M, n = trans ? M : N;
   const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
   const int64_t m_pad = cdiv(m, 8) * 8, n_pad = cdiv(n, 8) * 8;
-  const int64_t nt = cdiv(m, bm), tri = nt * (nt + 1) / 2;
+  const int64_t tri = gemm_sym_tiles(static_cast<int>(m));
   const int num_kb = static_cast<int>(cdiv(n, bk));
   const int64_t prep_tiles = cdiv(m, kPrepTile) * cdiv(n, kPrepTile);
 
@@ -152,7 +152,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   }
   const int kb_per_split = static_cast<int>(cdiv(num_kb, ks));
   const int ksplit = static_cast<int>(cdiv(num_kb, kb_per_split));
-  const size_t o_part = take(ksplit > 1 ? static_cast<size_t>(B * tri * ksplit) * bm * bm * 4 : 16);
+  const size_t o_part = take(ksplit > 1 ? static_cast<size_t>(B * tri * ksplit) * bm * bn * 4 : 16);
   if (off > kScratchBytes) return MUON_ERR_UNSUPPORTED;   // beyond the fixed scratch size
   const int64_t prep_blocks = B * cdiv(M, kPrepTile) * cdiv(N, kPrepTile);
   const int64_t fin_blocks = B * cdiv(M, kFinRows) * cdiv(N, kFinCols);
@@ -171,9 +171,11 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   // The array keeps the previous call's contents: clear status and counters.
   if (cudaMemsetAsync(base, 0, zero_bytes, stream) != cudaSuccess) return MUON_ERR_CUDA;
 
-  CUtensorMap mX, mA, mB, mXt[2];
+  CUtensorMap mX, mXq, mA, mAq, mB, mXt[2];
   if (!make_map(&mX, Xb, n, m, B, n_pad, m * n_pad, bm) ||
+      !make_map(&mXq, Xb, n, m, B, n_pad, m * n_pad, bn) ||
       !make_map(&mA, Ab, m, m, B, m_pad, m * m_pad, bm) ||
+      !make_map(&mAq, Ab, m, m, B, m_pad, m * m_pad, bn) ||
       !make_map(&mB, Bb, m, m, B, m_pad, m * m_pad, bn) ||
       !make_map(&mXt[0], Xt[0], m, n, B, m_pad, n * m_pad, bm) ||
       !make_map(&mXt[1], Xt[1], m, n, B, m_pad, n * m_pad, bm))
@@ -229,27 +231,29 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
       G.tile_base = 0;
       if (phase == kEpiGram) {
         G.mapA = mX;
-        G.mapB = mX;
+        G.mapB = mXq;
         G.out0 = Ab;
         G.pitch0 = m_pad;
         G.mstride0 = m * m_pad;
         G.partial = reinterpret_cast<float*>(base + o_part);
         G.tile_cnt = tcnt;
-        G.nt = static_cast<int>(nt);
+        G.nt = static_cast<int>(cdiv(m, bn));
+        G.mt = static_cast<int>(cdiv(m, bm));
         G.ksplit = ksplit;
         G.kb_per_split = kb_per_split;
         G.num_kb = num_kb;
         G.tiles_per_mat = static_cast<int>(tri * ksplit);
       } else if (phase == kEpiPoly) {
         G.mapA = mA;
-        G.mapB = mA;
+        G.mapB = mAq;
         G.epi_in = Ab;
         G.pitch_in = m_pad;
         G.mstride_in = m * m_pad;
         G.out0 = Bb;
         G.pitch0 = m_pad;
         G.mstride0 = m * m_pad;
-        G.nt = static_cast<int>(nt);
+        G.nt = static_cast<int>(cdiv(m, bn));
+        G.mt = static_cast<int>(cdiv(m, bm));
         G.ksplit = 1;
         G.num_kb = static_cast<int>(cdiv(m, bk));
         G.kb_per_split = G.num_kb;
