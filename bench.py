@@ -251,6 +251,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end pass (large workloads)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="c4 only: number of Llama layers (default 32; a small profiling case)")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="c5 only: divide every dimension (a small profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -275,7 +279,12 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     binding.load()
 
-    groups = synth.CONFIGS[args.config](dev)
+    if args.config == "c4" and args.layers:
+        groups = synth.config_c4(dev, layers=args.layers)
+    elif args.config == "c5" and args.scale_down > 1:
+        groups = synth.config_c5(dev, scale_down=args.scale_down)
+    else:
+        groups = synth.CONFIGS[args.config](dev)
     shapes = _shapes(groups)
     flops = nominal_flops(shapes)
     stream = torch.cuda.current_stream()
@@ -414,7 +423,10 @@ def _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": synth.WORKLOAD_NAMES[args.config], "config": args.config,
+        "config": {"workload": synth.WORKLOAD_NAMES[args.config] + (
+                       f" [{args.layers} layers]" if args.config == "c4" and args.layers else "") + (
+                       f" [dims / {args.scale_down}]" if args.config == "c5" and args.scale_down > 1
+                       else ""), "config": args.config,
                    "matrices": sum(s[0] for s in shapes), "nominal_gflop_per_step": flops / 1e9,
                    "l2": "512 MiB L2 flush between timed steps (outside events)",
                    "parallelism": f"replica x{world}" if world > 1 else "single GPU"},

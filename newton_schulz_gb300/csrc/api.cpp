@@ -151,19 +151,24 @@ void layout_chunk(ChunkP& ch, int sms) {
   };
   const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
   size_t ctr = 0;
+  // split-K for the Gram only when the launch's symmetric tiles (all groups
+  // together) cannot fill the GPU
+  int64_t launch_tiles = 0;
+  for (auto& g : ch.groups) launch_tiles += g.cnt * gemm_sym_tiles(static_cast<int>(g.m));
   for (auto& g : ch.groups) {
     g.m_pad = rup(g.m, 8);
     g.n_pad = rup(g.n, 8);
     g.tri = gemm_sym_tiles(static_cast<int>(g.m));
     g.num_kb_gram = static_cast<int>(cdiv(g.n, bk));
-    // split-K for the Gram when the symmetric tiles alone cannot fill the GPU
-    const int64_t tiles = g.cnt * g.tri;
+    const int64_t tiles = launch_tiles;
     const int64_t target = 2LL * sms;
     int ks = 1;
     if (tiles < target && g.num_kb_gram >= 8) {
-      ks = static_cast<int>(std::min<int64_t>(cdiv(target, tiles), g.num_kb_gram / 4));
+      ks = static_cast<int>(std::min<int64_t>(cdiv(target, std::max<int64_t>(tiles, 1)),
+                                               g.num_kb_gram / 4));
       ks = std::max(ks, 1);
     }
+    ks = std::min<int>(ks, static_cast<int>(env_size("MUON_MAX_KSPLIT", 64)));
     g.kb_per_split = static_cast<int>(cdiv(g.num_kb_gram, ks));
     g.ksplit = static_cast<int>(cdiv(g.num_kb_gram, g.kb_per_split));
     g.prep_tiles = cdiv(g.m, kPrepTile) * cdiv(g.n, kPrepTile);

@@ -395,13 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (gc0 + 31 < gr0) continue;                        // block entirely below the diagonal
           float v[32];
           if (split) {
+            // sum the splits in order; the 32 columns of a split are loaded together
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float a = 0.f;
-              if (gr < G.m && gc0 + j < G.m)
-                for (int q = 0; q < G.ksplit; ++q)
-                  a += __ldcg(part + (int64_t)q * (BM * BN) + (c0 + j) * BM + row);
-              v[j] = a;
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            if (gr < G.m) {
+              for (int q = 0; q < G.ksplit; ++q) {
+                const float* pq = part + (int64_t)q * (BM * BN) + c0 * BM + row;
+                float l[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) l[j] = gc0 + j < G.m ? __ldcg(pq + j * BM) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += l[j];
+              }
             }
           } else {
             uint32_t r[32];
