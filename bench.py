@@ -47,6 +47,29 @@ def _peaks():
                 "source": "fallback"}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of the dominant kernel (summaries in profiles/), keyed by
+# (kernel kind, workload), valid only while the kernel's sources hash to the
+# recorded value; otherwise the roofline reports traffic = null.
+TRAFFIC = {
+    ("fused_small", "c2"): {"bytes": 181.974016e6 + 85.388544e6, "src_hash": "d20e0c19e05ce08e",
+                            "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h"),
+                            "profile": "profiles/ns_small_c2_74x24x10240.md"},
+}
+
+
+def _traffic(kind, config):
+    import hashlib
+    rec = TRAFFIC.get((kind, config))
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, "newton_schulz_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["src_hash"] else None
+
+
 def _shapes(groups):
     out = []
     for g in groups:
@@ -398,13 +421,14 @@ def _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
         per_launch = byt[dom] / launches_kind
         achieved = per_launch / (avg_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                "kernel": dom, "peak_source": peaks["source"]}
+                "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(dom, args.config),
+                "algorithmic_bytes": per_launch, "kernel": dom, "peak_source": peaks["source"]}
     else:
         per_launch = fl[dom] / launches_kind
         achieved = per_launch / (avg_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": _traffic(dom, args.config), "algorithmic_flops": per_launch,
                 "kernel": dom, "peak_source": peaks["source"]}
 
     per_kind = {}
