@@ -60,6 +60,11 @@ struct Workspace {
   unsigned* ctr = nullptr;
   size_t ctr_bytes = 0;
   bool dirty = false;  // a kernel gave up mid-way: counters must be re-zeroed
+  // small-m path: per-matrix arrival counters and ready flags, tagged with a
+  // launch epoch (never reset; a fresh allocation is zero = no epoch)
+  unsigned long long* ep = nullptr;
+  size_t ep_cap = 0;   // matrices
+  unsigned epoch = 0;
 };
 
 struct DevState {
@@ -191,46 +196,68 @@ void layout_chunk(ChunkP& ch, int sms) {
   ch.ctrs = ctr;
 }
 
-// Shared-memory carve-up of the fused small-m kernel for cluster size cs.
-void small_layout(int64_t m, int64_t n, int cs, SmallParams* sp) {
-  sp->cs = cs;
-  sp->w = static_cast<int>(rup(cdiv(n, cs), 128));
-  sp->mr = static_cast<int>(rup(m, 8));
-  sp->nmm = static_cast<int>(rup(m, 16));
-  const size_t xbytes = static_cast<size_t>(sp->w / 64) * sp->mr * 128;
-  sp->off_bt = static_cast<int>(align_up(xbytes, 1024));
-  sp->off_part = sp->off_bt + 2 * kSmallBTile;
-  sp->off_a = sp->off_part + static_cast<int>(align_up(2 * m * m * 4, 16));
-  sp->off_misc = sp->off_a + static_cast<int>(align_up(m * (m + 1) * 4, 16));
-  // at least 80 KB: at most two CTAs per SM, so two TMEM allocations always fit
-  sp->smem_bytes = std::max(sp->off_misc + 128 + 1024, 80 * 1024);
-}
-
-// Cluster size of the fused small-m kernel for a core shape (m, n), or false
-// when the shape goes to the grouped GEMM path.  The largest cluster (up to
-// 8) that keeps every CTA busy wins: more CTAs per matrix shorten each
-// CTA's share of the streaming and of the products.  (Measured on the
-// 74 x [24,10240] workload: 8 CTAs 0.27 ms, 4 CTAs 0.40 ms per step; the
-// occupancy query under-counts the clusters of 8 that actually co-reside.)
-// MUON_SMALL_CS forces a size when it fits.
-bool small_shape(int64_t m, int64_t n, int* cs_out) {
+// Small-m path eligibility: core shapes with m <= 64 (MUON_SMALL_PATH=0 sends
+// every shape to the grouped GEMM path).
+bool small_shape(int64_t m) {
   const char* env = std::getenv("MUON_SMALL_PATH");
   if (env && env[0] == '0') return false;
-  if (m > kSmallMaxM) return false;
-  const int forced = static_cast<int>(env_size("MUON_SMALL_CS", 0));
-  int best = 0;
-  for (int cs = 1; cs <= kSmallMaxCluster; cs *= 2) {
-    if (forced && cs != forced) continue;
-    SmallParams sp;
-    small_layout(m, n, cs, &sp);
-    if (static_cast<int64_t>(sp.w / 64) * sp.mr * 128 > kSmallMaxXBytes) continue;
-    if (sp.smem_bytes > 227 * 1024) continue;
-    if (cs > 1 && static_cast<int64_t>(cs - 1) * sp.w >= n) continue;   // an idle CTA
-    best = cs;
+  return m <= kSmallMaxM;
+}
+
+// Work items and shared-memory carve-up of the small-m kernel for core shape
+// (m, n) over `mats` matrices; false when no carve-up fits one SM.  Shared
+// memory holds two X0 tiles of wb columns, two Q images, a ring of 24 KB
+// stages and the Gram-space matrices.  wb is the largest multiple of 128 that
+// fits (deeper rings first) such that four W rows fit one stage and the
+// item's O fits one 256-column TMEM buffer; then it shrinks while the launch
+// would leave SMs without an item.
+bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
+  sp->m = static_cast<int>(m);
+  sp->n = static_cast<int>(n);
+  sp->mr = static_cast<int>(rup(m, 8));
+  sp->mp = static_cast<int>(rup(m, 4));
+  sp->nmm = static_cast<int>(rup(m, 16));
+  sp->sc = 0;
+  sp->qbytes = 2 * sp->nmm * 128;
+  sp->pstride = static_cast<int>(rup(m * m, 4));
+  sp->stage_bytes = kSmallStageBytes;
+  const int tcol = static_cast<int>(rup(sp->nmm, 32));
+  const int64_t wcap = std::min<int64_t>(kSmallStageBytes / 16, 128 * (256 / tcol));
+  const size_t gs = align_up(static_cast<size_t>(4) * sp->mp * sp->mp * 4 + 64, 16);
+  const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns
+  int64_t wmax = 0;
+  for (int st = kSmallMaxStages; st >= 2 && wmax == 0; --st) {
+    const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) +
+                         static_cast<size_t>(st) * sp->stage_bytes + gs + 256 + 1024;
+    if (fixed >= static_cast<size_t>(kSmallSmemLimit)) continue;
+    const int64_t chunks = static_cast<int64_t>((kSmallSmemLimit - fixed) / 2 / chunk) / 2 * 2;
+    if (chunks >= 2) {
+      wmax = std::min<int64_t>(chunks * 64, wcap);
+      sp->stages = st;
+    }
   }
-  if (!best) return false;
-  *cs_out = best;
-  return true;
+  if (wmax == 0) return false;
+  int64_t wb = std::min<int64_t>(wmax, rup(n, 128));
+  wb = rup(cdiv(n, cdiv(n, wb)), 128);
+  while (wb > 128 && mats * cdiv(n, wb) < static_cast<int64_t>(sms)) wb -= 128;
+  sp->wb = static_cast<int>(wb);
+  sp->nb = static_cast<int>(cdiv(n, wb));
+  sp->total_mats = static_cast<int>(mats);
+  sp->items = static_cast<int>(mats * sp->nb);
+  sp->xbytes = static_cast<int>((wb / 64) * chunk);
+  sp->off_q = 2 * sp->xbytes;
+  sp->off_ring = sp->off_q + 2 * sp->qbytes;
+  sp->off_gs = sp->off_ring + sp->stages * sp->stage_bytes;
+  sp->off_bar = static_cast<int>(align_up(sp->off_gs + gs, 16));
+  sp->smem_bytes = sp->off_bar + 256 + 1024;
+  return sp->smem_bytes <= kSmallSmemLimit;
+}
+
+// Workspace bytes of one small-m launch: X0 images, partial Grams, Q images.
+size_t small_ws_bytes(const SmallParams& sp) {
+  return align_up(static_cast<size_t>(sp.items) * sp.xbytes, 256) +
+         align_up(static_cast<size_t>(sp.items) * sp.pstride * 4, 256) +
+         static_cast<size_t>(sp.total_mats) * sp.qbytes;
 }
 
 std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms) {
@@ -336,6 +363,37 @@ muon_status_t get_workspace(cudaStream_t stream, size_t bytes, size_t ctrs, char
   }
   *out = static_cast<char*>(w.ptr);
   *ctr_out = w.ctr;
+  return MUON_OK;
+}
+
+// Epoch-tagged counters of the small-m path for `mats` matrices: arrive
+// (64-bit) then ready (32-bit); returns the next epoch (never 0).
+muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned long long** arrive,
+                             unsigned** ready, unsigned* epoch) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  Workspace& w = g_ws[{dev, stream}];
+  mats = std::max<size_t>(mats, 1);
+  if (w.ep_cap < mats) {
+    if (w.ep) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+      cudaFree(w.ep);
+    }
+    w.ep = nullptr;
+    w.ep_cap = 0;
+    const size_t cap = align_up(mats, 1024);
+    if (cudaMalloc(&w.ep, cap * 12) != cudaSuccess) {
+      cudaGetLastError();
+      w.ep = nullptr;
+      return MUON_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemsetAsync(w.ep, 0, cap * 12, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    w.ep_cap = cap;
+  }
+  if (++w.epoch == 0) w.epoch = 1;
+  *arrive = w.ep;
+  *ready = reinterpret_cast<unsigned*>(w.ep + w.ep_cap);
+  *epoch = w.epoch;
   return MUON_OK;
 }
 
@@ -447,8 +505,9 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       static_cast<unsigned long long>(env_size("MUON_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
   Launcher L0{stream};
 
-  // ---- small core shapes: one fused cluster kernel per core shape -------------------
+  // ---- small core shapes: one Gram-space kernel launch per core shape ---------------
   std::vector<Req> large;
+  std::vector<SmallParams> smalls;
   {
     std::map<std::pair<int64_t, int64_t>, std::vector<int>> shapes;
     for (int i = 0; i < static_cast<int>(reqs.size()); ++i) {
@@ -458,13 +517,13 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     }
     for (auto& kv : shapes) {
       const int64_t m = kv.first.first, n = kv.first.second;
-      int cs = 0;
-      if (!small_shape(m, n, &cs)) {
+      if (!small_shape(m)) {
         for (int i : kv.second) large.push_back(reqs[i]);
         continue;
       }
       for (size_t b = 0; b < kv.second.size(); b += kMaxSlices) {
-        SmallParams sp;
+        smalls.emplace_back();
+        SmallParams& sp = smalls.back();
         std::memset(&sp, 0, sizeof(sp));
         int64_t mats = 0;
         const size_t e = std::min(kv.second.size(), b + kMaxSlices);
@@ -479,25 +538,24 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           ss.trans = q.trans ? 1 : 0;
           ss.g_dtype = q.g_dtype;
           ss.w_dtype = q.w_dtype;
+          // bulk copies move whole stored rows: every row start and length
+          // must be a multiple of 16 bytes
           const int64_t inner = q.c;   // contiguous extent of a stored row
-          ss.gvec = (q.g_dtype == MUON_F32 ? inner % 4 == 0 : inner % 8 == 0) &&
-                    aligned(q.G, 16) && inner % 4 == 0 && (!step_mode || aligned(q.Mom, 16));
-          ss.wvec = (q.w_dtype == MUON_F32 ? inner % 4 == 0 : inner % 8 == 0) && aligned(q.W, 16);
+          ss.gbulk = (inner * static_cast<int64_t>(esize(q.g_dtype))) % 16 == 0 &&
+                     aligned(q.G, 16) &&
+                     (!step_mode || ((inner * 4) % 16 == 0 && aligned(q.Mom, 16)));
+          ss.wbulk = (inner * static_cast<int64_t>(esize(q.w_dtype))) % 16 == 0 && aligned(q.W, 16);
           ss.scale = scale_value(q.r, q.c, scale_rule);
           mats += q.B;
         }
-        if (mats * cs >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+        if (mats * cdiv(n, 128) >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         sp.n_slices = static_cast<int>(e - b);
-        sp.m = static_cast<int>(m);
-        sp.n = static_cast<int>(n);
-        small_layout(m, n, cs, &sp);
+        if (!small_plan(m, n, mats, dev->sms, &sp)) return MUON_ERR_UNSUPPORTED;
         sp.steps = ns.steps;
         for (int it = 0; it < ns.steps; ++it) {
-          const float ca = ns.coeffs[3 * it], alpha = kShiftFrac * ca;
-          sp.coef[it][0] = ca - alpha;
+          sp.coef[it][0] = ns.coeffs[3 * it];
           sp.coef[it][1] = ns.coeffs[3 * it + 1];
           sp.coef[it][2] = ns.coeffs[3 * it + 2];
-          sp.coef[it][3] = alpha;
         }
         sp.step_mode = step_mode ? 1 : 0;
         sp.nesterov = nesterov ? 1 : 0;
@@ -507,25 +565,47 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         sp.eps = ns.eps;
         sp.status = dev->status;
         sp.timeout_ns = timeout_ns0;
-        st = L0.run(5, [&] { return launch_small(sp, static_cast<int>(mats), stream); });
-        if (st != MUON_OK) return st;
       }
     }
   }
   std::vector<ChunkP> plan = make_plan(large, dev->sms);
-  if (plan.empty()) {
-    t_last_launches = L0.count;
-    return MUON_OK;
+  size_t need = 0, need_ctr = 0, max_mats = 0;
+  for (const SmallParams& sp : smalls) {
+    need = std::max(need, small_ws_bytes(sp));
+    max_mats = std::max(max_mats, static_cast<size_t>(sp.total_mats));
   }
-  size_t need = 0, need_ctr = 0;
   for (auto& ch : plan) {
     need = std::max(need, ch.bytes);
     need_ctr = std::max(need_ctr, ch.ctrs);
+  }
+  if (smalls.empty() && plan.empty()) {
+    t_last_launches = 0;
+    return MUON_OK;
   }
   char* ws = nullptr;
   unsigned* ctr = nullptr;
   st = get_workspace(stream, need, need_ctr, &ws, &ctr);
   if (st != MUON_OK) return st;
+  for (SmallParams& sp : smalls) {
+    // the launches run in stream order, so each reuses the same workspace
+    char* w = ws;
+    sp.ximg = reinterpret_cast<uint8_t*>(w);
+    w += align_up(static_cast<size_t>(sp.items) * sp.xbytes, 256);
+    sp.part = reinterpret_cast<float*>(w);
+    w += align_up(static_cast<size_t>(sp.items) * sp.pstride * 4, 256);
+    sp.qimg = reinterpret_cast<uint8_t*>(w);
+    st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready, &sp.epoch);
+    if (st != MUON_OK) return st;
+    // one CTA per SM (all resident: the launch is cooperative)
+    if (small_blocks_per_sm(sp.smem_bytes) <= 0) return MUON_ERR_CUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(sp.items, dev->sms));
+    st = L0.run(5, [&] { return launch_small(sp, grid, stream); });
+    if (st != MUON_OK) return st;
+  }
+  if (plan.empty()) {
+    t_last_launches = L0.count;
+    return MUON_OK;
+  }
   const unsigned long long timeout_ns =
       static_cast<unsigned long long>(env_size("MUON_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
 

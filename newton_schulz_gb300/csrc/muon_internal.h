@@ -109,14 +109,14 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-// ---- fused small-m path (one thread-block cluster per matrix) ---------------
+// ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
-constexpr int kSmallMaxXBytes = 176 * 1024; // X columns held per CTA (bf16, swizzled)
-constexpr int kSmallMaxCluster = 8;        // portable cluster sizes 1..8
-constexpr int kSmallUnroll = 4;            // streaming items in flight per thread
-constexpr int kSmallThreads = 256;
-constexpr int kSmallTmemCols = 256;
-constexpr int kSmallBTile = 8192;          // one B' operand tile: 64 rows x 128 bytes
+constexpr int kSmallThreads = 320;         // warp 0 producer, warp 1 MMA, warps 2..9 consumers
+constexpr int kSmallCons = 256;            // consumer threads
+constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O buffers [0,256), [256,512)
+constexpr int kSmallMaxStages = 4;
+constexpr int kSmallStageBytes = 24 * 1024;
+constexpr int kSmallSmemLimit = 227 * 1024;
 
 struct SmallSlice {
   const void* G;     // step: gradient; NS only: the input
@@ -126,7 +126,8 @@ struct SmallSlice {
   int mat_base;      // index of its first matrix within the launch
   int trans;         // stored rows > cols
   int g_dtype, w_dtype;
-  int gvec, wvec;    // 16-byte vector paths legal for G/Mom and W
+  int gbulk;         // G (and Mom) rows may be moved by 16-byte bulk copies
+  int wbulk;         // W rows may be moved by 16-byte bulk copies
   float scale;       // update scale s(rows, cols)
 };
 
@@ -134,17 +135,32 @@ struct SmallParams {
   SmallSlice s[kMaxSlices];
   int n_slices;
   int m, n;          // core shape, m <= n
-  int cs;            // CTAs per matrix (cluster size)
-  int w;             // X columns per CTA (multiple of 128)
   int mr;            // X rows held: m rounded up to 8
+  int mp;            // leading dimension of the m x m fp32 matrices: m rounded up to 4
   int nmm;           // MMA N (and apply K): m rounded up to 16
+  int wb;            // X columns per work item (multiple of 128)
+  int nb;            // work items per matrix
+  int sc;            // transposed layout: X columns per ring stage (multiple of 64)
+  int stages;        // ring stages
+  int total_mats;
+  int items;         // total_mats * nb
+  int xbytes;        // one item's X0 image: (wb / 64) * mr * 128
+  int qbytes;        // one Q image: hi and lo, nmm rows x 128 bytes each
+  int pstride;       // floats per partial Gram (m * m rounded up to 4)
   int steps;
-  float coef[kMaxSteps][4];   // per step: a - alpha, b, c, alpha
+  float coef[kMaxSteps][3];
   int step_mode, nesterov;
   float mu, lr, wd, eps;
+  uint8_t* ximg;                // [items][xbytes] bf16 X0 images (shared-memory layout)
+  float* part;                  // [items][pstride] partial Gram matrices
+  uint8_t* qimg;                // [total_mats][qbytes] Q = hi + lo operand images
+  unsigned long long* arrive;   // [total_mats] (epoch << 32) | items arrived
+  unsigned* ready;              // [total_mats] epoch once Q is written
+  unsigned epoch;               // this launch's tag, never 0
   unsigned* status;
   unsigned long long timeout_ns;
-  int off_bt, off_part, off_a, off_misc;   // shared-memory carve-up (bytes)
+  // shared-memory carve-up (bytes from the 1024-aligned base)
+  int off_q, off_ring, stage_bytes, off_gs, off_bar;
   int smem_bytes;
 };
 
@@ -156,7 +172,7 @@ int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage
 int gemm_sym_tiles(int m);   // tiles of a symmetric m x m product (holding some col >= row)
-cudaError_t launch_small(const SmallParams& p, int total_mats, cudaStream_t s);
-int small_max_active_clusters(int cs, int smem_bytes);   // 0 when the query fails
+cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s);
+int small_blocks_per_sm(int smem_bytes);   // resident CTAs per SM, 0 when the query fails
 
 }  // namespace muon

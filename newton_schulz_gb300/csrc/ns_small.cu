@@ -1,30 +1,40 @@
-// Fused Muon step for matrices with a small side (m <= 64 after the
-// transpose-first rule), one thread-block cluster per matrix.
+// Fused Muon step for core shapes with a small side (m <= 64 after the
+// transpose-first rule): Gram-space Newton-Schulz in one persistent launch.
 //
-// HyperParallel-FSDP section 6.6 and RFC issue 204 item 3 fuse many small
-// matrices of one core shape into one batched launch because per-matrix
-// launches starve the device; this kernel goes one step further and runs the
-// whole step of a matrix -- momentum, norm, every Newton-Schulz iteration and
-// the update -- in one launch, with X resident in the distributed shared
-// memory of a cluster of `cs` CTAs (CTA r holds columns [r*w, (r+1)*w) of X).
+// Every NS step left-multiplies X by a polynomial of its Gram matrix, so the
+// iteration can run on the m x m Gram matrix and multiply back into X once at
+// the end; in exact arithmetic this equals the X-space iteration of the Muon
+// page (DMuon-2, Appendix C.3 "Gram Newton-Schulz and Its Fast Kernels"):
+//   R_0 = X0 X0^T / ||X0||_F^2,   P_k = a_k I + b_k R_k + c_k R_k^2,
+//   R_{k+1} = P_k R_k P_k,        Q = P_{K-1} ... P_1 P_0,
+//   O = Q X0 / ||X0||_F.
+// R, P and Q stay fp32 (m <= 64: 17 products of m x m per matrix, on CUDA
+// cores); X0 is bf16 and Q is applied as two bf16 operands Q = hi + lo, so
+// rounding X0 to bf16 is the only bf16 step of the iteration.
 //
-// Shared-memory layout of X (one layout serves both products): chunks of 64
-// columns, each chunk mr rows x 128 bytes with the 128-byte swizzle.
-//   Gram   A = X X^T: K-major view (rows = m, K = columns); M = 128 rows are
-//          issued, rows >= m read neighbouring memory and are ignored.  Each
-//          CTA forms its partial over its columns; the partials are summed in
-//          rank order over DSMEM after a cluster barrier, identically in every
-//          CTA.
-//   Poly   P = a*I + b*A + c*A^2 on CUDA cores (m^3 <= 262144 MACs), in fp32
-//          from the fp32 A, stored as two bf16 K-major MMA operands P = hi + lo
-//          (the apply issues both), so neither A nor P is rounded to bf16 as
-//          a whole; X' = a*X + (b*A + c*A^2)*X = P*X.
-//   Apply  X'^T = X^T P: the A operand is the MN-major view of the same X
-//          chunks (M = 128 columns of X, K = m), P the K-major B operand;
-//          the epilogue only converts and writes X' back in place.
-// Rows >= m of P and its columns >= m are zero, so the K padding of the
-// apply contributes nothing.  The two P tiles (hi at +0, lo at +8 KB) also
-// serve as the landing zone of the Gram's ignored rows past the last chunk.
+// A work item is (matrix, block of wb columns of X).  One cooperative launch,
+// one CTA per SM, every CTA resident; the CTA is warp-specialised:
+//   warp 0      producer: bulk copies (cp.async.bulk) of G/Mom, later W, row
+//               segments into a ring of shared-memory stages, and of the X0
+//               and Q images for the second phase;
+//   warp 1      allocates TMEM and issues the tcgen05 MMAs;
+//   warps 2..9  consumers: momentum, X0 and the epilogues.
+// Phase 1, per item: M' = mu M + G (written back), D = G + mu M' (Nesterov)
+// or M', X0 = bf16(D) into a double-buffered 128-byte-swizzled tile, whose
+// image is stored to the workspace by one bulk copy; the item's partial
+// Gram X0_blk X0_blk^T (fp32, TMEM) is read one item later, so its MMA
+// overlaps the next item's streaming.  The CTA whose item arrives last for a
+// matrix sums the partials in block order, normalises by the trace
+// (= ||X0||_F^2), runs the Gram-space steps and publishes Q.
+// Phase 2, per item: wait for the matrix's Q, bulk-load the X0 image and Q,
+// O = Q X0 on tcgen05 per 128-column tile (A = MN-major view of X0, M = 128
+// columns, K = m; B = Q) into one of several TMEM slots, while W tiles
+// stream through the ring; the consumers write W' = (1 - lr wd) W - lr s O
+// (or O itself) from TMEM.
+// Arrival counters carry a per-launch epoch tag, so a launch never depends on
+// what an earlier (possibly aborted) launch left in them.  Every wait is
+// bounded; a timeout sets a status bit and the CTA's abort flag, after which
+// every role runs to the end without waiting and no output is written.
 #include "muon_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -32,458 +42,994 @@ namespace muon {
 
 namespace {
 
-__device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, unsigned* status,
-                                         unsigned long long timeout_ns) {
+constexpr int kT = kSmallCons;      // consumer threads
+constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Shared-memory control block: mbarriers, the TMEM slot and CTA flags.
+struct SmallBars {
+  uint64_t ring_full[kSmallMaxStages], ring_empty[kSmallMaxStages];
+  uint64_t x_full[2], gram_full[2], xq_full[2], xq_free[2];
+  uint64_t o_full[2], o_empty[2];
+  uint32_t tslot;
+  int last;
+  int abort;
+};
+
+struct Ctx {
+  SmallBars* B;
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+// Bounded mbarrier wait.  False on timeout (which sets the status bit and the
+// CTA's abort flag) or once another role of the CTA has aborted.
+__device__ bool mwait(uint64_t* bar, uint32_t parity, const Ctx& c) {
   const uint32_t addr = ptx::smem_u32(bar);
   if (ptx::mbar_try_wait(addr, parity)) return true;
+  volatile int* ab = &c.B->abort;
+  if (*ab) return false;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(addr, parity)) return true;
-    if ((it & 255u) == 0 && ptx::globaltimer() - t0 > timeout_ns) {
-      atomicOr(status, kDevTimeout);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void load8(const void* base, int dtype, int64_t e, int nvalid, bool vec,
-                                      float* d) {
-  if (vec && nvalid == 8) {
-    if (dtype == 0) {
-      const float4 a = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + e));
-      const float4 b =
-          __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + e + 4));
-      d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
-      d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
-    } else {
-      const uint4 u = __ldcs(
-          reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + e));
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __bfloat1622float2(h[j]);
-        d[2 * j] = f.x;
-        d[2 * j + 1] = f.y;
+    if ((it & 63u) == 0) {
+      if (*ab) return false;
+      if (ptx::globaltimer() - t0 > c.timeout_ns) {
+        atomicOr(c.status, kDevTimeout);
+        *ab = 1;
+        return false;
       }
     }
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float v = 0.f;
-    if (j < nvalid)
-      v = dtype == 0 ? static_cast<const float*>(base)[e + j]
-                     : __bfloat162float(static_cast<const __nv_bfloat16*>(base)[e + j]);
-    d[j] = v;
   }
 }
 
-__device__ __forceinline__ void store8(void* base, int dtype, int64_t e, int nvalid, bool vec,
-                                       const float* d) {
-  if (vec && nvalid == 8) {
-    if (dtype == 0) {
-      float* f = static_cast<float*>(base) + e;
-      *reinterpret_cast<float4*>(f) = make_float4(d[0], d[1], d[2], d[3]);
-      *reinterpret_cast<float4*>(f + 4) = make_float4(d[4], d[5], d[6], d[7]);
-    } else {
-      uint4 u;
-      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + e) = u;
+// The same wait made once per warp (lane 0 polls), result broadcast.
+__device__ __forceinline__ bool mwait_warp(uint64_t* bar, uint32_t parity, const Ctx& c) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mwait(bar, parity, c) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Waits (bounded) until a matrix's Q carries this launch's epoch.
+__device__ bool wait_ready(const unsigned* flag, unsigned epoch, const Ctx& c) {
+  if (ld_acquire_u32(flag) == epoch) return true;
+  volatile int* ab = &c.B->abort;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(128);
+    if (ld_acquire_u32(flag) == epoch) return true;
+    if ((it & 63u) == 0) {
+      if (*ab) return false;
+      if (ptx::globaltimer() - t0 > c.timeout_ns) {
+        atomicOr(c.status, kDevTimeout);
+        *ab = 1;
+        return false;
+      }
     }
-    return;
+  }
+}
+
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int stages) {
+    if (++stage == stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+__device__ __forceinline__ const SmallSlice& slice_of(const SmallParams& p, int mat) {
+  int si = 0;
+  while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
+  return p.s[si];
+}
+
+__device__ __forceinline__ float ld_elem(const void* base, int dtype, int64_t e) {
+  return dtype == 0 ? static_cast<const float*>(base)[e]
+                    : __bfloat162float(static_cast<const __nv_bfloat16*>(base)[e]);
+}
+
+__device__ __forceinline__ void st_elem(void* base, int dtype, int64_t e, float v) {
+  if (dtype == 0) static_cast<float*>(base)[e] = v;
+  else static_cast<__nv_bfloat16*>(base)[e] = __float2bfloat16_rn(v);
+}
+
+// Counts one arrival of `epoch` on a matrix's counter (a counter still tagged
+// with an older epoch counts as empty); true for the arrival that completes
+// the matrix.
+__device__ bool arrive_is_last(unsigned long long* ctr, unsigned epoch, int nb, unsigned* status) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned tag = static_cast<unsigned>(cur >> 32);
+    const unsigned cnt = tag == epoch ? static_cast<unsigned>(cur) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return cnt + 1u == static_cast<unsigned>(nb);
+    cur = prev;
+  }
+  atomicOr(status, kDevTimeout);
+  return false;
+}
+
+// C = A B for m x m fp32 matrices in shared memory: row-major, leading
+// dimension mp (m rounded up to 4), entries outside m x m zero.  Consumer
+// thread t forms the TI x TJ block at rows TI (t / 16), columns TJ (t % 16):
+// per four k it loads TI float4 of A rows and four float4 (TJ = 4) or float2
+// (TJ = 2) of B rows.  The k-sum runs in index order, so every CTA forms the
+// same bits.
+template <int TI, int TJ>
+__device__ __forceinline__ void mm_small(const float* A, const float* B, float* C, int m, int mp,
+                                         int t) {
+  const int i0 = TI * (t >> 4), j0 = TJ * (t & 15);
+  if (i0 >= m || j0 >= m) return;
+  float acc[TI][TJ];
+#pragma unroll
+  for (int r = 0; r < TI; ++r)
+#pragma unroll
+    for (int c = 0; c < TJ; ++c) acc[r][c] = 0.f;
+  for (int k = 0; k < mp; k += 4) {
+    float a[TI][4], b[4][TJ];
+#pragma unroll
+    for (int r = 0; r < TI; ++r) {
+      const float4 v = *reinterpret_cast<const float4*>(A + (i0 + r) * mp + k);
+      a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      if constexpr (TJ == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(B + (k + kk) * mp + j0);
+        b[kk][0] = v.x; b[kk][1] = v.y; b[kk][2] = v.z; b[kk][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(B + (k + kk) * mp + j0);
+        b[kk][0] = v.x; b[kk][1] = v.y;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int r = 0; r < TI; ++r)
+#pragma unroll
+        for (int c = 0; c < TJ; ++c) acc[r][c] = fmaf(a[r][kk], b[kk][c], acc[r][c]);
   }
 #pragma unroll
+  for (int r = 0; r < TI; ++r)
+#pragma unroll
+    for (int c = 0; c < TJ; ++c)
+      if (i0 + r < m && j0 + c < m) C[(i0 + r) * mp + j0 + c] = acc[r][c];
+}
+
+__device__ __forceinline__ void cons_sync() { ptx::named_bar(kConsBar, kT); }
+
+// Gram-space NS of one matrix, run by the consumers of the CTA whose item
+// completed it: sums the partial Grams, normalises, iterates and writes
+// Q / ||X0|| as the bf16 B-operand image (hi rows, then lo rows).  `gs`
+// holds four mp x mp fp32 matrices plus a few scalars.
+template <int TI, int TJ>
+__device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
+  const int m = p.m, mp = p.mp;
+  const int cw = t >> 5, lane = t & 31;
+  const int mm = mp * mp;
+  float* R = gs;
+  float* T = gs + mm;
+  float* P = gs + 2 * mm;
+  float* Q = gs + 3 * mm;
+  float* sc = gs + 4 * mm;
+  for (int e = t; e < 4 * mm; e += kT) gs[e] = 0.f;
+  cons_sync();
+  // R_0 (unnormalised) = sum of the item partials in block order; up to 8
+  // partial loads of an element are in flight together
+  const float* part = p.part + static_cast<size_t>(mat) * p.nb * p.pstride;
+  for (int e = t; e < m * m; e += kT) {
+    float acc = 0.f;
+    for (int b0 = 0; b0 < p.nb; b0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b)
+        v[b] = b0 + b < p.nb ? __ldcg(part + static_cast<size_t>(b0 + b) * p.pstride + e) : 0.f;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) acc += v[b];
+    }
+    const int i = e / m, j = e - i * m;
+    R[i * mp + j] = acc;
+  }
+  cons_sync();
+  if (t == 0) {
+    double tr = 0.0;                       // trace(X0 X0^T) = ||X0||_F^2
+    for (int i = 0; i < m; ++i) tr += static_cast<double>(R[i * mp + i]);
+    if (!isfinite(tr)) atomicOr(p.status, kDevNonfinite);
+    sc[0] = static_cast<float>(1.0 / (sqrt(tr) + static_cast<double>(p.eps)));
+  }
+  cons_sync();
+  const float inv = sc[0];
+  const float s2 = inv * inv;
+  for (int e = t; e < mm; e += kT) R[e] *= s2;
+  cons_sync();
+  for (int k = 0; k < p.steps; ++k) {
+    const float a = p.coef[k][0], b = p.coef[k][1], c = p.coef[k][2];
+    mm_small<TI, TJ>(R, R, T, m, mp, t);                    // T = R^2
+    cons_sync();
+    for (int i = cw; i < m; i += kT / 32)
+      for (int j = lane; j < m; j += 32) {
+        const int x = i * mp + j;
+        const float v = fmaf(b, R[x], c * T[x]) + (i == j ? a : 0.f);   // P = aI + bR + cR^2
+        P[x] = v;
+        if (k == 0) Q[x] = v;
+      }
+    cons_sync();
+    if (k + 1 < p.steps) {
+      mm_small<TI, TJ>(P, R, T, m, mp, t);                  // T = P R
+      cons_sync();
+      mm_small<TI, TJ>(T, P, R, m, mp, t);                  // R <- P R P
+      cons_sync();
+    }
+    if (k > 0) {
+      mm_small<TI, TJ>(P, Q, T, m, mp, t);                  // Q <- P Q
+      cons_sync();
+      float* x = Q;
+      Q = T;
+      T = x;
+    }
+  }
+  if (p.steps == 0) {
+    for (int i = t; i < m; i += kT) Q[i * mp + i] = 1.f;
+    cons_sync();
+  }
+  // Q / ||X0|| as bf16 hi (rows 0..nmm-1) then lo, K-major 128-byte-swizzled
+  uint8_t* dst = p.qimg + static_cast<size_t>(mat) * p.qbytes;
+  const int lo_off = p.nmm * 128;
+  for (int cidx = t; cidx < p.nmm * 8; cidx += kT) {
+    const int q = cidx >> 3, k0 = (cidx & 7) * 8;
+    uint4 hi4, lo4;
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&hi4);
+    __nv_bfloat16* l = reinterpret_cast<__nv_bfloat16*>(&lo4);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int kx = k0 + j;
+      const float v = (q < m && kx < m) ? Q[q * mp + kx] * inv : 0.f;
+      h[j] = __float2bfloat16_rn(v);
+      l[j] = __float2bfloat16_rn(v - __bfloat162float(h[j]));
+    }
+    const uint32_t off = ptx::sw128_offset(q, (cidx & 7) * 16);
+    __stcg(reinterpret_cast<uint4*>(dst + off), hi4);
+    __stcg(reinterpret_cast<uint4*>(dst + lo_off + off), lo4);
+  }
+}
+
+// ---- ring-stage geometry (producer and consumers derive the same) --------------------
+// A row-major matrix streams as groups of whole rows of the item (one bulk
+// copy per row and tensor, wb columns long); a transposed matrix, whose item
+// is one contiguous block, as groups of columns.
+struct Geo {
+  int rows;    // rows per stage (row-major)
+  int cols;    // X columns per stage (transposed)
+  int count;   // stages per item
+};
+
+__device__ __forceinline__ Geo geo_p1(const SmallParams& p, const SmallSlice& S) {
+  const int per = (S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0);   // bytes per element
+  Geo g;
+  if (!S.trans) {
+    g.rows = min(p.m, max(1, p.stage_bytes / (p.wb * per)));
+    g.cols = p.wb;
+    g.count = (p.m + g.rows - 1) / g.rows;
+  } else {
+    g.rows = p.m;
+    g.cols = min(p.wb, max(16, p.stage_bytes / (p.m * per) / 16 * 16));
+    g.count = (p.wb + g.cols - 1) / g.cols;
+  }
+  return g;
+}
+
+// Second phase: 8 or 4 W rows per stage (the TMEM read width), or multiples
+// of 32 columns (one TMEM lane quarter) when transposed.
+__device__ __forceinline__ Geo geo_p2(const SmallParams& p, const SmallSlice& S) {
+  const int esw = S.w_dtype == 0 ? 4 : 2;
+  Geo g;
+  if (!S.trans) {
+    g.rows = 8 * p.wb * esw <= p.stage_bytes ? 8 : 4;
+    g.cols = p.wb;
+    g.count = (p.m + g.rows - 1) / g.rows;
+  } else {
+    g.rows = p.m;
+    g.cols = min(p.wb, max(32, p.stage_bytes / (p.m * esw) / 32 * 32));
+    g.count = (p.wb + g.cols - 1) / g.cols;
+  }
+  return g;
+}
+
+// ---- producer (warp 0) ------------------------------------------------------------
+// Stage s of a first-phase item: G, then Mom at byte rows * wb * esize(G)
+// (row-major: rows [s*rows, ...) of the item, each wb columns) or at byte
+// cols * m * esize(G) (transposed: X columns [s*cols, ...), stored rows of m).
+__device__ void produce_p1(const SmallParams& p, const SmallSlice& S, const Geo& g, int s,
+                           int64_t moff, int64_t col0, int nci, uint8_t* st, uint64_t* full,
+                           int lane) {
+  const int m = p.m, n = p.n, wb = p.wb;
+  const int esg = S.g_dtype == 0 ? 4 : 2;
+  int r0 = 0, r1 = 0, c0 = 0, ncs = 0;
+  if (!S.trans) {
+    r0 = s * g.rows;
+    r1 = min(m, r0 + g.rows);
+  } else {
+    c0 = s * g.cols;
+    ncs = min(g.cols, nci - c0);
+  }
+  const uint32_t mom_off =
+      static_cast<uint32_t>((S.trans ? g.cols * m : g.rows * wb) * esg);
+  uint32_t tx = 0;
+  if (S.gbulk) {
+    const int per = esg + (p.step_mode ? 4 : 0);
+    tx = S.trans ? (ncs > 0 ? static_cast<uint32_t>(ncs * m * per) : 0u)
+                 : static_cast<uint32_t>((r1 - r0) * nci * per);
+  } else {
+    // element-wise copy into the same layout (rows not 16-byte aligned)
+    const int tot = S.trans ? (ncs > 0 ? ncs * m : 0) : (r1 - r0) * nci;
+    for (int idx = lane; idx < tot; idx += 32) {
+      int64_t e;
+      uint32_t so;
+      if (!S.trans) {
+        const int rl = idx / nci, c = idx - rl * nci;
+        e = moff + static_cast<int64_t>(r0 + rl) * n + col0 + c;
+        so = static_cast<uint32_t>(rl * wb + c);
+      } else {
+        e = moff + (col0 + c0) * m + idx;
+        so = static_cast<uint32_t>(idx);
+      }
+      if (esg == 4) reinterpret_cast<float*>(st)[so] = static_cast<const float*>(S.G)[e];
+      else reinterpret_cast<__nv_bfloat16*>(st)[so] = static_cast<const __nv_bfloat16*>(S.G)[e];
+      if (p.step_mode) reinterpret_cast<float*>(st + mom_off)[so] = S.Mom[e];
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    if (tx) ptx::mbar_arrive_expect_tx(full, tx);
+    else ptx::mbar_arrive(full);
+  }
+  __syncwarp();
+  if (!tx) return;
+  if (!S.trans) {
+    for (int r = r0 + lane; r < r1; r += 32) {
+      const int64_t e = moff + static_cast<int64_t>(r) * n + col0;
+      ptx::bulk_load(st + (r - r0) * wb * esg, static_cast<const uint8_t*>(S.G) + e * esg,
+                     static_cast<uint32_t>(nci * esg), full);
+      if (p.step_mode)
+        ptx::bulk_load(st + mom_off + (r - r0) * wb * 4, S.Mom + e,
+                       static_cast<uint32_t>(nci * 4), full);
+    }
+  } else if (lane == 0) {
+    const int64_t e = moff + (col0 + c0) * m;
+    ptx::bulk_load(st, static_cast<const uint8_t*>(S.G) + e * esg,
+                   static_cast<uint32_t>(ncs * m * esg), full);
+    if (p.step_mode)
+      ptx::bulk_load(st + mom_off, S.Mom + e, static_cast<uint32_t>(ncs * m * 4), full);
+  }
+}
+
+// Stage s of a second-phase item: W rows [s*rows, ...) (row-major, wb columns
+// each) or X columns [s*cols, ...) (transposed).
+__device__ void produce_p2(const SmallParams& p, const SmallSlice& S, const Geo& g, int s,
+                           int64_t moff, int64_t col0, int nci, uint8_t* st, uint64_t* full,
+                           int lane) {
+  const int m = p.m, n = p.n, wb = p.wb;
+  const int esw = S.w_dtype == 0 ? 4 : 2;
+  int r0 = 0, r1 = 0, c0 = 0, ncs = 0;
+  if (!S.trans) {
+    r0 = s * g.rows;
+    r1 = min(m, r0 + g.rows);
+  } else {
+    c0 = s * g.cols;
+    ncs = min(g.cols, nci - c0);
+  }
+  uint32_t tx = 0;
+  if (S.wbulk) {
+    tx = S.trans ? (ncs > 0 ? static_cast<uint32_t>(ncs * m * esw) : 0u)
+                 : static_cast<uint32_t>((r1 - r0) * nci * esw);
+  } else {
+    const int tot = S.trans ? (ncs > 0 ? ncs * m : 0) : (r1 - r0) * nci;
+    for (int idx = lane; idx < tot; idx += 32) {
+      int64_t e;
+      uint32_t so;
+      if (!S.trans) {
+        const int rl = idx / nci, c = idx - rl * nci;
+        e = moff + static_cast<int64_t>(r0 + rl) * n + col0 + c;
+        so = static_cast<uint32_t>(rl * wb + c);
+      } else {
+        e = moff + (col0 + c0) * m + idx;
+        so = static_cast<uint32_t>(idx);
+      }
+      if (esw == 4) reinterpret_cast<float*>(st)[so] = static_cast<const float*>(S.W)[e];
+      else reinterpret_cast<__nv_bfloat16*>(st)[so] = static_cast<const __nv_bfloat16*>(S.W)[e];
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    if (tx) ptx::mbar_arrive_expect_tx(full, tx);
+    else ptx::mbar_arrive(full);
+  }
+  __syncwarp();
+  if (!tx) return;
+  if (!S.trans) {
+    for (int r = r0 + lane; r < r1; r += 32) {
+      const int64_t e = moff + static_cast<int64_t>(r) * n + col0;
+      ptx::bulk_load(st + (r - r0) * wb * esw, static_cast<const uint8_t*>(S.W) + e * esw,
+                     static_cast<uint32_t>(nci * esw), full);
+    }
+  } else if (lane == 0) {
+    const int64_t e = moff + (col0 + c0) * m;
+    ptx::bulk_load(st, static_cast<const uint8_t*>(S.W) + e * esw,
+                   static_cast<uint32_t>(ncs * m * esw), full);
+  }
+}
+
+// ---- consumers: first-phase stage ----------------------------------------------------
+template <int ESG>
+__device__ __forceinline__ void load8_smem(const uint8_t* base, int so, float* v) {
+  if constexpr (ESG == 2) {
+    const uint4 u = *reinterpret_cast<const uint4*>(base + so * 2);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(base + so * 4);
+    const float4 b = *reinterpret_cast<const float4*>(base + so * 4 + 16);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+// Momentum for 8 elements; d = the NS input (Nesterov or plain momentum).
+template <bool STEP>
+__device__ __forceinline__ void momentum8(const SmallParams& p, const float* gv, float* mo,
+                                          float* d) {
+#pragma unroll
   for (int j = 0; j < 8; ++j) {
-    if (j < nvalid) {
-      if (dtype == 0) static_cast<float*>(base)[e + j] = d[j];
-      else static_cast<__nv_bfloat16*>(base)[e + j] = __float2bfloat16_rn(d[j]);
+    if constexpr (STEP) {
+      mo[j] = fmaf(p.mu, mo[j], gv[j]);                       // M_t = mu M_{t-1} + G
+      d[j] = p.nesterov ? fmaf(p.mu, mo[j], gv[j]) : mo[j];
+    } else {
+      d[j] = gv[j];
+    }
+  }
+}
+
+__device__ __forceinline__ void store_mom8(float* base, int64_t e, int nv, bool vec, const float* v) {
+  if (vec && nv == 8) {
+    __stcs(reinterpret_cast<float4*>(base + e), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<float4*>(base + e + 4), make_float4(v[4], v[5], v[6], v[7]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nv) base[e + j] = v[j];
+  }
+}
+
+// Row-major stage: rows [r0, r1) x item columns [0, wb); X0 rows of the item's
+// tile, zero beyond the matrix.  Groups of 8 columns; the row index comes from
+// a float reciprocal (exact for these sizes).
+template <int ESG, bool STEP>
+__device__ void consume_p1_rows(const SmallParams& p, const SmallSlice& S, int r0, int r1,
+                                int rows_alloc, int64_t moff, int64_t col0, int nci,
+                                const uint8_t* st, uint8_t* sx, int t) {
+  const int wb = p.wb, n = p.n;
+  const int chunk_bytes = p.mr * 128;
+  const int gpr = wb >> 3;
+  const float inv_gpr = 1.f / static_cast<float>(gpr);
+  const uint8_t* smom = st + rows_alloc * wb * ESG;
+  const bool vec = S.gbulk != 0;
+  const int ng = (r1 - r0) * gpr;
+  for (int g = t; g < ng; g += kT) {
+    const int rl = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_gpr);
+    const int c8 = (g - rl * gpr) << 3;
+    const int nv = min(8, nci - c8);
+    float d[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j] = 0.f;
+    if (nv > 0) {
+      const int so = rl * wb + c8;
+      float gv[8], mo[8];
+      load8_smem<ESG>(st, so, gv);
+      if constexpr (STEP) load8_smem<4>(smom, so, mo);
+      momentum8<STEP>(p, gv, mo, d);
+      if constexpr (STEP)
+        store_mom8(S.Mom, moff + static_cast<int64_t>(r0 + rl) * n + col0 + c8, nv, vec, mo);
+      if (nv < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j >= nv) d[j] = 0.f;
+      }
+    }
+    uint4 q;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
+    *reinterpret_cast<uint4*>(sx + (c8 >> 6) * chunk_bytes +
+                              ptx::sw128_offset(r0 + rl, (c8 & 63) * 2)) = q;
+  }
+}
+
+// Transposed stage: X columns [c0, c0 + cols) of the item (stored rows of m
+// contiguous elements); groups of 8 rows of one column.
+template <int ESG, bool STEP>
+__device__ void consume_p1_cols(const SmallParams& p, const SmallSlice& S, int c0, int cols,
+                                int cols_alloc, int64_t moff, int64_t col0, int nci,
+                                const uint8_t* st, uint8_t* sx, int t) {
+  const int m = p.m;
+  const int chunk_bytes = p.mr * 128;
+  const int ig = p.mr >> 3;
+  const float inv_ig = 1.f / static_cast<float>(ig);
+  const uint8_t* smom = st + cols_alloc * m * ESG;   // where the producer put Mom
+  const bool vec = S.gbulk != 0;
+  for (int g = t; g < cols * ig; g += kT) {
+    const int c = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_ig);
+    const int r = (g - c * ig) << 3;
+    const int nv = c0 + c < nci ? min(8, m - r) : 0;
+    float d[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j] = 0.f;
+    if (nv > 0) {
+      const int so = c * m + r;
+      float gv[8], mo[8];
+      if (vec && nv == 8) {
+        load8_smem<ESG>(st, so, gv);
+        if constexpr (STEP) load8_smem<4>(smom, so, mo);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          gv[j] = j < nv ? ld_elem(st, ESG == 4 ? 0 : 1, so + j) : 0.f;
+          mo[j] = (STEP && j < nv) ? reinterpret_cast<const float*>(smom)[so + j] : 0.f;
+        }
+      }
+      momentum8<STEP>(p, gv, mo, d);
+      if constexpr (STEP) store_mom8(S.Mom, moff + (col0 + c0 + c) * m + r, nv, vec, mo);
+      if (nv < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j >= nv) d[j] = 0.f;
+      }
+    }
+    const int ci = c0 + c;
+    uint8_t* colp = sx + (ci >> 6) * chunk_bytes;
+    const uint32_t byte = (ci & 63) * 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<__nv_bfloat16*>(colp + ptx::sw128_offset(r + j, byte)) =
+          __float2bfloat16_rn(d[j]);
+  }
+}
+
+template <int ESG, bool STEP>
+__device__ __forceinline__ void consume_p1(const SmallParams& p, const SmallSlice& S, const Geo& g,
+                                           int s, int64_t moff, int64_t col0, int nci,
+                                           const uint8_t* st, uint8_t* sx, int t) {
+  if (!S.trans) {
+    const int r0 = s * g.rows;
+    consume_p1_rows<ESG, STEP>(p, S, r0, min(p.m, r0 + g.rows), g.rows, moff, col0, nci, st, sx, t);
+  } else {
+    consume_p1_cols<ESG, STEP>(p, S, s * g.cols, min(g.cols, p.wb - s * g.cols), g.cols, moff,
+                               col0, nci, st, sx, t);
+  }
+}
+
+__device__ void consume_p1_any(const SmallParams& p, const SmallSlice& S, const Geo& g, int s,
+                               int64_t moff, int64_t col0, int nci, const uint8_t* st,
+                               uint8_t* sx, int t) {
+  if (S.g_dtype == 0) {
+    if (p.step_mode) consume_p1<4, true>(p, S, g, s, moff, col0, nci, st, sx, t);
+    else consume_p1<4, false>(p, S, g, s, moff, col0, nci, st, sx, t);
+  } else {
+    if (p.step_mode) consume_p1<2, true>(p, S, g, s, moff, col0, nci, st, sx, t);
+    else consume_p1<2, false>(p, S, g, s, moff, col0, nci, st, sx, t);
+  }
+}
+
+// ---- consumers: second-phase stage -------------------------------------------------------
+// Row-major: W rows [q0, q0 + R) of the item, R = 8 or 4 consecutive TMEM
+// columns of O per tile.  Warp (set, q4) covers lanes 32 q4.. of tiles set,
+// set + 2, ...
+template <int R>
+__device__ void epi_rows(const SmallParams& p, const SmallSlice& S, int q0, int64_t moff,
+                         int64_t col0, int nci, const uint8_t* st, uint32_t obuf, int set, int q4,
+                         int lane, float decay, float stepk) {
+  const int m = p.m, n = p.n, wb = p.wb, tcol = (p.nmm + 31) & ~31;
+  for (int tt = set; tt < wb / 128; tt += 2) {
+    uint32_t r[R];
+    if constexpr (R == 8) ptx::tmem_ld_32x32b_x8(obuf + tt * tcol + q0 + (static_cast<uint32_t>(32 * q4) << 16), r);
+    else ptx::tmem_ld_32x32b_x4(obuf + tt * tcol + q0 + (static_cast<uint32_t>(32 * q4) << 16), r);
+    ptx::tmem_ld_wait();
+    const int col = tt * 128 + 32 * q4 + lane;
+    if (col >= nci) continue;
+    const int64_t gj = col0 + col;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int q = q0 + j;
+      if (q < m) {
+        const float o = __uint_as_float(r[j]);
+        float v = o;
+        if (p.step_mode) v = fmaf(decay, ld_elem(st, S.w_dtype, j * wb + col), -stepk * o);
+        st_elem(S.W, S.w_dtype, moff + static_cast<int64_t>(q) * n + gj, v);
+      }
+    }
+  }
+}
+
+// Transposed: X columns [c0, c0 + cols) in units of 32 (one TMEM lane
+// quarter); the two warp sets split the rows q.
+__device__ void epi_cols(const SmallParams& p, const SmallSlice& S, int c0, int cols,
+                         int64_t moff, int64_t col0, int nci, const uint8_t* st, uint32_t obuf,
+                         int set, int q4, int lane, float decay, float stepk) {
+  const int m = p.m, nmm = p.nmm, tcol = (nmm + 31) & ~31;
+  for (int u = 0; u < cols; u += 32) {
+    const int cu = c0 + u;
+    if (((cu >> 5) & 3) != q4) continue;
+    const int tile = cu >> 7;
+    const int col = cu + lane;
+    const bool live = col < nci;
+    const int64_t gj = col0 + col;
+    for (int h = 0; h < 2; ++h) {
+      const int cq = 16 * set + 32 * h;
+      if (cq >= nmm) continue;
+      uint32_t r[16];
+      ptx::tmem_ld_32x32b_x16(obuf + tile * tcol + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
+      ptx::tmem_ld_wait();
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int q = cq + j;
+        if (q < m) {
+          const float o = __uint_as_float(r[j]);
+          float v = o;
+          if (p.step_mode) v = fmaf(decay, ld_elem(st, S.w_dtype, (col - c0) * m + q), -stepk * o);
+          st_elem(S.W, S.w_dtype, moff + gj * m + q, v);
+        }
+      }
     }
   }
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kSmallThreads, 2)
+__global__ void __launch_bounds__(kSmallThreads, 1)
     ns_small_kernel(const __grid_constant__ SmallParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sX = sm;
-  uint8_t* sBt = sm + p.off_bt;
-  float* sP = reinterpret_cast<float*>(sm + p.off_part);   // [2][m*m]
-  float* sA = reinterpret_cast<float*>(sm + p.off_a);      // [m][m+1]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + p.off_misc);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
-  float* red = reinterpret_cast<float*>(tslot + 4);          // [8]
-  float* s_ssq = red + 8;
-  float* s_inv = red + 9;
+  // X0 tile b at sm + b * xbytes; Q image b at sm + off_q + b * qbytes
+  uint8_t* ring = sm + p.off_ring;
+  float* gs = reinterpret_cast<float*>(sm + p.off_gs);
+  SmallBars* B = reinterpret_cast<SmallBars*>(sm + p.off_bar);
+  const Ctx ctx{B, p.status, p.timeout_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = ptx::cluster_ctarank();
-  const int mat = blockIdx.x / p.cs;
-  int si = 0;
-  while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
-  const SmallSlice& S = p.s[si];
-  const int local = mat - S.mat_base;
-  const int m = p.m, n = p.n, w = p.w;
-  const int64_t col0 = static_cast<int64_t>(rank) * w;
+  const int m = p.m, n = p.n, nmm = p.nmm, wb = p.wb, NS = p.stages;
   const int chunk_bytes = p.mr * 128;
-  const int nchunks = w / 64;
+  const int tiles = wb / 128;
   const int64_t mn = static_cast<int64_t>(m) * n;
+  const int tcol = (nmm + 31) & ~31;       // TMEM columns of O per 128-column tile
 
-  // X (with its padding) and the B' tile start at zero.
-  for (int i = tid; i < p.off_part / 16; i += kSmallThreads)
-    reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
-    ptx::mbar_init(bar, 1);
+    for (int i = 0; i < kSmallMaxStages; ++i) {
+      ptx::mbar_init(&B->ring_full[i], 1);
+      ptx::mbar_init(&B->ring_empty[i], kT / 32);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&B->x_full[i], 1);
+      ptx::mbar_init(&B->gram_full[i], 1);
+      ptx::mbar_init(&B->xq_full[i], 1);
+      ptx::mbar_init(&B->xq_free[i], 1);
+      ptx::mbar_init(&B->o_full[i], 1);
+      ptx::mbar_init(&B->o_empty[i], kT / 32);
+    }
+    B->last = 0;
+    B->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0) ptx::tmem_alloc(tslot, kSmallTmemCols);
+  // The apply's K padding (rows mr..nmm-1) reads up to 15 rows past an X0
+  // tile, i.e. the start of the next buffer; those bytes must hold finite
+  // values (they meet zero rows of Q) even before the buffer is first used.
+  for (int i = tid; i < 2048 / 16; i += kSmallThreads) {
+    reinterpret_cast<uint4*>(sm + p.xbytes)[i] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + p.off_q)[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 1) ptx::tmem_alloc(&B->tslot, kSmallTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *tslot;
+  const uint32_t tmem = B->tslot;
 
-  // ---- momentum + Nesterov + cast into the cluster-resident X -------------------
-  // X[i][j] = D[i][j] (stored [m][n]) or D[j][i] (stored [n][m], transposed).
-  float ssq = 0.f;
-  const int64_t moff = static_cast<int64_t>(local) * mn;
-  // Items are 8 consecutive stored elements; each thread keeps kSmallUnroll
-  // items' loads in flight before using them.
-  const int ig = (m + 7) / 8;
-  const int items = S.trans ? w * ig : m * (w / 8);
-  for (int base = tid; base < items; base += kSmallUnroll * kSmallThreads) {
-    float g[kSmallUnroll][8], mo[kSmallUnroll][8];
-    int64_t e[kSmallUnroll];
-    int nv[kSmallUnroll], row[kSmallUnroll], jl[kSmallUnroll];
-#pragma unroll
-    for (int u = 0; u < kSmallUnroll; ++u) {
-      const int item = base + u * kSmallThreads;
-      nv[u] = 0;
-      if (item < items) {
-        if (!S.trans) {
-          const int gpr = w / 8;
-          row[u] = item / gpr;
-          jl[u] = (item - row[u] * gpr) * 8;
-          const int64_t gj = col0 + jl[u];
-          if (gj < n) {
-            nv[u] = (n - gj) < 8 ? static_cast<int>(n - gj) : 8;
-            e[u] = moff + static_cast<int64_t>(row[u]) * n + gj;
-          }
-        } else {
-          jl[u] = item / ig;
-          row[u] = (item - jl[u] * ig) * 8;
-          const int64_t gj = col0 + jl[u];
-          if (gj < n) {
-            nv[u] = min(8, m - row[u]);
-            e[u] = moff + gj * m + row[u];
-          }
+  if (warp == 0) {
+    // ======================= producer =======================
+    Ring rg;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x) {
+      const int mat = item / p.nb, blk = item - mat * p.nb;
+      const SmallSlice& S = slice_of(p, mat);
+      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+      const int64_t col0 = static_cast<int64_t>(blk) * wb;
+      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
+      const Geo g = geo_p1(p, S);
+      for (int s = 0; s < g.count; ++s) {
+        if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) {
+          ok = false;
+          break;
         }
-      }
-      if (nv[u] > 0) {
-        load8(S.G, S.g_dtype, e[u], nv[u], S.gvec, g[u]);
-        if (p.step_mode) load8(S.Mom, 0, e[u], nv[u], S.gvec, mo[u]);
+        produce_p1(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes,
+                   &B->ring_full[rg.stage], lane);
+        rg.next(NS);
       }
     }
-#pragma unroll
-    for (int u = 0; u < kSmallUnroll; ++u) {
-      if (nv[u] <= 0) continue;
-      float d[8];
-      if (p.step_mode) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          mo[u][j] = fmaf(p.mu, mo[u][j], g[u][j]);             // M_t = mu*M_{t-1} + G
-          d[j] = p.nesterov ? fmaf(p.mu, mo[u][j], g[u][j]) : mo[u][j];
+    __syncthreads();   // ---- phase boundary ----
+    ok = ok && !B->abort;
+    int k = 0;
+    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++k) {
+      const int b = k & 1;
+      const int mat = item / p.nb, blk = item - mat * p.nb;
+      const SmallSlice& S = slice_of(p, mat);
+      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+      const int64_t col0 = static_cast<int64_t>(blk) * wb;
+      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
+      int r = 0;
+      if (lane == 0) {
+        r = wait_ready(p.ready + mat, p.epoch, ctx) ? 1 : 0;
+        ptx::fence_proxy_async_global();
+        if (r) r = mwait(&B->xq_free[b], ((k >> 1) & 1) ^ 1u, ctx) ? 1 : 0;
+        if (r) {
+          ptx::mbar_arrive_expect_tx(&B->xq_full[b], static_cast<uint32_t>(p.xbytes + p.qbytes));
+          ptx::bulk_load(sm + b * p.xbytes, p.ximg + static_cast<size_t>(item) * p.xbytes,
+                         static_cast<uint32_t>(p.xbytes), &B->xq_full[b]);
+          ptx::bulk_load(sm + p.off_q + b * p.qbytes, p.qimg + static_cast<size_t>(mat) * p.qbytes,
+                         static_cast<uint32_t>(p.qbytes), &B->xq_full[b]);
         }
-        store8(S.Mom, 0, e[u], nv[u], S.gvec, mo[u]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) d[j] = g[u][j];
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= nv[u]) d[j] = 0.f;
-        ssq = fmaf(d[j], d[j], ssq);
-      }
-      uint8_t* col = sX + (jl[u] >> 6) * chunk_bytes;
-      if (!S.trans) {
-        uint4 q;
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
-        *reinterpret_cast<uint4*>(col + ptx::sw128_offset(row[u], (jl[u] & 63) * 2)) = q;
-      } else {
-        const uint32_t byte = (jl[u] & 63) * 2;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (j < nv[u])
-            *reinterpret_cast<__nv_bfloat16*>(col + ptx::sw128_offset(row[u] + j, byte)) =
-                __float2bfloat16_rn(d[j]);
+      ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+      if (!ok || !p.step_mode) continue;
+      const Geo g = geo_p2(p, S);
+      for (int s = 0; s < g.count; ++s) {
+        if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) {
+          ok = false;
+          break;
+        }
+        produce_p2(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes,
+                   &B->ring_full[rg.stage], lane);
+        rg.next(NS);
       }
     }
-  }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, nmm);
+    const uint32_t idesc_app = idesc_gram | (1u << 15);   // A MN-major
+    if (lane == 0) {
+      int k = 0;
+      for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++k) {
+        const int b = k & 1;
+        if (!mwait(&B->x_full[b], (k >> 1) & 1, ctx)) break;
+        ptx::tc_fence_after();
+        const uint32_t sx = ptx::smem_u32(sm + b * p.xbytes);
+        for (int kc = 0; kc < wb / 64; ++kc) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-  if (lane == 0) red[warp] = ssq;
-  __syncthreads();
-  if (tid == 0) {
-    float b = 0.f;
-    for (int i = 0; i < kSmallThreads / 32; ++i) b += red[i];
-    *s_ssq = b;
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::cluster_sync();
-  if (tid == 0) {
-    double tot = 0.0;
-    const uint32_t a = ptx::smem_u32(s_ssq);
-    for (int r = 0; r < p.cs; ++r) tot += (double)ptx::ld_shared_cluster_f32(ptx::mapa_shared(a, r));
-    if (!isfinite(tot) && rank == 0) atomicOr(p.status, kDevNonfinite);
-    *s_inv = static_cast<float>(1.0 / (sqrt(tot) + (double)p.eps));
-  }
-  __syncthreads();
-  const float inv = *s_inv;
-
-  // ---- Newton-Schulz iterations -----------------------------------------------------
-  const uint32_t sX_u = ptx::smem_u32(sX), sBt_u = ptx::smem_u32(sBt);
-  const int nmm = p.nmm;
-  const int tcol = (nmm + 31) & ~31;                 // TMEM columns per product tile
-  const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, nmm);
-  const uint32_t idesc_app = ptx::idesc_bf16_f32(128, nmm) | (1u << 15);   // A MN-major
-  const int tiles = w / 128;
-  const int per_batch = (kSmallTmemCols - tcol) / tcol;
-  uint32_t phase = 0;
-  bool ok = true;
-  for (int it = 0; it < p.steps; ++it) {
-    const float ca = p.coef[it][0], cb = p.coef[it][1], cc = p.coef[it][2], al = p.coef[it][3];
-    const bool first = it == 0;
-    const int par = it & 1;
-    // Gram partial over this CTA's columns
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      for (int kc = 0; kc < nchunks; ++kc) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t d = ptx::sdesc_kmajor_sw128(sX_u + kc * chunk_bytes + k * 32);
-          ptx::umma_bf16(tmem, d, d, idesc_gram, (kc | k) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kc * chunk_bytes + kk * 32);
+            ptx::umma_bf16(tmem + 64 * b, d, d, idesc_gram, (kc | kk) != 0 ? 1u : 0u);
+          }
         }
+        ptx::umma_commit(&B->gram_full[b]);
       }
-      ptx::umma_commit(bar);
     }
     __syncwarp();
-    ok = wait_mma(bar, phase, p.status, p.timeout_ns) && ok;
-    phase ^= 1;
-    ptx::tc_fence_after();
-    if (warp < 4 && warp * 32 < m) {
-      const int i = warp * 32 + lane;
-      for (int c0 = 0; c0 < nmm; c0 += 32) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
-        ptx::tmem_ld_wait();
-        if (i < m) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < m) sP[par * m * m + i * m + c0 + j] = __uint_as_float(r[j]);
-        }
-      }
-    }
-    ptx::tc_fence_before();
-    ptx::cluster_sync();
-    ptx::tc_fence_after();
-    // A = sum of the partials in rank order (every CTA gets the same bits);
-    // A stays fp32 here: it is never an MMA operand on this path.
-    const float gscale = first ? inv * inv : 1.f;
-    for (int e = tid; e < m * m; e += kSmallThreads) {
-      const uint32_t a = ptx::smem_u32(sP + par * m * m + e);
-      float v[kSmallMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kSmallMaxCluster; ++r)
-        v[r] = r < p.cs ? ptx::ld_shared_cluster_f32(ptx::mapa_shared(a, r)) : 0.f;
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < kSmallMaxCluster; ++r) acc += v[r];
-      const int i = e / m, j = e - i * m;
-      sA[i * (m + 1) + j] = acc * gscale;
-    }
-    __syncthreads();
-    // P = a*I + b*A + c*A^2 in fp32, stored as two bf16 K-major operands
-    // P = hi + lo (rows q < m, columns k < m): the apply multiplies by both,
-    // so the bf16 rounding of P no longer limits the accuracy.
-    for (int e = tid; e < m * m; e += kSmallThreads) {
-      const int i = e / m, j = e - i * m;
-      float s2 = 0.f;
-      for (int k = 0; k < m; ++k) s2 = fmaf(sA[i * (m + 1) + k], sA[k * (m + 1) + j], s2);
-      const float v = fmaf(cb, sA[i * (m + 1) + j], cc * s2) + (i == j ? ca + al : 0.f);
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      const uint32_t off = ptx::sw128_offset(i, j * 2);
-      *reinterpret_cast<__nv_bfloat16*>(sBt + off) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(sBt + kSmallBTile + off) =
-          __float2bfloat16_rn(v - __bfloat162float(hi));
-    }
-    ptx::fence_proxy_async_smem();
-    __syncthreads();
-    // Apply, in batches of product tiles that fit the TMEM allocation
-    const float xs = first ? inv : 1.f;
-    for (int t0 = 0; t0 < tiles; t0 += per_batch) {
-      const int nb = min(per_batch, tiles - t0);
-      if (tid == 0) {
+    __syncthreads();   // ---- phase boundary ----
+    if (lane == 0 && !B->abort) {
+      int k = 0;
+      for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++k) {
+        const int b = k & 1;
+        if (!mwait(&B->xq_full[b], (k >> 1) & 1, ctx)) break;
+        if (!mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) break;
         ptx::tc_fence_after();
-        for (int tt = 0; tt < nb; ++tt) {
-          const int t = t0 + tt;
+        const uint32_t sx = ptx::smem_u32(sm + b * p.xbytes);
+        const uint32_t sq = ptx::smem_u32(sm + p.off_q + b * p.qbytes);
+        for (int t = 0; t < tiles; ++t) {
+          const uint32_t ocol = 256 * b + tcol * t;
           for (int j = 0; j < nmm / 16; ++j) {
-            const uint64_t a = ptx::sdesc_mnmajor_sw128(sX_u + 2 * t * chunk_bytes + j * 2048,
+            const uint64_t a = ptx::sdesc_mnmajor_sw128(sx + 2 * t * chunk_bytes + j * 2048,
                                                         chunk_bytes, 1024);
-            ptx::umma_bf16(tmem + tcol * (1 + tt), a, ptx::sdesc_kmajor_sw128(sBt_u + j * 32),
-                           idesc_app, j != 0 ? 1u : 0u);
-            ptx::umma_bf16(tmem + tcol * (1 + tt), a,
-                           ptx::sdesc_kmajor_sw128(sBt_u + kSmallBTile + j * 32), idesc_app, 1u);
+            ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + j * 32), idesc_app,
+                           j != 0 ? 1u : 0u);
+            ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + nmm * 128 + j * 32),
+                           idesc_app, 1u);
           }
         }
-        ptx::umma_commit(bar);
+        ptx::umma_commit(&B->o_full[b]);
+        ptx::umma_commit(&B->xq_free[b]);
       }
-      __syncwarp();
-      ok = wait_mma(bar, phase, p.status, p.timeout_ns) && ok;
-      phase ^= 1;
+    }
+    __syncwarp();
+  } else {
+    // ======================= consumers =======================
+    const int t = tid - 64;
+    const int cw = warp - 2;
+    bool ok = true;
+    Ring rg;
+    int prev = -1, prevk = 0;
+    auto finish = [&](int item, int k, bool newer_store) {
+      const int g = k & 1;
+      const int mat = item / p.nb;
+      const bool gok = mwait_warp(&B->gram_full[g], (k >> 1) & 1, ctx);
       ptx::tc_fence_after();
-      const int q4 = warp & 3;
-      for (int tt = warp >> 2; tt < nb; tt += 2) {
-        const int gp = 128 * (t0 + tt) + q4 * 32 + lane;       // X column within the CTA
-        uint8_t* col = sX + (gp >> 6) * chunk_bytes;
-        const uint32_t byte = (gp & 63) * 2;
-        for (int c0 = 0; c0 < nmm; c0 += 32) {
+      if (gok && ok && (warp == 4 || warp == 5) && (warp - 4) * 32 < m) {
+        const int i = (warp - 4) * 32 + lane;
+        float* dstp = p.part + static_cast<size_t>(item) * p.pstride;
+        for (int c0 = 0; c0 < m; c0 += 32) {
           uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(
-              tmem + (static_cast<uint32_t>(q4 * 32) << 16) + tcol * (1 + tt) + c0, r);
+          ptx::tmem_ld_32x32b_x32(tmem + 64 * g + c0 + (static_cast<uint32_t>((warp - 4) * 32) << 16),
+                                  r);
           ptx::tmem_ld_wait();
+          if (i < m) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int q = c0 + j;
-            if (q < m)
-              *reinterpret_cast<__nv_bfloat16*>(col + ptx::sw128_offset(q, byte)) =
-                  __float2bfloat16_rn(xs * __uint_as_float(r[j]));
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < m) __stcg(dstp + i * m + c0 + j, __uint_as_float(r[j]));
           }
+        }
+      }
+      ok = ok && gok;
+      __threadfence();
+      ptx::tc_fence_before();
+      if (t == 0) {
+        // the image store of this item must be complete before it is announced
+        if (newer_store) ptx::bulk_wait_group<1>();
+        else ptx::bulk_wait_group<0>();
+        ptx::fence_proxy_async_global();
+        __threadfence();
+      }
+      cons_sync();
+      if (t == 0)
+        B->last = (ok && !B->abort && arrive_is_last(p.arrive + mat, p.epoch, p.nb, p.status)) ? 1 : 0;
+      cons_sync();
+      if (B->last) {
+        __threadfence();
+        if (m <= 32) gram_space<2, 2>(p, mat, gs, t);
+        else gram_space<4, 4>(p, mat, gs, t);
+        __threadfence();
+        cons_sync();
+        if (t == 0) st_release_u32(p.ready + mat, p.epoch);
+      }
+      cons_sync();
+    };
+    int k = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++k) {
+      const int b = k & 1;
+      const int mat = item / p.nb, blk = item - mat * p.nb;
+      const SmallSlice& S = slice_of(p, mat);
+      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+      const int64_t col0 = static_cast<int64_t>(blk) * wb;
+      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
+      uint8_t* sx = sm + b * p.xbytes;
+      if (k >= 2 && t == 0) ptx::bulk_wait_read<1>();   // item k-2's image store left this tile
+      cons_sync();
+      const Geo g = geo_p1(p, S);
+      for (int s = 0; s < g.count; ++s) {
+        const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
+        ok = ok && sok;
+        if (ok) consume_p1_any(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes, sx, t);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
+        rg.next(NS);
+      }
+      // padding rows m..mr-1 of a row-major item are zero
+      if (!S.trans && p.mr > m) {
+        const int gpr = wb >> 3;
+        for (int gi = t; gi < (p.mr - m) * gpr; gi += kT) {
+          const int r = m + gi / gpr, c8 = (gi % gpr) << 3;
+          *reinterpret_cast<uint4*>(sx + (c8 >> 6) * chunk_bytes +
+                                    ptx::sw128_offset(r, (c8 & 63) * 2)) = make_uint4(0, 0, 0, 0);
         }
       }
       ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncthreads();
-      ptx::tc_fence_after();
-    }
-  }
-
-  // ---- update (or copy-back) from the cluster-resident result -----------------------
-  const float os = p.steps == 0 ? inv : 1.f;
-  const float decay = 1.f - p.lr * p.wd, stepk = p.lr * S.scale * os;
-  if (ok) {
-    for (int base = tid; base < items; base += kSmallUnroll * kSmallThreads) {
-      float wv[kSmallUnroll][8];
-      int64_t e[kSmallUnroll];
-      int nv[kSmallUnroll], row[kSmallUnroll], jl[kSmallUnroll];
-#pragma unroll
-      for (int u = 0; u < kSmallUnroll; ++u) {
-        const int item = base + u * kSmallThreads;
-        nv[u] = 0;
-        if (item < items) {
-          if (!S.trans) {
-            const int gpr = w / 8;
-            row[u] = item / gpr;
-            jl[u] = (item - row[u] * gpr) * 8;
-            const int64_t gj = col0 + jl[u];
-            if (gj < n) {
-              nv[u] = (n - gj) < 8 ? static_cast<int>(n - gj) : 8;
-              e[u] = moff + static_cast<int64_t>(row[u]) * n + gj;
-            }
-          } else {
-            jl[u] = item / ig;
-            row[u] = (item - jl[u] * ig) * 8;
-            const int64_t gj = col0 + jl[u];
-            if (gj < n) {
-              nv[u] = min(8, m - row[u]);
-              e[u] = moff + gj * m + row[u];
-            }
-          }
-        }
-        if (nv[u] > 0 && p.step_mode) load8(S.W, S.w_dtype, e[u], nv[u], S.wvec, wv[u]);
+      cons_sync();
+      if (t == 0) {
+        if (ok && !B->abort)
+          ptx::bulk_store(p.ximg + static_cast<size_t>(item) * p.xbytes, sx,
+                          static_cast<uint32_t>(p.xbytes));
+        ptx::bulk_commit();
+        ptx::mbar_arrive(&B->x_full[b]);
       }
-#pragma unroll
-      for (int u = 0; u < kSmallUnroll; ++u) {
-        if (nv[u] <= 0) continue;
-        const uint8_t* col = sX + (jl[u] >> 6) * chunk_bytes;
-        const uint32_t byte = (jl[u] & 63) * 2;
-        float o[8];
-        if (!S.trans) {
-          const uint4 q = *reinterpret_cast<const uint4*>(col + ptx::sw128_offset(row[u], byte));
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(h[j]);
-            o[2 * j] = f.x;
-            o[2 * j + 1] = f.y;
+      if (prev >= 0) finish(prev, prevk, true);
+      prev = item;
+      prevk = k;
+    }
+    if (prev >= 0) finish(prev, prevk, false);
+    if (t == 0) ptx::bulk_wait_group<0>();
+    __syncthreads();   // ---- phase boundary ----
+    ok = ok && !B->abort;
+    const float decay = 1.f - p.lr * p.wd;
+    const int q4 = warp & 3, set = cw >> 2;
+    k = 0;
+    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++k) {
+      const int b = k & 1;
+      const int mat = item / p.nb, blk = item - mat * p.nb;
+      const SmallSlice& S = slice_of(p, mat);
+      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+      const int64_t col0 = static_cast<int64_t>(blk) * wb;
+      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
+      const float stepk = p.lr * S.scale;
+      ok = mwait_warp(&B->o_full[b], (k >> 1) & 1, ctx) && ok;
+      ptx::tc_fence_after();
+      const uint32_t obuf = tmem + 256 * b;
+      const Geo g = geo_p2(p, S);
+      for (int s = 0; s < g.count; ++s) {
+        if (p.step_mode) {
+          const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
+          ok = ok && sok;
+        }
+        const uint8_t* st = ring + rg.stage * p.stage_bytes;
+        if (ok) {
+          if (!S.trans) {
+            if (g.rows == 8)
+              epi_rows<8>(p, S, s * 8, moff, col0, nci, st, obuf, set, q4, lane, decay, stepk);
+            else
+              epi_rows<4>(p, S, s * 4, moff, col0, nci, st, obuf, set, q4, lane, decay, stepk);
+          } else {
+            epi_cols(p, S, s * g.cols, min(g.cols, wb - s * g.cols), moff, col0, nci, st, obuf,
+                     set, q4, lane, decay, stepk);
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            o[j] = j < nv[u] ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                                   col + ptx::sw128_offset(row[u] + j, byte)))
-                             : 0.f;
         }
         if (p.step_mode) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) wv[u][j] = fmaf(decay, wv[u][j], -stepk * o[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) wv[u][j] = o[j] * os;
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
+          rg.next(NS);
         }
-        store8(S.W, S.w_dtype, e[u], nv[u], S.wvec, wv[u]);
       }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&B->o_empty[b]);
     }
   }
-  // No CTA leaves while a peer may still read its shared memory.
   ptx::tc_fence_before();
-  ptx::cluster_sync();
-  if (warp == 0) ptx::tmem_dealloc(tmem, kSmallTmemCols);
+  __syncthreads();
+  if (warp == 1) ptx::tmem_dealloc(tmem, kSmallTmemCols);
 }
 
-int small_max_active_clusters(int cs, int smem_bytes) {
+int small_blocks_per_sm(int smem_bytes) {
   if (cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem_bytes) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
-  cfg.blockDim = dim3(kSmallThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_small_kernel, &cfg) != cudaSuccess) {
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ns_small_kernel, kSmallThreads,
+                                                    smem_bytes) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return n;
+  return nb;
 }
 
-cudaError_t launch_small(const SmallParams& p, int total_mats, cudaStream_t s) {
-  if (total_mats <= 0) return cudaSuccess;
+cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s) {
+  if (p.items <= 0 || grid <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(ns_small_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(total_mats) * p.cs, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kSmallThreads, 1, 1);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = s;
+  // The second phase waits on results of other CTAs' first phase: every CTA
+  // must be resident.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, ns_small_kernel, p);
