@@ -215,7 +215,7 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
   sp->m = static_cast<int>(m);
   sp->n = static_cast<int>(n);
   sp->mr = static_cast<int>(rup(m, 8));
-  sp->mp = static_cast<int>(rup(m, 4));
+  sp->mp = m <= 32 ? 32 : 64;
   sp->nmm = static_cast<int>(rup(m, 16));
   sp->sc = 0;
   sp->qbytes = 2 * sp->nmm * 128;
@@ -223,7 +223,7 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
   sp->stage_bytes = kSmallStageBytes;
   const int tcol = static_cast<int>(rup(sp->nmm, 32));
   const int64_t wcap = std::min<int64_t>(kSmallStageBytes / 16, 128 * (256 / tcol));
-  const size_t gs = align_up(static_cast<size_t>(4) * sp->mp * sp->mp * 4 + 64, 16);
+  const size_t gs = align_up(static_cast<size_t>(5) * sp->mp * sp->mp * 4 + 64, 16);
   const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns
   int64_t wmax = 0;
   for (int st = kSmallMaxStages; st >= 2 && wmax == 0; --st) {
@@ -366,10 +366,11 @@ muon_status_t get_workspace(cudaStream_t stream, size_t bytes, size_t ctrs, char
   return MUON_OK;
 }
 
-// Epoch-tagged counters of the small-m path for `mats` matrices: arrive
-// (64-bit) then ready (32-bit); returns the next epoch (never 0).
+// Epoch-tagged words of the small-m path for `mats` matrices: arrive[cap],
+// ready_list[cap], then the ring of per-launch counter slots; returns the
+// next epoch (never 0).
 muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned long long** arrive,
-                             unsigned** ready, unsigned* epoch) {
+                             unsigned long long** ready_list, unsigned** ctr, unsigned* epoch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
   Workspace& w = g_ws[{dev, stream}];
@@ -382,17 +383,19 @@ muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned long lon
     w.ep = nullptr;
     w.ep_cap = 0;
     const size_t cap = align_up(mats, 1024);
-    if (cudaMalloc(&w.ep, cap * 12) != cudaSuccess) {
+    const size_t bytes = 2 * cap * sizeof(unsigned long long) + kSmallCtrSlots * 4 * sizeof(unsigned);
+    if (cudaMalloc(&w.ep, bytes) != cudaSuccess) {
       cudaGetLastError();
       w.ep = nullptr;
       return MUON_ERR_OUT_OF_MEMORY;
     }
-    if (cudaMemsetAsync(w.ep, 0, cap * 12, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    if (cudaMemsetAsync(w.ep, 0, bytes, stream) != cudaSuccess) return MUON_ERR_CUDA;
     w.ep_cap = cap;
   }
   if (++w.epoch == 0) w.epoch = 1;
   *arrive = w.ep;
-  *ready = reinterpret_cast<unsigned*>(w.ep + w.ep_cap);
+  *ready_list = w.ep + w.ep_cap;
+  *ctr = reinterpret_cast<unsigned*>(w.ep + 2 * w.ep_cap);
   *epoch = w.epoch;
   return MUON_OK;
 }
@@ -594,7 +597,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     sp.part = reinterpret_cast<float*>(w);
     w += align_up(static_cast<size_t>(sp.items) * sp.pstride * 4, 256);
     sp.qimg = reinterpret_cast<uint8_t*>(w);
-    st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready, &sp.epoch);
+    st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready_list, &sp.ctr, &sp.epoch);
     if (st != MUON_OK) return st;
     // one CTA per SM (all resident: the launch is cooperative)
     if (small_blocks_per_sm(sp.smem_bytes) <= 0) return MUON_ERR_CUDA;

@@ -116,6 +116,7 @@ constexpr int kSmallCons = 256;            // consumer threads
 constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O buffers [0,256), [256,512)
 constexpr int kSmallMaxStages = 4;
 constexpr int kSmallStageBytes = 24 * 1024;
+constexpr int kSmallCtrSlots = 64;         // ring of per-launch counter slots
 constexpr int kSmallSmemLimit = 227 * 1024;
 
 struct SmallSlice {
@@ -136,7 +137,7 @@ struct SmallParams {
   int n_slices;
   int m, n;          // core shape, m <= n
   int mr;            // X rows held: m rounded up to 8
-  int mp;            // leading dimension of the m x m fp32 matrices: m rounded up to 4
+  int mp;            // leading dimension of the Gram-space fp32 matrices: 32 (m <= 32) or 64
   int nmm;           // MMA N (and apply K): m rounded up to 16
   int wb;            // X columns per work item (multiple of 128)
   int nb;            // work items per matrix
@@ -155,7 +156,9 @@ struct SmallParams {
   float* part;                  // [items][pstride] partial Gram matrices
   uint8_t* qimg;                // [total_mats][qbytes] Q = hi + lo operand images
   unsigned long long* arrive;   // [total_mats] (epoch << 32) | items arrived
-  unsigned* ready;              // [total_mats] epoch once Q is written
+  unsigned long long* ready_list;   // [total_mats] (epoch << 32) | matrix, in publication order
+  unsigned* ctr;                // [kSmallCtrSlots][4]: per launch (slot epoch % slots)
+                                // ready-list length, claimed second- and first-phase items
   unsigned epoch;               // this launch's tag, never 0
   unsigned* status;
   unsigned long long timeout_ns;

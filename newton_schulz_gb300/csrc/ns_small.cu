@@ -45,24 +45,18 @@ namespace {
 constexpr int kT = kSmallCons;      // consumer threads
 constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Shared-memory control block: mbarriers, the TMEM slot and CTA flags.
 struct SmallBars {
   uint64_t ring_full[kSmallMaxStages], ring_empty[kSmallMaxStages];
-  uint64_t x_full[2], gram_full[2], xq_full[2], xq_free[2];
+  uint64_t x_full[2], gram_full[2], xq_full[2];
   uint64_t o_full[2], o_empty[2];
   uint32_t tslot;
   int last;
   int abort;
+  int slot[2];   // second phase: item held by X0 buffer b (-1: no more items)
+  int stage_item[kSmallMaxStages];   // first phase: item of each ring stage (-1: no more)
+  int x_item[2];     // first phase: item whose X0 tile b is complete (-1: no more)
+  int cur_item;      // first phase: the consumers' current item (-2: abort)
 };
 
 struct Ctx {
@@ -80,6 +74,7 @@ __device__ bool mwait(uint64_t* bar, uint32_t parity, const Ctx& c) {
   if (*ab) return false;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
+    if (it > 4) __nanosleep(64);   // leave issue slots to the working warps
     if (ptx::mbar_try_wait(addr, parity)) return true;
     if ((it & 63u) == 0) {
       if (*ab) return false;
@@ -99,20 +94,51 @@ __device__ __forceinline__ bool mwait_warp(uint64_t* bar, uint32_t parity, const
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Waits (bounded) until a matrix's Q carries this launch's epoch.
-__device__ bool wait_ready(const unsigned* flag, unsigned epoch, const Ctx& c) {
-  if (ld_acquire_u32(flag) == epoch) return true;
+// Epoch-tagged counter: (epoch << 32) | count.  Returns the count before this
+// increment (a counter still tagged with an older epoch counts as zero), or
+// 0xffffffff if the update kept failing.
+__device__ unsigned claim(unsigned long long* ctr, unsigned epoch, unsigned* status) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned tag = static_cast<unsigned>(cur >> 32);
+    const unsigned cnt = tag == epoch ? static_cast<unsigned>(cur) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return cnt;
+    cur = prev;
+  }
+  atomicOr(status, kDevTimeout);
+  return 0xffffffffu;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Waits (bounded) until position j of the ready list carries this launch's
+// epoch; returns the matrix published there, or -1.
+__device__ int wait_ready_pos(const unsigned long long* list, int j, unsigned epoch,
+                              const Ctx& c) {
+  unsigned long long v = ld_acquire_u64(list + j);
+  if (static_cast<unsigned>(v >> 32) == epoch) return static_cast<int>(static_cast<unsigned>(v));
   volatile int* ab = &c.B->abort;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(128);
-    if (ld_acquire_u32(flag) == epoch) return true;
+    v = ld_acquire_u64(list + j);
+    if (static_cast<unsigned>(v >> 32) == epoch) return static_cast<int>(static_cast<unsigned>(v));
     if ((it & 63u) == 0) {
-      if (*ab) return false;
+      if (*ab) return -1;
       if (ptx::globaltimer() - t0 > c.timeout_ns) {
         atomicOr(c.status, kDevTimeout);
         *ab = 1;
-        return false;
+        return -1;
       }
     }
   }
@@ -145,53 +171,34 @@ __device__ __forceinline__ void st_elem(void* base, int dtype, int64_t e, float 
   else static_cast<__nv_bfloat16*>(base)[e] = __float2bfloat16_rn(v);
 }
 
-// Counts one arrival of `epoch` on a matrix's counter (a counter still tagged
-// with an older epoch counts as empty); true for the arrival that completes
-// the matrix.
-__device__ bool arrive_is_last(unsigned long long* ctr, unsigned epoch, int nb, unsigned* status) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned tag = static_cast<unsigned>(cur >> 32);
-    const unsigned cnt = tag == epoch ? static_cast<unsigned>(cur) : 0u;
-    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
-    const unsigned long long prev = atomicCAS(ctr, cur, want);
-    if (prev == cur) return cnt + 1u == static_cast<unsigned>(nb);
-    cur = prev;
-  }
-  atomicOr(status, kDevTimeout);
-  return false;
-}
 
-// C = A B for m x m fp32 matrices in shared memory: row-major, leading
-// dimension mp (m rounded up to 4), entries outside m x m zero.  Consumer
-// thread t forms the TI x TJ block at rows TI (t / 16), columns TJ (t % 16):
-// per four k it loads TI float4 of A rows and four float4 (TJ = 4) or float2
-// (TJ = 2) of B rows.  The k-sum runs in index order, so every CTA forms the
-// same bits.
-template <int TI, int TJ>
-__device__ __forceinline__ void mm_small(const float* A, const float* B, float* C, int m, int mp,
-                                         int t) {
-  const int i0 = TI * (t >> 4), j0 = TJ * (t & 15);
-  if (i0 >= m || j0 >= m) return;
-  float acc[TI][TJ];
+// Block of C = A B owned by consumer thread t: rows TI (t / 16), columns
+// TJ (t % 16) of LD x LD fp32 matrices in shared memory (row-major, leading
+// dimension LD, entries outside m x m zero).  LD is 32 (m <= 32, 2 x 2
+// blocks) or 64 (4 x 4 blocks), so the k loop is fully unrolled with no
+// bounds; the k-sum runs in index order, so every CTA forms the same bits.
+template <int TI, int TJ, int LD>
+__device__ __forceinline__ void mm_block(const float* A, const float* B, int i0, int j0,
+                                         float (&acc)[TI][TJ]) {
 #pragma unroll
   for (int r = 0; r < TI; ++r)
 #pragma unroll
     for (int c = 0; c < TJ; ++c) acc[r][c] = 0.f;
-  for (int k = 0; k < mp; k += 4) {
+#pragma unroll
+  for (int k = 0; k < LD; k += 4) {
     float a[TI][4], b[4][TJ];
 #pragma unroll
     for (int r = 0; r < TI; ++r) {
-      const float4 v = *reinterpret_cast<const float4*>(A + (i0 + r) * mp + k);
+      const float4 v = *reinterpret_cast<const float4*>(A + (i0 + r) * LD + k);
       a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
     }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       if constexpr (TJ == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(B + (k + kk) * mp + j0);
+        const float4 v = *reinterpret_cast<const float4*>(B + (k + kk) * LD + j0);
         b[kk][0] = v.x; b[kk][1] = v.y; b[kk][2] = v.z; b[kk][3] = v.w;
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(B + (k + kk) * mp + j0);
+        const float2 v = *reinterpret_cast<const float2*>(B + (k + kk) * LD + j0);
         b[kk][0] = v.x; b[kk][1] = v.y;
       }
     }
@@ -202,11 +209,17 @@ __device__ __forceinline__ void mm_small(const float* A, const float* B, float* 
 #pragma unroll
         for (int c = 0; c < TJ; ++c) acc[r][c] = fmaf(a[r][kk], b[kk][c], acc[r][c]);
   }
+}
+
+template <int TI, int TJ, int LD>
+__device__ __forceinline__ void st_block(float* C, int i0, int j0, const float (&v)[TI][TJ]) {
 #pragma unroll
-  for (int r = 0; r < TI; ++r)
-#pragma unroll
-    for (int c = 0; c < TJ; ++c)
-      if (i0 + r < m && j0 + c < m) C[(i0 + r) * mp + j0 + c] = acc[r][c];
+  for (int r = 0; r < TI; ++r) {
+    if constexpr (TJ == 4)
+      *reinterpret_cast<float4*>(C + (i0 + r) * LD + j0) = make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
+    else
+      *reinterpret_cast<float2*>(C + (i0 + r) * LD + j0) = make_float2(v[r][0], v[r][1]);
+  }
 }
 
 __device__ __forceinline__ void cons_sync() { ptx::named_bar(kConsBar, kT); }
@@ -214,75 +227,102 @@ __device__ __forceinline__ void cons_sync() { ptx::named_bar(kConsBar, kT); }
 // Gram-space NS of one matrix, run by the consumers of the CTA whose item
 // completed it: sums the partial Grams, normalises, iterates and writes
 // Q / ||X0|| as the bf16 B-operand image (hi rows, then lo rows).  `gs`
-// holds four mp x mp fp32 matrices plus a few scalars.
-template <int TI, int TJ>
+// holds five LD x LD fp32 matrices (R, T, P, Q, Q') plus a few scalars.
+// Per step three phases: {T = R^2, P = aI + bR + cT}, {T = P R, Q' = P Q},
+// {R = T P} (the first step takes Q = P, the last needs neither R nor T).
+template <int TI, int TJ, int LD>
 __device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
-  const int m = p.m, mp = p.mp;
-  const int cw = t >> 5, lane = t & 31;
-  const int mm = mp * mp;
+  const int m = p.m;
+  constexpr int MM = LD * LD;
   float* R = gs;
-  float* T = gs + mm;
-  float* P = gs + 2 * mm;
-  float* Q = gs + 3 * mm;
-  float* sc = gs + 4 * mm;
-  for (int e = t; e < 4 * mm; e += kT) gs[e] = 0.f;
-  cons_sync();
+  float* T = gs + MM;
+  float* P = gs + 2 * MM;
+  float* Q = gs + 3 * MM;
+  float* Qn = gs + 4 * MM;
+  float* sc = gs + 5 * MM;
+  const int i0 = TI * (t >> 4), j0 = TJ * (t & 15);
   // R_0 (unnormalised) = sum of the item partials in block order; up to 8
-  // partial loads of an element are in flight together
+  // partial loads of an element are in flight together; the padding is zero
   const float* part = p.part + static_cast<size_t>(mat) * p.nb * p.pstride;
-  for (int e = t; e < m * m; e += kT) {
+  for (int e = t; e < MM; e += kT) {
+    const int i = e / LD, j = e - i * LD;
     float acc = 0.f;
-    for (int b0 = 0; b0 < p.nb; b0 += 8) {
-      float v[8];
+    if (i < m && j < m) {
+      const int src = i * m + j;
+      for (int b0 = 0; b0 < p.nb; b0 += 8) {
+        float v[8];
 #pragma unroll
-      for (int b = 0; b < 8; ++b)
-        v[b] = b0 + b < p.nb ? __ldcg(part + static_cast<size_t>(b0 + b) * p.pstride + e) : 0.f;
+        for (int b = 0; b < 8; ++b)
+          v[b] = b0 + b < p.nb ? __ldcg(part + static_cast<size_t>(b0 + b) * p.pstride + src) : 0.f;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) acc += v[b];
+        for (int b = 0; b < 8; ++b) acc += v[b];
+      }
     }
-    const int i = e / m, j = e - i * m;
-    R[i * mp + j] = acc;
+    R[e] = acc;
   }
   cons_sync();
-  if (t == 0) {
-    double tr = 0.0;                       // trace(X0 X0^T) = ||X0||_F^2
-    for (int i = 0; i < m; ++i) tr += static_cast<double>(R[i * mp + i]);
-    if (!isfinite(tr)) atomicOr(p.status, kDevNonfinite);
-    sc[0] = static_cast<float>(1.0 / (sqrt(tr) + static_cast<double>(p.eps)));
+  if (t < 32) {   // trace(X0 X0^T) = ||X0||_F^2, fp32, fixed reduction order
+    float v = (t < m ? R[t * LD + t] : 0.f) + (t + 32 < m ? R[(t + 32) * LD + t + 32] : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (t == 0) {
+      if (!isfinite(v)) atomicOr(p.status, kDevNonfinite);
+      sc[0] = 1.f / (sqrtf(v) + p.eps);
+    }
   }
   cons_sync();
   const float inv = sc[0];
   const float s2 = inv * inv;
-  for (int e = t; e < mm; e += kT) R[e] *= s2;
+  for (int e = t; e < MM; e += kT) R[e] *= s2;
   cons_sync();
   for (int k = 0; k < p.steps; ++k) {
     const float a = p.coef[k][0], b = p.coef[k][1], c = p.coef[k][2];
-    mm_small<TI, TJ>(R, R, T, m, mp, t);                    // T = R^2
-    cons_sync();
-    for (int i = cw; i < m; i += kT / 32)
-      for (int j = lane; j < m; j += 32) {
-        const int x = i * mp + j;
-        const float v = fmaf(b, R[x], c * T[x]) + (i == j ? a : 0.f);   // P = aI + bR + cR^2
-        P[x] = v;
-        if (k == 0) Q[x] = v;
-      }
-    cons_sync();
-    if (k + 1 < p.steps) {
-      mm_small<TI, TJ>(P, R, T, m, mp, t);                  // T = P R
-      cons_sync();
-      mm_small<TI, TJ>(T, P, R, m, mp, t);                  // R <- P R P
-      cons_sync();
+    const bool more = k + 1 < p.steps;
+    {   // T = R^2 (in registers), P = aI + bR + cR^2 (zero outside m x m)
+      float acc[TI][TJ], pv[TI][TJ];
+      mm_block<TI, TJ, LD>(R, R, i0, j0, acc);
+#pragma unroll
+      for (int r = 0; r < TI; ++r)
+#pragma unroll
+        for (int cc = 0; cc < TJ; ++cc) {
+          const int i = i0 + r, j = j0 + cc;
+          pv[r][cc] = (i < m && j < m)
+                          ? fmaf(b, R[i * LD + j], c * acc[r][cc]) + (i == j ? a : 0.f)
+                          : 0.f;
+        }
+      st_block<TI, TJ, LD>(P, i0, j0, pv);
+      if (k == 0) st_block<TI, TJ, LD>(Q, i0, j0, pv);
     }
-    if (k > 0) {
-      mm_small<TI, TJ>(P, Q, T, m, mp, t);                  // Q <- P Q
+    cons_sync();
+    if (more || k > 0) {
+      float acc[TI][TJ];
+      if (more) {
+        mm_block<TI, TJ, LD>(P, R, i0, j0, acc);     // T = P R
+        st_block<TI, TJ, LD>(T, i0, j0, acc);
+      }
+      if (k > 0) {
+        mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);     // Q' = P Q
+        st_block<TI, TJ, LD>(Qn, i0, j0, acc);
+      }
       cons_sync();
-      float* x = Q;
-      Q = T;
-      T = x;
+      if (k > 0) {
+        float* x = Q;
+        Q = Qn;
+        Qn = x;
+      }
+    }
+    if (more) {
+      float acc[TI][TJ];
+      mm_block<TI, TJ, LD>(T, P, i0, j0, acc);       // R <- P R P
+      st_block<TI, TJ, LD>(R, i0, j0, acc);
+      cons_sync();
     }
   }
-  if (p.steps == 0) {
-    for (int i = t; i < m; i += kT) Q[i * mp + i] = 1.f;
+  if (p.steps == 0) {   // Q = I (the whole buffer: nothing else wrote it)
+    for (int e = t; e < MM; e += kT) {
+      const int i = e / LD;
+      Q[e] = (i < m && e == i * LD + i) ? 1.f : 0.f;
+    }
     cons_sync();
   }
   // Q / ||X0|| as bf16 hi (rows 0..nmm-1) then lo, K-major 128-byte-swizzled
@@ -296,7 +336,7 @@ __device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int kx = k0 + j;
-      const float v = (q < m && kx < m) ? Q[q * mp + kx] * inv : 0.f;
+      const float v = (q < m && kx < m) ? Q[q * LD + kx] * inv : 0.f;
       h[j] = __float2bfloat16_rn(v);
       l[j] = __float2bfloat16_rn(v - __bfloat162float(h[j]));
     }
@@ -712,6 +752,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   float* gs = reinterpret_cast<float*>(sm + p.off_gs);
   SmallBars* B = reinterpret_cast<SmallBars*>(sm + p.off_bar);
   const Ctx ctx{B, p.status, p.timeout_ns};
+  // This launch's counters (ready-list length, claimed second- and first-
+  // phase items) are slot epoch % 64 of a ring that the previous launch
+  // zeroed; CTA 0 zeroes the slot of the next launch.
+  unsigned* lctr = p.ctr + (p.epoch % kSmallCtrSlots) * 4;
+  if (blockIdx.x == 0 && threadIdx.x < 4)
+    p.ctr[((p.epoch + 1) % kSmallCtrSlots) * 4 + threadIdx.x] = 0u;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m = p.m, n = p.n, nmm = p.nmm, wb = p.wb, NS = p.stages;
@@ -729,7 +775,6 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       ptx::mbar_init(&B->x_full[i], 1);
       ptx::mbar_init(&B->gram_full[i], 1);
       ptx::mbar_init(&B->xq_full[i], 1);
-      ptx::mbar_init(&B->xq_free[i], 1);
       ptx::mbar_init(&B->o_full[i], 1);
       ptx::mbar_init(&B->o_empty[i], kT / 32);
     }
@@ -752,9 +797,26 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 
   if (warp == 0) {
     // ======================= producer =======================
+    // First phase: items are claimed in increasing order from a launch-wide
+    // counter, so a CTA that spends time on a Gram-space step simply takes
+    // fewer items; each stage carries its item id for the consumers.
     Ring rg;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x) {
+    for (;;) {
+      int item = -1;
+      if (lane == 0) {
+        const unsigned c = atomicAdd(lctr + 2, 1u);
+        if (c < static_cast<unsigned>(p.items)) item = static_cast<int>(c);
+      }
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item < 0) {   // end token: one stage carrying -1
+        if (mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx) && lane == 0) {
+          B->stage_item[rg.stage] = -1;
+          ptx::mbar_arrive(&B->ring_full[rg.stage]);
+        }
+        rg.next(NS);
+        break;
+      }
       const int mat = item / p.nb, blk = item - mat * p.nb;
       const SmallSlice& S = slice_of(p, mat);
       const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
@@ -766,36 +828,52 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           ok = false;
           break;
         }
+        if (lane == 0) B->stage_item[rg.stage] = item;
         produce_p1(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes,
                    &B->ring_full[rg.stage], lane);
         rg.next(NS);
       }
+      if (!ok) break;
     }
     __syncthreads();   // ---- phase boundary ----
+    // Second phase: items are claimed in the order matrices were published
+    // (position j of the ready list, block blk), so no CTA waits for a late
+    // matrix while published work remains.
     ok = ok && !B->abort;
-    int k = 0;
-    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++k) {
+    for (int k = 0;; ++k) {
       const int b = k & 1;
-      const int mat = item / p.nb, blk = item - mat * p.nb;
-      const SmallSlice& S = slice_of(p, mat);
-      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-      const int64_t col0 = static_cast<int64_t>(blk) * wb;
-      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
-      int r = 0;
+      int item = -1;
       if (lane == 0) {
-        r = wait_ready(p.ready + mat, p.epoch, ctx) ? 1 : 0;
-        ptx::fence_proxy_async_global();
-        if (r) r = mwait(&B->xq_free[b], ((k >> 1) & 1) ^ 1u, ctx) ? 1 : 0;
-        if (r) {
+        // X0 buffer b is free once item k-2 has been consumed entirely
+        if (ok && mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) {
+          const unsigned next = atomicAdd(lctr + 1, 1u);
+          const int j = static_cast<int>(next / static_cast<unsigned>(p.nb));
+          if (j < p.total_mats) {
+            const int mat = wait_ready_pos(p.ready_list, j, p.epoch, ctx);
+            if (mat >= 0) item = mat * p.nb + static_cast<int>(next - j * p.nb);
+          }
+        }
+        B->slot[b] = item;
+        if (item >= 0) {
+          ptx::fence_proxy_async_global();
+          const int mat = item / p.nb;
           ptx::mbar_arrive_expect_tx(&B->xq_full[b], static_cast<uint32_t>(p.xbytes + p.qbytes));
           ptx::bulk_load(sm + b * p.xbytes, p.ximg + static_cast<size_t>(item) * p.xbytes,
                          static_cast<uint32_t>(p.xbytes), &B->xq_full[b]);
           ptx::bulk_load(sm + p.off_q + b * p.qbytes, p.qimg + static_cast<size_t>(mat) * p.qbytes,
                          static_cast<uint32_t>(p.qbytes), &B->xq_full[b]);
+        } else {
+          ptx::mbar_arrive(&B->xq_full[b]);   // wakes the other roles to finish
         }
       }
-      ok = __shfl_sync(0xffffffffu, r, 0) != 0;
-      if (!ok || !p.step_mode) continue;
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item < 0) break;
+      if (!p.step_mode) continue;
+      const int mat = item / p.nb, blk = item - mat * p.nb;
+      const SmallSlice& S = slice_of(p, mat);
+      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+      const int64_t col0 = static_cast<int64_t>(blk) * wb;
+      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
       const Geo g = geo_p2(p, S);
       for (int s = 0; s < g.count; ++s) {
         if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) {
@@ -812,10 +890,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, nmm);
     const uint32_t idesc_app = idesc_gram | (1u << 15);   // A MN-major
     if (lane == 0) {
-      int k = 0;
-      for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++k) {
+      for (int k = 0;; ++k) {
         const int b = k & 1;
         if (!mwait(&B->x_full[b], (k >> 1) & 1, ctx)) break;
+        if (B->x_item[b] < 0) break;
         ptx::tc_fence_after();
         const uint32_t sx = ptx::smem_u32(sm + b * p.xbytes);
         for (int kc = 0; kc < wb / 64; ++kc) {
@@ -830,11 +908,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
     __syncwarp();
     __syncthreads();   // ---- phase boundary ----
-    if (lane == 0 && !B->abort) {
-      int k = 0;
-      for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++k) {
+    if (lane == 0) {
+      for (int k = 0;; ++k) {
         const int b = k & 1;
         if (!mwait(&B->xq_full[b], (k >> 1) & 1, ctx)) break;
+        if (B->slot[b] < 0) break;
         if (!mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) break;
         ptx::tc_fence_after();
         const uint32_t sx = ptx::smem_u32(sm + b * p.xbytes);
@@ -851,7 +929,6 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           }
         }
         ptx::umma_commit(&B->o_full[b]);
-        ptx::umma_commit(&B->xq_free[b]);
       }
     }
     __syncwarp();
@@ -894,20 +971,47 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       cons_sync();
       if (t == 0)
-        B->last = (ok && !B->abort && arrive_is_last(p.arrive + mat, p.epoch, p.nb, p.status)) ? 1 : 0;
+        B->last = (ok && !B->abort &&
+                   claim(p.arrive + mat, p.epoch, p.status) + 1u == static_cast<unsigned>(p.nb))
+                      ? 1 : 0;
       cons_sync();
       if (B->last) {
         __threadfence();
-        if (m <= 32) gram_space<2, 2>(p, mat, gs, t);
-        else gram_space<4, 4>(p, mat, gs, t);
+        if (p.mp == 32) gram_space<2, 2, 32>(p, mat, gs, t);
+        else gram_space<4, 4, 64>(p, mat, gs, t);
         __threadfence();
         cons_sync();
-        if (t == 0) st_release_u32(p.ready + mat, p.epoch);
+        if (t == 0) {   // publish: next free position of the ready list
+          const unsigned pos = atomicAdd(lctr, 1u);
+          if (pos < static_cast<unsigned>(p.total_mats))
+            st_release_u64(p.ready_list + pos, (static_cast<unsigned long long>(p.epoch) << 32) |
+                                                   static_cast<unsigned>(mat));
+        }
       }
       cons_sync();
     };
     int k = 0;
-    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++k) {
+    for (;; ++k) {
+      // One thread takes the per-item decision (next item, end, abort) so
+      // that every consumer warp runs the same sequence of named barriers.
+      if (t == 0) {
+        int it = -2;
+        if (mwait(&B->ring_full[rg.stage], rg.phase, ctx)) it = B->stage_item[rg.stage];
+        B->cur_item = it;
+      }
+      cons_sync();
+      const int item = B->cur_item;
+      if (item == -2) {
+        ok = false;
+        break;
+      }
+      if (item < 0) {   // end token
+        mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
+        rg.next(NS);
+        break;
+      }
       const int b = k & 1;
       const int mat = item / p.nb, blk = item - mat * p.nb;
       const SmallSlice& S = slice_of(p, mat);
@@ -942,11 +1046,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           ptx::bulk_store(p.ximg + static_cast<size_t>(item) * p.xbytes, sx,
                           static_cast<uint32_t>(p.xbytes));
         ptx::bulk_commit();
+        B->x_item[b] = item;
         ptx::mbar_arrive(&B->x_full[b]);
       }
       if (prev >= 0) finish(prev, prevk, true);
       prev = item;
       prevk = k;
+    }
+    if (t == 0) {   // tell the MMA issuer that no tile follows
+      B->x_item[k & 1] = -1;
+      ptx::mbar_arrive(&B->x_full[k & 1]);
     }
     if (prev >= 0) finish(prev, prevk, false);
     if (t == 0) ptx::bulk_wait_group<0>();
@@ -954,9 +1063,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     ok = ok && !B->abort;
     const float decay = 1.f - p.lr * p.wd;
     const int q4 = warp & 3, set = cw >> 2;
-    k = 0;
-    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++k) {
+    for (k = 0; ok; ++k) {
       const int b = k & 1;
+      if (!mwait_warp(&B->xq_full[b], (k >> 1) & 1, ctx)) break;
+      const int item = B->slot[b];
+      if (item < 0) break;
       const int mat = item / p.nb, blk = item - mat * p.nb;
       const SmallSlice& S = slice_of(p, mat);
       const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
