@@ -206,37 +206,37 @@ bool small_shape(int64_t m) {
 
 // Work items and shared-memory carve-up of the small-m kernel for core shape
 // (m, n) over `mats` matrices; false when no carve-up fits one SM.  Shared
-// memory holds two X0 tiles of wb columns, two Q images, a ring of 24 KB
-// stages and the Gram-space matrices.  wb is the largest multiple of 128 that
-// fits (deeper rings first) such that four W rows fit one stage and the
-// item's O fits one 256-column TMEM buffer; then it shrinks while the launch
-// would leave SMs without an item.
+// memory holds two X0 tiles of wb columns, two Q images, a ring of stages
+// (one m x cw1 G + Mom tile or one m x 128 W tile each) and the Gram-space
+// matrices.  The ring gets about 96 KB; wb is the largest multiple of 128
+// that fits such that the item's O fits one 256-column TMEM buffer; then it
+// shrinks while the launch would leave SMs without an item.
 bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
   sp->m = static_cast<int>(m);
   sp->n = static_cast<int>(n);
   sp->mr = static_cast<int>(rup(m, 8));
   sp->mp = m <= 32 ? 32 : 64;
   sp->nmm = static_cast<int>(rup(m, 16));
-  sp->sc = 0;
+  sp->cw1 = m <= 32 ? 128 : 64;
   sp->qbytes = 2 * sp->nmm * 128;
   sp->pstride = static_cast<int>(rup(m * m, 4));
-  sp->stage_bytes = kSmallStageBytes;
+  sp->stage_bytes = static_cast<int>(
+      align_up(static_cast<size_t>(m) * std::max(sp->cw1 * 8, 128 * 4), 1024));
   const int tcol = static_cast<int>(rup(sp->nmm, 32));
-  const int64_t wcap = std::min<int64_t>(kSmallStageBytes / 16, 128 * (256 / tcol));
+  const int64_t wcap = 128 * (256 / tcol);
   const size_t gs = align_up(static_cast<size_t>(5) * sp->mp * sp->mp * 4 + 64, 16);
   const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns
-  int64_t wmax = 0;
-  for (int st = kSmallMaxStages; st >= 2 && wmax == 0; --st) {
+  int64_t chunks = 0;
+  for (sp->stages = std::max(2, std::min(kSmallMaxStages, (96 * 1024) / sp->stage_bytes));
+       sp->stages >= 2; --sp->stages) {
     const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) +
-                         static_cast<size_t>(st) * sp->stage_bytes + gs + 256 + 1024;
+                         static_cast<size_t>(sp->stages) * sp->stage_bytes + gs + 512 + 1024;
     if (fixed >= static_cast<size_t>(kSmallSmemLimit)) continue;
-    const int64_t chunks = static_cast<int64_t>((kSmallSmemLimit - fixed) / 2 / chunk) / 2 * 2;
-    if (chunks >= 2) {
-      wmax = std::min<int64_t>(chunks * 64, wcap);
-      sp->stages = st;
-    }
+    chunks = static_cast<int64_t>((kSmallSmemLimit - fixed) / 2 / chunk) / 2 * 2;
+    if (chunks >= 2) break;
   }
-  if (wmax == 0) return false;
+  if (chunks < 2) return false;
+  const int64_t wmax = std::min<int64_t>(chunks * 64, wcap);
   int64_t wb = std::min<int64_t>(wmax, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);
   while (wb > 128 && mats * cdiv(n, wb) < static_cast<int64_t>(sms)) wb -= 128;
@@ -249,7 +249,7 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
   sp->off_ring = sp->off_q + 2 * sp->qbytes;
   sp->off_gs = sp->off_ring + sp->stages * sp->stage_bytes;
   sp->off_bar = static_cast<int>(align_up(sp->off_gs + gs, 16));
-  sp->smem_bytes = sp->off_bar + 256 + 1024;
+  sp->smem_bytes = sp->off_bar + 512 + 1024;
   return sp->smem_bytes <= kSmallSmemLimit;
 }
 
@@ -418,6 +418,27 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, i
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map of a stored [cnt][rows][inner] tensor for unswizzled tile copies
+// of box {box_inner, box_rows, 1}; false when the layout is not TMA-legal.
+bool make_tile_map(CUtensorMap* map, const void* base, int dtype, int64_t inner, int64_t rows,
+                   int64_t cnt, int box_inner, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int64_t es = dtype == MUON_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(cnt)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * es),
+                           static_cast<cuuint64_t>(inner * rows * es)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype == MUON_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ---- launches ----------------------------------------------------------------------
 struct Launcher {
   cudaStream_t stream;
@@ -524,12 +545,12 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         for (int i : kv.second) large.push_back(reqs[i]);
         continue;
       }
-      for (size_t b = 0; b < kv.second.size(); b += kMaxSlices) {
+      for (size_t b = 0; b < kv.second.size(); b += kSmallMaxSlices) {
         smalls.emplace_back();
         SmallParams& sp = smalls.back();
         std::memset(&sp, 0, sizeof(sp));
         int64_t mats = 0;
-        const size_t e = std::min(kv.second.size(), b + kMaxSlices);
+        const size_t e = std::min(kv.second.size(), b + kSmallMaxSlices);
         for (size_t k = b; k < e; ++k) {
           const Req& q = reqs[kv.second[k]];
           SmallSlice& ss = sp.s[k - b];
@@ -541,19 +562,30 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           ss.trans = q.trans ? 1 : 0;
           ss.g_dtype = q.g_dtype;
           ss.w_dtype = q.w_dtype;
-          // bulk copies move whole stored rows: every row start and length
-          // must be a multiple of 16 bytes
-          const int64_t inner = q.c;   // contiguous extent of a stored row
-          ss.gbulk = (inner * static_cast<int64_t>(esize(q.g_dtype))) % 16 == 0 &&
-                     aligned(q.G, 16) &&
-                     (!step_mode || ((inner * 4) % 16 == 0 && aligned(q.Mom, 16)));
-          ss.wbulk = (inner * static_cast<int64_t>(esize(q.w_dtype))) % 16 == 0 && aligned(q.W, 16);
           ss.scale = scale_value(q.r, q.c, scale_rule);
           mats += q.B;
         }
         if (mats * cdiv(n, 128) >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         sp.n_slices = static_cast<int>(e - b);
         if (!small_plan(m, n, mats, dev->sms, &sp)) return MUON_ERR_UNSUPPORTED;
+        // TMA tile maps (stored layout): rows of 16-byte multiples, 16-byte
+        // aligned bases; otherwise the kernel copies element-wise
+        for (size_t k = b; k < e; ++k) {
+          const Req& q = reqs[kv.second[k]];
+          SmallSlice& ss = sp.s[k - b];
+          const int bi_g = q.trans ? sp.m : sp.cw1, br_g = q.trans ? sp.cw1 : sp.m;
+          const int bi_w = q.trans ? sp.m : 128, br_w = q.trans ? 128 : sp.m;
+          auto legal = [&](const void* ptr, int dt, int box_inner) {
+            const int64_t es = static_cast<int64_t>(esize(dt));
+            return aligned(ptr, 16) && (q.c * es) % 16 == 0 && (box_inner * es) % 16 == 0;
+          };
+          ss.gbulk = legal(q.G, q.g_dtype, bi_g) && (!step_mode || legal(q.Mom, MUON_F32, bi_g)) &&
+                     make_tile_map(&sp.tm[k - b][0], q.G, q.g_dtype, q.c, q.r, q.B, bi_g, br_g) &&
+                     (!step_mode ||
+                      make_tile_map(&sp.tm[k - b][1], q.Mom, MUON_F32, q.c, q.r, q.B, bi_g, br_g));
+          ss.wbulk = legal(q.W, q.w_dtype, bi_w) &&
+                     make_tile_map(&sp.tm[k - b][2], q.W, q.w_dtype, q.c, q.r, q.B, bi_w, br_w);
+        }
         sp.steps = ns.steps;
         for (int it = 0; it < ns.steps; ++it) {
           sp.coef[it][0] = ns.coeffs[3 * it];

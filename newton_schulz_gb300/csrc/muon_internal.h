@@ -111,12 +111,13 @@ struct GemmParams {
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
-constexpr int kSmallThreads = 320;         // warp 0 producer, warp 1 MMA, warps 2..9 consumers
+constexpr int kSmallThreads = 352;         // warp 0 loads, 1 MMA, 2..9 consumers, 10 stores
 constexpr int kSmallCons = 256;            // consumer threads
 constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O buffers [0,256), [256,512)
 constexpr int kSmallMaxStages = 4;
 constexpr int kSmallStageBytes = 24 * 1024;
 constexpr int kSmallCtrSlots = 64;         // ring of per-launch counter slots
+constexpr int kSmallMaxSlices = 16;        // slices per launch (their tensor maps are parameters)
 constexpr int kSmallSmemLimit = 227 * 1024;
 
 struct SmallSlice {
@@ -127,13 +128,16 @@ struct SmallSlice {
   int mat_base;      // index of its first matrix within the launch
   int trans;         // stored rows > cols
   int g_dtype, w_dtype;
-  int gbulk;         // G (and Mom) rows may be moved by 16-byte bulk copies
-  int wbulk;         // W rows may be moved by 16-byte bulk copies
+  int gbulk;         // G and Mom tiles move by TMA (tensor maps tm[.][0], tm[.][1])
+  int wbulk;         // W tiles move by TMA (tensor map tm[.][2])
   float scale;       // update scale s(rows, cols)
 };
 
 struct SmallParams {
-  SmallSlice s[kMaxSlices];
+  // per slice: tiles of G and Mom (box: cw1 X columns x m rows) and of W (box:
+  // 128 X columns x m rows), in the stored layout
+  alignas(128) CUtensorMap tm[kSmallMaxSlices][3];
+  SmallSlice s[kSmallMaxSlices];
   int n_slices;
   int m, n;          // core shape, m <= n
   int mr;            // X rows held: m rounded up to 8
@@ -141,7 +145,7 @@ struct SmallParams {
   int nmm;           // MMA N (and apply K): m rounded up to 16
   int wb;            // X columns per work item (multiple of 128)
   int nb;            // work items per matrix
-  int sc;            // transposed layout: X columns per ring stage (multiple of 64)
+  int cw1;           // X columns per first-phase stage (128, or 64 when m > 32)
   int stages;        // ring stages
   int total_mats;
   int items;         // total_mats * nb

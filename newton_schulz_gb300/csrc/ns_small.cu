@@ -47,14 +47,14 @@ constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
 
 // Shared-memory control block: mbarriers, the TMEM slot and CTA flags.
 struct SmallBars {
-  uint64_t ring_full[kSmallMaxStages], ring_empty[kSmallMaxStages];
+  uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], ring_empty[kSmallMaxStages];
   uint64_t x_full[2], gram_full[2], xq_full[2];
   uint64_t o_full[2], o_empty[2];
   uint32_t tslot;
   int last;
   int abort;
   int slot[2];   // second phase: item held by X0 buffer b (-1: no more items)
-  int stage_item[kSmallMaxStages];   // first phase: item of each ring stage (-1: no more)
+  int desc[kSmallMaxStages][3];      // per stage: kind, item (-1: none), first X column
   int x_item[2];     // first phase: item whose X0 tile b is complete (-1: no more)
   int cur_item;      // first phase: the consumers' current item (-2: abort)
 };
@@ -166,10 +166,6 @@ __device__ __forceinline__ float ld_elem(const void* base, int dtype, int64_t e)
                     : __bfloat162float(static_cast<const __nv_bfloat16*>(base)[e]);
 }
 
-__device__ __forceinline__ void st_elem(void* base, int dtype, int64_t e, float v) {
-  if (dtype == 0) static_cast<float*>(base)[e] = v;
-  else static_cast<__nv_bfloat16*>(base)[e] = __float2bfloat16_rn(v);
-}
 
 
 // Block of C = A B owned by consumer thread t: rows TI (t / 16), columns
@@ -346,169 +342,48 @@ __device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
   }
 }
 
-// ---- ring-stage geometry (producer and consumers derive the same) --------------------
-// A row-major matrix streams as groups of whole rows of the item (one bulk
-// copy per row and tensor, wb columns long); a transposed matrix, whose item
-// is one contiguous block, as groups of columns.
-struct Geo {
-  int rows;    // rows per stage (row-major)
-  int cols;    // X columns per stage (transposed)
-  int count;   // stages per item
-};
+// ---- stage layout ---------------------------------------------------------------------
+// A stage holds one tile of the stored tensor(s) for a range of X columns:
+//   first phase:  G tile (cw1 X columns) at byte 0, Mom tile at mom_off;
+//   second phase: W tile (128 X columns) at byte 0.
+// Row-major matrices give [m][cols] tiles (row pitch cols), transposed ones
+// [cols][m] tiles (stored rows of m).  TMA fills out-of-matrix elements with
+// zero and clips them on the way back.
+enum StageKind : int { kStageP1 = 0, kStageP2 = 1, kStageP1End = 2, kStageEnd = 3 };
 
-__device__ __forceinline__ Geo geo_p1(const SmallParams& p, const SmallSlice& S) {
-  const int per = (S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0);   // bytes per element
-  Geo g;
-  if (!S.trans) {
-    g.rows = min(p.m, max(1, p.stage_bytes / (p.wb * per)));
-    g.cols = p.wb;
-    g.count = (p.m + g.rows - 1) / g.rows;
-  } else {
-    g.rows = p.m;
-    g.cols = min(p.wb, max(16, p.stage_bytes / (p.m * per) / 16 * 16));
-    g.count = (p.wb + g.cols - 1) / g.cols;
-  }
-  return g;
+__device__ __forceinline__ uint32_t mom_off(const SmallParams& p, const SmallSlice& S) {
+  return static_cast<uint32_t>(p.m * p.cw1 * (S.g_dtype == 0 ? 4 : 2));
 }
 
-// Second phase: 8 or 4 W rows per stage (the TMEM read width), or multiples
-// of 32 columns (one TMEM lane quarter) when transposed.
-__device__ __forceinline__ Geo geo_p2(const SmallParams& p, const SmallSlice& S) {
-  const int esw = S.w_dtype == 0 ? 4 : 2;
-  Geo g;
-  if (!S.trans) {
-    g.rows = 8 * p.wb * esw <= p.stage_bytes ? 8 : 4;
-    g.cols = p.wb;
-    g.count = (p.m + g.rows - 1) / g.rows;
-  } else {
-    g.rows = p.m;
-    g.cols = min(p.wb, max(32, p.stage_bytes / (p.m * esw) / 32 * 32));
-    g.count = (p.wb + g.cols - 1) / g.cols;
-  }
-  return g;
-}
-
-// ---- producer (warp 0) ------------------------------------------------------------
-// Stage s of a first-phase item: G, then Mom at byte rows * wb * esize(G)
-// (row-major: rows [s*rows, ...) of the item, each wb columns) or at byte
-// cols * m * esize(G) (transposed: X columns [s*cols, ...), stored rows of m).
-__device__ void produce_p1(const SmallParams& p, const SmallSlice& S, const Geo& g, int s,
-                           int64_t moff, int64_t col0, int nci, uint8_t* st, uint64_t* full,
-                           int lane) {
-  const int m = p.m, n = p.n, wb = p.wb;
-  const int esg = S.g_dtype == 0 ? 4 : 2;
-  int r0 = 0, r1 = 0, c0 = 0, ncs = 0;
-  if (!S.trans) {
-    r0 = s * g.rows;
-    r1 = min(m, r0 + g.rows);
-  } else {
-    c0 = s * g.cols;
-    ncs = min(g.cols, nci - c0);
-  }
-  const uint32_t mom_off =
-      static_cast<uint32_t>((S.trans ? g.cols * m : g.rows * wb) * esg);
-  uint32_t tx = 0;
-  if (S.gbulk) {
-    const int per = esg + (p.step_mode ? 4 : 0);
-    tx = S.trans ? (ncs > 0 ? static_cast<uint32_t>(ncs * m * per) : 0u)
-                 : static_cast<uint32_t>((r1 - r0) * nci * per);
-  } else {
-    // element-wise copy into the same layout (rows not 16-byte aligned)
-    const int tot = S.trans ? (ncs > 0 ? ncs * m : 0) : (r1 - r0) * nci;
-    for (int idx = lane; idx < tot; idx += 32) {
-      int64_t e;
-      uint32_t so;
-      if (!S.trans) {
-        const int rl = idx / nci, c = idx - rl * nci;
-        e = moff + static_cast<int64_t>(r0 + rl) * n + col0 + c;
-        so = static_cast<uint32_t>(rl * wb + c);
-      } else {
-        e = moff + (col0 + c0) * m + idx;
-        so = static_cast<uint32_t>(idx);
-      }
-      if (esg == 4) reinterpret_cast<float*>(st)[so] = static_cast<const float*>(S.G)[e];
-      else reinterpret_cast<__nv_bfloat16*>(st)[so] = static_cast<const __nv_bfloat16*>(S.G)[e];
-      if (p.step_mode) reinterpret_cast<float*>(st + mom_off)[so] = S.Mom[e];
+// Element-wise tile copy between global memory and a stage (slices whose rows
+// are not TMA-legal): `cols` X columns from column gj0; to_smem also writes
+// zero outside the matrix.
+template <bool TO_SMEM>
+__device__ void copy_tile(const SmallParams& p, const SmallSlice& S, int dtype, void* gbase,
+                          int64_t moff, int64_t gj0, int cols, uint8_t* st, int lane) {
+  const int m = p.m, n = p.n;
+  const int es = dtype == 0 ? 4 : 2;
+  for (int idx = lane; idx < m * cols; idx += 32) {
+    int r, c;
+    if (!S.trans) {
+      r = idx / cols;
+      c = idx - r * cols;
+    } else {
+      c = idx / m;
+      r = idx - c * m;
     }
-  }
-  __syncwarp();
-  if (lane == 0) {
-    if (tx) ptx::mbar_arrive_expect_tx(full, tx);
-    else ptx::mbar_arrive(full);
-  }
-  __syncwarp();
-  if (!tx) return;
-  if (!S.trans) {
-    for (int r = r0 + lane; r < r1; r += 32) {
-      const int64_t e = moff + static_cast<int64_t>(r) * n + col0;
-      ptx::bulk_load(st + (r - r0) * wb * esg, static_cast<const uint8_t*>(S.G) + e * esg,
-                     static_cast<uint32_t>(nci * esg), full);
-      if (p.step_mode)
-        ptx::bulk_load(st + mom_off + (r - r0) * wb * 4, S.Mom + e,
-                       static_cast<uint32_t>(nci * 4), full);
+    const uint32_t so = static_cast<uint32_t>(S.trans ? c * m + r : r * cols + c);
+    const bool in = gj0 + c < n;
+    const int64_t e = moff + (S.trans ? (gj0 + c) * m + r : static_cast<int64_t>(r) * n + gj0 + c);
+    if (TO_SMEM) {
+      if (es == 4) reinterpret_cast<float*>(st)[so] = in ? static_cast<const float*>(gbase)[e] : 0.f;
+      else
+        reinterpret_cast<__nv_bfloat16*>(st)[so] =
+            in ? static_cast<const __nv_bfloat16*>(gbase)[e] : __float2bfloat16_rn(0.f);
+    } else if (in) {
+      if (es == 4) static_cast<float*>(gbase)[e] = reinterpret_cast<const float*>(st)[so];
+      else static_cast<__nv_bfloat16*>(gbase)[e] = reinterpret_cast<const __nv_bfloat16*>(st)[so];
     }
-  } else if (lane == 0) {
-    const int64_t e = moff + (col0 + c0) * m;
-    ptx::bulk_load(st, static_cast<const uint8_t*>(S.G) + e * esg,
-                   static_cast<uint32_t>(ncs * m * esg), full);
-    if (p.step_mode)
-      ptx::bulk_load(st + mom_off, S.Mom + e, static_cast<uint32_t>(ncs * m * 4), full);
-  }
-}
-
-// Stage s of a second-phase item: W rows [s*rows, ...) (row-major, wb columns
-// each) or X columns [s*cols, ...) (transposed).
-__device__ void produce_p2(const SmallParams& p, const SmallSlice& S, const Geo& g, int s,
-                           int64_t moff, int64_t col0, int nci, uint8_t* st, uint64_t* full,
-                           int lane) {
-  const int m = p.m, n = p.n, wb = p.wb;
-  const int esw = S.w_dtype == 0 ? 4 : 2;
-  int r0 = 0, r1 = 0, c0 = 0, ncs = 0;
-  if (!S.trans) {
-    r0 = s * g.rows;
-    r1 = min(m, r0 + g.rows);
-  } else {
-    c0 = s * g.cols;
-    ncs = min(g.cols, nci - c0);
-  }
-  uint32_t tx = 0;
-  if (S.wbulk) {
-    tx = S.trans ? (ncs > 0 ? static_cast<uint32_t>(ncs * m * esw) : 0u)
-                 : static_cast<uint32_t>((r1 - r0) * nci * esw);
-  } else {
-    const int tot = S.trans ? (ncs > 0 ? ncs * m : 0) : (r1 - r0) * nci;
-    for (int idx = lane; idx < tot; idx += 32) {
-      int64_t e;
-      uint32_t so;
-      if (!S.trans) {
-        const int rl = idx / nci, c = idx - rl * nci;
-        e = moff + static_cast<int64_t>(r0 + rl) * n + col0 + c;
-        so = static_cast<uint32_t>(rl * wb + c);
-      } else {
-        e = moff + (col0 + c0) * m + idx;
-        so = static_cast<uint32_t>(idx);
-      }
-      if (esw == 4) reinterpret_cast<float*>(st)[so] = static_cast<const float*>(S.W)[e];
-      else reinterpret_cast<__nv_bfloat16*>(st)[so] = static_cast<const __nv_bfloat16*>(S.W)[e];
-    }
-  }
-  __syncwarp();
-  if (lane == 0) {
-    if (tx) ptx::mbar_arrive_expect_tx(full, tx);
-    else ptx::mbar_arrive(full);
-  }
-  __syncwarp();
-  if (!tx) return;
-  if (!S.trans) {
-    for (int r = r0 + lane; r < r1; r += 32) {
-      const int64_t e = moff + static_cast<int64_t>(r) * n + col0;
-      ptx::bulk_load(st + (r - r0) * wb * esw, static_cast<const uint8_t*>(S.W) + e * esw,
-                     static_cast<uint32_t>(nci * esw), full);
-    }
-  } else if (lane == 0) {
-    const int64_t e = moff + (col0 + c0) * m;
-    ptx::bulk_load(st, static_cast<const uint8_t*>(S.W) + e * esw,
-                   static_cast<uint32_t>(ncs * m * esw), full);
   }
 }
 
@@ -532,6 +407,11 @@ __device__ __forceinline__ void load8_smem(const uint8_t* base, int so, float* v
   }
 }
 
+__device__ __forceinline__ void store8_smem_f32(uint8_t* base, int so, const float* v) {
+  *reinterpret_cast<float4*>(base + so * 4) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(base + so * 4 + 16) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 // Momentum for 8 elements; d = the NS input (Nesterov or plain momentum).
 template <bool STEP>
 __device__ __forceinline__ void momentum8(const SmallParams& p, const float* gv, float* mo,
@@ -547,84 +427,43 @@ __device__ __forceinline__ void momentum8(const SmallParams& p, const float* gv,
   }
 }
 
-__device__ __forceinline__ void store_mom8(float* base, int64_t e, int nv, bool vec, const float* v) {
-  if (vec && nv == 8) {
-    __stcs(reinterpret_cast<float4*>(base + e), make_float4(v[0], v[1], v[2], v[3]));
-    __stcs(reinterpret_cast<float4*>(base + e + 4), make_float4(v[4], v[5], v[6], v[7]));
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < nv) base[e + j] = v[j];
-  }
-}
-
-// Row-major stage: rows [r0, r1) x item columns [0, wb); X0 rows of the item's
-// tile, zero beyond the matrix.  Groups of 8 columns; the row index comes from
-// a float reciprocal (exact for these sizes).
+// Stage of X columns [c0, c0 + cw1) of the item: M' written back in place
+// (the storer warp moves it out), X0 = bf16(D) into the item's tile.
 template <int ESG, bool STEP>
-__device__ void consume_p1_rows(const SmallParams& p, const SmallSlice& S, int r0, int r1,
-                                int rows_alloc, int64_t moff, int64_t col0, int nci,
-                                const uint8_t* st, uint8_t* sx, int t) {
-  const int wb = p.wb, n = p.n;
+__device__ void consume_p1(const SmallParams& p, const SmallSlice& S, int c0, uint8_t* st,
+                           uint8_t* sx, int t) {
+  const int m = p.m, cw = p.cw1;
   const int chunk_bytes = p.mr * 128;
-  const int gpr = wb >> 3;
-  const float inv_gpr = 1.f / static_cast<float>(gpr);
-  const uint8_t* smom = st + rows_alloc * wb * ESG;
-  const bool vec = S.gbulk != 0;
-  const int ng = (r1 - r0) * gpr;
-  for (int g = t; g < ng; g += kT) {
-    const int rl = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_gpr);
-    const int c8 = (g - rl * gpr) << 3;
-    const int nv = min(8, nci - c8);
-    float d[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) d[j] = 0.f;
-    if (nv > 0) {
-      const int so = rl * wb + c8;
-      float gv[8], mo[8];
+  uint8_t* smom = st + mom_off(p, S);
+  if (!S.trans) {
+    const int gpr = cw >> 3;
+    const int sh = gpr == 16 ? 4 : 3;                  // cw1 is 128 or 64
+    for (int g = t; g < m * gpr; g += kT) {
+      const int r = g >> sh, c8 = (g & (gpr - 1)) << 3;
+      const int so = r * cw + c8;
+      float gv[8], mo[8], d[8];
       load8_smem<ESG>(st, so, gv);
       if constexpr (STEP) load8_smem<4>(smom, so, mo);
       momentum8<STEP>(p, gv, mo, d);
-      if constexpr (STEP)
-        store_mom8(S.Mom, moff + static_cast<int64_t>(r0 + rl) * n + col0 + c8, nv, vec, mo);
-      if (nv < 8) {
+      if constexpr (STEP) store8_smem_f32(smom, so, mo);
+      const int ci = c0 + c8;
+      uint4 q;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (j >= nv) d[j] = 0.f;
-      }
+      for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
+      *reinterpret_cast<uint4*>(sx + (ci >> 6) * chunk_bytes +
+                                ptx::sw128_offset(r, (ci & 63) * 2)) = q;
     }
-    uint4 q;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
-    *reinterpret_cast<uint4*>(sx + (c8 >> 6) * chunk_bytes +
-                              ptx::sw128_offset(r0 + rl, (c8 & 63) * 2)) = q;
-  }
-}
-
-// Transposed stage: X columns [c0, c0 + cols) of the item (stored rows of m
-// contiguous elements); groups of 8 rows of one column.
-template <int ESG, bool STEP>
-__device__ void consume_p1_cols(const SmallParams& p, const SmallSlice& S, int c0, int cols,
-                                int cols_alloc, int64_t moff, int64_t col0, int nci,
-                                const uint8_t* st, uint8_t* sx, int t) {
-  const int m = p.m;
-  const int chunk_bytes = p.mr * 128;
-  const int ig = p.mr >> 3;
-  const float inv_ig = 1.f / static_cast<float>(ig);
-  const uint8_t* smom = st + cols_alloc * m * ESG;   // where the producer put Mom
-  const bool vec = S.gbulk != 0;
-  for (int g = t; g < cols * ig; g += kT) {
-    const int c = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_ig);
-    const int r = (g - c * ig) << 3;
-    const int nv = c0 + c < nci ? min(8, m - r) : 0;
-    float d[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) d[j] = 0.f;
-    if (nv > 0) {
+  } else {
+    const int ig = p.mr >> 3;
+    const float inv_ig = 1.f / static_cast<float>(ig);
+    for (int g = t; g < cw * ig; g += kT) {
+      const int c = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_ig);
+      const int r = (g - c * ig) << 3;
+      const int nv = min(8, m - r);
       const int so = c * m + r;
-      float gv[8], mo[8];
-      if (vec && nv == 8) {
+      float gv[8], mo[8], d[8];
+      if (nv == 8 && S.gbulk) {
         load8_smem<ESG>(st, so, gv);
         if constexpr (STEP) load8_smem<4>(smom, so, mo);
       } else {
@@ -635,110 +474,93 @@ __device__ void consume_p1_cols(const SmallParams& p, const SmallSlice& S, int c
         }
       }
       momentum8<STEP>(p, gv, mo, d);
-      if constexpr (STEP) store_mom8(S.Mom, moff + (col0 + c0 + c) * m + r, nv, vec, mo);
-      if (nv < 8) {
+      if constexpr (STEP) {
+        if (nv == 8 && S.gbulk) {
+          store8_smem_f32(smom, so, mo);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (j >= nv) d[j] = 0.f;
+          for (int j = 0; j < 8; ++j)
+            if (j < nv) reinterpret_cast<float*>(smom)[so + j] = mo[j];
+        }
       }
-    }
-    const int ci = c0 + c;
-    uint8_t* colp = sx + (ci >> 6) * chunk_bytes;
-    const uint32_t byte = (ci & 63) * 2;
+      const int ci = c0 + c;
+      uint8_t* colp = sx + (ci >> 6) * chunk_bytes;
+      const uint32_t byte = (ci & 63) * 2;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<__nv_bfloat16*>(colp + ptx::sw128_offset(r + j, byte)) =
-          __float2bfloat16_rn(d[j]);
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<__nv_bfloat16*>(colp + ptx::sw128_offset(r + j, byte)) =
+            __float2bfloat16_rn(j < nv ? d[j] : 0.f);
+    }
   }
 }
 
-template <int ESG, bool STEP>
-__device__ __forceinline__ void consume_p1(const SmallParams& p, const SmallSlice& S, const Geo& g,
-                                           int s, int64_t moff, int64_t col0, int nci,
-                                           const uint8_t* st, uint8_t* sx, int t) {
-  if (!S.trans) {
-    const int r0 = s * g.rows;
-    consume_p1_rows<ESG, STEP>(p, S, r0, min(p.m, r0 + g.rows), g.rows, moff, col0, nci, st, sx, t);
-  } else {
-    consume_p1_cols<ESG, STEP>(p, S, s * g.cols, min(g.cols, p.wb - s * g.cols), g.cols, moff,
-                               col0, nci, st, sx, t);
-  }
-}
-
-__device__ void consume_p1_any(const SmallParams& p, const SmallSlice& S, const Geo& g, int s,
-                               int64_t moff, int64_t col0, int nci, const uint8_t* st,
+__device__ void consume_p1_any(const SmallParams& p, const SmallSlice& S, int c0, uint8_t* st,
                                uint8_t* sx, int t) {
   if (S.g_dtype == 0) {
-    if (p.step_mode) consume_p1<4, true>(p, S, g, s, moff, col0, nci, st, sx, t);
-    else consume_p1<4, false>(p, S, g, s, moff, col0, nci, st, sx, t);
+    if (p.step_mode) consume_p1<4, true>(p, S, c0, st, sx, t);
+    else consume_p1<4, false>(p, S, c0, st, sx, t);
   } else {
-    if (p.step_mode) consume_p1<2, true>(p, S, g, s, moff, col0, nci, st, sx, t);
-    else consume_p1<2, false>(p, S, g, s, moff, col0, nci, st, sx, t);
+    if (p.step_mode) consume_p1<2, true>(p, S, c0, st, sx, t);
+    else consume_p1<2, false>(p, S, c0, st, sx, t);
   }
 }
 
 // ---- consumers: second-phase stage -------------------------------------------------------
-// Row-major: W rows [q0, q0 + R) of the item, R = 8 or 4 consecutive TMEM
-// columns of O per tile.  Warp (set, q4) covers lanes 32 q4.. of tiles set,
-// set + 2, ...
-template <int R>
-__device__ void epi_rows(const SmallParams& p, const SmallSlice& S, int q0, int64_t moff,
-                         int64_t col0, int nci, const uint8_t* st, uint32_t obuf, int set, int q4,
-                         int lane, float decay, float stepk) {
-  const int m = p.m, n = p.n, wb = p.wb, tcol = (p.nmm + 31) & ~31;
-  for (int tt = set; tt < wb / 128; tt += 2) {
-    uint32_t r[R];
-    if constexpr (R == 8) ptx::tmem_ld_32x32b_x8(obuf + tt * tcol + q0 + (static_cast<uint32_t>(32 * q4) << 16), r);
-    else ptx::tmem_ld_32x32b_x4(obuf + tt * tcol + q0 + (static_cast<uint32_t>(32 * q4) << 16), r);
+template <typename WT>
+__device__ __forceinline__ float w_ld(const WT* p, int i) {
+  if constexpr (sizeof(WT) == 4) return p[i];
+  else return __bfloat162float(p[i]);
+}
+
+template <typename WT>
+__device__ __forceinline__ void w_st(WT* p, int i, float v) {
+  if constexpr (sizeof(WT) == 4) p[i] = v;
+  else p[i] = __float2bfloat16_rn(v);
+}
+
+// 128-column W tile of tile index `tile` of the item: W' = decay W - stepk O
+// (or O) written back in place.  Warp (set, q4) owns lanes 32 q4.. (the
+// columns) and rows 16 set + 32 h .. + 16 of O in TMEM.
+template <typename WT, bool STEP>
+__device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S, int tile,
+                                      uint8_t* st, uint32_t obuf, int set, int q4, int lane,
+                                      float decay, float stepk) {
+  const int m = p.m, nmm = p.nmm, tcol = (nmm + 31) & ~31;
+  WT* ws = reinterpret_cast<WT*>(st);
+  const int col = 32 * q4 + lane;
+  for (int h = 0; h < 2; ++h) {
+    const int cq = 16 * set + 32 * h;
+    if (cq >= nmm) continue;
+    uint32_t r[16];
+    ptx::tmem_ld_32x32b_x16(obuf + tile * tcol + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
     ptx::tmem_ld_wait();
-    const int col = tt * 128 + 32 * q4 + lane;
-    if (col >= nci) continue;
-    const int64_t gj = col0 + col;
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      const int q = q0 + j;
+    for (int j = 0; j < 16; ++j) {
+      const int q = cq + j;
       if (q < m) {
+        const int so = S.trans ? col * m + q : q * 128 + col;
         const float o = __uint_as_float(r[j]);
-        float v = o;
-        if (p.step_mode) v = fmaf(decay, ld_elem(st, S.w_dtype, j * wb + col), -stepk * o);
-        st_elem(S.W, S.w_dtype, moff + static_cast<int64_t>(q) * n + gj, v);
+        w_st(ws, so, STEP ? fmaf(decay, w_ld(ws, so), -stepk * o) : o);
       }
     }
   }
 }
 
-// Transposed: X columns [c0, c0 + cols) in units of 32 (one TMEM lane
-// quarter); the two warp sets split the rows q.
-__device__ void epi_cols(const SmallParams& p, const SmallSlice& S, int c0, int cols,
-                         int64_t moff, int64_t col0, int nci, const uint8_t* st, uint32_t obuf,
-                         int set, int q4, int lane, float decay, float stepk) {
-  const int m = p.m, nmm = p.nmm, tcol = (nmm + 31) & ~31;
-  for (int u = 0; u < cols; u += 32) {
-    const int cu = c0 + u;
-    if (((cu >> 5) & 3) != q4) continue;
-    const int tile = cu >> 7;
-    const int col = cu + lane;
-    const bool live = col < nci;
-    const int64_t gj = col0 + col;
-    for (int h = 0; h < 2; ++h) {
-      const int cq = 16 * set + 32 * h;
-      if (cq >= nmm) continue;
-      uint32_t r[16];
-      ptx::tmem_ld_32x32b_x16(obuf + tile * tcol + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
-      ptx::tmem_ld_wait();
-      if (!live) continue;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int q = cq + j;
-        if (q < m) {
-          const float o = __uint_as_float(r[j]);
-          float v = o;
-          if (p.step_mode) v = fmaf(decay, ld_elem(st, S.w_dtype, (col - c0) * m + q), -stepk * o);
-          st_elem(S.W, S.w_dtype, moff + gj * m + q, v);
-        }
-      }
-    }
+__device__ void epi_tile_any(const SmallParams& p, const SmallSlice& S, int tile, uint8_t* st,
+                             uint32_t obuf, int set, int q4, int lane, float decay, float stepk) {
+  if (S.w_dtype == 0) {
+    if (p.step_mode) epi_tile<float, true>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
+    else epi_tile<float, false>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
+  } else {
+    if (p.step_mode) epi_tile<__nv_bfloat16, true>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
+    else epi_tile<__nv_bfloat16, false>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
   }
+}
+
+// TMA coordinates of the tile at X column gj0 of local matrix z.
+__device__ __forceinline__ void tile_xy(const SmallSlice& S, int64_t gj0, int& x, int& y) {
+  x = S.trans ? 0 : static_cast<int>(gj0);
+  y = S.trans ? static_cast<int>(gj0) : 0;
 }
 
 }  // namespace
@@ -763,13 +585,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const int m = p.m, n = p.n, nmm = p.nmm, wb = p.wb, NS = p.stages;
   const int chunk_bytes = p.mr * 128;
   const int tiles = wb / 128;
+  const int s1 = wb / p.cw1;               // first-phase stages per item
   const int64_t mn = static_cast<int64_t>(m) * n;
   const int tcol = (nmm + 31) & ~31;       // TMEM columns of O per 128-column tile
 
   if (tid == 0) {
     for (int i = 0; i < kSmallMaxStages; ++i) {
       ptx::mbar_init(&B->ring_full[i], 1);
-      ptx::mbar_init(&B->ring_empty[i], kT / 32);
+      ptx::mbar_init(&B->cons_done[i], kT / 32);
+      ptx::mbar_init(&B->ring_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&B->x_full[i], 1);
@@ -796,12 +620,66 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const uint32_t tmem = B->tslot;
 
   if (warp == 0) {
-    // ======================= producer =======================
-    // First phase: items are claimed in increasing order from a launch-wide
-    // counter, so a CTA that spends time on a Gram-space step simply takes
-    // fewer items; each stage carries its item id for the consumers.
+    // ======================= producer (loads) =======================
     Ring rg;
     bool ok = true;
+    // Hands the next stage to the consumers: descriptor, then the tile(s).
+    auto put = [&](int kind, int item, int c0, bool load_g, bool load_w) -> bool {
+      if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) return false;
+      uint8_t* st = ring + rg.stage * p.stage_bytes;
+      uint64_t* full = &B->ring_full[rg.stage];
+      uint32_t tx = 0;
+      int si = -1;
+      int64_t moff = 0, gj0 = 0;
+      if (item >= 0) {
+        const int mat = item / p.nb;
+        si = 0;
+        while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
+        const SmallSlice& S = p.s[si];
+        moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+        gj0 = static_cast<int64_t>(item - mat * p.nb) * wb + c0;
+        const int cols = load_g ? p.cw1 : 128;
+        if ((load_g && !S.gbulk) || (load_w && !S.wbulk)) {
+          if (load_g) {
+            copy_tile<true>(p, S, S.g_dtype, const_cast<void*>(S.G), moff, gj0, cols, st, lane);
+            if (p.step_mode) copy_tile<true>(p, S, 0, S.Mom, moff, gj0, cols, st + mom_off(p, S), lane);
+          } else {
+            copy_tile<true>(p, S, S.w_dtype, S.W, moff, gj0, cols, st, lane);
+          }
+        } else if (load_g) {
+          tx = static_cast<uint32_t>(p.m * cols * ((S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0)));
+        } else if (load_w) {
+          tx = static_cast<uint32_t>(p.m * cols * (S.w_dtype == 0 ? 4 : 2));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        B->desc[rg.stage][0] = kind;
+        B->desc[rg.stage][1] = item;
+        B->desc[rg.stage][2] = c0;
+        if (tx) {
+          const SmallSlice& S = p.s[si];
+          const int z = item / p.nb - S.mat_base;
+          int x, y;
+          tile_xy(S, gj0, x, y);
+          ptx::mbar_arrive_expect_tx(full, tx);
+          if (load_g) {
+            ptx::tma_load_3d(st, &p.tm[si][0], full, x, y, z);
+            if (p.step_mode) ptx::tma_load_3d(st + mom_off(p, S), &p.tm[si][1], full, x, y, z);
+          } else {
+            ptx::tma_load_3d(st, &p.tm[si][2], full, x, y, z);
+          }
+        } else {
+          ptx::mbar_arrive(full);
+        }
+      }
+      __syncwarp();
+      rg.next(NS);
+      return true;
+    };
+    // First phase: items are claimed in increasing order from a launch-wide
+    // counter, so a CTA that spends time on a Gram-space step simply takes
+    // fewer items.
     for (;;) {
       int item = -1;
       if (lane == 0) {
@@ -809,43 +687,22 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         if (c < static_cast<unsigned>(p.items)) item = static_cast<int>(c);
       }
       item = __shfl_sync(0xffffffffu, item, 0);
-      if (item < 0) {   // end token: one stage carrying -1
-        if (mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx) && lane == 0) {
-          B->stage_item[rg.stage] = -1;
-          ptx::mbar_arrive(&B->ring_full[rg.stage]);
-        }
-        rg.next(NS);
-        break;
-      }
-      const int mat = item / p.nb, blk = item - mat * p.nb;
-      const SmallSlice& S = slice_of(p, mat);
-      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-      const int64_t col0 = static_cast<int64_t>(blk) * wb;
-      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
-      const Geo g = geo_p1(p, S);
-      for (int s = 0; s < g.count; ++s) {
-        if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) B->stage_item[rg.stage] = item;
-        produce_p1(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes,
-                   &B->ring_full[rg.stage], lane);
-        rg.next(NS);
-      }
+      if (item < 0) break;
+      for (int s = 0; s < s1 && ok; ++s) ok = put(kStageP1, item, s * p.cw1, true, false);
       if (!ok) break;
     }
+    if (ok) ok = put(kStageP1End, -1, 0, false, false);
     __syncthreads();   // ---- phase boundary ----
     // Second phase: items are claimed in the order matrices were published
     // (position j of the ready list, block blk), so no CTA waits for a late
     // matrix while published work remains.
     ok = ok && !B->abort;
-    for (int k = 0;; ++k) {
+    for (int k = 0; ok; ++k) {
       const int b = k & 1;
       int item = -1;
       if (lane == 0) {
         // X0 buffer b is free once item k-2 has been consumed entirely
-        if (ok && mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) {
+        if (mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) {
           const unsigned next = atomicAdd(lctr + 1, 1u);
           const int j = static_cast<int>(next / static_cast<unsigned>(p.nb));
           if (j < p.total_mats) {
@@ -868,23 +725,57 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item < 0) break;
-      if (!p.step_mode) continue;
-      const int mat = item / p.nb, blk = item - mat * p.nb;
-      const SmallSlice& S = slice_of(p, mat);
-      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-      const int64_t col0 = static_cast<int64_t>(blk) * wb;
-      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
-      const Geo g = geo_p2(p, S);
-      for (int s = 0; s < g.count; ++s) {
-        if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) {
-          ok = false;
-          break;
+      for (int t = 0; t < tiles && ok; ++t) ok = put(kStageP2, item, 128 * t, false, p.step_mode != 0);
+    }
+    put(kStageEnd, -1, 0, false, false);
+  } else if (warp == 10) {
+    // ======================= storer =======================
+    // Moves each finished stage's output (M' in the first phase, W' or O in
+    // the second) back to global memory, then frees the stage.
+    Ring rg;
+    bool boundary = false;
+    for (;;) {
+      if (!mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx)) break;
+      const int kind = B->desc[rg.stage][0];
+      const int item = B->desc[rg.stage][1];
+      const int c0 = B->desc[rg.stage][2];
+      if (kind == kStageEnd) break;
+      if (!mwait_warp(&B->cons_done[rg.stage], rg.phase, ctx)) break;
+      uint8_t* st = ring + rg.stage * p.stage_bytes;
+      if (item >= 0 && (kind == kStageP2 || p.step_mode)) {
+        const int mat = item / p.nb;
+        int si = 0;
+        while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
+        const SmallSlice& S = p.s[si];
+        const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
+        const int64_t gj0 = static_cast<int64_t>(item - mat * p.nb) * wb + c0;
+        const bool w = kind == kStageP2;
+        if (w ? S.wbulk : S.gbulk) {
+          if (lane == 0) {
+            int x, y;
+            tile_xy(S, gj0, x, y);
+            ptx::tma_store_3d(&p.tm[si][w ? 2 : 1], w ? st : st + mom_off(p, S), x, y,
+                              mat - S.mat_base);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read<0>();
+          }
+        } else if (w) {
+          copy_tile<false>(p, S, S.w_dtype, S.W, moff, gj0, 128, st, lane);
+        } else {
+          copy_tile<false>(p, S, 0, S.Mom, moff, gj0, p.cw1, st + mom_off(p, S), lane);
         }
-        produce_p2(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes,
-                   &B->ring_full[rg.stage], lane);
-        rg.next(NS);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
+      rg.next(NS);
+      if (kind == kStageP1End) {
+        __syncthreads();   // ---- phase boundary ----
+        boundary = true;
       }
     }
+    if (!boundary) __syncthreads();
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, nmm);
@@ -990,13 +881,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       cons_sync();
     };
+    auto release = [&]() {   // this warp is done with the current stage
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&B->cons_done[rg.stage]);
+      rg.next(NS);
+    };
     int k = 0;
     for (;; ++k) {
       // One thread takes the per-item decision (next item, end, abort) so
       // that every consumer warp runs the same sequence of named barriers.
       if (t == 0) {
         int it = -2;
-        if (mwait(&B->ring_full[rg.stage], rg.phase, ctx)) it = B->stage_item[rg.stage];
+        if (mwait(&B->ring_full[rg.stage], rg.phase, ctx))
+          it = B->desc[rg.stage][0] == kStageP1End ? -1 : B->desc[rg.stage][1];
         B->cur_item = it;
       }
       cons_sync();
@@ -1005,33 +903,25 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         ok = false;
         break;
       }
-      if (item < 0) {   // end token
+      if (item < 0) {   // end of the first phase
         mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
-        rg.next(NS);
+        release();
         break;
       }
       const int b = k & 1;
-      const int mat = item / p.nb, blk = item - mat * p.nb;
+      const int mat = item / p.nb;
       const SmallSlice& S = slice_of(p, mat);
-      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-      const int64_t col0 = static_cast<int64_t>(blk) * wb;
-      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
       uint8_t* sx = sm + b * p.xbytes;
       if (k >= 2 && t == 0) ptx::bulk_wait_read<1>();   // item k-2's image store left this tile
       cons_sync();
-      const Geo g = geo_p1(p, S);
-      for (int s = 0; s < g.count; ++s) {
+      for (int s = 0; s < s1; ++s) {
         const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
         ok = ok && sok;
-        if (ok) consume_p1_any(p, S, g, s, moff, col0, nci, ring + rg.stage * p.stage_bytes, sx, t);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
-        rg.next(NS);
+        if (ok) consume_p1_any(p, S, s * p.cw1, ring + rg.stage * p.stage_bytes, sx, t);
+        release();
       }
-      // padding rows m..mr-1 of a row-major item are zero
-      if (!S.trans && p.mr > m) {
+      // padding rows m..mr-1 are zero
+      if (p.mr > m) {
         const int gpr = wb >> 3;
         for (int gi = t; gi < (p.mr - m) * gpr; gi += kT) {
           const int r = m + gi / gpr, c8 = (gi % gpr) << 3;
@@ -1068,38 +958,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       if (!mwait_warp(&B->xq_full[b], (k >> 1) & 1, ctx)) break;
       const int item = B->slot[b];
       if (item < 0) break;
-      const int mat = item / p.nb, blk = item - mat * p.nb;
-      const SmallSlice& S = slice_of(p, mat);
-      const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-      const int64_t col0 = static_cast<int64_t>(blk) * wb;
-      const int nci = static_cast<int>(min(static_cast<int64_t>(wb), n - col0));
+      const SmallSlice& S = slice_of(p, item / p.nb);
       const float stepk = p.lr * S.scale;
       ok = mwait_warp(&B->o_full[b], (k >> 1) & 1, ctx) && ok;
       ptx::tc_fence_after();
       const uint32_t obuf = tmem + 256 * b;
-      const Geo g = geo_p2(p, S);
-      for (int s = 0; s < g.count; ++s) {
-        if (p.step_mode) {
-          const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
-          ok = ok && sok;
-        }
-        const uint8_t* st = ring + rg.stage * p.stage_bytes;
-        if (ok) {
-          if (!S.trans) {
-            if (g.rows == 8)
-              epi_rows<8>(p, S, s * 8, moff, col0, nci, st, obuf, set, q4, lane, decay, stepk);
-            else
-              epi_rows<4>(p, S, s * 4, moff, col0, nci, st, obuf, set, q4, lane, decay, stepk);
-          } else {
-            epi_cols(p, S, s * g.cols, min(g.cols, wb - s * g.cols), moff, col0, nci, st, obuf,
-                     set, q4, lane, decay, stepk);
-          }
-        }
-        if (p.step_mode) {
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
-          rg.next(NS);
-        }
+      for (int tt = 0; tt < tiles; ++tt) {
+        const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
+        ok = ok && sok;
+        if (ok) epi_tile_any(p, S, tt, ring + rg.stage * p.stage_bytes, obuf, set, q4, lane, decay, stepk);
+        release();
       }
       ptx::tc_fence_before();
       __syncwarp();
