@@ -436,16 +436,30 @@ __device__ void consume_p1(const SmallParams& p, const SmallSlice& S, int c0, ui
   const int chunk_bytes = p.mr * 128;
   uint8_t* smom = st + mom_off(p, S);
   if (!S.trans) {
+    // m * cw1 / 8 <= 512 groups of 8: at most two per thread, whose loads are
+    // all issued before the in-place stores
     const int gpr = cw >> 3;
     const int sh = gpr == 16 ? 4 : 3;                  // cw1 is 128 or 64
-    for (int g = t; g < m * gpr; g += kT) {
+    const int ng = m * gpr;
+    float gv[2][8], mo[2][8];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int g = t + u * kT;
+      if (g < ng) {
+        const int so = (g >> sh) * cw + ((g & (gpr - 1)) << 3);
+        load8_smem<ESG>(st, so, gv[u]);
+        if constexpr (STEP) load8_smem<4>(smom, so, mo[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int g = t + u * kT;
+      if (g >= ng) continue;
       const int r = g >> sh, c8 = (g & (gpr - 1)) << 3;
       const int so = r * cw + c8;
-      float gv[8], mo[8], d[8];
-      load8_smem<ESG>(st, so, gv);
-      if constexpr (STEP) load8_smem<4>(smom, so, mo);
-      momentum8<STEP>(p, gv, mo, d);
-      if constexpr (STEP) store8_smem_f32(smom, so, mo);
+      float d[8];
+      momentum8<STEP>(p, gv[u], mo[u], d);
+      if constexpr (STEP) store8_smem_f32(smom, so, mo[u]);
       const int ci = c0 + c8;
       uint4 q;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
@@ -528,19 +542,22 @@ __device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S,
   const int m = p.m, nmm = p.nmm, tcol = (nmm + 31) & ~31;
   WT* ws = reinterpret_cast<WT*>(st);
   const int col = 32 * q4 + lane;
+  const int rs = S.trans ? 1 : 128, cs = S.trans ? m : 1;   // element (q, col) at q rs + col cs
   for (int h = 0; h < 2; ++h) {
     const int cq = 16 * set + 32 * h;
     if (cq >= nmm) continue;
     uint32_t r[16];
     ptx::tmem_ld_32x32b_x16(obuf + tile * tcol + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
+    // all W loads before any store (the stores may alias later loads otherwise)
+    float w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = (STEP && cq + j < m) ? w_ld(ws, (cq + j) * rs + col * cs) : 0.f;
     ptx::tmem_ld_wait();
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const int q = cq + j;
-      if (q < m) {
-        const int so = S.trans ? col * m + q : q * 128 + col;
+      if (cq + j < m) {
         const float o = __uint_as_float(r[j]);
-        w_st(ws, so, STEP ? fmaf(decay, w_ld(ws, so), -stepk * o) : o);
+        w_st(ws, (cq + j) * rs + col * cs, STEP ? fmaf(decay, w[j], -stepk * o) : o);
       }
     }
   }
