@@ -206,12 +206,14 @@ bool small_shape(int64_t m) {
 
 // Work items and shared-memory carve-up of the small-m kernel for core shape
 // (m, n) over `mats` matrices; false when no carve-up fits one SM.  Shared
-// memory holds two X0 tiles of wb columns, two Q images, a ring of stages
-// (one m x cw1 G + Mom tile or one m x 128 W tile each) and the Gram-space
-// matrices.  The ring gets about 96 KB; wb is the largest multiple of 128
-// that fits such that the item's O fits one 256-column TMEM buffer; then it
-// shrinks while the launch would leave SMs without an item.
-bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
+// memory holds a ring of stages, two Q images and the Gram-space matrices.
+// A stage holds the data tile(s) of its phase (G + Mom: m x cw1, or W:
+// m x 128, for the widest dtypes in the launch), then an X0 tile of 128
+// columns at x_off and a 2 KB zero gap.  Items are up to 2048 columns (the
+// X0 image of an item streams through the stages), shrinking while the
+// launch would leave SMs without an item.
+bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, bool step,
+                SmallParams* sp) {
   sp->m = static_cast<int>(m);
   sp->n = static_cast<int>(n);
   sp->mr = static_cast<int>(rup(m, 8));
@@ -220,34 +222,29 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, SmallParams* sp) {
   sp->cw1 = m <= 32 ? 128 : 64;
   sp->qbytes = 2 * sp->nmm * 128;
   sp->pstride = static_cast<int>(rup(m * m, 4));
-  sp->stage_bytes = static_cast<int>(
-      align_up(static_cast<size_t>(m) * std::max(sp->cw1 * 8, 128 * 4), 1024));
-  const int tcol = static_cast<int>(rup(sp->nmm, 32));
-  const int64_t wcap = 128 * (256 / tcol);
+  const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns of X0
+  const size_t p1 = static_cast<size_t>(m) * sp->cw1 * (esg + (step ? 4 : 0));
+  const size_t p2 = static_cast<size_t>(m) * 128 * esw;
+  sp->x_off = static_cast<int>(align_up(std::max(p1, p2), 1024));
+  sp->stage_bytes = static_cast<int>(align_up(sp->x_off + 2 * chunk + 2048, 1024));
   const size_t gs = align_up(static_cast<size_t>(5) * sp->mp * sp->mp * 4 + 64, 16);
-  const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns
-  int64_t chunks = 0;
-  for (sp->stages = std::max(2, std::min(kSmallMaxStages, (96 * 1024) / sp->stage_bytes));
-       sp->stages >= 2; --sp->stages) {
-    const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) +
-                         static_cast<size_t>(sp->stages) * sp->stage_bytes + gs + 512 + 1024;
-    if (fixed >= static_cast<size_t>(kSmallSmemLimit)) continue;
-    chunks = static_cast<int64_t>((kSmallSmemLimit - fixed) / 2 / chunk) / 2 * 2;
-    if (chunks >= 2) break;
-  }
-  if (chunks < 2) return false;
-  const int64_t wmax = std::min<int64_t>(chunks * 64, wcap);
-  int64_t wb = std::min<int64_t>(wmax, rup(n, 128));
+  const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) + gs + 512 + 1024;
+  if (fixed >= static_cast<size_t>(kSmallSmemLimit)) return false;
+  const int tcol = static_cast<int>(rup(sp->nmm, 32));
+  sp->stages = static_cast<int>(std::min<size_t>((kSmallSmemLimit - fixed) / sp->stage_bytes,
+                                                 std::min(kSmallMaxStages, 384 / tcol)));
+  if (sp->stages < 2) return false;
+  int64_t wb = std::min<int64_t>(2048, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);
-  while (wb > 128 && mats * cdiv(n, wb) < static_cast<int64_t>(sms)) wb -= 128;
+  while (wb > 128 && mats * cdiv(n, wb) < 2 * static_cast<int64_t>(sms)) wb -= 128;
   sp->wb = static_cast<int>(wb);
   sp->nb = static_cast<int>(cdiv(n, wb));
   sp->total_mats = static_cast<int>(mats);
   sp->items = static_cast<int>(mats * sp->nb);
   sp->xbytes = static_cast<int>((wb / 64) * chunk);
-  sp->off_q = 2 * sp->xbytes;
-  sp->off_ring = sp->off_q + 2 * sp->qbytes;
-  sp->off_gs = sp->off_ring + sp->stages * sp->stage_bytes;
+  sp->off_ring = 0;
+  sp->off_q = sp->stages * sp->stage_bytes;
+  sp->off_gs = sp->off_q + 2 * sp->qbytes;
   sp->off_bar = static_cast<int>(align_up(sp->off_gs + gs, 16));
   sp->smem_bytes = sp->off_bar + 512 + 1024;
   return sp->smem_bytes <= kSmallSmemLimit;
@@ -366,11 +363,12 @@ muon_status_t get_workspace(cudaStream_t stream, size_t bytes, size_t ctrs, char
   return MUON_OK;
 }
 
-// Epoch-tagged words of the small-m path for `mats` matrices: arrive[cap],
-// ready_list[cap], then the ring of per-launch counter slots; returns the
-// next epoch (never 0).
-muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned long long** arrive,
-                             unsigned long long** ready_list, unsigned** ctr, unsigned* epoch) {
+// Launch-tagged words of the small-m path for `mats` matrices: ready_list[cap]
+// (epoch-tagged entries), the two arrive slots [2][cap] and the ring of
+// per-launch counter slots; returns the next epoch (never 0) and cap.
+muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned** arrive,
+                             unsigned long long** ready_list, unsigned** ctr, unsigned* epoch,
+                             int* cap_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
   Workspace& w = g_ws[{dev, stream}];
@@ -383,7 +381,8 @@ muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned long lon
     w.ep = nullptr;
     w.ep_cap = 0;
     const size_t cap = align_up(mats, 1024);
-    const size_t bytes = 2 * cap * sizeof(unsigned long long) + kSmallCtrSlots * 4 * sizeof(unsigned);
+    const size_t bytes = cap * sizeof(unsigned long long) + 2 * cap * sizeof(unsigned) +
+                         kSmallCtrSlots * 4 * sizeof(unsigned);
     if (cudaMalloc(&w.ep, bytes) != cudaSuccess) {
       cudaGetLastError();
       w.ep = nullptr;
@@ -393,9 +392,10 @@ muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned long lon
     w.ep_cap = cap;
   }
   if (++w.epoch == 0) w.epoch = 1;
-  *arrive = w.ep;
-  *ready_list = w.ep + w.ep_cap;
-  *ctr = reinterpret_cast<unsigned*>(w.ep + 2 * w.ep_cap);
+  *ready_list = w.ep;
+  *arrive = reinterpret_cast<unsigned*>(w.ep + w.ep_cap);
+  *ctr = *arrive + 2 * w.ep_cap;
+  *cap_out = static_cast<int>(w.ep_cap);
   *epoch = w.epoch;
   return MUON_OK;
 }
@@ -567,7 +567,12 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         }
         if (mats * cdiv(n, 128) >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         sp.n_slices = static_cast<int>(e - b);
-        if (!small_plan(m, n, mats, dev->sms, &sp)) return MUON_ERR_UNSUPPORTED;
+        int esg = 2, esw = 2;
+        for (size_t k = b; k < e; ++k) {
+          esg = std::max(esg, static_cast<int>(esize(reqs[kv.second[k]].g_dtype)));
+          esw = std::max(esw, static_cast<int>(esize(reqs[kv.second[k]].w_dtype)));
+        }
+        if (!small_plan(m, n, mats, dev->sms, esg, esw, step_mode, &sp)) return MUON_ERR_UNSUPPORTED;
         // TMA tile maps (stored layout): rows of 16-byte multiples, 16-byte
         // aligned bases; otherwise the kernel copies element-wise
         for (size_t k = b; k < e; ++k) {
@@ -629,7 +634,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     sp.part = reinterpret_cast<float*>(w);
     w += align_up(static_cast<size_t>(sp.items) * sp.pstride * 4, 256);
     sp.qimg = reinterpret_cast<uint8_t*>(w);
-    st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready_list, &sp.ctr, &sp.epoch);
+    st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready_list, &sp.ctr, &sp.epoch, &sp.cap);
     if (st != MUON_OK) return st;
     // one CTA per SM (all resident: the launch is cooperative)
     if (small_blocks_per_sm(sp.smem_bytes) <= 0) return MUON_ERR_CUDA;

@@ -113,9 +113,8 @@ struct GemmParams {
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
 constexpr int kSmallThreads = 352;         // warp 0 loads, 1 MMA, 2..9 consumers, 10 stores
 constexpr int kSmallCons = 256;            // consumer threads
-constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O buffers [0,256), [256,512)
-constexpr int kSmallMaxStages = 4;
-constexpr int kSmallStageBytes = 24 * 1024;
+constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O slot s at 128 + s * tcol
+constexpr int kSmallMaxStages = 8;
 constexpr int kSmallCtrSlots = 64;         // ring of per-launch counter slots
 constexpr int kSmallMaxSlices = 16;        // slices per launch (their tensor maps are parameters)
 constexpr int kSmallSmemLimit = 227 * 1024;
@@ -150,6 +149,7 @@ struct SmallParams {
   int total_mats;
   int items;         // total_mats * nb
   int xbytes;        // one item's X0 image: (wb / 64) * mr * 128
+  int x_off;         // X0 tile inside a stage (1024-aligned); a zero gap follows it
   int qbytes;        // one Q image: hi and lo, nmm rows x 128 bytes each
   int pstride;       // floats per partial Gram (m * m rounded up to 4)
   int steps;
@@ -159,13 +159,14 @@ struct SmallParams {
   uint8_t* ximg;                // [items][xbytes] bf16 X0 images (shared-memory layout)
   float* part;                  // [items][pstride] partial Gram matrices
   uint8_t* qimg;                // [total_mats][qbytes] Q = hi + lo operand images
-  unsigned long long* arrive;   // [total_mats] (epoch << 32) | items arrived
+  unsigned* arrive;             // [2][cap]: items arrived per matrix, slot epoch % 2
   unsigned long long* ready_list;   // [total_mats] (epoch << 32) | matrix, in publication order
   unsigned* ctr;                // [kSmallCtrSlots][4]: per launch (slot epoch % slots)
                                 // ready-list length, claimed second- and first-phase items
   unsigned epoch;               // this launch's tag, never 0
   unsigned* status;
   unsigned long long timeout_ns;
+  int cap;                      // matrices per arrive slot
   // shared-memory carve-up (bytes from the 1024-aligned base)
   int off_q, off_ring, stage_bytes, off_gs, off_bar;
   int smem_bytes;

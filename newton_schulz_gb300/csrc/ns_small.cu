@@ -47,15 +47,13 @@ constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
 
 // Shared-memory control block: mbarriers, the TMEM slot and CTA flags.
 struct SmallBars {
-  uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], ring_empty[kSmallMaxStages];
-  uint64_t x_full[2], gram_full[2], xq_full[2];
-  uint64_t o_full[2], o_empty[2];
+  uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], mma_done[kSmallMaxStages],
+      ring_empty[kSmallMaxStages];
+  uint64_t gram_full[2], img_done[2], q_full[2], q_free[2];
   uint32_t tslot;
   int last;
   int abort;
-  int slot[2];   // second phase: item held by X0 buffer b (-1: no more items)
-  int desc[kSmallMaxStages][3];      // per stage: kind, item (-1: none), first X column
-  int x_item[2];     // first phase: item whose X0 tile b is complete (-1: no more)
+  int desc[kSmallMaxStages][4];      // per stage: kind, item (-1: none), first X column, flags
   int cur_item;      // first phase: the consumers' current item (-2: abort)
 };
 
@@ -92,23 +90,6 @@ __device__ __forceinline__ bool mwait_warp(uint64_t* bar, uint32_t parity, const
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = mwait(bar, parity, c) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Epoch-tagged counter: (epoch << 32) | count.  Returns the count before this
-// increment (a counter still tagged with an older epoch counts as zero), or
-// 0xffffffff if the update kept failing.
-__device__ unsigned claim(unsigned long long* ctr, unsigned epoch, unsigned* status) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned tag = static_cast<unsigned>(cur >> 32);
-    const unsigned cnt = tag == epoch ? static_cast<unsigned>(cur) : 0u;
-    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
-    const unsigned long long prev = atomicCAS(ctr, cur, want);
-    if (prev == cur) return cnt;
-    cur = prev;
-  }
-  atomicOr(status, kDevTimeout);
-  return 0xffffffffu;
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -343,13 +324,19 @@ __device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
 }
 
 // ---- stage layout ---------------------------------------------------------------------
-// A stage holds one tile of the stored tensor(s) for a range of X columns:
-//   first phase:  G tile (cw1 X columns) at byte 0, Mom tile at mom_off;
-//   second phase: W tile (128 X columns) at byte 0.
-// Row-major matrices give [m][cols] tiles (row pitch cols), transposed ones
-// [cols][m] tiles (stored rows of m).  TMA fills out-of-matrix elements with
-// zero and clips them on the way back.
+// A stage holds, for one range of X columns of one item:
+//   first phase:  G tile (cw1 X columns) at byte 0, Mom tile at mom_off, and
+//                 the X0 tile the consumers write (cw1 / 64 chunks) at x_off;
+//   second phase: W tile (128 X columns) at byte 0 and the X0 tile (2 chunks,
+//                 reloaded from the item's image) at x_off.
+// A 2 KB zero gap follows the X0 tile: the apply's K padding (rows mr..nmm-1
+// of the second chunk) reads it.  Row-major matrices give [m][cols] tiles,
+// transposed ones [cols][m].  TMA fills out-of-matrix elements with zero and
+// clips them on the way back.
 enum StageKind : int { kStageP1 = 0, kStageP2 = 1, kStageP1End = 2, kStageEnd = 3 };
+
+// Stage descriptor flags
+constexpr int kFirst = 1, kLast = 2;
 
 __device__ __forceinline__ uint32_t mom_off(const SmallParams& p, const SmallSlice& S) {
   return static_cast<uint32_t>(p.m * p.cw1 * (S.g_dtype == 0 ? 4 : 2));
@@ -427,28 +414,33 @@ __device__ __forceinline__ void momentum8(const SmallParams& p, const float* gv,
   }
 }
 
-// Stage of X columns [c0, c0 + cw1) of the item: M' written back in place
-// (the storer warp moves it out), X0 = bf16(D) into the item's tile.
+// First-phase stage: M' written back in place (the storer moves it out), and
+// X0 = bf16(D) into the stage's X0 tile (rows mr, cw1 / 64 chunks; rows m..mr-1
+// zero).
 template <int ESG, bool STEP>
-__device__ void consume_p1(const SmallParams& p, const SmallSlice& S, int c0, uint8_t* st,
-                           uint8_t* sx, int t) {
+__device__ void consume_p1(const SmallParams& p, const SmallSlice& S, uint8_t* st, int t) {
   const int m = p.m, cw = p.cw1;
   const int chunk_bytes = p.mr * 128;
   uint8_t* smom = st + mom_off(p, S);
+  uint8_t* sx = st + p.x_off;
   if (!S.trans) {
-    // m * cw1 / 8 <= 512 groups of 8: at most two per thread, whose loads are
+    // mr * cw1 / 8 <= 512 groups of 8: at most two per thread, whose loads are
     // all issued before the in-place stores
     const int gpr = cw >> 3;
     const int sh = gpr == 16 ? 4 : 3;                  // cw1 is 128 or 64
-    const int ng = m * gpr;
+    const int ng = p.mr * gpr;
     float gv[2][8], mo[2][8];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int g = t + u * kT;
-      if (g < ng) {
-        const int so = (g >> sh) * cw + ((g & (gpr - 1)) << 3);
+      const int r = g >> sh;
+      if (g < ng && r < m) {
+        const int so = r * cw + ((g & (gpr - 1)) << 3);
         load8_smem<ESG>(st, so, gv[u]);
         if constexpr (STEP) load8_smem<4>(smom, so, mo[u]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gv[u][j] = mo[u][j] = 0.f;
       }
     }
 #pragma unroll
@@ -456,17 +448,16 @@ __device__ void consume_p1(const SmallParams& p, const SmallSlice& S, int c0, ui
       const int g = t + u * kT;
       if (g >= ng) continue;
       const int r = g >> sh, c8 = (g & (gpr - 1)) << 3;
-      const int so = r * cw + c8;
       float d[8];
       momentum8<STEP>(p, gv[u], mo[u], d);
-      if constexpr (STEP) store8_smem_f32(smom, so, mo[u]);
-      const int ci = c0 + c8;
+      if constexpr (STEP) {
+        if (r < m) store8_smem_f32(smom, r * cw + c8, mo[u]);
+      }
       uint4 q;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
 #pragma unroll
       for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
-      *reinterpret_cast<uint4*>(sx + (ci >> 6) * chunk_bytes +
-                                ptx::sw128_offset(r, (ci & 63) * 2)) = q;
+      *reinterpret_cast<uint4*>(sx + (c8 >> 6) * chunk_bytes + ptx::sw128_offset(r, (c8 & 63) * 2)) = q;
     }
   } else {
     const int ig = p.mr >> 3;
@@ -497,9 +488,8 @@ __device__ void consume_p1(const SmallParams& p, const SmallSlice& S, int c0, ui
             if (j < nv) reinterpret_cast<float*>(smom)[so + j] = mo[j];
         }
       }
-      const int ci = c0 + c;
-      uint8_t* colp = sx + (ci >> 6) * chunk_bytes;
-      const uint32_t byte = (ci & 63) * 2;
+      uint8_t* colp = sx + (c >> 6) * chunk_bytes;
+      const uint32_t byte = (c & 63) * 2;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         *reinterpret_cast<__nv_bfloat16*>(colp + ptx::sw128_offset(r + j, byte)) =
@@ -508,14 +498,13 @@ __device__ void consume_p1(const SmallParams& p, const SmallSlice& S, int c0, ui
   }
 }
 
-__device__ void consume_p1_any(const SmallParams& p, const SmallSlice& S, int c0, uint8_t* st,
-                               uint8_t* sx, int t) {
+__device__ void consume_p1_any(const SmallParams& p, const SmallSlice& S, uint8_t* st, int t) {
   if (S.g_dtype == 0) {
-    if (p.step_mode) consume_p1<4, true>(p, S, c0, st, sx, t);
-    else consume_p1<4, false>(p, S, c0, st, sx, t);
+    if (p.step_mode) consume_p1<4, true>(p, S, st, t);
+    else consume_p1<4, false>(p, S, st, t);
   } else {
-    if (p.step_mode) consume_p1<2, true>(p, S, c0, st, sx, t);
-    else consume_p1<2, false>(p, S, c0, st, sx, t);
+    if (p.step_mode) consume_p1<2, true>(p, S, st, t);
+    else consume_p1<2, false>(p, S, st, t);
   }
 }
 
@@ -532,14 +521,14 @@ __device__ __forceinline__ void w_st(WT* p, int i, float v) {
   else p[i] = __float2bfloat16_rn(v);
 }
 
-// 128-column W tile of tile index `tile` of the item: W' = decay W - stepk O
-// (or O) written back in place.  Warp (set, q4) owns lanes 32 q4.. (the
-// columns) and rows 16 set + 32 h .. + 16 of O in TMEM.
+// 128-column W tile: W' = decay W - stepk O (or O) written back in place from
+// the TMEM slot at `oslot`.  Warp (set, q4) owns lanes 32 q4.. (the columns)
+// and rows 16 set + 32 h .. + 16 of O.
 template <typename WT, bool STEP>
-__device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S, int tile,
-                                      uint8_t* st, uint32_t obuf, int set, int q4, int lane,
-                                      float decay, float stepk) {
-  const int m = p.m, nmm = p.nmm, tcol = (nmm + 31) & ~31;
+__device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S, uint8_t* st,
+                                      uint32_t oslot, int set, int q4, int lane, float decay,
+                                      float stepk) {
+  const int m = p.m, nmm = p.nmm;
   WT* ws = reinterpret_cast<WT*>(st);
   const int col = 32 * q4 + lane;
   const int rs = S.trans ? 1 : 128, cs = S.trans ? m : 1;   // element (q, col) at q rs + col cs
@@ -547,7 +536,7 @@ __device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S,
     const int cq = 16 * set + 32 * h;
     if (cq >= nmm) continue;
     uint32_t r[16];
-    ptx::tmem_ld_32x32b_x16(obuf + tile * tcol + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
+    ptx::tmem_ld_32x32b_x16(oslot + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
     // all W loads before any store (the stores may alias later loads otherwise)
     float w[16];
 #pragma unroll
@@ -563,21 +552,38 @@ __device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S,
   }
 }
 
-__device__ void epi_tile_any(const SmallParams& p, const SmallSlice& S, int tile, uint8_t* st,
-                             uint32_t obuf, int set, int q4, int lane, float decay, float stepk) {
+__device__ void epi_tile_any(const SmallParams& p, const SmallSlice& S, uint8_t* st,
+                             uint32_t oslot, int set, int q4, int lane, float decay, float stepk) {
   if (S.w_dtype == 0) {
-    if (p.step_mode) epi_tile<float, true>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
-    else epi_tile<float, false>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
+    if (p.step_mode) epi_tile<float, true>(p, S, st, oslot, set, q4, lane, decay, stepk);
+    else epi_tile<float, false>(p, S, st, oslot, set, q4, lane, decay, stepk);
   } else {
-    if (p.step_mode) epi_tile<__nv_bfloat16, true>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
-    else epi_tile<__nv_bfloat16, false>(p, S, tile, st, obuf, set, q4, lane, decay, stepk);
+    if (p.step_mode) epi_tile<__nv_bfloat16, true>(p, S, st, oslot, set, q4, lane, decay, stepk);
+    else epi_tile<__nv_bfloat16, false>(p, S, st, oslot, set, q4, lane, decay, stepk);
   }
 }
 
-// TMA coordinates of the tile at X column gj0 of local matrix z.
+// TMA coordinates of the tile at X column gj0.
 __device__ __forceinline__ void tile_xy(const SmallSlice& S, int64_t gj0, int& x, int& y) {
   x = S.trans ? 0 : static_cast<int>(gj0);
   y = S.trans ? static_cast<int>(gj0) : 0;
+}
+
+struct ItemRef {
+  int si;          // slice
+  int mat;         // matrix within the launch
+  int64_t moff;    // element offset of the matrix
+  int64_t col0;    // first X column of the item
+};
+
+__device__ __forceinline__ ItemRef item_ref(const SmallParams& p, int item) {
+  ItemRef r;
+  r.mat = item / p.nb;
+  r.si = 0;
+  while (r.si + 1 < p.n_slices && r.mat >= p.s[r.si + 1].mat_base) ++r.si;
+  r.moff = static_cast<int64_t>(r.mat - p.s[r.si].mat_base) * p.m * p.n;
+  r.col0 = static_cast<int64_t>(item - r.mat * p.nb) * p.wb;
+  return r;
 }
 
 }  // namespace
@@ -586,50 +592,51 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     ns_small_kernel(const __grid_constant__ SmallParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-  // X0 tile b at sm + b * xbytes; Q image b at sm + off_q + b * qbytes
-  uint8_t* ring = sm + p.off_ring;
+  uint8_t* ring = sm + p.off_ring;          // stage s at ring + s * stage_bytes
   float* gs = reinterpret_cast<float*>(sm + p.off_gs);
   SmallBars* B = reinterpret_cast<SmallBars*>(sm + p.off_bar);
   const Ctx ctx{B, p.status, p.timeout_ns};
   // This launch's counters (ready-list length, claimed second- and first-
-  // phase items) are slot epoch % 64 of a ring that the previous launch
-  // zeroed; CTA 0 zeroes the slot of the next launch.
+  // phase items) are slot epoch % 64 of a ring, its per-matrix arrivals slot
+  // epoch % 2 of two; the previous launch zeroed both, CTA 0 zeroes the next
+  // launch's.
   unsigned* lctr = p.ctr + (p.epoch % kSmallCtrSlots) * 4;
-  if (blockIdx.x == 0 && threadIdx.x < 4)
-    p.ctr[((p.epoch + 1) % kSmallCtrSlots) * 4 + threadIdx.x] = 0u;
+  unsigned* larr = p.arrive + static_cast<size_t>(p.epoch & 1u) * p.cap;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x < 4) p.ctr[((p.epoch + 1) % kSmallCtrSlots) * 4 + threadIdx.x] = 0u;
+    unsigned* nxt = p.arrive + static_cast<size_t>((p.epoch + 1) & 1u) * p.cap;
+    for (int i = threadIdx.x; i < p.cap; i += kSmallThreads) nxt[i] = 0u;
+  }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m = p.m, n = p.n, nmm = p.nmm, wb = p.wb, NS = p.stages;
+  const int m = p.m, nmm = p.nmm, wb = p.wb, NS = p.stages;
   const int chunk_bytes = p.mr * 128;
   const int tiles = wb / 128;
   const int s1 = wb / p.cw1;               // first-phase stages per item
-  const int64_t mn = static_cast<int64_t>(m) * n;
   const int tcol = (nmm + 31) & ~31;       // TMEM columns of O per 128-column tile
 
   if (tid == 0) {
     for (int i = 0; i < kSmallMaxStages; ++i) {
       ptx::mbar_init(&B->ring_full[i], 1);
       ptx::mbar_init(&B->cons_done[i], kT / 32);
+      ptx::mbar_init(&B->mma_done[i], 1);
       ptx::mbar_init(&B->ring_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&B->x_full[i], 1);
       ptx::mbar_init(&B->gram_full[i], 1);
-      ptx::mbar_init(&B->xq_full[i], 1);
-      ptx::mbar_init(&B->o_full[i], 1);
-      ptx::mbar_init(&B->o_empty[i], kT / 32);
+      ptx::mbar_init(&B->img_done[i], 1);
+      ptx::mbar_init(&B->q_full[i], 1);
+      ptx::mbar_init(&B->q_free[i], 1);
     }
     B->last = 0;
     B->abort = 0;
     ptx::fence_mbar_init();
   }
-  // The apply's K padding (rows mr..nmm-1) reads up to 15 rows past an X0
-  // tile, i.e. the start of the next buffer; those bytes must hold finite
-  // values (they meet zero rows of Q) even before the buffer is first used.
-  for (int i = tid; i < 2048 / 16; i += kSmallThreads) {
-    reinterpret_cast<uint4*>(sm + p.xbytes)[i] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(sm + p.off_q)[i] = make_uint4(0, 0, 0, 0);
-  }
+  // zero gap after every stage's X0 tile (read as the apply's K padding)
+  for (int s = 0; s < NS; ++s)
+    for (int i = tid; i < 2048 / 16; i += kSmallThreads)
+      reinterpret_cast<uint4*>(ring + s * p.stage_bytes + p.x_off + 2 * chunk_bytes)[i] =
+          make_uint4(0, 0, 0, 0);
   if (warp == 1) ptx::tmem_alloc(&B->tslot, kSmallTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
@@ -640,33 +647,36 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     // ======================= producer (loads) =======================
     Ring rg;
     bool ok = true;
-    // Hands the next stage to the consumers: descriptor, then the tile(s).
-    auto put = [&](int kind, int item, int c0, bool load_g, bool load_w) -> bool {
+    // Hands the next stage to the other roles: descriptor, then the tile(s).
+    auto put = [&](int kind, int item, int c0, int flags) -> bool {
       if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) return false;
       uint8_t* st = ring + rg.stage * p.stage_bytes;
       uint64_t* full = &B->ring_full[rg.stage];
       uint32_t tx = 0;
-      int si = -1;
-      int64_t moff = 0, gj0 = 0;
+      ItemRef ir{};
+      bool tma = false;
       if (item >= 0) {
-        const int mat = item / p.nb;
-        si = 0;
-        while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
-        const SmallSlice& S = p.s[si];
-        moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-        gj0 = static_cast<int64_t>(item - mat * p.nb) * wb + c0;
-        const int cols = load_g ? p.cw1 : 128;
-        if ((load_g && !S.gbulk) || (load_w && !S.wbulk)) {
-          if (load_g) {
-            copy_tile<true>(p, S, S.g_dtype, const_cast<void*>(S.G), moff, gj0, cols, st, lane);
-            if (p.step_mode) copy_tile<true>(p, S, 0, S.Mom, moff, gj0, cols, st + mom_off(p, S), lane);
+        ir = item_ref(p, item);
+        const SmallSlice& S = p.s[ir.si];
+        const int64_t gj0 = ir.col0 + c0;
+        if (kind == kStageP1) {
+          if (S.gbulk) {
+            tma = true;
+            tx = static_cast<uint32_t>(m * p.cw1 * ((S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0)));
           } else {
-            copy_tile<true>(p, S, S.w_dtype, S.W, moff, gj0, cols, st, lane);
+            copy_tile<true>(p, S, S.g_dtype, const_cast<void*>(S.G), ir.moff, gj0, p.cw1, st, lane);
+            if (p.step_mode) copy_tile<true>(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
           }
-        } else if (load_g) {
-          tx = static_cast<uint32_t>(p.m * cols * ((S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0)));
-        } else if (load_w) {
-          tx = static_cast<uint32_t>(p.m * cols * (S.w_dtype == 0 ? 4 : 2));
+        } else {   // second phase: W tile (step mode) and the X0 tile from the image
+          tx = static_cast<uint32_t>(2 * chunk_bytes);
+          if (p.step_mode) {
+            if (S.wbulk) {
+              tma = true;
+              tx += static_cast<uint32_t>(m * 128 * (S.w_dtype == 0 ? 4 : 2));
+            } else {
+              copy_tile<true>(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
+            }
+          }
         }
       }
       __syncwarp();
@@ -674,17 +684,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         B->desc[rg.stage][0] = kind;
         B->desc[rg.stage][1] = item;
         B->desc[rg.stage][2] = c0;
+        B->desc[rg.stage][3] = flags;
         if (tx) {
-          const SmallSlice& S = p.s[si];
-          const int z = item / p.nb - S.mat_base;
+          const SmallSlice& S = p.s[ir.si];
+          const int z = ir.mat - S.mat_base;
           int x, y;
-          tile_xy(S, gj0, x, y);
+          tile_xy(S, ir.col0 + c0, x, y);
           ptx::mbar_arrive_expect_tx(full, tx);
-          if (load_g) {
-            ptx::tma_load_3d(st, &p.tm[si][0], full, x, y, z);
-            if (p.step_mode) ptx::tma_load_3d(st + mom_off(p, S), &p.tm[si][1], full, x, y, z);
+          if (kind == kStageP1) {
+            ptx::tma_load_3d(st, &p.tm[ir.si][0], full, x, y, z);
+            if (p.step_mode) ptx::tma_load_3d(st + mom_off(p, S), &p.tm[ir.si][1], full, x, y, z);
           } else {
-            ptx::tma_load_3d(st, &p.tm[si][2], full, x, y, z);
+            if (tma) ptx::tma_load_3d(st, &p.tm[ir.si][2], full, x, y, z);
+            ptx::bulk_load(st + p.x_off,
+                           p.ximg + static_cast<size_t>(item) * p.xbytes + (c0 / 64) * chunk_bytes,
+                           static_cast<uint32_t>(2 * chunk_bytes), full);
           }
         } else {
           ptx::mbar_arrive(full);
@@ -705,92 +719,98 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item < 0) break;
-      for (int s = 0; s < s1 && ok; ++s) ok = put(kStageP1, item, s * p.cw1, true, false);
+      for (int s = 0; s < s1 && ok; ++s)
+        ok = put(kStageP1, item, s * p.cw1, (s == 0 ? kFirst : 0) | (s == s1 - 1 ? kLast : 0));
       if (!ok) break;
     }
-    if (ok) ok = put(kStageP1End, -1, 0, false, false);
-    __syncthreads();   // ---- phase boundary ----
+    if (ok) ok = put(kStageP1End, -1, 0, 0);
     // Second phase: items are claimed in the order matrices were published
     // (position j of the ready list, block blk), so no CTA waits for a late
     // matrix while published work remains.
-    ok = ok && !B->abort;
     for (int k = 0; ok; ++k) {
       const int b = k & 1;
       int item = -1;
       if (lane == 0) {
-        // X0 buffer b is free once item k-2 has been consumed entirely
-        if (mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) {
-          const unsigned next = atomicAdd(lctr + 1, 1u);
-          const int j = static_cast<int>(next / static_cast<unsigned>(p.nb));
-          if (j < p.total_mats) {
-            const int mat = wait_ready_pos(p.ready_list, j, p.epoch, ctx);
-            if (mat >= 0) item = mat * p.nb + static_cast<int>(next - j * p.nb);
-          }
+        const unsigned next = atomicAdd(lctr + 1, 1u);
+        const int j = static_cast<int>(next / static_cast<unsigned>(p.nb));
+        if (j < p.total_mats) {
+          const int mat = wait_ready_pos(p.ready_list, j, p.epoch, ctx);
+          if (mat >= 0) item = mat * p.nb + static_cast<int>(next - j * p.nb);
         }
-        B->slot[b] = item;
+        // Q buffer b is free once the MMAs of item k-2 are done
+        if (item >= 0 && !mwait(&B->q_free[b], ((k >> 1) & 1) ^ 1u, ctx)) item = -1;
         if (item >= 0) {
           ptx::fence_proxy_async_global();
-          const int mat = item / p.nb;
-          ptx::mbar_arrive_expect_tx(&B->xq_full[b], static_cast<uint32_t>(p.xbytes + p.qbytes));
-          ptx::bulk_load(sm + b * p.xbytes, p.ximg + static_cast<size_t>(item) * p.xbytes,
-                         static_cast<uint32_t>(p.xbytes), &B->xq_full[b]);
-          ptx::bulk_load(sm + p.off_q + b * p.qbytes, p.qimg + static_cast<size_t>(mat) * p.qbytes,
-                         static_cast<uint32_t>(p.qbytes), &B->xq_full[b]);
-        } else {
-          ptx::mbar_arrive(&B->xq_full[b]);   // wakes the other roles to finish
+          ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(p.qbytes));
+          ptx::bulk_load(sm + p.off_q + b * p.qbytes,
+                         p.qimg + static_cast<size_t>(item / p.nb) * p.qbytes,
+                         static_cast<uint32_t>(p.qbytes), &B->q_full[b]);
         }
       }
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item < 0) break;
-      for (int t = 0; t < tiles && ok; ++t) ok = put(kStageP2, item, 128 * t, false, p.step_mode != 0);
+      for (int t = 0; t < tiles && ok; ++t)
+        ok = put(kStageP2, item, 128 * t, (t == 0 ? kFirst : 0) | (t == tiles - 1 ? kLast : 0));
     }
-    put(kStageEnd, -1, 0, false, false);
+    put(kStageEnd, -1, 0, 0);
   } else if (warp == 10) {
     // ======================= storer =======================
-    // Moves each finished stage's output (M' in the first phase, W' or O in
-    // the second) back to global memory, then frees the stage.
+    // Moves each finished stage's outputs back to global memory (first
+    // phase: M' and the X0 slice of the item's image; second phase: W' or
+    // O), then frees the stage.
     Ring rg;
-    bool boundary = false;
+    int k1 = 0;   // first-phase items completed
     for (;;) {
       if (!mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx)) break;
       const int kind = B->desc[rg.stage][0];
       const int item = B->desc[rg.stage][1];
       const int c0 = B->desc[rg.stage][2];
+      const int flags = B->desc[rg.stage][3];
       if (kind == kStageEnd) break;
-      if (!mwait_warp(&B->cons_done[rg.stage], rg.phase, ctx)) break;
+      bool sok = mwait_warp(&B->cons_done[rg.stage], rg.phase, ctx);
+      if (sok && kind == kStageP1) sok = mwait_warp(&B->mma_done[rg.stage], rg.phase, ctx);
+      if (!sok) break;
       uint8_t* st = ring + rg.stage * p.stage_bytes;
-      if (item >= 0 && (kind == kStageP2 || p.step_mode)) {
-        const int mat = item / p.nb;
-        int si = 0;
-        while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
-        const SmallSlice& S = p.s[si];
-        const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * mn;
-        const int64_t gj0 = static_cast<int64_t>(item - mat * p.nb) * wb + c0;
-        const bool w = kind == kStageP2;
-        if (w ? S.wbulk : S.gbulk) {
-          if (lane == 0) {
-            int x, y;
-            tile_xy(S, gj0, x, y);
-            ptx::tma_store_3d(&p.tm[si][w ? 2 : 1], w ? st : st + mom_off(p, S), x, y,
-                              mat - S.mat_base);
-            ptx::bulk_commit();
-            ptx::bulk_wait_read<0>();
+      if (item >= 0) {
+        const ItemRef ir = item_ref(p, item);
+        const SmallSlice& S = p.s[ir.si];
+        const int64_t gj0 = ir.col0 + c0;
+        int x, y;
+        tile_xy(S, gj0, x, y);
+        const int z = ir.mat - S.mat_base;
+        if (kind == kStageP1) {
+          if (p.step_mode) {
+            if (S.gbulk) {
+              if (lane == 0) ptx::tma_store_3d(&p.tm[ir.si][1], st + mom_off(p, S), x, y, z);
+            } else {
+              copy_tile<false>(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
+            }
           }
-        } else if (w) {
-          copy_tile<false>(p, S, S.w_dtype, S.W, moff, gj0, 128, st, lane);
+          if (lane == 0)
+            ptx::bulk_store(p.ximg + static_cast<size_t>(item) * p.xbytes + (c0 / 64) * chunk_bytes,
+                            st + p.x_off, static_cast<uint32_t>((p.cw1 / 64) * chunk_bytes));
+        } else if (S.wbulk) {
+          if (lane == 0) ptx::tma_store_3d(&p.tm[ir.si][2], st, x, y, z);
         } else {
-          copy_tile<false>(p, S, 0, S.Mom, moff, gj0, p.cw1, st + mom_off(p, S), lane);
+          copy_tile<false>(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
         }
+        if (lane == 0) {
+          ptx::bulk_commit();
+          ptx::bulk_wait_read<0>();
+          if (kind == kStageP1 && (flags & kLast)) {
+            // the item's image is complete in global memory
+            ptx::bulk_wait_group<0>();
+            ptx::fence_proxy_async_global();
+            __threadfence();
+            ptx::mbar_arrive(&B->img_done[k1 & 1]);
+          }
+        }
+        if (kind == kStageP1 && (flags & kLast)) ++k1;
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
       rg.next(NS);
-      if (kind == kStageP1End) {
-        __syncthreads();   // ---- phase boundary ----
-        boundary = true;
-      }
     }
-    if (!boundary) __syncthreads();
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
   } else if (warp == 1) {
@@ -798,45 +818,54 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, nmm);
     const uint32_t idesc_app = idesc_gram | (1u << 15);   // A MN-major
     if (lane == 0) {
-      for (int k = 0;; ++k) {
-        const int b = k & 1;
-        if (!mwait(&B->x_full[b], (k >> 1) & 1, ctx)) break;
-        if (B->x_item[b] < 0) break;
-        ptx::tc_fence_after();
-        const uint32_t sx = ptx::smem_u32(sm + b * p.xbytes);
-        for (int kc = 0; kc < wb / 64; ++kc) {
+      Ring rg;
+      int k1 = 0, k2 = -1;
+      for (;;) {
+        if (!mwait(&B->ring_full[rg.stage], rg.phase, ctx)) break;
+        const int kind = B->desc[rg.stage][0];
+        const int flags = B->desc[rg.stage][3];
+        if (kind == kStageEnd) break;
+        const uint32_t sx = ptx::smem_u32(ring + rg.stage * p.stage_bytes + p.x_off);
+        if (kind == kStageP1) {
+          // partial Gram of this stage's X0 columns into accumulator k1 & 1
+          if (!mwait(&B->cons_done[rg.stage], rg.phase, ctx)) break;
+          ptx::tc_fence_after();
+          const int g = k1 & 1;
+          for (int kc = 0; kc < p.cw1 / 64; ++kc) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kc * chunk_bytes + kk * 32);
-            ptx::umma_bf16(tmem + 64 * b, d, d, idesc_gram, (kc | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kc * chunk_bytes + kk * 32);
+              ptx::umma_bf16(tmem + 64 * g, d, d, idesc_gram,
+                             ((flags & kFirst) && kc == 0 && kk == 0) ? 0u : 1u);
+            }
           }
-        }
-        ptx::umma_commit(&B->gram_full[b]);
-      }
-    }
-    __syncwarp();
-    __syncthreads();   // ---- phase boundary ----
-    if (lane == 0) {
-      for (int k = 0;; ++k) {
-        const int b = k & 1;
-        if (!mwait(&B->xq_full[b], (k >> 1) & 1, ctx)) break;
-        if (B->slot[b] < 0) break;
-        if (!mwait(&B->o_empty[b], ((k >> 1) & 1) ^ 1u, ctx)) break;
-        ptx::tc_fence_after();
-        const uint32_t sx = ptx::smem_u32(sm + b * p.xbytes);
-        const uint32_t sq = ptx::smem_u32(sm + p.off_q + b * p.qbytes);
-        for (int t = 0; t < tiles; ++t) {
-          const uint32_t ocol = 256 * b + tcol * t;
+          ptx::umma_commit(&B->mma_done[rg.stage]);
+          if (flags & kLast) {
+            ptx::umma_commit(&B->gram_full[g]);
+            ++k1;
+          }
+        } else if (kind == kStageP2) {
+          if (flags & kFirst) {
+            ++k2;
+            if (!mwait(&B->q_full[k2 & 1], (k2 >> 1) & 1, ctx)) break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sq = ptx::smem_u32(sm + p.off_q + (k2 & 1) * p.qbytes);
+          const uint32_t ocol = 128 + tcol * rg.stage;
           for (int j = 0; j < nmm / 16; ++j) {
-            const uint64_t a = ptx::sdesc_mnmajor_sw128(sx + 2 * t * chunk_bytes + j * 2048,
-                                                        chunk_bytes, 1024);
+            const uint64_t a = ptx::sdesc_mnmajor_sw128(sx + j * 2048, chunk_bytes, 1024);
             ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + j * 32), idesc_app,
                            j != 0 ? 1u : 0u);
             ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + nmm * 128 + j * 32),
                            idesc_app, 1u);
           }
+          ptx::umma_commit(&B->mma_done[rg.stage]);
+          if (flags & kLast) ptx::umma_commit(&B->q_free[k2 & 1]);
+        } else {
+          // keep mma_done[s] at one completion per use of the stage
+          ptx::mbar_arrive(&B->mma_done[rg.stage]);
         }
-        ptx::umma_commit(&B->o_full[b]);
+        rg.next(NS);
       }
     }
     __syncwarp();
@@ -846,11 +875,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const int cw = warp - 2;
     bool ok = true;
     Ring rg;
-    int prev = -1, prevk = 0;
-    auto finish = [&](int item, int k, bool newer_store) {
+    // Deferred end of a first-phase item: partial Gram to the workspace,
+    // arrival, and the Gram-space step if it completed its matrix.
+    auto finish = [&](int item, int k) {
       const int g = k & 1;
       const int mat = item / p.nb;
-      const bool gok = mwait_warp(&B->gram_full[g], (k >> 1) & 1, ctx);
+      bool gok = mwait_warp(&B->gram_full[g], (k >> 1) & 1, ctx);
       ptx::tc_fence_after();
       if (gok && ok && (warp == 4 || warp == 5) && (warp - 4) * 32 < m) {
         const int i = (warp - 4) * 32 + lane;
@@ -866,22 +896,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
               if (c0 + j < m) __stcg(dstp + i * m + c0 + j, __uint_as_float(r[j]));
           }
         }
-      }
-      ok = ok && gok;
-      __threadfence();
-      ptx::tc_fence_before();
-      if (t == 0) {
-        // the image store of this item must be complete before it is announced
-        if (newer_store) ptx::bulk_wait_group<1>();
-        else ptx::bulk_wait_group<0>();
-        ptx::fence_proxy_async_global();
         __threadfence();
       }
+      ok = ok && gok;
+      ptx::tc_fence_before();
       cons_sync();
-      if (t == 0)
-        B->last = (ok && !B->abort &&
-                   claim(p.arrive + mat, p.epoch, p.status) + 1u == static_cast<unsigned>(p.nb))
-                      ? 1 : 0;
+      if (t == 0) {
+        // the image must be complete in global memory before the arrival
+        const bool iok = mwait(&B->img_done[g], (k >> 1) & 1, ctx);
+        __threadfence();
+        B->last = (ok && iok && !B->abort &&
+                   atomicAdd(larr + mat, 1u) + 1u == static_cast<unsigned>(p.nb)) ? 1 : 0;
+      }
       cons_sync();
       if (B->last) {
         __threadfence();
@@ -895,16 +921,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             st_release_u64(p.ready_list + pos, (static_cast<unsigned long long>(p.epoch) << 32) |
                                                    static_cast<unsigned>(mat));
         }
+        cons_sync();
       }
-      cons_sync();
     };
     auto release = [&]() {   // this warp is done with the current stage
       ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&B->cons_done[rg.stage]);
       rg.next(NS);
     };
-    int k = 0;
+    int prev = -1, prevk = 0, k = 0;
+    // ---- first phase ----
     for (;; ++k) {
       // One thread takes the per-item decision (next item, end, abort) so
       // that every consumer warp runs the same sequence of named barriers.
@@ -925,70 +953,34 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         release();
         break;
       }
-      const int b = k & 1;
-      const int mat = item / p.nb;
-      const SmallSlice& S = slice_of(p, mat);
-      uint8_t* sx = sm + b * p.xbytes;
-      if (k >= 2 && t == 0) ptx::bulk_wait_read<1>();   // item k-2's image store left this tile
-      cons_sync();
+      const SmallSlice& S = slice_of(p, item / p.nb);
       for (int s = 0; s < s1; ++s) {
         const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
         ok = ok && sok;
-        if (ok) consume_p1_any(p, S, s * p.cw1, ring + rg.stage * p.stage_bytes, sx, t);
+        if (ok) consume_p1_any(p, S, ring + rg.stage * p.stage_bytes, t);
         release();
       }
-      // padding rows m..mr-1 are zero
-      if (p.mr > m) {
-        const int gpr = wb >> 3;
-        for (int gi = t; gi < (p.mr - m) * gpr; gi += kT) {
-          const int r = m + gi / gpr, c8 = (gi % gpr) << 3;
-          *reinterpret_cast<uint4*>(sx + (c8 >> 6) * chunk_bytes +
-                                    ptx::sw128_offset(r, (c8 & 63) * 2)) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      cons_sync();
-      if (t == 0) {
-        if (ok && !B->abort)
-          ptx::bulk_store(p.ximg + static_cast<size_t>(item) * p.xbytes, sx,
-                          static_cast<uint32_t>(p.xbytes));
-        ptx::bulk_commit();
-        B->x_item[b] = item;
-        ptx::mbar_arrive(&B->x_full[b]);
-      }
-      if (prev >= 0) finish(prev, prevk, true);
+      if (prev >= 0) finish(prev, prevk);
       prev = item;
       prevk = k;
     }
-    if (t == 0) {   // tell the MMA issuer that no tile follows
-      B->x_item[k & 1] = -1;
-      ptx::mbar_arrive(&B->x_full[k & 1]);
-    }
-    if (prev >= 0) finish(prev, prevk, false);
-    if (t == 0) ptx::bulk_wait_group<0>();
-    __syncthreads();   // ---- phase boundary ----
-    ok = ok && !B->abort;
+    if (prev >= 0) finish(prev, prevk);
+    // ---- second phase: every stage until the end token ----
     const float decay = 1.f - p.lr * p.wd;
     const int q4 = warp & 3, set = cw >> 2;
-    for (k = 0; ok; ++k) {
-      const int b = k & 1;
-      if (!mwait_warp(&B->xq_full[b], (k >> 1) & 1, ctx)) break;
-      const int item = B->slot[b];
-      if (item < 0) break;
+    while (ok) {
+      if (!mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx)) break;
+      const int kind = B->desc[rg.stage][0];
+      if (kind == kStageEnd) break;
+      const int item = B->desc[rg.stage][1];
       const SmallSlice& S = slice_of(p, item / p.nb);
-      const float stepk = p.lr * S.scale;
-      ok = mwait_warp(&B->o_full[b], (k >> 1) & 1, ctx) && ok;
+      const bool sok = mwait_warp(&B->mma_done[rg.stage], rg.phase, ctx);
+      ok = ok && sok;
       ptx::tc_fence_after();
-      const uint32_t obuf = tmem + 256 * b;
-      for (int tt = 0; tt < tiles; ++tt) {
-        const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
-        ok = ok && sok;
-        if (ok) epi_tile_any(p, S, tt, ring + rg.stage * p.stage_bytes, obuf, set, q4, lane, decay, stepk);
-        release();
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&B->o_empty[b]);
+      if (ok)
+        epi_tile_any(p, S, ring + rg.stage * p.stage_bytes, tmem + 128 + tcol * rg.stage, set, q4,
+                     lane, decay, p.lr * S.scale);
+      release();
     }
   }
   ptx::tc_fence_before();

@@ -109,3 +109,21 @@ def test_small_and_large_groups_in_one_call():
         w = _np(g["W"])
         for i in range(w.shape[0]):
             assert np.linalg.norm(w[i] - w2[i]) <= DW_TOL * np.linalg.norm(w2[i] - h["W"][i])
+
+
+@pytest.mark.parametrize("trans", [False, True])
+def test_small_step_multistage_items(trans):
+    """Enough matrices that a work item spans many ring stages (2048 columns),
+    so the ring wraps several times within an item and across the phases."""
+    shape = (160, 4096, 16) if trans else (160, 16, 4096)
+    g = synth.random_group(shape, torch.bfloat16, torch.float32, "cuda", 51, 1e-3, 1e-3)
+    host = {k: _np(g[k]) for k in ("W", "G", "Mom")}
+    binding.muon_step_grouped([g], mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    w2, m2, _ = R.muon_step_ref(host["W"][:8], host["G"][:8], host["Mom"][:8])
+    assert _rel(_np(g["Mom"])[:8], m2) <= MOM_TOL
+    w = _np(g["W"])
+    for i in range(8):
+        assert np.linalg.norm(w[i] - w2[i]) <= DW_TOL * np.linalg.norm(w2[i] - host["W"][i])
+    assert binding.muon_last_launch_count() == 1
