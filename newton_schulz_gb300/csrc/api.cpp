@@ -221,7 +221,7 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   sp->nmm = static_cast<int>(rup(m, 16));
   sp->cw1 = m <= 32 ? 128 : 64;
   sp->qbytes = 2 * sp->nmm * 128;
-  sp->pstride = static_cast<int>(rup(m * m, 4));
+  sp->pstride = static_cast<int>(rup(2 * m * m, 4));
   const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns of X0
   const size_t p1 = static_cast<size_t>(m) * sp->cw1 * (esg + (step ? 4 : 0));
   const size_t p2 = static_cast<size_t>(m) * 128 * esw;
@@ -231,8 +231,9 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) + gs + 512 + 1024;
   if (fixed >= static_cast<size_t>(kSmallSmemLimit)) return false;
   const int tcol = static_cast<int>(rup(sp->nmm, 32));
+  // TMEM: Gram accumulators in [0, 128), one O slot (2 tcol columns) per stage
   sp->stages = static_cast<int>(std::min<size_t>((kSmallSmemLimit - fixed) / sp->stage_bytes,
-                                                 std::min(kSmallMaxStages, 384 / tcol)));
+                                                 std::min(kSmallMaxStages, 384 / (2 * tcol))));
   if (sp->stages < 2) return false;
   int64_t wb = std::min<int64_t>(2048, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);

@@ -111,7 +111,7 @@ struct GemmParams {
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
-constexpr int kSmallThreads = 352;         // warp 0 loads, 1 MMA, 2..9 consumers, 10 stores
+constexpr int kSmallThreads = 320;         // warp 0 loads, 1 MMA, 2..9 consumers
 constexpr int kSmallCons = 256;            // consumer threads
 constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O slot s at 128 + s * tcol
 constexpr int kSmallMaxStages = 8;
@@ -151,13 +151,13 @@ struct SmallParams {
   int xbytes;        // one item's X0 image: (wb / 64) * mr * 128
   int x_off;         // X0 tile inside a stage (1024-aligned); a zero gap follows it
   int qbytes;        // one Q image: hi and lo, nmm rows x 128 bytes each
-  int pstride;       // floats per partial Gram (m * m rounded up to 4)
+  int pstride;       // floats per item's partial Gram blocks (2 m^2 rounded up to 4)
   int steps;
   float coef[kMaxSteps][3];
   int step_mode, nesterov;
   float mu, lr, wd, eps;
   uint8_t* ximg;                // [items][xbytes] bf16 X0 images (shared-memory layout)
-  float* part;                  // [items][pstride] partial Gram matrices
+  float* part;                  // [items][pstride] partial Grams (two stacked blocks when cw1 = 128)
   uint8_t* qimg;                // [total_mats][qbytes] Q = hi + lo operand images
   unsigned* arrive;             // [2][cap]: items arrived per matrix, slot epoch % 2
   unsigned long long* ready_list;   // [total_mats] (epoch << 32) | matrix, in publication order

@@ -47,9 +47,8 @@ constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
 
 // Shared-memory control block: mbarriers, the TMEM slot and CTA flags.
 struct SmallBars {
-  uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], mma_done[kSmallMaxStages],
-      ring_empty[kSmallMaxStages];
-  uint64_t gram_full[2], img_done[2], q_full[2], q_free[2];
+  uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], mma_done[kSmallMaxStages];
+  uint64_t gram_full[2], q_full[2], q_free[2];
   uint32_t tslot;
   int last;
   int abort;
@@ -136,11 +135,6 @@ struct Ring {
   }
 };
 
-__device__ __forceinline__ const SmallSlice& slice_of(const SmallParams& p, int mat) {
-  int si = 0;
-  while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
-  return p.s[si];
-}
 
 __device__ __forceinline__ float ld_elem(const void* base, int dtype, int64_t e) {
   return dtype == 0 ? static_cast<const float*>(base)[e]
@@ -208,7 +202,7 @@ __device__ __forceinline__ void cons_sync() { ptx::named_bar(kConsBar, kT); }
 // Per step three phases: {T = R^2, P = aI + bR + cT}, {T = P R, Q' = P Q},
 // {R = T P} (the first step takes Q = P, the last needs neither R nor T).
 template <int TI, int TJ, int LD>
-__device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
+__device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
   const int m = p.m;
   constexpr int MM = LD * LD;
   float* R = gs;
@@ -220,17 +214,24 @@ __device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
   const int i0 = TI * (t >> 4), j0 = TJ * (t & 15);
   // R_0 (unnormalised) = sum of the item partials in block order; up to 8
   // partial loads of an element are in flight together; the padding is zero
+  // partial block q (item q / nblk, stacked block q % nblk) at
+  // part + (mat nb + q / nblk) pstride + (q % nblk) m^2
   const float* part = p.part + static_cast<size_t>(mat) * p.nb * p.pstride;
+  const int nblk = p.cw1 == 128 ? 2 : 1;
+  const int nq = p.nb * nblk;
   for (int e = t; e < MM; e += kT) {
     const int i = e / LD, j = e - i * LD;
     float acc = 0.f;
     if (i < m && j < m) {
       const int src = i * m + j;
-      for (int b0 = 0; b0 < p.nb; b0 += 8) {
+      for (int b0 = 0; b0 < nq; b0 += 8) {
         float v[8];
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
-          v[b] = b0 + b < p.nb ? __ldcg(part + static_cast<size_t>(b0 + b) * p.pstride + src) : 0.f;
+        for (int b = 0; b < 8; ++b) {
+          const int q = b0 + b;
+          v[b] = q < nq ? __ldcg(part + static_cast<size_t>(q / nblk) * p.pstride + (q % nblk) * m * m + src)
+                        : 0.f;
+        }
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc += v[b];
       }
@@ -331,8 +332,10 @@ __device__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
 //                 reloaded from the item's image) at x_off.
 // A 2 KB zero gap follows the X0 tile: the apply's K padding (rows mr..nmm-1
 // of the second chunk) reads it.  Row-major matrices give [m][cols] tiles,
-// transposed ones [cols][m].  TMA fills out-of-matrix elements with zero and
-// clips them on the way back.
+// transposed ones [cols][m].  TMA fills out-of-matrix elements with zero.
+// Results (M', the X0 image, W' or O) go from registers straight to global
+// memory, so a stage is free once the consumers and the MMA issuer are done
+// with it.
 enum StageKind : int { kStageP1 = 0, kStageP2 = 1, kStageP1End = 2, kStageEnd = 3 };
 
 // Stage descriptor flags
@@ -342,14 +345,12 @@ __device__ __forceinline__ uint32_t mom_off(const SmallParams& p, const SmallSli
   return static_cast<uint32_t>(p.m * p.cw1 * (S.g_dtype == 0 ? 4 : 2));
 }
 
-// Element-wise tile copy between global memory and a stage (slices whose rows
-// are not TMA-legal): `cols` X columns from column gj0; to_smem also writes
-// zero outside the matrix.
-template <bool TO_SMEM>
-__device__ void copy_tile(const SmallParams& p, const SmallSlice& S, int dtype, void* gbase,
-                          int64_t moff, int64_t gj0, int cols, uint8_t* st, int lane) {
+// Element-wise copy of a tile from global memory into a stage (slices whose
+// rows are not TMA-legal), zero outside the matrix: `cols` X columns from gj0.
+__device__ void copy_tile_in(const SmallParams& p, const SmallSlice& S, int dtype,
+                             const void* gbase, int64_t moff, int64_t gj0, int cols, uint8_t* st,
+                             int lane) {
   const int m = p.m, n = p.n;
-  const int es = dtype == 0 ? 4 : 2;
   for (int idx = lane; idx < m * cols; idx += 32) {
     int r, c;
     if (!S.trans) {
@@ -362,16 +363,60 @@ __device__ void copy_tile(const SmallParams& p, const SmallSlice& S, int dtype, 
     const uint32_t so = static_cast<uint32_t>(S.trans ? c * m + r : r * cols + c);
     const bool in = gj0 + c < n;
     const int64_t e = moff + (S.trans ? (gj0 + c) * m + r : static_cast<int64_t>(r) * n + gj0 + c);
-    if (TO_SMEM) {
-      if (es == 4) reinterpret_cast<float*>(st)[so] = in ? static_cast<const float*>(gbase)[e] : 0.f;
-      else
-        reinterpret_cast<__nv_bfloat16*>(st)[so] =
-            in ? static_cast<const __nv_bfloat16*>(gbase)[e] : __float2bfloat16_rn(0.f);
-    } else if (in) {
-      if (es == 4) static_cast<float*>(gbase)[e] = reinterpret_cast<const float*>(st)[so];
-      else static_cast<__nv_bfloat16*>(gbase)[e] = reinterpret_cast<const __nv_bfloat16*>(st)[so];
-    }
+    if (dtype == 0) reinterpret_cast<float*>(st)[so] = in ? static_cast<const float*>(gbase)[e] : 0.f;
+    else
+      reinterpret_cast<__nv_bfloat16*>(st)[so] =
+          in ? static_cast<const __nv_bfloat16*>(gbase)[e] : __float2bfloat16_rn(0.f);
   }
+}
+
+// Per-item constants of the consumers, read once from the parameters (the
+// per-stage code then touches no parameter memory).
+struct ItemCfg {
+  int m, mr, cw, nmm, n;
+  int trans, gvec, wvec;   // transposed layout; 16-byte vector global access legal
+  int esg, wdt;            // G element size; W dtype (0 f32, 1 bf16)
+  int step;                // momentum step (else NS only)
+  uint32_t mom_off, x_off;
+  int chunk_bytes;
+  float mu, decay, stepk;
+  int nesterov;
+  float* Mom;              // matrix base pointers (elements)
+  void* W;
+  int64_t col0;            // first X column of the item
+  uint8_t* img;            // the item's X0 image
+};
+
+__device__ __forceinline__ ItemCfg item_cfg(const SmallParams& p, int item) {
+  const int mat = item / p.nb;
+  int si = 0;
+  while (si + 1 < p.n_slices && mat >= p.s[si + 1].mat_base) ++si;
+  const SmallSlice& S = p.s[si];
+  const int64_t moff = static_cast<int64_t>(mat - S.mat_base) * p.m * p.n;
+  ItemCfg c;
+  c.m = p.m;
+  c.mr = p.mr;
+  c.cw = p.cw1;
+  c.nmm = p.nmm;
+  c.n = p.n;
+  c.trans = S.trans;
+  c.gvec = S.gbulk;
+  c.wvec = S.wbulk;
+  c.esg = S.g_dtype == 0 ? 4 : 2;
+  c.wdt = S.w_dtype;
+  c.step = p.step_mode;
+  c.mom_off = static_cast<uint32_t>(p.m * p.cw1 * c.esg);
+  c.x_off = static_cast<uint32_t>(p.x_off);
+  c.chunk_bytes = p.mr * 128;
+  c.mu = p.mu;
+  c.decay = 1.f - p.lr * p.wd;
+  c.stepk = p.lr * S.scale;
+  c.nesterov = p.nesterov;
+  c.Mom = S.Mom ? S.Mom + moff : nullptr;
+  c.W = static_cast<uint8_t*>(S.W) + moff * (S.w_dtype == 0 ? 4 : 2);
+  c.col0 = static_cast<int64_t>(item - mat * p.nb) * p.wb;
+  c.img = p.ximg + static_cast<size_t>(item) * p.xbytes;
+  return c;
 }
 
 // ---- consumers: first-phase stage ----------------------------------------------------
@@ -394,41 +439,48 @@ __device__ __forceinline__ void load8_smem(const uint8_t* base, int so, float* v
   }
 }
 
-__device__ __forceinline__ void store8_smem_f32(uint8_t* base, int so, const float* v) {
-  *reinterpret_cast<float4*>(base + so * 4) = make_float4(v[0], v[1], v[2], v[3]);
-  *reinterpret_cast<float4*>(base + so * 4 + 16) = make_float4(v[4], v[5], v[6], v[7]);
-}
-
 // Momentum for 8 elements; d = the NS input (Nesterov or plain momentum).
 template <bool STEP>
-__device__ __forceinline__ void momentum8(const SmallParams& p, const float* gv, float* mo,
-                                          float* d) {
+__device__ __forceinline__ void momentum8(const ItemCfg& c, const float* gv, float* mo, float* d) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if constexpr (STEP) {
-      mo[j] = fmaf(p.mu, mo[j], gv[j]);                       // M_t = mu M_{t-1} + G
-      d[j] = p.nesterov ? fmaf(p.mu, mo[j], gv[j]) : mo[j];
+      mo[j] = fmaf(c.mu, mo[j], gv[j]);                       // M_t = mu M_{t-1} + G
+      d[j] = c.nesterov ? fmaf(c.mu, mo[j], gv[j]) : mo[j];
     } else {
       d[j] = gv[j];
     }
   }
 }
 
-// First-phase stage: M' written back in place (the storer moves it out), and
-// X0 = bf16(D) into the stage's X0 tile (rows mr, cw1 / 64 chunks; rows m..mr-1
-// zero).
+// 8 contiguous M' values to global memory (nv of them inside the matrix).
+__device__ __forceinline__ void store_mom8(float* dst, int nv, bool vec, const float* v) {
+  if (vec && nv == 8) {
+    __stcs(reinterpret_cast<float4*>(dst), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<float4*>(dst + 4), make_float4(v[4], v[5], v[6], v[7]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nv) dst[j] = v[j];
+  }
+}
+
+// First-phase stage of X columns [c0, c0 + cw1) of the item: M' to global
+// memory, X0 = bf16(D) into the stage's X0 tile (rows mr, cw1 / 64 chunks;
+// rows m..mr-1 and columns outside the matrix zero) and to the item's image.
 template <int ESG, bool STEP>
-__device__ void consume_p1(const SmallParams& p, const SmallSlice& S, uint8_t* st, int t) {
-  const int m = p.m, cw = p.cw1;
-  const int chunk_bytes = p.mr * 128;
-  uint8_t* smom = st + mom_off(p, S);
-  uint8_t* sx = st + p.x_off;
-  if (!S.trans) {
-    // mr * cw1 / 8 <= 512 groups of 8: at most two per thread, whose loads are
-    // all issued before the in-place stores
+__device__ void consume_p1(const ItemCfg& c, int c0, uint8_t* st, int t) {
+  const int m = c.m, cw = c.cw, cb = c.chunk_bytes;
+  const uint8_t* smom = st + c.mom_off;
+  uint8_t* sx = st + c.x_off;
+  const int64_t gjs = c.col0 + c0;             // first global X column of the stage
+  const int ncols = static_cast<int>(min(static_cast<int64_t>(cw), c.n - gjs));
+  if (!c.trans) {
+    // mr * cw1 / 8 <= 512 groups of 8: at most two per thread, whose shared
+    // loads are all issued first
     const int gpr = cw >> 3;
     const int sh = gpr == 16 ? 4 : 3;                  // cw1 is 128 or 64
-    const int ng = p.mr * gpr;
+    const int ng = c.mr * gpr;
     float gv[2][8], mo[2][8];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -449,26 +501,29 @@ __device__ void consume_p1(const SmallParams& p, const SmallSlice& S, uint8_t* s
       if (g >= ng) continue;
       const int r = g >> sh, c8 = (g & (gpr - 1)) << 3;
       float d[8];
-      momentum8<STEP>(p, gv[u], mo[u], d);
+      momentum8<STEP>(c, gv[u], mo[u], d);
       if constexpr (STEP) {
-        if (r < m) store8_smem_f32(smom, r * cw + c8, mo[u]);
+        if (r < m && c8 < ncols)
+          store_mom8(c.Mom + static_cast<int64_t>(r) * c.n + gjs + c8, min(8, ncols - c8), c.gvec, mo[u]);
       }
       uint4 q;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
 #pragma unroll
       for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
-      *reinterpret_cast<uint4*>(sx + (c8 >> 6) * chunk_bytes + ptx::sw128_offset(r, (c8 & 63) * 2)) = q;
+      const uint32_t off = ptx::sw128_offset(r, (c8 & 63) * 2);
+      *reinterpret_cast<uint4*>(sx + (c8 >> 6) * cb + off) = q;
+      __stcg(reinterpret_cast<uint4*>(c.img + ((c0 + c8) >> 6) * cb + off), q);
     }
   } else {
-    const int ig = p.mr >> 3;
+    const int ig = c.mr >> 3;
     const float inv_ig = 1.f / static_cast<float>(ig);
     for (int g = t; g < cw * ig; g += kT) {
-      const int c = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_ig);
-      const int r = (g - c * ig) << 3;
+      const int cc = __float2int_rd((static_cast<float>(g) + 0.5f) * inv_ig);
+      const int r = (g - cc * ig) << 3;
       const int nv = min(8, m - r);
-      const int so = c * m + r;
+      const int so = cc * m + r;
       float gv[8], mo[8], d[8];
-      if (nv == 8 && S.gbulk) {
+      if (nv == 8 && c.gvec) {
         load8_smem<ESG>(st, so, gv);
         if constexpr (STEP) load8_smem<4>(smom, so, mo);
       } else {
@@ -478,33 +533,29 @@ __device__ void consume_p1(const SmallParams& p, const SmallSlice& S, uint8_t* s
           mo[j] = (STEP && j < nv) ? reinterpret_cast<const float*>(smom)[so + j] : 0.f;
         }
       }
-      momentum8<STEP>(p, gv, mo, d);
+      momentum8<STEP>(c, gv, mo, d);
       if constexpr (STEP) {
-        if (nv == 8 && S.gbulk) {
-          store8_smem_f32(smom, so, mo);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (j < nv) reinterpret_cast<float*>(smom)[so + j] = mo[j];
-        }
+        if (cc < ncols && nv > 0) store_mom8(c.Mom + (gjs + cc) * m + r, nv, c.gvec != 0, mo);
       }
-      uint8_t* colp = sx + (c >> 6) * chunk_bytes;
-      const uint32_t byte = (c & 63) * 2;
+      const int ci = c0 + cc;
+      const uint32_t byte = (cc & 63) * 2, ibyte = (ci & 63) * 2;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<__nv_bfloat16*>(colp + ptx::sw128_offset(r + j, byte)) =
-            __float2bfloat16_rn(j < nv ? d[j] : 0.f);
+      for (int j = 0; j < 8; ++j) {
+        const __nv_bfloat16 v = __float2bfloat16_rn(j < nv ? d[j] : 0.f);
+        *reinterpret_cast<__nv_bfloat16*>(sx + (cc >> 6) * cb + ptx::sw128_offset(r + j, byte)) = v;
+        *reinterpret_cast<__nv_bfloat16*>(c.img + (ci >> 6) * cb + ptx::sw128_offset(r + j, ibyte)) = v;
+      }
     }
   }
 }
 
-__device__ void consume_p1_any(const SmallParams& p, const SmallSlice& S, uint8_t* st, int t) {
-  if (S.g_dtype == 0) {
-    if (p.step_mode) consume_p1<4, true>(p, S, st, t);
-    else consume_p1<4, false>(p, S, st, t);
+__device__ void consume_p1_any(const ItemCfg& c, int c0, uint8_t* st, int t) {
+  if (c.esg == 4) {
+    if (c.step) consume_p1<4, true>(c, c0, st, t);
+    else consume_p1<4, false>(c, c0, st, t);
   } else {
-    if (p.step_mode) consume_p1<2, true>(p, S, st, t);
-    else consume_p1<2, false>(p, S, st, t);
+    if (c.step) consume_p1<2, true>(c, c0, st, t);
+    else consume_p1<2, false>(c, c0, st, t);
   }
 }
 
@@ -516,50 +567,57 @@ __device__ __forceinline__ float w_ld(const WT* p, int i) {
 }
 
 template <typename WT>
-__device__ __forceinline__ void w_st(WT* p, int i, float v) {
-  if constexpr (sizeof(WT) == 4) p[i] = v;
+__device__ __forceinline__ void w_st(WT* p, int64_t i, float v) {
+  if constexpr (sizeof(WT) == 4) __stcs(p + i, v);
   else p[i] = __float2bfloat16_rn(v);
 }
 
-// 128-column W tile: W' = decay W - stepk O (or O) written back in place from
-// the TMEM slot at `oslot`.  Warp (set, q4) owns lanes 32 q4.. (the columns)
-// and rows 16 set + 32 h .. + 16 of O.
+// 128-column tile at item column c0: O = D[:, q] + D[:, nmm + q] (X0 Q_hi^T +
+// X0 Q_lo^T) from the TMEM slot, W' = decay W - stepk O (W from the stage)
+// or O, to global memory.  Warp (set, q4) owns lanes 32 q4.. (the columns)
+// and rows 16 set + 32 h .. + 16.
 template <typename WT, bool STEP>
-__device__ __noinline__ void epi_tile(const SmallParams& p, const SmallSlice& S, uint8_t* st,
-                                      uint32_t oslot, int set, int q4, int lane, float decay,
-                                      float stepk) {
-  const int m = p.m, nmm = p.nmm;
-  WT* ws = reinterpret_cast<WT*>(st);
+__device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, const uint8_t* st,
+                                         uint32_t oslot, int set, int q4, int lane) {
+  const int m = c.m, nmm = c.nmm;
+  const float decay = c.decay, stepk = c.stepk;
+  const WT* ws = reinterpret_cast<const WT*>(st);
   const int col = 32 * q4 + lane;
-  const int rs = S.trans ? 1 : 128, cs = S.trans ? m : 1;   // element (q, col) at q rs + col cs
+  const int64_t gj = c.col0 + c0 + col;
+  const bool live = gj < c.n;
+  const int rs = c.trans ? 1 : 128, cs = c.trans ? m : 1;   // stage element (q, col)
+  WT* wg = static_cast<WT*>(c.W);
+  const int64_t grs = c.trans ? 1 : c.n;                     // global element (q, gj)
+  const int64_t gbase = c.trans ? gj * m : gj;
   for (int h = 0; h < 2; ++h) {
     const int cq = 16 * set + 32 * h;
     if (cq >= nmm) continue;
-    uint32_t r[16];
-    ptx::tmem_ld_32x32b_x16(oslot + cq + (static_cast<uint32_t>(32 * q4) << 16), r);
-    // all W loads before any store (the stores may alias later loads otherwise)
+    uint32_t rh[16], rl[16];
+    ptx::tmem_ld_32x32b_x16(oslot + cq + (static_cast<uint32_t>(32 * q4) << 16), rh);
+    ptx::tmem_ld_32x32b_x16(oslot + nmm + cq + (static_cast<uint32_t>(32 * q4) << 16), rl);
     float w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) w[j] = (STEP && cq + j < m) ? w_ld(ws, (cq + j) * rs + col * cs) : 0.f;
     ptx::tmem_ld_wait();
+    if (!live) continue;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       if (cq + j < m) {
-        const float o = __uint_as_float(r[j]);
-        w_st(ws, (cq + j) * rs + col * cs, STEP ? fmaf(decay, w[j], -stepk * o) : o);
+        const float o = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+        w_st(wg, gbase + (cq + j) * grs, STEP ? fmaf(decay, w[j], -stepk * o) : o);
       }
     }
   }
 }
 
-__device__ void epi_tile_any(const SmallParams& p, const SmallSlice& S, uint8_t* st,
-                             uint32_t oslot, int set, int q4, int lane, float decay, float stepk) {
-  if (S.w_dtype == 0) {
-    if (p.step_mode) epi_tile<float, true>(p, S, st, oslot, set, q4, lane, decay, stepk);
-    else epi_tile<float, false>(p, S, st, oslot, set, q4, lane, decay, stepk);
+__device__ void epi_tile_any(const ItemCfg& c, int c0, const uint8_t* st, uint32_t oslot, int set,
+                             int q4, int lane) {
+  if (c.wdt == 0) {
+    if (c.step) epi_tile<float, true>(c, c0, st, oslot, set, q4, lane);
+    else epi_tile<float, false>(c, c0, st, oslot, set, q4, lane);
   } else {
-    if (p.step_mode) epi_tile<__nv_bfloat16, true>(p, S, st, oslot, set, q4, lane, decay, stepk);
-    else epi_tile<__nv_bfloat16, false>(p, S, st, oslot, set, q4, lane, decay, stepk);
+    if (c.step) epi_tile<__nv_bfloat16, true>(c, c0, st, oslot, set, q4, lane);
+    else epi_tile<__nv_bfloat16, false>(c, c0, st, oslot, set, q4, lane);
   }
 }
 
@@ -613,18 +671,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const int chunk_bytes = p.mr * 128;
   const int tiles = wb / 128;
   const int s1 = wb / p.cw1;               // first-phase stages per item
-  const int tcol = (nmm + 31) & ~31;       // TMEM columns of O per 128-column tile
+  const int oslot_cols = 2 * ((nmm + 31) & ~31);   // O slot: X0 Q_hi^T then X0 Q_lo^T
+  const bool stack = p.cw1 == 128;         // first phase: both chunks of a stage as one operand
+  const int ngram = stack ? 2 * p.mr : nmm;          // Gram MMA N
 
   if (tid == 0) {
     for (int i = 0; i < kSmallMaxStages; ++i) {
       ptx::mbar_init(&B->ring_full[i], 1);
       ptx::mbar_init(&B->cons_done[i], kT / 32);
       ptx::mbar_init(&B->mma_done[i], 1);
-      ptx::mbar_init(&B->ring_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&B->gram_full[i], 1);
-      ptx::mbar_init(&B->img_done[i], 1);
       ptx::mbar_init(&B->q_full[i], 1);
       ptx::mbar_init(&B->q_free[i], 1);
     }
@@ -647,9 +705,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     // ======================= producer (loads) =======================
     Ring rg;
     bool ok = true;
-    // Hands the next stage to the other roles: descriptor, then the tile(s).
+    // Hands the next stage to the other roles once its previous use is done
+    // (consumers and MMA issuer): descriptor, then the tile(s).
     auto put = [&](int kind, int item, int c0, int flags) -> bool {
-      if (!mwait_warp(&B->ring_empty[rg.stage], rg.phase ^ 1u, ctx)) return false;
+      if (!mwait_warp(&B->cons_done[rg.stage], rg.phase ^ 1u, ctx)) return false;
+      if (!mwait_warp(&B->mma_done[rg.stage], rg.phase ^ 1u, ctx)) return false;
       uint8_t* st = ring + rg.stage * p.stage_bytes;
       uint64_t* full = &B->ring_full[rg.stage];
       uint32_t tx = 0;
@@ -664,8 +724,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             tma = true;
             tx = static_cast<uint32_t>(m * p.cw1 * ((S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0)));
           } else {
-            copy_tile<true>(p, S, S.g_dtype, const_cast<void*>(S.G), ir.moff, gj0, p.cw1, st, lane);
-            if (p.step_mode) copy_tile<true>(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
+            copy_tile_in(p, S, S.g_dtype, S.G, ir.moff, gj0, p.cw1, st, lane);
+            if (p.step_mode) copy_tile_in(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
           }
         } else {   // second phase: W tile (step mode) and the X0 tile from the image
           tx = static_cast<uint32_t>(2 * chunk_bytes);
@@ -674,7 +734,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
               tma = true;
               tx += static_cast<uint32_t>(m * 128 * (S.w_dtype == 0 ? 4 : 2));
             } else {
-              copy_tile<true>(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
+              copy_tile_in(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
             }
           }
         }
@@ -753,70 +813,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         ok = put(kStageP2, item, 128 * t, (t == 0 ? kFirst : 0) | (t == tiles - 1 ? kLast : 0));
     }
     put(kStageEnd, -1, 0, 0);
-  } else if (warp == 10) {
-    // ======================= storer =======================
-    // Moves each finished stage's outputs back to global memory (first
-    // phase: M' and the X0 slice of the item's image; second phase: W' or
-    // O), then frees the stage.
-    Ring rg;
-    int k1 = 0;   // first-phase items completed
-    for (;;) {
-      if (!mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx)) break;
-      const int kind = B->desc[rg.stage][0];
-      const int item = B->desc[rg.stage][1];
-      const int c0 = B->desc[rg.stage][2];
-      const int flags = B->desc[rg.stage][3];
-      if (kind == kStageEnd) break;
-      bool sok = mwait_warp(&B->cons_done[rg.stage], rg.phase, ctx);
-      if (sok && kind == kStageP1) sok = mwait_warp(&B->mma_done[rg.stage], rg.phase, ctx);
-      if (!sok) break;
-      uint8_t* st = ring + rg.stage * p.stage_bytes;
-      if (item >= 0) {
-        const ItemRef ir = item_ref(p, item);
-        const SmallSlice& S = p.s[ir.si];
-        const int64_t gj0 = ir.col0 + c0;
-        int x, y;
-        tile_xy(S, gj0, x, y);
-        const int z = ir.mat - S.mat_base;
-        if (kind == kStageP1) {
-          if (p.step_mode) {
-            if (S.gbulk) {
-              if (lane == 0) ptx::tma_store_3d(&p.tm[ir.si][1], st + mom_off(p, S), x, y, z);
-            } else {
-              copy_tile<false>(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
-            }
-          }
-          if (lane == 0)
-            ptx::bulk_store(p.ximg + static_cast<size_t>(item) * p.xbytes + (c0 / 64) * chunk_bytes,
-                            st + p.x_off, static_cast<uint32_t>((p.cw1 / 64) * chunk_bytes));
-        } else if (S.wbulk) {
-          if (lane == 0) ptx::tma_store_3d(&p.tm[ir.si][2], st, x, y, z);
-        } else {
-          copy_tile<false>(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
-        }
-        if (lane == 0) {
-          ptx::bulk_commit();
-          ptx::bulk_wait_read<0>();
-          if (kind == kStageP1 && (flags & kLast)) {
-            // the item's image is complete in global memory
-            ptx::bulk_wait_group<0>();
-            ptx::fence_proxy_async_global();
-            __threadfence();
-            ptx::mbar_arrive(&B->img_done[k1 & 1]);
-          }
-        }
-        if (kind == kStageP1 && (flags & kLast)) ++k1;
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&B->ring_empty[rg.stage]);
-      rg.next(NS);
-    }
-    if (lane == 0) ptx::bulk_wait_group<0>();
-    __syncwarp();
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
-    const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, nmm);
-    const uint32_t idesc_app = idesc_gram | (1u << 15);   // A MN-major
+    const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, ngram);
+    const uint32_t idesc_app = ptx::idesc_bf16_f32(128, 2 * nmm) | (1u << 15);   // A MN-major
     if (lane == 0) {
       Ring rg;
       int k1 = 0, k2 = -1;
@@ -827,17 +827,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         if (kind == kStageEnd) break;
         const uint32_t sx = ptx::smem_u32(ring + rg.stage * p.stage_bytes + p.x_off);
         if (kind == kStageP1) {
-          // partial Gram of this stage's X0 columns into accumulator k1 & 1
+          // partial Gram of this stage's X0 tile into accumulator k1 & 1: the
+          // two 64-column chunks stacked as 2 mr rows (or one chunk), 4 K-steps
           if (!mwait(&B->cons_done[rg.stage], rg.phase, ctx)) break;
           ptx::tc_fence_after();
           const int g = k1 & 1;
-          for (int kc = 0; kc < p.cw1 / 64; ++kc) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kc * chunk_bytes + kk * 32);
-              ptx::umma_bf16(tmem + 64 * g, d, d, idesc_gram,
-                             ((flags & kFirst) && kc == 0 && kk == 0) ? 0u : 1u);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kk * 32);
+            ptx::umma_bf16(tmem + 64 * g, d, d, idesc_gram, ((flags & kFirst) && kk == 0) ? 0u : 1u);
           }
           ptx::umma_commit(&B->mma_done[rg.stage]);
           if (flags & kLast) {
@@ -850,14 +848,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             if (!mwait(&B->q_full[k2 & 1], (k2 >> 1) & 1, ctx)) break;
           }
           ptx::tc_fence_after();
+          // X0 (MN-major, 128 columns) times [Q_hi; Q_lo]^T: one MMA per K-step
           const uint32_t sq = ptx::smem_u32(sm + p.off_q + (k2 & 1) * p.qbytes);
-          const uint32_t ocol = 128 + tcol * rg.stage;
+          const uint32_t ocol = 128 + oslot_cols * rg.stage;
           for (int j = 0; j < nmm / 16; ++j) {
             const uint64_t a = ptx::sdesc_mnmajor_sw128(sx + j * 2048, chunk_bytes, 1024);
             ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + j * 32), idesc_app,
                            j != 0 ? 1u : 0u);
-            ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + nmm * 128 + j * 32),
-                           idesc_app, 1u);
           }
           ptx::umma_commit(&B->mma_done[rg.stage]);
           if (flags & kLast) ptx::umma_commit(&B->q_free[k2 & 1]);
@@ -875,39 +872,42 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const int cw = warp - 2;
     bool ok = true;
     Ring rg;
-    // Deferred end of a first-phase item: partial Gram to the workspace,
-    // arrival, and the Gram-space step if it completed its matrix.
+    // Deferred end of a first-phase item: partial Gram (both stacked blocks)
+    // to the workspace, arrival, and the Gram-space step if it completed its
+    // matrix.
     auto finish = [&](int item, int k) {
       const int g = k & 1;
       const int mat = item / p.nb;
-      bool gok = mwait_warp(&B->gram_full[g], (k >> 1) & 1, ctx);
+      const bool gok = mwait_warp(&B->gram_full[g], (k >> 1) & 1, ctx);
       ptx::tc_fence_after();
-      if (gok && ok && (warp == 4 || warp == 5) && (warp - 4) * 32 < m) {
-        const int i = (warp - 4) * 32 + lane;
-        float* dstp = p.part + static_cast<size_t>(item) * p.pstride;
+      const int nblk = stack ? 2 : 1;
+      if (gok && ok && (warp == 4 || warp == 5) && (warp - 4) * 32 < nblk * p.mr) {
+        // lane L holds row L of D: block b = L / mr, row i = L - b mr, whose
+        // diagonal block starts at column b mr
+        const int L = (warp - 4) * 32 + lane;
+        const int bb = L >= p.mr ? 1 : 0, i = L - bb * p.mr;
+        float* dstp = p.part + static_cast<size_t>(item) * p.pstride + bb * m * m;
+        const uint32_t lbase = tmem + 64 * g + (static_cast<uint32_t>((warp - 4) * 32) << 16);
         for (int c0 = 0; c0 < m; c0 += 32) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(tmem + 64 * g + c0 + (static_cast<uint32_t>((warp - 4) * 32) << 16),
-                                  r);
+          uint32_t r0[32], r1[32];
+          ptx::tmem_ld_32x32b_x32(lbase + c0, r0);
+          if (stack) ptx::tmem_ld_32x32b_x32(lbase + p.mr + c0, r1);
           ptx::tmem_ld_wait();
-          if (i < m) {
+          if (L < nblk * p.mr && i < m) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (c0 + j < m) __stcg(dstp + i * m + c0 + j, __uint_as_float(r[j]));
+              if (c0 + j < m) __stcg(dstp + i * m + c0 + j, __uint_as_float(bb ? r1[j] : r0[j]));
           }
         }
-        __threadfence();
       }
       ok = ok && gok;
+      // the item's image and partial must be visible before the arrival
+      __threadfence();
       ptx::tc_fence_before();
       cons_sync();
-      if (t == 0) {
-        // the image must be complete in global memory before the arrival
-        const bool iok = mwait(&B->img_done[g], (k >> 1) & 1, ctx);
-        __threadfence();
-        B->last = (ok && iok && !B->abort &&
+      if (t == 0)
+        B->last = (ok && !B->abort &&
                    atomicAdd(larr + mat, 1u) + 1u == static_cast<unsigned>(p.nb)) ? 1 : 0;
-      }
       cons_sync();
       if (B->last) {
         __threadfence();
@@ -953,11 +953,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         release();
         break;
       }
-      const SmallSlice& S = slice_of(p, item / p.nb);
+      const ItemCfg ic = item_cfg(p, item);
       for (int s = 0; s < s1; ++s) {
         const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
         ok = ok && sok;
-        if (ok) consume_p1_any(p, S, ring + rg.stage * p.stage_bytes, t);
+        if (ok) consume_p1_any(ic, s * p.cw1, ring + rg.stage * p.stage_bytes, t);
         release();
       }
       if (prev >= 0) finish(prev, prevk);
@@ -966,20 +966,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
     if (prev >= 0) finish(prev, prevk);
     // ---- second phase: every stage until the end token ----
-    const float decay = 1.f - p.lr * p.wd;
     const int q4 = warp & 3, set = cw >> 2;
+    int cur = -1;
+    ItemCfg ic{};
     while (ok) {
       if (!mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx)) break;
       const int kind = B->desc[rg.stage][0];
       if (kind == kStageEnd) break;
       const int item = B->desc[rg.stage][1];
-      const SmallSlice& S = slice_of(p, item / p.nb);
+      if (item != cur) {
+        cur = item;
+        ic = item_cfg(p, item);
+      }
       const bool sok = mwait_warp(&B->mma_done[rg.stage], rg.phase, ctx);
       ok = ok && sok;
       ptx::tc_fence_after();
       if (ok)
-        epi_tile_any(p, S, ring + rg.stage * p.stage_bytes, tmem + 128 + tcol * rg.stage, set, q4,
-                     lane, decay, p.lr * S.scale);
+        epi_tile_any(ic, B->desc[rg.stage][2], ring + rg.stage * p.stage_bytes,
+                     tmem + 128 + oslot_cols * rg.stage, set, q4, lane);
       release();
     }
   }
