@@ -112,7 +112,7 @@ struct GemmParams {
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
 constexpr int kSmallThreads = 320;         // warp 0 loads, 1 MMA, 2..9 consumers
-constexpr int kSmallCons = 256;            // consumer threads
+constexpr int kSmallCons = 256;            // consumer threads (a multiple of 128)
 constexpr int kSmallTmemCols = 512;        // Gram accumulators [0,128); O slot s at 128 + s * tcol
 constexpr int kSmallMaxStages = 8;
 constexpr int kSmallCtrSlots = 64;         // ring of per-launch counter slots

@@ -43,6 +43,7 @@ namespace muon {
 namespace {
 
 constexpr int kT = kSmallCons;      // consumer threads
+constexpr int kSets = kT / 128;     // consumer warp sets (4 warps cover the 128 TMEM lanes)
 constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
 
 // Shared-memory control block: mbarriers, the TMEM slot and CTA flags.
@@ -211,7 +212,10 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
   float* Q = gs + 3 * MM;
   float* Qn = gs + 4 * MM;
   float* sc = gs + 5 * MM;
-  const int i0 = TI * (t >> 4), j0 = TJ * (t & 15);
+  // the 16 x 16 blocks of TI x TJ cover LD x LD: consumer threads 0..255
+  // form the products, the others only take part in the barriers
+  const bool blk = t < 256;
+  const int i0 = TI * ((t & 255) >> 4), j0 = TJ * (t & 15);
   // R_0 (unnormalised) = sum of the item partials in block order; up to 8
   // partial loads of an element are in flight together; the padding is zero
   // partial block q (item q / nblk, stacked block q % nblk) at
@@ -258,7 +262,7 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
     const bool more = k + 1 < p.steps;
     {   // T = R^2 (in registers), P = aI + bR + cR^2 (zero outside m x m)
       float acc[TI][TJ], pv[TI][TJ];
-      mm_block<TI, TJ, LD>(R, R, i0, j0, acc);
+      if (blk) mm_block<TI, TJ, LD>(R, R, i0, j0, acc);
 #pragma unroll
       for (int r = 0; r < TI; ++r)
 #pragma unroll
@@ -268,19 +272,23 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
                           ? fmaf(b, R[i * LD + j], c * acc[r][cc]) + (i == j ? a : 0.f)
                           : 0.f;
         }
-      st_block<TI, TJ, LD>(P, i0, j0, pv);
-      if (k == 0) st_block<TI, TJ, LD>(Q, i0, j0, pv);
+      if (blk) st_block<TI, TJ, LD>(P, i0, j0, pv);
+      if (blk && k == 0) st_block<TI, TJ, LD>(Q, i0, j0, pv);
     }
     cons_sync();
     if (more || k > 0) {
       float acc[TI][TJ];
       if (more) {
-        mm_block<TI, TJ, LD>(P, R, i0, j0, acc);     // T = P R
-        st_block<TI, TJ, LD>(T, i0, j0, acc);
+        if (blk) {
+          mm_block<TI, TJ, LD>(P, R, i0, j0, acc);     // T = P R
+          st_block<TI, TJ, LD>(T, i0, j0, acc);
+        }
       }
       if (k > 0) {
-        mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);     // Q' = P Q
-        st_block<TI, TJ, LD>(Qn, i0, j0, acc);
+        if (blk) {
+          mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);     // Q' = P Q
+          st_block<TI, TJ, LD>(Qn, i0, j0, acc);
+        }
       }
       cons_sync();
       if (k > 0) {
@@ -291,8 +299,10 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
     }
     if (more) {
       float acc[TI][TJ];
-      mm_block<TI, TJ, LD>(T, P, i0, j0, acc);       // R <- P R P
-      st_block<TI, TJ, LD>(R, i0, j0, acc);
+      if (blk) {
+        mm_block<TI, TJ, LD>(T, P, i0, j0, acc);       // R <- P R P
+        st_block<TI, TJ, LD>(R, i0, j0, acc);
+      }
       cons_sync();
     }
   }
@@ -573,44 +583,83 @@ __device__ __forceinline__ void w_st(WT* p, int64_t i, float v) {
 }
 
 // 128-column tile at item column c0: O = D[:, q] + D[:, nmm + q] (X0 Q_hi^T +
-// X0 Q_lo^T) from the TMEM slot, W' = decay W - stepk O (W from the stage)
-// or O, to global memory.  Warp (set, q4) owns lanes 32 q4.. (the columns)
-// and rows 16 set + 32 h .. + 16.
+// X0 Q_lo^T) from the TMEM slot, W' = decay W - stepk O (W from the stage) or
+// O, to global memory.  Warp (set, q4) owns lanes 32 q4.. (the columns) and
+// the 4-row blocks of O with index = set (mod sets), so all sets carry the
+// same number of rows.  Row-major tiles are written back into the stage first and
+// leave as 4-column vectors (one 128-bit store per lane and 4 rows per warp
+// instruction instead of one scalar store per element).
 template <typename WT, bool STEP>
-__device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, const uint8_t* st,
-                                         uint32_t oslot, int set, int q4, int lane) {
+__device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, uint32_t oslot,
+                                         int set, int q4, int lane) {
   const int m = c.m, nmm = c.nmm;
   const float decay = c.decay, stepk = c.stepk;
-  const WT* ws = reinterpret_cast<const WT*>(st);
+  WT* ws = reinterpret_cast<WT*>(st);
   const int col = 32 * q4 + lane;
   const int64_t gj = c.col0 + c0 + col;
-  const bool live = gj < c.n;
-  const int rs = c.trans ? 1 : 128, cs = c.trans ? m : 1;   // stage element (q, col)
+  const uint32_t lq = static_cast<uint32_t>(32 * q4) << 16;
   WT* wg = static_cast<WT*>(c.W);
-  const int64_t grs = c.trans ? 1 : c.n;                     // global element (q, gj)
-  const int64_t gbase = c.trans ? gj * m : gj;
-  for (int h = 0; h < 2; ++h) {
-    const int cq = 16 * set + 32 * h;
-    if (cq >= nmm) continue;
-    uint32_t rh[16], rl[16];
-    ptx::tmem_ld_32x32b_x16(oslot + cq + (static_cast<uint32_t>(32 * q4) << 16), rh);
-    ptx::tmem_ld_32x32b_x16(oslot + nmm + cq + (static_cast<uint32_t>(32 * q4) << 16), rl);
-    float w[16];
+  if (!c.trans) {
+    const int64_t gjw = c.col0 + c0 + 32 * q4;    // first global column of this warp
+    const bool vec = c.wvec && sizeof(WT) == 4 && gjw + 32 <= c.n;
+    for (int q0 = 4 * set; q0 < m; q0 += 4 * kSets) {
+      uint32_t rh[4], rl[4];
+      ptx::tmem_ld_32x32b_x4(oslot + q0 + lq, rh);
+      ptx::tmem_ld_32x32b_x4(oslot + nmm + q0 + lq, rl);
+      float w[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = (STEP && cq + j < m) ? w_ld(ws, (cq + j) * rs + col * cs) : 0.f;
-    ptx::tmem_ld_wait();
-    if (!live) continue;
+      for (int j = 0; j < 4; ++j) w[j] = (STEP && q0 + j < m) ? w_ld(ws, (q0 + j) * 128 + col) : 0.f;
+      ptx::tmem_ld_wait();
+      float v[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (cq + j < m) {
+      for (int j = 0; j < 4; ++j) {
         const float o = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
-        w_st(wg, gbase + (cq + j) * grs, STEP ? fmaf(decay, w[j], -stepk * o) : o);
+        v[j] = STEP ? fmaf(decay, w[j], -stepk * o) : o;
+      }
+      if (vec) {
+        // rows q0..q0+3 x the warp's 32 columns: back into the stage, then lane
+        // l stores row q0 + l / 8, columns 4 (l % 8) .. + 3 of the warp
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (q0 + j < m) reinterpret_cast<float*>(ws)[(q0 + j) * 128 + col] = v[j];
+        __syncwarp();
+        const int rr = q0 + (lane >> 3), cc = 32 * q4 + 4 * (lane & 7);
+        if (rr < m) {
+          const float4 x = *reinterpret_cast<const float4*>(reinterpret_cast<float*>(ws) + rr * 128 + cc);
+          __stcs(reinterpret_cast<float4*>(reinterpret_cast<float*>(wg) + static_cast<int64_t>(rr) * c.n +
+                                           c.col0 + c0 + cc), x);
+        }
+        __syncwarp();
+      } else if (gj < c.n) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (q0 + j < m) w_st(wg, static_cast<int64_t>(q0 + j) * c.n + gj, v[j]);
+      }
+    }
+  } else {
+    const bool live = gj < c.n;
+    WT* wrow = wg + gj * m;
+    for (int cq = 16 * set; cq < nmm; cq += 16 * kSets) {
+      uint32_t rh[16], rl[16];
+      ptx::tmem_ld_32x32b_x16(oslot + cq + lq, rh);
+      ptx::tmem_ld_32x32b_x16(oslot + nmm + cq + lq, rl);
+      float w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = (STEP && cq + j < m) ? w_ld(ws, col * m + cq + j) : 0.f;
+      ptx::tmem_ld_wait();
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (cq + j < m) {
+          const float o = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+          w_st(wrow, cq + j, STEP ? fmaf(decay, w[j], -stepk * o) : o);
+        }
       }
     }
   }
 }
 
-__device__ void epi_tile_any(const ItemCfg& c, int c0, const uint8_t* st, uint32_t oslot, int set,
+__device__ void epi_tile_any(const ItemCfg& c, int c0, uint8_t* st, uint32_t oslot, int set,
                              int q4, int lane) {
   if (c.wdt == 0) {
     if (c.step) epi_tile<float, true>(c, c0, st, oslot, set, q4, lane);
