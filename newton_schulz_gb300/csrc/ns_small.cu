@@ -14,23 +14,26 @@
 //
 // A work item is (matrix, block of wb columns of X).  One cooperative launch,
 // one CTA per SM, every CTA resident; the CTA is warp-specialised:
-//   warp 0      producer: bulk copies (cp.async.bulk) of G/Mom, later W, row
-//               segments into a ring of shared-memory stages, and of the X0
-//               and Q images for the second phase;
+//   warp 0      producer: TMA tile loads of G/Mom (first phase) and W (second
+//               phase) into a ring of shared-memory stages, bulk copies of
+//               the X0 tiles and Q images for the second phase;
 //   warp 1      allocates TMEM and issues the tcgen05 MMAs;
 //   warps 2..9  consumers: momentum, X0 and the epilogues.
-// Phase 1, per item: M' = mu M + G (written back), D = G + mu M' (Nesterov)
-// or M', X0 = bf16(D) into a double-buffered 128-byte-swizzled tile, whose
-// image is stored to the workspace by one bulk copy; the item's partial
-// Gram X0_blk X0_blk^T (fp32, TMEM) is read one item later, so its MMA
-// overlaps the next item's streaming.  The CTA whose item arrives last for a
-// matrix sums the partials in block order, normalises by the trace
-// (= ||X0||_F^2), runs the Gram-space steps and publishes Q.
-// Phase 2, per item: wait for the matrix's Q, bulk-load the X0 image and Q,
-// O = Q X0 on tcgen05 per 128-column tile (A = MN-major view of X0, M = 128
-// columns, K = m; B = Q) into one of several TMEM slots, while W tiles
-// stream through the ring; the consumers write W' = (1 - lr wd) W - lr s O
-// (or O itself) from TMEM.
+// Phase 1, per stage (a range of columns of one item): M' = mu M + G (written
+// back), D = G + mu M' (Nesterov) or M', X0 = bf16(D) written both to the
+// stage's 128-byte-swizzled X0 tile and to the matrix's X0 image in the
+// workspace; the MMA warp accumulates the item's Gram X0_blk X0_blk^T (fp32,
+// TMEM, two 64-column chunks stacked as one 2m-row operand) stage by stage.
+// The item's Gram is read back one item later, so its MMAs overlap the next
+// item's streaming.  The CTA whose item arrives last for a matrix sums the
+// partials in block order, normalises by the trace (= ||X0||_F^2), runs the
+// Gram-space steps and publishes Q.
+// Phase 2, per item: wait for the matrix's Q, bulk-load Q (hi rows, then lo
+// rows); per 128-column tile the producer brings the W tile (TMA) and the X0
+// tile (bulk copy from the image), and the MMA warp forms O = Q X0 (A =
+// MN-major view of X0, M = 128 columns, K = m; B = [Q_hi; Q_lo], N = 2 nmm)
+// into the stage's TMEM slot; the consumers write W' = (1 - lr wd) W - lr s O
+// (or O itself) from TMEM, summing the hi and lo halves.
 // Arrival counters carry a per-launch epoch tag, so a launch never depends on
 // what an earlier (possibly aborted) launch left in them.  Every wait is
 // bounded; a timeout sets a status bit and the CTA's abort flag, after which

@@ -1,5 +1,6 @@
-"""GPU parity of the fused small-m cluster kernel (m <= 64), and of the grouped
-GEMM path on the same shapes (MUON_SMALL_PATH=0), against the float64 oracle."""
+"""GPU parity of the fused small-m kernel (m <= 64, Gram-space Newton-Schulz),
+and of the grouped GEMM path on the same shapes (MUON_SMALL_PATH=0), against
+the float64 oracle."""
 import os
 
 import numpy as np
@@ -31,10 +32,10 @@ SHAPES = [
     (3, 8, 300),        # m = 8
     (2, 33, 1000),      # m = 33: 48-wide MMA N, ragged n
     (2, 1000, 48),      # transposed, m = 48
-    (6, 64, 4097),      # m = 64, several CTAs per matrix, ragged tail
+    (6, 64, 4097),      # m = 64, several items per matrix, ragged tail, element-wise copies
     (20, 24, 2048),     # many matrices
-    (1, 24, 10240),     # the tall-skinny shape, eight CTAs
-    (3, 5000, 17),      # transposed, odd m
+    (1, 24, 10240),     # the tall-skinny shape, one matrix split into many items
+    (3, 5000, 17),      # transposed, odd m, element-wise copies (17 fp32 = 68 B rows)
 ]
 
 
@@ -127,3 +128,19 @@ def test_small_step_multistage_items(trans):
     for i in range(8):
         assert np.linalg.norm(w[i] - w2[i]) <= DW_TOL * np.linalg.norm(w2[i] - host["W"][i])
     assert binding.muon_last_launch_count() == 1
+
+
+def test_small_repeat_bitwise_across_counter_ring():
+    """70 launches in a row (more than the 64 per-launch counter slots) give
+    the same bits: no launch depends on counters an earlier one left."""
+    x = torch.randn((5, 24, 3000), generator=torch.Generator().manual_seed(12)).cuda()
+    outs = [torch.empty_like(x) for _ in range(70)]
+    for o in outs:
+        binding.muon_ns_batched_ex(x, binding.make_config(), o)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref = R.ns_batched_ref(_np(x.cpu()))
+    for i in range(5):
+        assert _rel(_np(outs[0])[i], ref[i]) <= NS_TOL
