@@ -88,13 +88,14 @@ def nominal_flops(shapes, steps=STEPS_NS):
 
 
 def algorithmic_bytes(shapes):
-    """Per kernel kind: prep reads G, Mom and writes Mom, X, X^T (bf16);
-    update reads W, the bf16 result and writes W; the fused small-m kernel
-    moves only the compulsory bytes (G read, Mom and W read and written)."""
+    """Per kernel kind: prep reads G, Mom and writes Mom and the bf16 NS
+    operand (one layout); update reads W, the bf16 result and writes W; the
+    fused small-m kernel moves only the compulsory bytes (G read, Mom and W
+    read and written)."""
     prep = upd = fused = 0
     for b, r, c, we, ge in shapes:
         e = b * r * c
-        prep += e * (ge + 4 + 4 + 2 + 2)
+        prep += e * (ge + 4 + 4 + 2)
         upd += e * (we + we + 2)
         fused += e * (ge + 4 + 4 + we + we)
     return {"prep": prep, "update": upd, "fused_small": fused}
@@ -276,6 +277,8 @@ def main():
                     help="skip the host-buffer end-to-end pass (large workloads)")
     ap.add_argument("--layers", type=int, default=None,
                     help="c4 only: number of Llama layers (default 32; a small profiling case)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="c3 only: experts per weight (default 128; a small profiling case)")
     ap.add_argument("--scale-down", type=int, default=1,
                     help="c5 only: divide every dimension (a small profiling case)")
     args = ap.parse_args()
@@ -306,6 +309,8 @@ def main():
         groups = synth.config_c4(dev, layers=args.layers)
     elif args.config == "c5" and args.scale_down > 1:
         groups = synth.config_c5(dev, scale_down=args.scale_down)
+    elif args.config == "c3" and args.experts:
+        groups = synth.config_c3(dev, experts=args.experts)
     else:
         groups = synth.CONFIGS[args.config](dev)
     shapes = _shapes(groups)
@@ -455,6 +460,7 @@ def _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
         "data": "synthetic",
         "config": {"workload": synth.WORKLOAD_NAMES[args.config] + (
                        f" [{args.layers} layers]" if args.config == "c4" and args.layers else "") + (
+                       f" [{args.experts} experts]" if args.config == "c3" and args.experts else "") + (
                        f" [dims / {args.scale_down}]" if args.config == "c5" and args.scale_down > 1
                        else ""), "config": args.config,
                    "matrices": sum(s[0] for s in shapes), "nominal_gflop_per_step": flops / 1e9,

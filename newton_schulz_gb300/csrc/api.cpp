@@ -29,26 +29,6 @@ constexpr float kDefA = 3.4445f, kDefB = -4.7750f, kDefC = 2.0315f, kDefEps = 1e
 constexpr int kDefSteps = 5;
 constexpr float kShiftFrac = 0.58f;   // alpha_k = 0.58 a_k (about 2 for the default quintic)
 
-// ---- driver entry point for tensor maps (no link-time libcuda dependency) ----
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 // ---- global state ---------------------------------------------------------------
 // Data workspace (operands, Gram/polynomial buffers, partials) plus a
 // separate counter buffer.  Every kernel leaves the counters it uses at zero,
@@ -133,10 +113,10 @@ struct SliceP {
 
 struct NsGroupP {
   int64_t m, n, cnt = 0;
-  int64_t m_pad, n_pad;
+  int64_t m_pad;
   int ksplit = 1, kb_per_split = 1, num_kb_gram = 1;
   int64_t tri = 1, prep_tiles = 1;
-  size_t off_X, off_Xt0, off_Xt1, off_A, off_B, off_inv, off_ssq, off_part;
+  size_t off_Xt0, off_Xt1, off_A, off_B, off_inv, off_ssq, off_part;
   size_t ctr_prep, ctr_tile;   // element offsets in the counter buffer
 };
 
@@ -162,7 +142,6 @@ void layout_chunk(ChunkP& ch, int sms) {
   for (auto& g : ch.groups) launch_tiles += g.cnt * gemm_sym_tiles(static_cast<int>(g.m));
   for (auto& g : ch.groups) {
     g.m_pad = rup(g.m, 8);
-    g.n_pad = rup(g.n, 8);
     g.tri = gemm_sym_tiles(static_cast<int>(g.m));
     g.num_kb_gram = static_cast<int>(cdiv(g.n, bk));
     const int64_t tiles = launch_tiles;
@@ -178,7 +157,6 @@ void layout_chunk(ChunkP& ch, int sms) {
     g.ksplit = static_cast<int>(cdiv(g.num_kb_gram, g.kb_per_split));
     g.prep_tiles = cdiv(g.m, kPrepTile) * cdiv(g.n, kPrepTile);
     const size_t e2 = 2;
-    g.off_X = take(static_cast<size_t>(g.cnt * g.m * g.n_pad) * e2);
     g.off_Xt0 = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
     g.off_Xt1 = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
     g.off_A = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
@@ -402,42 +380,17 @@ muon_status_t get_epoch_ctrs(cudaStream_t stream, size_t mats, unsigned** arrive
 }
 
 // ---- tensor maps ---------------------------------------------------------------------
-bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t cnt,
-              int64_t pitch, int64_t mstride, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(cnt)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch * 2),
-                           static_cast<cuuint64_t>(mstride * 2)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(gemm_block_k()),
-                       static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // Tensor map of a stored [cnt][rows][inner] tensor for unswizzled tile copies
 // of box {box_inner, box_rows, 1}; false when the layout is not TMA-legal.
 bool make_tile_map(CUtensorMap* map, const void* base, int dtype, int64_t inner, int64_t rows,
                    int64_t cnt, int box_inner, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   const int64_t es = dtype == MUON_F32 ? 4 : 2;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(cnt)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * es),
-                           static_cast<cuuint64_t>(inner * rows * es)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, dtype == MUON_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                  3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const uint64_t dims[3] = {static_cast<uint64_t>(inner), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(cnt)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(inner * es),
+                               static_cast<uint64_t>(inner * rows * es)};
+  const uint32_t box[3] = {static_cast<uint32_t>(box_inner), static_cast<uint32_t>(box_rows), 1};
+  return encode_tiled(map, dtype == MUON_F32, base, dims, strides, box, false);
 }
 
 // ---- launches ----------------------------------------------------------------------
@@ -665,14 +618,12 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         const int64_t per = q.r * q.c;
         ps.G = static_cast<const char*>(q.G) + s.b0 * per * esize(q.g_dtype);
         ps.Mom = step_mode ? q.Mom + s.b0 * per : nullptr;
-        auto* X = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X) + s.idx0 * g.m * g.n_pad;
+        // the NS operand is kept as Xt = X^T: the stored layout when rows > cols
         auto* Xt = reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt0) + s.idx0 * g.n * g.m_pad;
-        ps.direct = q.trans ? Xt : X;
-        ps.transp = q.trans ? X : Xt;
-        ps.pitch_d = q.trans ? g.m_pad : g.n_pad;
-        ps.pitch_t = q.trans ? g.n_pad : g.m_pad;
-        ps.mstride_d = q.trans ? g.n * g.m_pad : g.m * g.n_pad;
-        ps.mstride_t = q.trans ? g.m * g.n_pad : g.n * g.m_pad;
+        ps.direct = q.trans ? Xt : nullptr;
+        ps.transp = q.trans ? nullptr : Xt;
+        ps.pitch_d = ps.pitch_t = g.m_pad;
+        ps.mstride_d = ps.mstride_t = g.n * g.m_pad;
         ps.ssq_part = reinterpret_cast<float*>(ws + g.off_ssq) + s.idx0 * g.prep_tiles;
         ps.inv = reinterpret_cast<float*>(ws + g.off_inv) + s.idx0;
         ps.cnt = ctr + g.ctr_prep + s.idx0;
@@ -700,96 +651,42 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       if (st != MUON_OK) return st;
     }
     // ---- tensor maps -------------------------------------------------------------
-    // operand P tiles are 128 rows (box bm), operand Q tiles 256 rows (box bn)
-    struct Maps {
-      CUtensorMap Xp, Xq, Ap, Aq, B, Xt[2];
-    };
-    std::vector<Maps> maps(ch.groups.size());
+    std::vector<NsGroupDev> dg(ch.groups.size());
     for (size_t k = 0; k < ch.groups.size(); ++k) {
       const NsGroupP& g = ch.groups[k];
-      const int bm = gemm_block_m(), bn = gemm_block_n();
-      bool ok = make_map(&maps[k].Xp, ws + g.off_X, g.n, g.m, g.cnt, g.n_pad, g.m * g.n_pad, bm) &&
-                make_map(&maps[k].Xq, ws + g.off_X, g.n, g.m, g.cnt, g.n_pad, g.m * g.n_pad, bn) &&
-                make_map(&maps[k].Ap, ws + g.off_A, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bm) &&
-                make_map(&maps[k].Aq, ws + g.off_A, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bn) &&
-                make_map(&maps[k].B, ws + g.off_B, g.m, g.m, g.cnt, g.m_pad, g.m * g.m_pad, bn) &&
-                make_map(&maps[k].Xt[0], ws + g.off_Xt0, g.m, g.n, g.cnt, g.m_pad, g.n * g.m_pad,
-                         bm) &&
-                make_map(&maps[k].Xt[1], ws + g.off_Xt1, g.m, g.n, g.cnt, g.m_pad, g.n * g.m_pad,
-                         bm);
-      if (!ok) return MUON_ERR_CUDA;
+      NsGroupDev& d = dg[k];
+      d.m = g.m;
+      d.n = g.n;
+      d.cnt = g.cnt;
+      d.m_pad = g.m_pad;
+      d.Xt[0] = reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt0);
+      d.Xt[1] = reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt1);
+      d.A = reinterpret_cast<__nv_bfloat16*>(ws + g.off_A);
+      d.B = reinterpret_cast<__nv_bfloat16*>(ws + g.off_B);
+      d.inv = reinterpret_cast<const float*>(ws + g.off_inv);
+      d.partial = reinterpret_cast<float*>(ws + g.off_part);
+      d.tile_cnt = ctr + g.ctr_tile;
+      d.ksplit = g.ksplit;
+      d.kb_per_split = g.kb_per_split;
+      d.num_kb_gram = g.num_kb_gram;
+      d.tri = g.tri;
+      if (!ns_group_maps(d)) return MUON_ERR_CUDA;
     }
     // ---- NS iterations -----------------------------------------------------------
-    const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
     for (int it = 0; it < ns.steps; ++it) {
       const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
       for (int phase = 0; phase < 3; ++phase) {
         GemmParams gp;
         std::memset(&gp, 0, sizeof(gp));
         int64_t tiles = 0;
+        int min_kb = 1 << 30;
         for (size_t k = 0; k < ch.groups.size(); ++k) {
-          const NsGroupP& g = ch.groups[k];
           GemmGroup& G = gp.g[k];
-          auto* Xb = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X);
-          auto* Ab = reinterpret_cast<__nv_bfloat16*>(ws + g.off_A);
-          auto* Bb = reinterpret_cast<__nv_bfloat16*>(ws + g.off_B);
-          __nv_bfloat16* Xt[2] = {reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt0),
-                                  reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt1)};
-          G.m = static_cast<int>(g.m);
-          G.n = static_cast<int>(g.n);
-          G.count = static_cast<int>(g.cnt);
-          G.inv = reinterpret_cast<const float*>(ws + g.off_inv);
-          G.tile_base = static_cast<int>(tiles);
-          if (phase == kEpiGram) {
-            G.mapA = maps[k].Xp;
-            G.mapB = maps[k].Xq;
-            G.out0 = Ab;
-            G.pitch0 = g.m_pad;
-            G.mstride0 = g.m * g.m_pad;
-            G.partial = reinterpret_cast<float*>(ws + g.off_part);
-            G.tile_cnt = ctr + g.ctr_tile;
-            G.nt = static_cast<int>(cdiv(g.m, bn));
-            G.mt = static_cast<int>(cdiv(g.m, bm));
-            G.ksplit = g.ksplit;
-            G.kb_per_split = g.kb_per_split;
-            G.num_kb = g.num_kb_gram;
-            G.tiles_per_mat = static_cast<int>(g.tri * g.ksplit);
-          } else if (phase == kEpiPoly) {
-            G.mapA = maps[k].Ap;
-            G.mapB = maps[k].Aq;
-            G.epi_in = Ab;
-            G.pitch_in = g.m_pad;
-            G.mstride_in = g.m * g.m_pad;
-            G.out0 = Bb;
-            G.pitch0 = g.m_pad;
-            G.mstride0 = g.m * g.m_pad;
-            G.nt = static_cast<int>(cdiv(g.m, bn));
-            G.mt = static_cast<int>(cdiv(g.m, bm));
-            G.ksplit = 1;
-            G.num_kb = static_cast<int>(cdiv(g.m, bk));
-            G.kb_per_split = G.num_kb;
-            G.tiles_per_mat = static_cast<int>(g.tri);
-          } else {
-            G.mapA = maps[k].Xt[it & 1];
-            G.mapB = maps[k].B;
-            G.epi_in = Xt[it & 1];
-            G.pitch_in = g.m_pad;
-            G.mstride_in = g.n * g.m_pad;
-            G.out0 = Xt[(it + 1) & 1];
-            G.pitch0 = g.m_pad;
-            G.mstride0 = g.n * g.m_pad;
-            G.out1 = Xb;
-            G.pitch1 = g.n_pad;
-            G.mstride1 = g.m * g.n_pad;
-            G.nt = static_cast<int>(cdiv(g.m, bn));
-            G.mt = static_cast<int>(cdiv(g.n, bm));
-            G.ksplit = 1;
-            G.num_kb = static_cast<int>(cdiv(g.m, bk));
-            G.kb_per_split = G.num_kb;
-            G.tiles_per_mat = G.nt * G.mt;
-          }
-          tiles += static_cast<int64_t>(G.tiles_per_mat) * g.cnt;
+          ns_fill_group(G, dg[k], phase, it, static_cast<int>(tiles));
+          tiles += static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
+          min_kb = std::min(min_kb, G.kb_per_split);
         }
+        gp.deep = min_kb >= kDeepKBlocks ? 1 : 0;
         if (tiles >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         gp.n_groups = static_cast<int>(ch.groups.size());
         gp.total_tiles = static_cast<int>(tiles);
@@ -821,20 +718,20 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         const int64_t per = q.r * q.c;
         fs.W = static_cast<char*>(q.W) + s.b0 * per * esize(q.w_dtype);
         const int fin = ns.steps & 1;
-        auto* X = reinterpret_cast<__nv_bfloat16*>(ws + g.off_X) + s.idx0 * g.m * g.n_pad;
-        auto* Xt = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
-                   s.idx0 * g.n * g.m_pad;
-        fs.O = q.trans ? Xt : X;
-        fs.pitch_o = q.trans ? g.m_pad : g.n_pad;
-        fs.mstride_o = q.trans ? g.n * g.m_pad : g.m * g.n_pad;
+        // O = Xt in the stored layout when rows > cols, else its transpose
+        fs.O = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
+               s.idx0 * g.n * g.m_pad;
+        fs.o_trans = q.trans ? 0 : 1;
+        fs.pitch_o = g.m_pad;
+        fs.mstride_o = g.n * g.m_pad;
         fs.inv = ns.steps == 0 ? reinterpret_cast<const float*>(ws + g.off_inv) + s.idx0
                                : nullptr;
         fs.r = q.r;
         fs.c = q.c;
         fs.count = static_cast<int>(s.cnt);
         fs.w_dtype = q.w_dtype;
-        fs.tiles_r = static_cast<int>(cdiv(q.r, kFinRows));
-        fs.tiles_c = static_cast<int>(cdiv(q.c, kFinCols));
+        fs.tiles_r = static_cast<int>(cdiv(q.r, fs.o_trans ? kFinTRows : kFinRows));
+        fs.tiles_c = static_cast<int>(cdiv(q.c, fs.o_trans ? kFinTCols : kFinCols));
         fs.tile_base = static_cast<int>(blocks);
         fs.vec = (q.w_dtype == MUON_F32 ? (q.c % 4 == 0) : (q.c % 8 == 0)) && aligned(fs.W, 16);
         fs.scale = scale_value(q.r, q.c, scale_rule);

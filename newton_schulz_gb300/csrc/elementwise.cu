@@ -1,13 +1,16 @@
 // Memory-bound kernels of the Muon step.
 //
 //  prep_kernel   (K1)  momentum + Nesterov, per-matrix ||D||_F^2 partials,
-//                      bf16 cast, and both layouts ([r][c] and [c][r]) of the
-//                      Newton-Schulz operand, in one pass over G and Mom.
+//                      bf16 cast into the Newton-Schulz workspace layout
+//                      Xt = X^T ([n][m]: the stored layout when rows > cols,
+//                      else the transpose), in one pass over G and Mom.
 //                      DMuon-2 section 2.1 (M_t = mu*M_{t-1} + G, Nesterov);
 //                      HyperParallel-FSDP section 2.3 Eq. (1) (X0 = G/(||G||+eps))
 //                      and section 6.6 (transpose-first, bf16 NS path).
 //  finish_kernel (K6)  W <- (1 - lr*wd)*W - lr*s*O (RFC issue 204 item 6,
-//                      DMuon-2 section 2.1), or the copy-back of an NS-only call.
+//                      DMuon-2 section 2.1), or the copy-back of an NS-only call;
+//                      O is read from Xt, through a shared-memory transpose
+//                      when the stored layout is [m][n].
 //
 // Both are HBM-bound streaming kernels: 16-byte vector loads and stores,
 // warp-shuffle reductions, deterministic two-stage norm (per-tile partials,
@@ -136,8 +139,9 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
       for (int j = 0; j < 8; ++j)
         if (j >= nvalid) d[j] = 0.f;
       // [r][c] copy: the padded workspace row always has room for 8 elements.
-      *reinterpret_cast<uint4*>(s.direct + (int64_t)mat * s.mstride_d + gr * s.pitch_d + gc) =
-          pack8_bf16(d);
+      if (s.direct)
+        *reinterpret_cast<uint4*>(s.direct + (int64_t)mat * s.mstride_d + gr * s.pitch_d + gc) =
+            pack8_bf16(d);
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) sD[lr][lc + j] = d[j];
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
     const int64_t gcc = c0 + lcc;
     const int lrr = tx * 8;
     const int64_t grr = r0 + lrr;
-    if (gcc < s.c && grr < s.r) {
+    if (s.transp && gcc < s.c && grr < s.r) {
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = sD[lrr + j][lcc];
@@ -212,6 +216,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
 // K6
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinParams p) {
+  // o_trans tiles: the O tile [kFinTRows][kFinTCols], transposed from Xt on
+  // the way in; the odd word pitch (66 bf16) keeps both the scattered writes
+  // and the row reads free of bank conflicts
+  __shared__ __align__(16) __nv_bfloat16 sO[kFinTRows][kFinTCols + 2];
   const int si = find_slice(p.s, p.n_slices, blockIdx.x);
   const FinSlice& s = p.s[si];
   const int local = blockIdx.x - s.tile_base;
@@ -219,14 +227,51 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   const int mat = local / tiles;
   const int t = local - mat * tiles;
   const int ti = t / s.tiles_c, tj = t - ti * s.tiles_c;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t gr = (int64_t)ti * kFinRows + ty;
-  const int64_t gc = (int64_t)tj * kFinCols + tx * 8;
+  int64_t gr, gc;
+  float o[8];
+  if (s.o_trans) {
+    // O[gr][gc] = Xt[gc][gr]: each thread brings 8 consecutive gr of one Xt
+    // row (a 64-byte segment per 4 threads), then reads 8 consecutive gc
+    const int64_t r0 = (int64_t)ti * kFinTRows, c0 = (int64_t)tj * kFinTCols;
+    {
+      const int lc = threadIdx.x >> 2, q = threadIdx.x & 3;
+      const int64_t xr = c0 + lc, xc = r0 + 8 * q;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (xr < s.c) {
+        const __nv_bfloat16* src = s.O + (int64_t)mat * s.mstride_o + xr * s.pitch_o + xc;
+        if (xc + 8 <= s.r) {
+          u = *reinterpret_cast<const uint4*>(src);
+        } else {
+          __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&u);
+          for (int j = 0; j < 8; ++j)
+            if (xc + j < s.r) h[j] = src[j];
+        }
+      }
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sO[8 * q + j][lc] = h[j];
+    }
+    __syncthreads();
+    const int lr = threadIdx.x >> 3, lc0 = (threadIdx.x & 7) * 8;
+    gr = r0 + lr;
+    gc = c0 + lc0;
+    const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(&sO[lr][lc0]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(src[j]);
+      o[2 * j] = f.x;
+      o[2 * j + 1] = f.y;
+    }
+  } else {
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    gr = (int64_t)ti * kFinRows + ty;
+    gc = (int64_t)tj * kFinCols + tx * 8;
+    if (gr < s.r && gc < s.c)
+      load8_bf16(s.O + (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc, o);
+  }
   if (gr >= s.r || gc >= s.c) return;
   const int nvalid = (int)min((int64_t)8, s.c - gc);
 
-  float o[8];
-  load8_bf16(s.O + (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc, o);
   const float os = s.inv ? s.inv[mat] : 1.f;
   const int64_t e = (int64_t)mat * s.r * s.c + gr * s.c + gc;
 

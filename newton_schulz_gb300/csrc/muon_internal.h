@@ -25,8 +25,8 @@ constexpr int kPrepTile = 64;     // 64 x 64 tile of the stored [r][c] matrix
 struct PrepSlice {
   const void* G;          // [count][r][c] (gradient, or the NS input)
   float* Mom;             // [count][r][c] fp32 (step mode), else null
-  __nv_bfloat16* direct;  // workspace copy in [r][c] layout
-  __nv_bfloat16* transp;  // workspace copy in [c][r] layout
+  __nv_bfloat16* direct;  // workspace Xt in [r][c] layout (rows > cols), else null
+  __nv_bfloat16* transp;  // workspace Xt in [c][r] layout (rows <= cols), else null
   float* ssq_part;        // [count][tiles] per-tile partial sum of squares
   float* inv;             // [count] 1/(||D||_F + eps)
   unsigned* cnt;          // [count] arrival counters (left at zero)
@@ -53,11 +53,12 @@ struct PrepParams {
 };
 
 // ---- K6: update / copy-back --------------------------------------------------
-constexpr int kFinRows = 8, kFinCols = 256;
+constexpr int kFinRows = 8, kFinCols = 256;     // tile when O is stored [r][c]
+constexpr int kFinTRows = 32, kFinTCols = 64;   // tile when O is read transposed from Xt
 
 struct FinSlice {
   void* W;                     // step: weights [count][r][c]; ns: output
-  const __nv_bfloat16* O;      // NS result in [r][c] layout (workspace)
+  const __nv_bfloat16* O;      // NS result (workspace Xt): [r][c], or [c][r] when o_trans
   const float* inv;            // [count] extra factor when steps == 0, else null
   int64_t r, c, pitch_o, mstride_o;
   int count;
@@ -65,6 +66,7 @@ struct FinSlice {
   int tiles_r, tiles_c, tile_base;
   int vec;
   float scale;                 // update scale s(r, c)
+  int o_trans;                 // 1: O[r][c] = Xt[c][r] (stored rows <= cols)
 };
 
 struct FinParams {
@@ -79,16 +81,14 @@ struct FinParams {
 enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiApply = 2 };
 
 struct alignas(128) GemmGroup {
-  CUtensorMap mapA;       // operand A (rows = tile M dim, inner = K)
-  CUtensorMap mapB;       // operand B (rows = tile N dim, inner = K)
-  const __nv_bfloat16* epi_in;   // poly: A; apply: Xt_old
-  __nv_bfloat16* out0;           // gram: A; poly: B; apply: Xt_new
-  __nv_bfloat16* out1;           // apply: X
+  CUtensorMap mapA;       // operand A: K-major (rows = M dim, inner = K), box 64 x 128;
+                          // gram: Xt viewed MN-major (inner = m, rows = n), box 64 x 64
+  CUtensorMap mapB;       // operand B: K-major box 64 x 256; gram: as mapA
+  CUtensorMap mapC;       // output, box 64 x 128 (TMA store): gram A, poly B, apply Xt_new
+  CUtensorMap mapD;       // gram / poly: the output's transposed boxes, box 64 x 64
   const float* inv;              // first iteration scale (per matrix) or null
   float* partial;                // gram split-K partials
   unsigned* tile_cnt;            // gram split-K arrival counters
-  int64_t pitch_in, pitch0, pitch1;
-  int64_t mstride_in, mstride0, mstride1;
   int m, n;
   int count;
   int tiles_per_mat;
@@ -105,9 +105,36 @@ struct GemmParams {
   float a, b, c;           // apply uses a - alpha; poly adds alpha on the diagonal
   float alpha;             // shift: X' = (a - alpha) X + (b A + c A^2 + alpha I) X
   int first;              // 1: operands are unnormalised, apply inv scale
+  int deep;               // 1: every tile has >= kDeepKBlocks K blocks (4-stage ring)
   unsigned* status;
   unsigned long long timeout_ns;
 };
+
+// One core-shape group of the GEMM path on the device: workspace buffers,
+// split-K plan and tensor maps (ns_plan.cpp).
+struct NsGroupDev {
+  int64_t m = 0, n = 0, cnt = 0, m_pad = 0;
+  __nv_bfloat16* Xt[2] = {nullptr, nullptr};   // [cnt][n][m_pad] ping-pong
+  __nv_bfloat16* A = nullptr;                  // [cnt][m][m_pad]
+  __nv_bfloat16* B = nullptr;                  // [cnt][m][m_pad]
+  const float* inv = nullptr;                  // [cnt] 1 / (||X0|| + eps)
+  float* partial = nullptr;                    // Gram split-K partials
+  unsigned* tile_cnt = nullptr;                // Gram split-K counters
+  int ksplit = 1, kb_per_split = 1, num_kb_gram = 1;
+  int64_t tri = 1;
+  CUtensorMap map_gram[2], map_xt[2], map_ap, map_aq, map_a64, map_bp, map_bq, map_b64;
+};
+
+// Tiled bf16/f32 tensor map of a [dims[2]][dims[1]][dims[0]] tensor with
+// byte strides strides[0] (rows) and strides[1] (matrices).
+bool encode_tiled(CUtensorMap* map, bool f32, const void* base, const uint64_t* dims,
+                  const uint64_t* strides, const uint32_t* box, bool swizzle128);
+// bf16, 128-byte swizzle, box {64, box_rows, 1}.
+bool make_ns_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t cnt,
+                 int64_t pitch, int64_t mstride, int box_rows);
+bool ns_group_maps(NsGroupDev& g);
+// Fill the launch descriptor of group g for `phase` (Epi) of NS step `it`.
+void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base);
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
@@ -180,6 +207,7 @@ int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage
 int gemm_sym_tiles(int m);   // tiles of a symmetric m x m product (holding some col >= row)
+constexpr int kDeepKBlocks = 32;   // K blocks per tile from which a launch takes the deep ring
 cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s);
 int small_blocks_per_sm(int smem_bytes);   // resident CTAs per SM, 0 when the query fails
 

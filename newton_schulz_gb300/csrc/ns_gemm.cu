@@ -1,28 +1,34 @@
 // Tensor-core GEMMs of one Newton-Schulz step (HyperParallel-FSDP section 2.3,
 // Eq. (1), evaluated as A = X X^T; B' = b*A + c*A^2 + alpha*I;
-// X' = (a - alpha)*X + B' X):
+// X' = (a - alpha)*X + B' X).  The iterate is kept in one layout only,
+// Xt = X^T ([n][m], m <= n), ping-ponged between two buffers:
 //
-//   Gram   A  = X X^T        symmetric: only tiles holding an element with
+//   Gram   A  = X X^T = Xt^T Xt   both operands MN-major views of Xt tiles;
+//                            symmetric: only tiles holding an element with
 //                            col >= row are computed, each such element is
 //                            written at (r, c) and mirrored to (c, r)
 //                            (DMuon-2 section 5, symmetric products);
 //                            split-K over the long side for few tiles.
-//   Poly   B' = b*A + c*A A + alpha*I   A is symmetric, so A A = A A^T: the
-//                            same K-major operands as the Gram; the rest is
-//                            fused in the epilogue; symmetric output.
-//   Apply  X'^T = (a - alpha)*X^T + X^T B'   (B' symmetric), i.e.
-//                            X' = (a - alpha)*X + B' X; writes both layouts
-//                            of X' (the next Gram reads X, the next Apply X^T).
+//   Poly   B' = b*A + c*A A + alpha*I   A is symmetric, so A A = A A^T:
+//                            K-major operands; the rest is fused in the
+//                            epilogue; symmetric output.
+//   Apply  Xt' = (a - alpha)*Xt + Xt B'   (B' symmetric), K-major operands;
+//                            the epilogue reads the Xt tile and writes the
+//                            Xt' tile through shared memory with TMA.
 //
-// Every product is D = P Q^T with P and Q K-major bf16 in global memory, so
-// one persistent kernel body serves all three.  Per CTA (one per SM):
+// Per CTA (one per SM):
 //   warp 0      TMA producer: 128x64 (P) and 256x64 (Q) tiles, 128-byte
-//               swizzle, into a 4-stage shared-memory ring;
+//               swizzle, into a shared-memory ring;
 //   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=256, K=16)
 //               from one elected thread into one of two TMEM accumulators;
-//   warps 2..5  epilogue: tcgen05.ld, fused arithmetic, 16-byte stores; the
-//               transposed / mirrored copies go through a per-warp
-//               shared-memory transpose so they are written as whole rows.
+//   warps 2..9  epilogue, two sets of four warps (each set covers the 128
+//               TMEM lanes and one half of the accumulator's columns):
+//               tcgen05.ld, fused arithmetic.  Apply: each set stages its
+//               half tile in shared memory (TMA load of Xt, in-place update,
+//               TMA store of Xt').  Gram / Poly: 16-byte stores of the
+//               upper part and a per-warp shared-memory transpose for the
+//               mirrored copy; the polynomial's A operand is loaded before
+//               the accumulator is waited for.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
 // tile t+1.  Tiles of all matrices of all core-shape groups of a chunk form
 // one static round-robin schedule.  Every wait is bounded; on a timeout a
@@ -39,16 +45,29 @@ constexpr int BM = 128;          // MMA M = TMEM lanes
 constexpr int BN = 256;          // MMA N = TMEM columns per accumulator
 constexpr int BK = 64;           // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
-constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytes = BN * BK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;
 constexpr int kEpiWarp0 = 2;
-constexpr int kTpitch = 40;      // bf16 pitch of a 32x32 transpose block (80 B rows)
-constexpr int kTBytes = 32 * kTpitch * 2;
-constexpr int kBarOff = kStages * kStageBytes + 4 * kTBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;
+constexpr int kEpiWarps = 8;                 // two sets of four
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr int kSetCols = BN / 2;             // accumulator columns per epilogue set
+constexpr int kChunkBytes = 64 * 128;      // 64 rows of 128 bytes (one MN-major operand chunk)
+constexpr int kBoxBytes = BM * 128;        // apply staging: 128 rows x 64 columns of bf16
+
+// Shared-memory carve-up: the operand ring and the epilogue's output staging.
+// Short-K launches take a 3-stage ring and 32 KB of staging per epilogue set
+// (two boxes: both halves of the set's columns, or a tile half and its
+// transpose, in flight together); long-K launches (DEEP) take a 4-stage ring
+// and one 16 KB box per set, which the set's stores then use in turn.
+template <bool DEEP>
+struct Layout {
+  static constexpr int stages = DEEP ? 4 : 3;
+  static constexpr int set_bytes = DEEP ? kBoxBytes : 2 * kBoxBytes;
+  static constexpr int bar_off = stages * kStageBytes + 2 * set_bytes;
+  static constexpr int smem = bar_off + 256 + 1024;
+};
 constexpr uint32_t kTmemCols = 2 * BN;
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
@@ -70,8 +89,8 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ void epi_bar() {   // the four epilogue warps only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+__device__ __forceinline__ void epi_bar() {   // the epilogue warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
 struct TileInfo {
@@ -120,11 +139,10 @@ __device__ __forceinline__ TileInfo decode(const GemmParams& p, int tile) {
   return t;
 }
 
-__device__ __forceinline__ void ld_bf16x32(const __nv_bfloat16* p, float* v) {
+__device__ __forceinline__ void cvt_bf16x32(const uint4 (&u)[4], float* v) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p + 8 * q);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[q]);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 f = __bfloat1622float2(h[k]);
@@ -134,60 +152,27 @@ __device__ __forceinline__ void ld_bf16x32(const __nv_bfloat16* p, float* v) {
   }
 }
 
-__device__ __forceinline__ void st_bf16x32(__nv_bfloat16* p, const __nv_bfloat16* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(p + 8 * q) = *reinterpret_cast<const uint4*>(v + 8 * q);
-}
-
-// Write the warp's 32x32 block transposed: lane l owns row (r0 + l) of the
-// block and the 32 values h[0..31] at columns c0..c0+31; afterwards lane l
-// writes column (c0 + l) as a row of 32 values at dst + (c0 + l)*pitch + r0.
-// Elements outside [0, rows_lim) x [0, cols_lim) are skipped, and when
-// `upper_only` is set only elements with column > row are written.
-__device__ __forceinline__ void store_transposed(__nv_bfloat16* tb, const __nv_bfloat16* h,
-                                                 __nv_bfloat16* dst, int64_t pitch, int64_t r0,
-                                                 int64_t c0, int64_t rows_lim, int64_t cols_lim,
-                                                 bool upper_only) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) tb[j * kTpitch + lane] = h[j];
-  __syncwarp();
-  const int64_t c = c0 + lane;                 // row of dst
-  const __nv_bfloat16* src = tb + lane * kTpitch;
-  const bool full = (r0 + 32 <= rows_lim) && (!upper_only || c0 > r0 + 31);
-  if (c < cols_lim) {
-    __nv_bfloat16* d = dst + c * pitch + r0;
-    if (full) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(d + 8 * q) = *reinterpret_cast<const uint4*>(src + 8 * q);
-    } else {
-      for (int k = 0; k < 32; ++k) {
-        const int64_t r = r0 + k;
-        if (r < rows_lim && (!upper_only || c > r)) d[k] = src[k];
-      }
-    }
-  }
-  __syncwarp();
-}
 
 }  // namespace
 
-template <int EPI>
+template <int EPI, bool DEEP>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+  using L = Layout<DEEP>;
+  constexpr int kStages = L::stages;
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(smem + kStages * kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint8_t* sX = smem + kStages * kStageBytes;   // epilogue output staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;      // [2] accumulator ready
   uint64_t* tempty = tfull + 2;           // [2] accumulator drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* xfull = tempty + 2;           // [2] apply: staged Xt tile of epilogue set s landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
+  volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);   // [2] per-tile decision
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -199,13 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
-      ptx::mbar_init(&tempty[b], 128);
+      ptx::mbar_init(&tempty[b], kEpiThreads);
+      ptx::mbar_init(&xfull[b], 1);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
     for (int g = 0; g < p.n_groups; ++g) {
       ptx::prefetch_tmap(&p.g[g].mapA);
       ptx::prefetch_tmap(&p.g[g].mapB);
+      ptx::prefetch_tmap(&p.g[g].mapC);
+      if (EPI != kEpiApply) ptx::prefetch_tmap(&p.g[g].mapD);
     }
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
@@ -230,8 +218,20 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
           ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
           const int kx = (t.kb0 + i) * BK;
-          ptx::tma_load_3d(sA + stage * kABytes, &G.mapA, &full[stage], kx, t.row_tile * BM, t.mat);
-          ptx::tma_load_3d(sB + stage * kBBytes, &G.mapB, &full[stage], kx, t.col_tile * BN, t.mat);
+          if (EPI == kEpiGram) {
+            // MN-major chunks of Xt: 64 columns (m) x 64 rows (n, the K dim) each
+#pragma unroll
+            for (int h = 0; h < BM / 64; ++h)
+              ptx::tma_load_3d(sA + stage * kABytes + h * kChunkBytes, &G.mapA, &full[stage],
+                               t.row_tile * BM + 64 * h, kx, t.mat);
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h)
+              ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, &G.mapB, &full[stage],
+                               t.col_tile * BN + 64 * h, kx, t.mat);
+          } else {
+            ptx::tma_load_3d(sA + stage * kABytes, &G.mapA, &full[stage], kx, t.row_tile * BM, t.mat);
+            ptx::tma_load_3d(sB + stage * kBBytes, &G.mapB, &full[stage], kx, t.col_tile * BN, t.mat);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -248,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   } else if (warp == 1) {
     // ---- MMA issuer --------------------------------------------------------------------
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+      // the Gram reads both operands MN-major (A and B transpose bits)
+      constexpr uint32_t idesc =
+          ptx::idesc_bf16_f32(BM, BN) | (EPI == kEpiGram ? (1u << 15) | (1u << 16) : 0u);
       int stage = 0, acc = 0;
       uint32_t phase = 0;
       bool stop = false;
@@ -271,10 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           const uint32_t a0 = ptx::smem_u32(sA + stage * kABytes);
           const uint32_t b0 = ptx::smem_u32(sB + stage * kBBytes);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k)
-            ptx::umma_bf16(d, ptx::sdesc_kmajor_sw128(a0 + k * UMMA_K * 2),
-                           ptx::sdesc_kmajor_sw128(b0 + k * UMMA_K * 2), idesc,
-                           (i > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // K-major: K advances within the 128-byte row; MN-major: by 16
+            // rows (two 1024-byte swizzle atoms) within each 64-column chunk
+            const uint64_t da = EPI == kEpiGram
+                                    ? ptx::sdesc_mnmajor_sw128(a0 + k * 2048, kChunkBytes, 1024)
+                                    : ptx::sdesc_kmajor_sw128(a0 + k * UMMA_K * 2);
+            const uint64_t db = EPI == kEpiGram
+                                    ? ptx::sdesc_mnmajor_sw128(b0 + k * 2048, kChunkBytes, 1024)
+                                    : ptx::sdesc_kmajor_sw128(b0 + k * UMMA_K * 2);
+            ptx::umma_bf16(d, da, db, idesc, (i > 0 || k > 0) ? 1u : 0u);
+          }
           ptx::umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
@@ -286,19 +295,42 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     __syncwarp();
   } else {
-    // ---- epilogue (warps 2..5; TMEM lane quadrant = warp % 4) ---------------------------------
+    // ---- epilogue (warps 2..9; TMEM lane quadrant = warp % 4, column half = set) ----------
     const int q4 = warp & 3;
+    const int set = (warp - kEpiWarp0) >> 2;
+    const int cbase = set * kSetCols;
     const int row = q4 * 32 + lane;
-    __nv_bfloat16* tb = sT + (warp - kEpiWarp0) * (32 * kTpitch);
+    const bool leader = (warp - kEpiWarp0) % 4 == 0 && lane == 0;   // one thread per set
+    uint8_t* stg = sX + set * L::set_bytes;    // this set's staging
+    uint32_t xphase = 0;
+    bool xpend = false;   // leader: a staged-tile load is in flight and not yet waited for
     int acc = 0;
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++acc) {
       const TileInfo t = decode<EPI>(p, tile);
       const GemmGroup& G = p.g[t.gi];
       const int buf = acc & 1;
+      const int row0 = t.row_tile * BM, col0 = t.col_tile * BN;
+      // Apply: the Xt tile half of this set does not depend on the
+      // accumulator, so the leader requests it first (once the previous
+      // tile's stores have read the staging boxes).
+      if (EPI == kEpiApply && leader && !xpend && !*abort_flag) {
+        xpend = true;
+        ptx::bulk_wait_read<0>();
+        constexpr int nh = DEEP ? 1 : 2;    // halves staged now
+        ptx::mbar_arrive_expect_tx(&xfull[set], nh * kBoxBytes);
+#pragma unroll
+        for (int h = 0; h < nh; ++h)
+          ptx::tma_load_3d(stg + h * kBoxBytes, &G.mapA, &xfull[set], col0 + cbase + 64 * h, row0,
+                           t.mat);
+      }
       wait_bounded(&tfull[buf], (acc >> 1) & 1, abort_flag, p.status, p.timeout_ns, false);
-      // one decision for all four epilogue warps (they share named barriers)
+      // One decision for all epilogue warps (they share named barriers): one
+      // thread samples the abort flag, the barrier publishes it.  The slot
+      // alternates, so it is rewritten only after everyone passed the next
+      // tile's barrier (and so had read it).
+      if (threadIdx.x == kEpiWarp0 * 32) s_ok[acc & 1] = !*abort_flag;
       epi_bar();
-      const bool ok = !*abort_flag;
+      const bool ok = s_ok[acc & 1] != 0;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q4 * 32) << 16);
       if (!ok) {
@@ -307,64 +339,82 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         break;
       }
       if (EPI == kEpiApply) {
-        const int64_t gp = (int64_t)t.row_tile * BM + row;      // index along n
-        const int64_t gp0 = (int64_t)t.row_tile * BM + q4 * 32; // first row of this warp
         const float s = p.first ? G.inv[t.mat] : 1.f;
-        const __nv_bfloat16* xin = G.epi_in + (int64_t)t.mat * G.mstride_in + gp * G.pitch_in;
-        __nv_bfloat16* xt_out = G.out0 + (int64_t)t.mat * G.mstride0 + gp * G.pitch0;
-        __nv_bfloat16* x_out = G.out1 + (int64_t)t.mat * G.mstride1;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          const int64_t gq0 = (int64_t)t.col_tile * BN + c0;   // index along m
-          if (gq0 >= G.m) break;                                // warp-uniform
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c0, r);
-          ptx::tmem_ld_wait();
-          const bool fullc = gq0 + 32 <= G.m;
-          float x[32];
-          if (gp < G.n) {
-            if (fullc) {
-              ld_bf16x32(xin + gq0, x);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) x[j] = gq0 + j < G.m ? __bfloat162float(xin[gq0 + j]) : 0.f;
-            }
+        for (int h = 0; h < 2; ++h) {
+          uint8_t* box = stg + (DEEP ? 0 : h * kBoxBytes);
+          if (DEEP && h == 1 && leader && !xpend && !*abort_flag) {
+            // the first half's store has read the box: stage the second half
+            xpend = true;
+            ptx::bulk_wait_read<0>();
+            ptx::mbar_arrive_expect_tx(&xfull[set], kBoxBytes);
+            ptx::tma_load_3d(box, &G.mapA, &xfull[set], col0 + cbase + 64, row0, t.mat);
+          }
+          bool xok = true;
+          if (!DEEP && h == 1) {
+            // both halves arrived with the first wait
           } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = 0.f;
-          }
-          __align__(16) __nv_bfloat16 h[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            h[j] = __float2bfloat16_rn(s * fmaf(p.a, x[j], __uint_as_float(r[j])));
-          if (gp < G.n) {
-            if (fullc) {
-              st_bf16x32(xt_out + gq0, h);
-            } else {
-              for (int j = 0; j < 32; ++j)
-                if (gq0 + j < G.m) xt_out[gq0 + j] = h[j];
+            // every thread of the set waits for the staged half (bounded)
+            xok = wait_bounded(&xfull[set], xphase, abort_flag, p.status, p.timeout_ns, false);
+            if (xok) {
+              xphase ^= 1u;
+              xpend = false;
             }
           }
-          // X'[q][p]: rows gq0.., columns gp0..gp0+31
-          store_transposed(tb, h, x_out, G.pitch1, gp0, gq0, G.n, G.m, false);
+          if (xok) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c0 = cbase + 64 * h + 32 * cc;   // accumulator column
+              uint32_t r[32];
+              ptx::tmem_ld_32x32b_x32(taddr + c0, r);
+              ptx::tmem_ld_wait();
+              // this row's 64 bytes of the chunk in the swizzled box
+              uint32_t off[4];
+              uint4 xv[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                off[q] = ptx::sw128_offset(row, (cc * 4 + q) * 16);
+                xv[q] = *reinterpret_cast<const uint4*>(box + off[q]);
+              }
+              float x[32];
+              cvt_bf16x32(xv, x);
+              __align__(16) __nv_bfloat16 hv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                hv[j] = __float2bfloat16_rn(s * fmaf(p.a, x[j], __uint_as_float(r[j])));
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(box + off[q]) = *reinterpret_cast<const uint4*>(hv + 8 * q);
+            }
+          }
+          if (h == 1) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[buf]);
+          }
+          // make the generic-proxy writes visible to the TMA store, then one
+          // thread stores the half if it holds part of the matrix
+          ptx::fence_proxy_async_smem();
+          ptx::named_bar(2 + set, 128);
+          if (leader && xok) {
+            const int x = col0 + cbase + 64 * h;
+            if (x < G.m && row0 < G.n) ptx::tma_store_3d(&G.mapC, box, x, row0, t.mat);
+            ptx::bulk_commit();
+          }
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&tempty[buf]);
       } else {
-        const int64_t gr = (int64_t)t.row_tile * BM + row;
-        const int64_t gr0 = (int64_t)t.row_tile * BM + q4 * 32;
+        const int64_t gr = (int64_t)row0 + row;
         const bool split = G.ksplit > 1;
         const int64_t slot = (int64_t)t.mat * G.tiles_per_mat / G.ksplit + t.sym_idx;
         float* part = split ? G.partial + slot * G.ksplit * (int64_t)(BM * BN) : nullptr;
         if (split) {
           // partial tile -> global (valid entries only), then the last split reduces
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = cbase; c0 < cbase + kSetCols; c0 += 32) {
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(taddr + c0, r);
             ptx::tmem_ld_wait();
             if (gr < G.m) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                const int64_t gc = (int64_t)t.col_tile * BN + c0 + j;
+                const int64_t gc = (int64_t)col0 + c0 + j;
                 if (gc < G.m)
                   __stcg(part + (int64_t)t.ksp * (BM * BN) + (c0 + j) * BM + row,
                          __uint_as_float(r[j]));
@@ -385,68 +435,124 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (!last) continue;
           __threadfence();
         }
+        // Output: every computed tile stores its whole box (a tile that
+        // crosses the diagonal thus also writes the elements below it, which
+        // no other tile writes); a tile entirely above the diagonal also
+        // stores its transpose, whose region no computed tile covers.  Each
+        // element of the m x m result is written exactly once.
         const float scale = (EPI == kEpiGram && p.first) ? G.inv[t.mat] * G.inv[t.mat] : 1.f;
-        __nv_bfloat16* out = G.out0 + (int64_t)t.mat * G.mstride0;
-        const __nv_bfloat16* ain =
-            (EPI == kEpiPoly) ? G.epi_in + (int64_t)t.mat * G.mstride_in : nullptr;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          const int64_t gc0 = (int64_t)t.col_tile * BN + c0;
-          if (gc0 >= G.m) break;                               // warp-uniform
-          if (gc0 + 31 < gr0) continue;                        // block entirely below the diagonal
-          float v[32];
-          if (split) {
-            // sum the splits in order; the 32 columns of a split are loaded together
+        const bool mirror = row0 + BM <= col0;
+        uint8_t* sd = stg;                                // direct box: 128 rows x 64 columns
+        uint8_t* sm = stg + (DEEP ? 0 : kBoxBytes);      // transposed boxes: 2 x (64 x 64)
+        for (int h = 0; h < 2; ++h) {
+          const int c_h = cbase + 64 * h;   // accumulator column of this half
+          const int gc_h = col0 + c_h;
+          if (gc_h >= G.m) break;           // uniform within the set
+          if (leader) {
+            ptx::bulk_wait_read<0>();       // the previous stores have read the boxes
+            if (EPI == kEpiPoly && !xpend && !*abort_flag) {
+              xpend = true;
+              ptx::mbar_arrive_expect_tx(&xfull[set], kBoxBytes);
+              ptx::tma_load_3d(sd, &G.mapA, &xfull[set], gc_h, row0, t.mat);   // A tile
+            }
+          }
+          ptx::named_bar(2 + set, 128);
+          bool xok = true;
+          if (EPI == kEpiPoly) {
+            xok = wait_bounded(&xfull[set], xphase, abort_flag, p.status, p.timeout_ns, false);
+            if (xok) {
+              xphase ^= 1u;
+              xpend = false;
+            }
+          }
+          uint4 keep[2][4];   // this row's 64 results (bf16), for the transposed copy
+          if (xok) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            if (gr < G.m) {
-              for (int q = 0; q < G.ksplit; ++q) {
-                const float* pq = part + (int64_t)q * (BM * BN) + c0 * BM + row;
-                float l[32];
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c0 = c_h + 32 * cc;
+              const int64_t gc0 = (int64_t)col0 + c0;
+              float v[32];
+              if (split) {
+                // sum the splits in order; the 32 columns of a split are loaded together
 #pragma unroll
-                for (int j = 0; j < 32; ++j) l[j] = gc0 + j < G.m ? __ldcg(pq + j * BM) : 0.f;
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                if (gr < G.m) {
+                  for (int q = 0; q < G.ksplit; ++q) {
+                    const float* pq = part + (int64_t)q * (BM * BN) + c0 * BM + row;
+                    float l[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] += l[j];
+                    for (int j = 0; j < 32; ++j) l[j] = gc0 + j < G.m ? __ldcg(pq + j * BM) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += l[j];
+                  }
+                }
+              } else {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c0, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+              }
+              uint32_t off[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) off[q] = ptx::sw128_offset(row, (cc * 4 + q) * 16);
+              if (EPI == kEpiPoly) {
+                uint4 av4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) av4[q] = *reinterpret_cast<const uint4*>(sd + off[q]);
+                float av[32];
+                cvt_bf16x32(av4, av);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  v[j] = fmaf(p.b, av[j], p.c * v[j]) + (gr == gc0 + j ? p.alpha : 0.f);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= scale;
+              }
+              __align__(16) __nv_bfloat16 hv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) hv[j] = __float2bfloat16_rn(v[j]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                keep[cc][q] = *reinterpret_cast<const uint4*>(hv + 8 * q);
+                *reinterpret_cast<uint4*>(sd + off[q]) = keep[cc][q];
               }
             }
-          } else {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr + c0, r);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           }
-          const bool fullc = gc0 + 32 <= G.m;
-          float av[32];
-          if (EPI == kEpiPoly) {
-            if (gr < G.m && fullc) {
-              ld_bf16x32(ain + gr * G.pitch_in + gc0, av);
-            } else {
+          ptx::fence_proxy_async_smem();
+          ptx::named_bar(2 + set, 128);
+          if (leader && xok) {
+            ptx::tma_store_3d(&G.mapC, sd, gc_h, row0, t.mat);
+            ptx::bulk_commit();
+          }
+          if (mirror) {
+            if (DEEP) {
+              // one box per set: the direct store must have read it first
+              if (leader) ptx::bulk_wait_read<0>();
+              ptx::named_bar(2 + set, 128);
+            }
+            if (xok) {
+              // element (row, c) goes to row c, column `row` of the transpose
+              uint8_t* tbox = sm + (row >> 6) * (kBoxBytes / 2);
+              const uint32_t tb = static_cast<uint32_t>(row & 63) * 2;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                av[j] = (gr < G.m && gc0 + j < G.m) ? __bfloat162float(ain[gr * G.pitch_in + gc0 + j])
-                                                    : 0.f;
+              for (int cc = 0; cc < 2; ++cc) {
+                const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(keep[cc]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  *reinterpret_cast<__nv_bfloat16*>(tbox + ptx::sw128_offset(cc * 32 + j, tb)) = hv[j];
+              }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(2 + set, 128);
+            if (leader && xok) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b)
+                if (row0 + 64 * b < G.m)
+                  ptx::tma_store_3d(&G.mapD, sm + b * (kBoxBytes / 2), row0 + 64 * b, gc_h, t.mat);
+              ptx::bulk_commit();
             }
           }
-          __align__(16) __nv_bfloat16 h[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float val = v[j] * scale;
-            if (EPI == kEpiPoly)
-              val = fmaf(p.b, av[j], p.c * val) + (gr == gc0 + j ? p.alpha : 0.f);
-            h[j] = __float2bfloat16_rn(val);
-          }
-          // direct (r, c) for c >= r
-          if (gr < G.m) {
-            __nv_bfloat16* o = out + gr * G.pitch0 + gc0;
-            if (fullc && gc0 >= gr) {
-              st_bf16x32(o, h);
-            } else {
-              for (int j = 0; j < 32; ++j)
-                if (gc0 + j < G.m && gc0 + j >= gr) o[j] = h[j];
-            }
-          }
-          // mirror (c, r) for c > r
-          store_transposed(tb, h, out, G.pitch0, gr0, gc0, G.m, G.m, true);
         }
         if (!split) {
           ptx::tc_fence_before();
@@ -455,6 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           G.tile_cnt[slot] = 0u;
         }
       }
+    }
+    if (leader) {
+      // no copy may still target or read this CTA's shared memory at exit
+      if (xpend) wait_bounded(&xfull[set], xphase, abort_flag, p.status, p.timeout_ns, false);
+      ptx::bulk_wait_all();
     }
   }
 
@@ -477,12 +588,13 @@ int gemm_sym_tiles(int m) {
   return t;
 }
 
-template <int EPI>
+template <int EPI, bool DEEP>
 static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<EPI>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<EPI, DEEP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout<DEEP>::smem);
   if (e != cudaSuccess) return e;
-  ns_gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(p);
+  ns_gemm_kernel<EPI, DEEP><<<grid, kThreads, Layout<DEEP>::smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -496,10 +608,14 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s) {
     if (sms <= 0) sms = 1;
   }
   const int grid = p.total_tiles < sms ? p.total_tiles : sms;
+  const bool deep = p.deep != 0;
   switch (epi) {
-    case kEpiGram: return launch_one<kEpiGram>(p, grid, s);
-    case kEpiPoly: return launch_one<kEpiPoly>(p, grid, s);
-    case kEpiApply: return launch_one<kEpiApply>(p, grid, s);
+    case kEpiGram: return deep ? launch_one<kEpiGram, true>(p, grid, s)
+                               : launch_one<kEpiGram, false>(p, grid, s);
+    case kEpiPoly: return deep ? launch_one<kEpiPoly, true>(p, grid, s)
+                               : launch_one<kEpiPoly, false>(p, grid, s);
+    case kEpiApply: return deep ? launch_one<kEpiApply, true>(p, grid, s)
+                                : launch_one<kEpiApply, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,128 @@
+// Host-side pieces of the grouped GEMM path shared by the allocating entry
+// points (api.cpp) and the allocation-free one (noalloc.cu): the tensor maps
+// of one core-shape group and the per-phase GEMM group descriptors.
+//
+// One Newton-Schulz step (HyperParallel-FSDP section 2.3, Eq. (1)) runs as
+// three launches over every group of a chunk: Gram A = X X^T, polynomial
+// B' = b A + c A^2 + alpha I, apply Xt' = (a - alpha) Xt + Xt B'.  The
+// iterate lives only as Xt = X^T ([n][m_pad] bf16 per matrix), ping-ponged
+// between two buffers: step `it` reads Xt[it & 1] and writes Xt[(it + 1) & 1].
+#include <mutex>
+
+#include "muon_internal.h"
+
+namespace muon {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+bool encode_tiled(CUtensorMap* map, bool f32, const void* base, const uint64_t* dims,
+                  const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t b[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_ns_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t cnt,
+                 int64_t pitch, int64_t mstride, int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(inner), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(cnt)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(pitch * 2),
+                               static_cast<uint64_t>(mstride * 2)};
+  const uint32_t box[3] = {static_cast<uint32_t>(gemm_block_k()),
+                           static_cast<uint32_t>(box_rows), 1};
+  return encode_tiled(map, false, base, dims, strides, box, true);
+}
+
+bool ns_group_maps(NsGroupDev& g) {
+  const int bm = gemm_block_m(), bn = gemm_block_n();
+  const int64_t xs = g.n * g.m_pad, as = g.m * g.m_pad;
+  bool ok = true;
+  for (int b = 0; b < 2; ++b) {
+    // Gram: MN-major 64 (m) x 64 (n) chunks; apply: 128 rows (n) x 64 (m)
+    ok = ok && make_ns_map(&g.map_gram[b], g.Xt[b], g.m, g.n, g.cnt, g.m_pad, xs, 64);
+    ok = ok && make_ns_map(&g.map_xt[b], g.Xt[b], g.m, g.n, g.cnt, g.m_pad, xs, bm);
+  }
+  ok = ok && make_ns_map(&g.map_ap, g.A, g.m, g.m, g.cnt, g.m_pad, as, bm) &&
+       make_ns_map(&g.map_aq, g.A, g.m, g.m, g.cnt, g.m_pad, as, bn) &&
+       make_ns_map(&g.map_a64, g.A, g.m, g.m, g.cnt, g.m_pad, as, 64) &&
+       make_ns_map(&g.map_bp, g.B, g.m, g.m, g.cnt, g.m_pad, as, bm) &&
+       make_ns_map(&g.map_bq, g.B, g.m, g.m, g.cnt, g.m_pad, as, bn) &&
+       make_ns_map(&g.map_b64, g.B, g.m, g.m, g.cnt, g.m_pad, as, 64);
+  return ok;
+}
+
+void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base) {
+  const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
+  G.m = static_cast<int>(g.m);
+  G.n = static_cast<int>(g.n);
+  G.count = static_cast<int>(g.cnt);
+  G.inv = g.inv;
+  G.tile_base = tile_base;
+  if (phase == kEpiGram) {
+    G.mapA = g.map_gram[it & 1];
+    G.mapB = g.map_gram[it & 1];
+    G.mapC = g.map_ap;
+    G.mapD = g.map_a64;
+    G.partial = g.partial;
+    G.tile_cnt = g.tile_cnt;
+    G.nt = static_cast<int>(cdiv64(g.m, bn));
+    G.mt = static_cast<int>(cdiv64(g.m, bm));
+    G.ksplit = g.ksplit;
+    G.kb_per_split = g.kb_per_split;
+    G.num_kb = g.num_kb_gram;
+    G.tiles_per_mat = static_cast<int>(g.tri * g.ksplit);
+  } else if (phase == kEpiPoly) {
+    G.mapA = g.map_ap;      // operand rows and the epilogue's A tiles
+    G.mapB = g.map_aq;
+    G.mapC = g.map_bp;
+    G.mapD = g.map_b64;
+    G.nt = static_cast<int>(cdiv64(g.m, bn));
+    G.mt = static_cast<int>(cdiv64(g.m, bm));
+    G.ksplit = 1;
+    G.num_kb = static_cast<int>(cdiv64(g.m, bk));
+    G.kb_per_split = G.num_kb;
+    G.tiles_per_mat = static_cast<int>(g.tri);
+  } else {
+    G.mapA = g.map_xt[it & 1];
+    G.mapB = g.map_bq;
+    G.mapC = g.map_xt[(it + 1) & 1];
+    G.nt = static_cast<int>(cdiv64(g.m, bn));
+    G.mt = static_cast<int>(cdiv64(g.n, bm));
+    G.ksplit = 1;
+    G.num_kb = static_cast<int>(cdiv64(g.m, bk));
+    G.kb_per_split = G.num_kb;
+    G.tiles_per_mat = G.nt * G.mt;
+  }
+}
+
+}  // namespace muon

@@ -198,3 +198,18 @@ def test_checkpoint_resume_bitwise():
     binding.muon_step_grouped(c, **hp)
     torch.cuda.synchronize()
     assert torch.equal(a[0]["W"], c[0]["W"]) and torch.equal(a[0]["Mom"], c[0]["Mom"])
+
+
+@pytest.mark.parametrize("shape", [(160, 256, 2048), (2, 2048, 2304)])
+def test_long_k_launches(shape):
+    """Launches whose every tile has at least 32 K blocks take the deeper
+    operand ring with one staging box per epilogue set: 160 x [256, 2048]
+    (Gram, no split-K), 2 x [2048, 2304] (polynomial and apply)."""
+    g = torch.Generator().manual_seed(shape[0] + shape[1])
+    x = torch.randn(shape, generator=g)
+    out = _ns_gpu_f32(x)
+    idx = list(range(0, shape[0], max(1, shape[0] // 6)))
+    ref = R.ns_batched_ref(_np(x[idx]))
+    got = _np(out)
+    for k, i in enumerate(idx):
+        assert _rel(got[i], ref[k]) <= NS_TOL, (shape, i, _rel(got[i], ref[k]))
