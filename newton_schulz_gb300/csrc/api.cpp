@@ -686,7 +686,8 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           tiles += static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
           min_kb = std::min(min_kb, G.kb_per_split);
         }
-        gp.deep = min_kb >= kDeepKBlocks ? 1 : 0;
+        gp.deep = gemm_deep(phase, min_kb);
+        if (const char* d = std::getenv("MUON_GEMM_DEEP")) gp.deep = d[0] == '1';   // tuning override
         if (tiles >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         gp.n_groups = static_cast<int>(ch.groups.size());
         gp.total_tiles = static_cast<int>(tiles);

@@ -105,7 +105,7 @@ struct GemmParams {
   float a, b, c;           // apply uses a - alpha; poly adds alpha on the diagonal
   float alpha;             // shift: X' = (a - alpha) X + (b A + c A^2 + alpha I) X
   int first;              // 1: operands are unnormalised, apply inv scale
-  int deep;               // 1: every tile has >= kDeepKBlocks K blocks (4-stage ring)
+  int deep;               // 1: 4-stage ring, one staging box per epilogue set
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -207,7 +207,14 @@ int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage
 int gemm_sym_tiles(int m);   // tiles of a symmetric m x m product (holding some col >= row)
-constexpr int kDeepKBlocks = 32;   // K blocks per tile from which a launch takes the deep ring
+// Ring depth of a launch (GemmParams::deep): the Gram and the apply always
+// take the 4-stage ring (their epilogues need one staging box per set); the
+// polynomial, whose mirrored output wants two boxes per set in flight, only
+// when every tile has at least 32 K blocks (measured on the MoE-expert and
+// Llama-shaped workloads).
+inline int gemm_deep(int phase, int min_kblocks) {
+  return (phase != kEpiPoly || min_kblocks >= 32) ? 1 : 0;
+}
 cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s);
 int small_blocks_per_sm(int smem_bytes);   // resident CTAs per SM, 0 when the query fails
 

@@ -200,7 +200,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
       gp.c = c;
       gp.alpha = alpha;
       gp.first = it == 0 ? 1 : 0;
-      gp.deep = G.kb_per_split >= kDeepKBlocks ? 1 : 0;
+      gp.deep = gemm_deep(phase, G.kb_per_split);
       gp.status = status;
       gp.timeout_ns = timeout_ns;
       if (launch_gemm(phase, gp, stream) != cudaSuccess) return MUON_ERR_CUDA;

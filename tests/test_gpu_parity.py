@@ -202,9 +202,9 @@ def test_checkpoint_resume_bitwise():
 
 @pytest.mark.parametrize("shape", [(160, 256, 2048), (2, 2048, 2304)])
 def test_long_k_launches(shape):
-    """Launches whose every tile has at least 32 K blocks take the deeper
-    operand ring with one staging box per epilogue set: 160 x [256, 2048]
-    (Gram, no split-K), 2 x [2048, 2304] (polynomial and apply)."""
+    """Long-K launches: 160 x [256, 2048] (Gram over K = 2048 without
+    split-K), 2 x [2048, 2304] (the polynomial's tiles have 32 K blocks, so
+    it takes the 4-stage ring with one staging box per epilogue set)."""
     g = torch.Generator().manual_seed(shape[0] + shape[1])
     x = torch.randn(shape, generator=g)
     out = _ns_gpu_f32(x)
