@@ -191,7 +191,7 @@ bool small_shape(int64_t m) {
 // X0 image of an item streams through the stages), shrinking while the
 // launch would leave SMs without an item.
 bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, bool step,
-                SmallParams* sp) {
+                bool precise, SmallParams* sp) {
   sp->m = static_cast<int>(m);
   sp->n = static_cast<int>(n);
   sp->mr = static_cast<int>(rup(m, 8));
@@ -200,18 +200,26 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   sp->cw1 = m <= 32 ? 128 : 64;
   sp->qbytes = 2 * sp->nmm * 128;
   sp->pstride = static_cast<int>(rup(2 * m * m, 4));
+  sp->precise = precise ? 1 : 0;
+  sp->nblk = (sp->cw1 == 128 || precise) ? 2 : 1;
+  sp->gcols = (precise && m > 32) ? 128 : 64;
+  const size_t xs = precise ? 2 : 1;                          // X0 regions per 64 columns
   const size_t chunk = static_cast<size_t>(sp->mr) * 128;   // 64 X columns of X0
   const size_t p1 = static_cast<size_t>(m) * sp->cw1 * (esg + (step ? 4 : 0));
   const size_t p2 = static_cast<size_t>(m) * 128 * esw;
   sp->x_off = static_cast<int>(align_up(std::max(p1, p2), 1024));
-  sp->stage_bytes = static_cast<int>(align_up(sp->x_off + 2 * chunk + 2048, 1024));
-  const size_t gs = align_up(static_cast<size_t>(5) * sp->mp * sp->mp * 4 + 64, 16);
+  sp->stage_bytes = static_cast<int>(align_up(sp->x_off + 2 * xs * chunk + 2048, 1024));
+  // the precise carve-up with 64 x 64 Gram-space matrices keeps three of them
+  sp->gs_lowmem = (precise && sp->mp == 64) ? 1 : 0;
+  const size_t gs =
+      align_up(static_cast<size_t>(sp->gs_lowmem ? 3 : 5) * sp->mp * sp->mp * 4 + 64, 16);
   const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) + gs + 512 + 1024;
   if (fixed >= static_cast<size_t>(kSmallSmemLimit)) return false;
   const int tcol = static_cast<int>(rup(sp->nmm, 32));
-  // TMEM: Gram accumulators in [0, 128), one O slot (2 tcol columns) per stage
+  // TMEM: two Gram accumulators in [0, 2 gcols), one O slot (2 tcol columns) per stage
+  const int ocols = kSmallTmemCols - 2 * sp->gcols;
   sp->stages = static_cast<int>(std::min<size_t>((kSmallSmemLimit - fixed) / sp->stage_bytes,
-                                                 std::min(kSmallMaxStages, 384 / (2 * tcol))));
+                                                 std::min(kSmallMaxStages, ocols / (2 * tcol))));
   if (sp->stages < 2) return false;
   int64_t wb = std::min<int64_t>(2048, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);
@@ -220,7 +228,7 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   sp->nb = static_cast<int>(cdiv(n, wb));
   sp->total_mats = static_cast<int>(mats);
   sp->items = static_cast<int>(mats * sp->nb);
-  sp->xbytes = static_cast<int>((wb / 64) * chunk);
+  sp->xbytes = static_cast<int>((wb / 64) * xs * chunk);
   sp->off_ring = 0;
   sp->off_q = sp->stages * sp->stage_bytes;
   sp->off_gs = sp->off_q + 2 * sp->qbytes;
@@ -424,6 +432,7 @@ struct NsCfg {
   int steps;
   std::vector<float> coeffs;   // [steps][3]
   float eps;
+  bool precise = false;        // MUON_NS_TF32: X0 carried as bf16 hi + lo
 };
 
 muon_status_t check_ns_cfg(const muon_ns_config_t* cfg, NsCfg* out) {
@@ -435,10 +444,9 @@ muon_status_t check_ns_cfg(const muon_ns_config_t* cfg, NsCfg* out) {
     return MUON_OK;
   }
   if (cfg->steps < 0 || cfg->steps > kMaxSteps) return MUON_ERR_INVALID_ARGUMENT;
-  if (cfg->precision != MUON_NS_BF16) {
-    if (cfg->precision == MUON_NS_TF32) return MUON_ERR_UNSUPPORTED;
+  if (cfg->precision != MUON_NS_BF16 && cfg->precision != MUON_NS_TF32)
     return MUON_ERR_INVALID_ARGUMENT;
-  }
+  out->precise = cfg->precision == MUON_NS_TF32;
   if (!std::isfinite(cfg->eps) || cfg->eps < 0.f) return MUON_ERR_INVALID_ARGUMENT;
   out->steps = cfg->steps;
   out->eps = cfg->eps;
@@ -476,6 +484,11 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // NS-only: reqs[i].G is the input, reqs[i].W the output (dtype w_dtype).
 muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int nesterov, float lr,
                   float wd, int scale_rule, const NsCfg& ns, cudaStream_t stream) {
+  // the high-precision NS mode exists on the small-m path only: refuse the
+  // call before anything is planned or enqueued
+  if (ns.precise)
+    for (const Req& q : reqs)
+      if (q.B > 0 && q.m > 0 && !small_shape(q.m)) return MUON_ERR_UNSUPPORTED;
   DevState* dev = nullptr;
   muon_status_t st = dev_state(&dev);
   if (st != MUON_OK) return st;
@@ -526,7 +539,8 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           esg = std::max(esg, static_cast<int>(esize(reqs[kv.second[k]].g_dtype)));
           esw = std::max(esw, static_cast<int>(esize(reqs[kv.second[k]].w_dtype)));
         }
-        if (!small_plan(m, n, mats, dev->sms, esg, esw, step_mode, &sp)) return MUON_ERR_UNSUPPORTED;
+        if (!small_plan(m, n, mats, dev->sms, esg, esw, step_mode, ns.precise, &sp))
+          return MUON_ERR_UNSUPPORTED;
         // TMA tile maps (stored layout): rows of 16-byte multiples, 16-byte
         // aligned bases; otherwise the kernel copies element-wise
         for (size_t k = b; k < e; ++k) {
@@ -591,7 +605,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready_list, &sp.ctr, &sp.epoch, &sp.cap);
     if (st != MUON_OK) return st;
     // one CTA per SM (all resident: the launch is cooperative)
-    if (small_blocks_per_sm(sp.smem_bytes) <= 0) return MUON_ERR_CUDA;
+    if (small_blocks_per_sm(sp.smem_bytes, sp.precise != 0) <= 0) return MUON_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(sp.items, dev->sms));
     st = L0.run(5, [&] { return launch_small(sp, grid, stream); });
     if (st != MUON_OK) return st;

@@ -179,6 +179,11 @@ struct SmallParams {
   int x_off;         // X0 tile inside a stage (1024-aligned); a zero gap follows it
   int qbytes;        // one Q image: hi and lo, nmm rows x 128 bytes each
   int pstride;       // floats per item's partial Gram blocks (2 m^2 rounded up to 4)
+  int precise;       // 1: X0 kept as bf16 hi + lo (each 64-column chunk is [hi][lo])
+  int nblk;          // partial Gram blocks per item (1 or 2)
+  int gcols;         // TMEM columns per Gram accumulator (64, or 128 for precise m > 32);
+                     // the O slots start at column 2 gcols
+  int gs_lowmem;     // Gram-space job in three LD x LD buffers instead of five
   int steps;
   float coef[kMaxSteps][3];
   int step_mode, nesterov;
@@ -216,6 +221,6 @@ inline int gemm_deep(int phase, int min_kblocks) {
   return (phase != kEpiPoly || min_kblocks >= 32) ? 1 : 0;
 }
 cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s);
-int small_blocks_per_sm(int smem_bytes);   // resident CTAs per SM, 0 when the query fails
+int small_blocks_per_sm(int smem_bytes, bool precise);   // resident CTAs per SM, 0 on failure
 
 }  // namespace muon

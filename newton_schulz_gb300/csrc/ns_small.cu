@@ -205,16 +205,21 @@ __device__ __forceinline__ void cons_sync() { ptx::named_bar(kConsBar, kT); }
 // holds five LD x LD fp32 matrices (R, T, P, Q, Q') plus a few scalars.
 // Per step three phases: {T = R^2, P = aI + bR + cT}, {T = P R, Q' = P Q},
 // {R = T P} (the first step takes Q = P, the last needs neither R nor T).
-template <int TI, int TJ, int LD>
+template <int TI, int TJ, int LD, bool LOWMEM>
 __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs, int t) {
   const int m = p.m;
   constexpr int MM = LD * LD;
+  // Five LD x LD matrices: R, T = P R, P, Q and the next Q.  LOWMEM keeps
+  // three (R also holds T between the two products of a step, Q is updated
+  // in place): each product then goes through registers and a barrier, two
+  // more barriers per step, which the latency-bound small Gram-space job
+  // feels, so only the carve-ups that need the space use it.
   float* R = gs;
-  float* T = gs + MM;
-  float* P = gs + 2 * MM;
-  float* Q = gs + 3 * MM;
-  float* Qn = gs + 4 * MM;
-  float* sc = gs + 5 * MM;
+  float* P = gs + MM;
+  float* Q = gs + 2 * MM;
+  float* T = LOWMEM ? R : gs + 3 * MM;
+  float* Qn = LOWMEM ? Q : gs + 4 * MM;
+  float* sc = gs + (LOWMEM ? 3 : 5) * MM;
   // the 16 x 16 blocks of TI x TJ cover LD x LD: consumer threads 0..255
   // form the products, the others only take part in the barriers
   const bool blk = t < 256;
@@ -224,8 +229,9 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
   // partial block q (item q / nblk, stacked block q % nblk) at
   // part + (mat nb + q / nblk) pstride + (q % nblk) m^2
   const float* part = p.part + static_cast<size_t>(mat) * p.nb * p.pstride;
-  const int nblk = p.cw1 == 128 ? 2 : 1;
-  const int nq = p.nb * nblk;
+  const int nblk = p.nblk;                 // 1 or 2: q / nblk and q % nblk as shift and mask
+  const int bsh = nblk - 1;                // (a division by a run-time divisor here costs
+  const int nq = p.nb * nblk;              // the job about 15 us at m = 24)
   for (int e = t; e < MM; e += kT) {
     const int i = e / LD, j = e - i * LD;
     float acc = 0.f;
@@ -236,7 +242,7 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           const int q = b0 + b;
-          v[b] = q < nq ? __ldcg(part + static_cast<size_t>(q / nblk) * p.pstride + (q % nblk) * m * m + src)
+          v[b] = q < nq ? __ldcg(part + static_cast<size_t>(q >> bsh) * p.pstride + (q & bsh) * m * m + src)
                         : 0.f;
         }
 #pragma unroll
@@ -280,21 +286,33 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
     }
     cons_sync();
     if (more || k > 0) {
-      float acc[TI][TJ];
-      if (more) {
-        if (blk) {
+      if (LOWMEM) {
+        // one product in registers at a time (the register budget of the
+        // whole kernel follows its largest callee)
+        float acc[TI][TJ];
+        if (more) {
+          if (blk) mm_block<TI, TJ, LD>(P, R, i0, j0, acc);   // T = P R
+          cons_sync();   // every thread has read R
+          if (blk) st_block<TI, TJ, LD>(T, i0, j0, acc);
+        }
+        if (k > 0) {
+          if (blk) mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);   // Q' = P Q
+          cons_sync();   // every thread has read Q
+          if (blk) st_block<TI, TJ, LD>(Qn, i0, j0, acc);
+        }
+      } else {
+        float acc[TI][TJ];
+        if (blk && more) {
           mm_block<TI, TJ, LD>(P, R, i0, j0, acc);     // T = P R
           st_block<TI, TJ, LD>(T, i0, j0, acc);
         }
-      }
-      if (k > 0) {
-        if (blk) {
+        if (blk && k > 0) {
           mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);     // Q' = P Q
           st_block<TI, TJ, LD>(Qn, i0, j0, acc);
         }
       }
       cons_sync();
-      if (k > 0) {
+      if (!LOWMEM && k > 0) {
         float* x = Q;
         Q = Qn;
         Qn = x;
@@ -302,10 +320,9 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
     }
     if (more) {
       float acc[TI][TJ];
-      if (blk) {
-        mm_block<TI, TJ, LD>(T, P, i0, j0, acc);       // R <- P R P
-        st_block<TI, TJ, LD>(R, i0, j0, acc);
-      }
+      if (blk) mm_block<TI, TJ, LD>(T, P, i0, j0, acc);          // R <- (P R) P
+      if (LOWMEM) cons_sync();
+      if (blk) st_block<TI, TJ, LD>(R, i0, j0, acc);
       cons_sync();
     }
   }
@@ -481,7 +498,7 @@ __device__ __forceinline__ void store_mom8(float* dst, int nv, bool vec, const f
 // First-phase stage of X columns [c0, c0 + cw1) of the item: M' to global
 // memory, X0 = bf16(D) into the stage's X0 tile (rows mr, cw1 / 64 chunks;
 // rows m..mr-1 and columns outside the matrix zero) and to the item's image.
-template <int ESG, bool STEP>
+template <int ESG, bool STEP, bool PRECISE>
 __device__ void consume_p1(const ItemCfg& c, int c0, uint8_t* st, int t) {
   const int m = c.m, cw = c.cw, cb = c.chunk_bytes;
   const uint8_t* smom = st + c.mom_off;
@@ -524,8 +541,21 @@ __device__ void consume_p1(const ItemCfg& c, int c0, uint8_t* st, int t) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(d[2 * j], d[2 * j + 1]);
       const uint32_t off = ptx::sw128_offset(r, (c8 & 63) * 2);
-      *reinterpret_cast<uint4*>(sx + (c8 >> 6) * cb + off) = q;
-      __stcg(reinterpret_cast<uint4*>(c.img + ((c0 + c8) >> 6) * cb + off), q);
+      constexpr int xs = PRECISE ? 2 : 1;   // chunk regions per 64 columns
+      *reinterpret_cast<uint4*>(sx + (c8 >> 6) * xs * cb + off) = q;
+      __stcg(reinterpret_cast<uint4*>(c.img + ((c0 + c8) >> 6) * xs * cb + off), q);
+      if constexpr (PRECISE) {
+        // lo = bf16(d - hi): X0 = hi + lo to about 16 significant bits
+        uint4 ql;
+        __nv_bfloat162* l = reinterpret_cast<__nv_bfloat162*>(&ql);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 hf = __bfloat1622float2(h[j]);
+          l[j] = __floats2bfloat162_rn(d[2 * j] - hf.x, d[2 * j + 1] - hf.y);
+        }
+        *reinterpret_cast<uint4*>(sx + ((c8 >> 6) * 2 + 1) * cb + off) = ql;
+        __stcg(reinterpret_cast<uint4*>(c.img + (((c0 + c8) >> 6) * 2 + 1) * cb + off), ql);
+      }
     }
   } else {
     const int ig = c.mr >> 3;
@@ -552,25 +582,35 @@ __device__ void consume_p1(const ItemCfg& c, int c0, uint8_t* st, int t) {
       }
       const int ci = c0 + cc;
       const uint32_t byte = (cc & 63) * 2, ibyte = (ci & 63) * 2;
+      constexpr int xs = PRECISE ? 2 : 1;   // chunk regions per 64 columns
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const __nv_bfloat16 v = __float2bfloat16_rn(j < nv ? d[j] : 0.f);
-        *reinterpret_cast<__nv_bfloat16*>(sx + (cc >> 6) * cb + ptx::sw128_offset(r + j, byte)) = v;
-        *reinterpret_cast<__nv_bfloat16*>(c.img + (ci >> 6) * cb + ptx::sw128_offset(r + j, ibyte)) = v;
+        const float dv = j < nv ? d[j] : 0.f;
+        const __nv_bfloat16 v = __float2bfloat16_rn(dv);
+        *reinterpret_cast<__nv_bfloat16*>(sx + (cc >> 6) * xs * cb + ptx::sw128_offset(r + j, byte)) = v;
+        *reinterpret_cast<__nv_bfloat16*>(c.img + (ci >> 6) * xs * cb + ptx::sw128_offset(r + j, ibyte)) = v;
+        if constexpr (PRECISE) {
+          const __nv_bfloat16 lv = __float2bfloat16_rn(dv - __bfloat162float(v));
+          *reinterpret_cast<__nv_bfloat16*>(sx + ((cc >> 6) * 2 + 1) * cb + ptx::sw128_offset(r + j, byte)) = lv;
+          *reinterpret_cast<__nv_bfloat16*>(c.img + ((ci >> 6) * 2 + 1) * cb + ptx::sw128_offset(r + j, ibyte)) = lv;
+        }
       }
     }
   }
 }
 
-__device__ void consume_p1_any(const ItemCfg& c, int c0, uint8_t* st, int t) {
+template <bool PRECISE>
+__device__ void consume_p1_dt(const ItemCfg& c, int c0, uint8_t* st, int t) {
   if (c.esg == 4) {
-    if (c.step) consume_p1<4, true>(c, c0, st, t);
-    else consume_p1<4, false>(c, c0, st, t);
+    if (c.step) consume_p1<4, true, PRECISE>(c, c0, st, t);
+    else consume_p1<4, false, PRECISE>(c, c0, st, t);
   } else {
-    if (c.step) consume_p1<2, true>(c, c0, st, t);
-    else consume_p1<2, false>(c, c0, st, t);
+    if (c.step) consume_p1<2, true, PRECISE>(c, c0, st, t);
+    else consume_p1<2, false, PRECISE>(c, c0, st, t);
   }
 }
+
+
 
 // ---- consumers: second-phase stage -------------------------------------------------------
 template <typename WT>
@@ -698,6 +738,9 @@ __device__ __forceinline__ ItemRef item_ref(const SmallParams& p, int item) {
 
 }  // namespace
 
+// PRECISE: X0 carried as bf16 hi + lo (its own instantiation, so that the
+// common path carries none of it).
+template <bool PRECISE>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     ns_small_kernel(const __grid_constant__ SmallParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -724,8 +767,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const int tiles = wb / 128;
   const int s1 = wb / p.cw1;               // first-phase stages per item
   const int oslot_cols = 2 * ((nmm + 31) & ~31);   // O slot: X0 Q_hi^T then X0 Q_lo^T
-  const bool stack = p.cw1 == 128;         // first phase: both chunks of a stage as one operand
+  // First-phase Gram MMA: the stage's two 64-column chunks stacked as one
+  // 2 mr-row operand (m <= 32), or, precise, each chunk's [hi; lo] stacked
+  // (the four blocks hi hi^T, hi lo^T, lo hi^T, lo lo^T sum to X0 X0^T).
+  const bool stack = p.cw1 == 128 || PRECISE;
   const int ngram = stack ? 2 * p.mr : nmm;          // Gram MMA N
+  constexpr int xs = PRECISE ? 2 : 1;                // chunk regions per 64 X0 columns
+  const uint32_t obase = 2 * p.gcols;                // first O slot column
 
   if (tid == 0) {
     for (int i = 0; i < kSmallMaxStages; ++i) {
@@ -745,7 +793,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   // zero gap after every stage's X0 tile (read as the apply's K padding)
   for (int s = 0; s < NS; ++s)
     for (int i = tid; i < 2048 / 16; i += kSmallThreads)
-      reinterpret_cast<uint4*>(ring + s * p.stage_bytes + p.x_off + 2 * chunk_bytes)[i] =
+      reinterpret_cast<uint4*>(ring + s * p.stage_bytes + p.x_off + 2 * xs * chunk_bytes)[i] =
           make_uint4(0, 0, 0, 0);
   if (warp == 1) ptx::tmem_alloc(&B->tslot, kSmallTmemCols);
   ptx::tc_fence_before();
@@ -780,7 +828,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             if (p.step_mode) copy_tile_in(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
           }
         } else {   // second phase: W tile (step mode) and the X0 tile from the image
-          tx = static_cast<uint32_t>(2 * chunk_bytes);
+          tx = static_cast<uint32_t>(2 * xs * chunk_bytes);
           if (p.step_mode) {
             if (S.wbulk) {
               tma = true;
@@ -809,8 +857,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           } else {
             if (tma) ptx::tma_load_3d(st, &p.tm[ir.si][2], full, x, y, z);
             ptx::bulk_load(st + p.x_off,
-                           p.ximg + static_cast<size_t>(item) * p.xbytes + (c0 / 64) * chunk_bytes,
-                           static_cast<uint32_t>(2 * chunk_bytes), full);
+                           p.ximg + static_cast<size_t>(item) * p.xbytes + (c0 / 64) * xs * chunk_bytes,
+                           static_cast<uint32_t>(2 * xs * chunk_bytes), full);
           }
         } else {
           ptx::mbar_arrive(full);
@@ -884,10 +932,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           if (!mwait(&B->cons_done[rg.stage], rg.phase, ctx)) break;
           ptx::tc_fence_after();
           const int g = k1 & 1;
+          if (PRECISE) {
+            // each 64-column chunk's [hi; lo] is one operand
+            for (int ch = 0; ch < p.cw1 / 64; ++ch)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kk * 32);
-            ptx::umma_bf16(tmem + 64 * g, d, d, idesc_gram, ((flags & kFirst) && kk == 0) ? 0u : 1u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t d = ptx::sdesc_kmajor_sw128(sx + ch * 2 * chunk_bytes + kk * 32);
+                ptx::umma_bf16(tmem + p.gcols * g, d, d, idesc_gram,
+                               ((flags & kFirst) && ch == 0 && kk == 0) ? 0u : 1u);
+              }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t d = ptx::sdesc_kmajor_sw128(sx + kk * 32);
+              ptx::umma_bf16(tmem + 64 * g, d, d, idesc_gram, ((flags & kFirst) && kk == 0) ? 0u : 1u);
+            }
           }
           ptx::umma_commit(&B->mma_done[rg.stage]);
           if (flags & kLast) {
@@ -902,11 +961,23 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           ptx::tc_fence_after();
           // X0 (MN-major, 128 columns) times [Q_hi; Q_lo]^T: one MMA per K-step
           const uint32_t sq = ptx::smem_u32(sm + p.off_q + (k2 & 1) * p.qbytes);
-          const uint32_t ocol = 128 + oslot_cols * rg.stage;
-          for (int j = 0; j < nmm / 16; ++j) {
-            const uint64_t a = ptx::sdesc_mnmajor_sw128(sx + j * 2048, chunk_bytes, 1024);
-            ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + j * 32), idesc_app,
-                           j != 0 ? 1u : 0u);
+          const uint32_t ocol = obase + oslot_cols * rg.stage;
+          if (PRECISE) {
+            // the hi chunks, then the lo chunks one region later
+            for (int j = 0; j < nmm / 16; ++j) {
+              const uint64_t b = ptx::sdesc_kmajor_sw128(sq + j * 32);
+              for (int hl = 0; hl < 2; ++hl) {
+                const uint64_t a =
+                    ptx::sdesc_mnmajor_sw128(sx + hl * chunk_bytes + j * 2048, 2 * chunk_bytes, 1024);
+                ptx::umma_bf16(tmem + ocol, a, b, idesc_app, (j != 0 || hl != 0) ? 1u : 0u);
+              }
+            }
+          } else {
+            for (int j = 0; j < nmm / 16; ++j) {
+              const uint64_t a = ptx::sdesc_mnmajor_sw128(sx + j * 2048, chunk_bytes, 1024);
+              ptx::umma_bf16(tmem + ocol, a, ptx::sdesc_kmajor_sw128(sq + j * 32), idesc_app,
+                             j != 0 ? 1u : 0u);
+            }
           }
           ptx::umma_commit(&B->mma_done[rg.stage]);
           if (flags & kLast) ptx::umma_commit(&B->q_free[k2 & 1]);
@@ -933,13 +1004,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       const bool gok = mwait_warp(&B->gram_full[g], (k >> 1) & 1, ctx);
       ptx::tc_fence_after();
       const int nblk = stack ? 2 : 1;
-      if (gok && ok && (warp == 4 || warp == 5) && (warp - 4) * 32 < nblk * p.mr) {
+      if (gok && ok && warp >= 4 && warp <= 7 && (warp - 4) * 32 < nblk * p.mr) {
+        // stacked chunks: block bb is row block bb's diagonal block; precise:
+        // row L's partial is D[L][j] + D[L][mr + j] (hi and lo columns), and
+        // the two row blocks are summed with the other partials
         // lane L holds row L of D: block b = L / mr, row i = L - b mr, whose
         // diagonal block starts at column b mr
         const int L = (warp - 4) * 32 + lane;
         const int bb = L >= p.mr ? 1 : 0, i = L - bb * p.mr;
         float* dstp = p.part + static_cast<size_t>(item) * p.pstride + bb * m * m;
-        const uint32_t lbase = tmem + 64 * g + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+        const uint32_t lbase = tmem + p.gcols * g + (static_cast<uint32_t>((warp - 4) * 32) << 16);
         for (int c0 = 0; c0 < m; c0 += 32) {
           uint32_t r0[32], r1[32];
           ptx::tmem_ld_32x32b_x32(lbase + c0, r0);
@@ -948,7 +1022,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           if (L < nblk * p.mr && i < m) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (c0 + j < m) __stcg(dstp + i * m + c0 + j, __uint_as_float(bb ? r1[j] : r0[j]));
+              if (c0 + j < m)
+                __stcg(dstp + i * m + c0 + j,
+                       PRECISE ? __uint_as_float(r0[j]) + __uint_as_float(r1[j])
+                                 : __uint_as_float(bb ? r1[j] : r0[j]));
           }
         }
       }
@@ -963,8 +1040,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       cons_sync();
       if (B->last) {
         __threadfence();
-        if (p.mp == 32) gram_space<2, 2, 32>(p, mat, gs, t);
-        else gram_space<4, 4, 64>(p, mat, gs, t);
+        if (p.mp == 32) gram_space<2, 2, 32, false>(p, mat, gs, t);
+        else if (p.gs_lowmem) gram_space<4, 4, 64, true>(p, mat, gs, t);
+        else gram_space<4, 4, 64, false>(p, mat, gs, t);
         __threadfence();
         cons_sync();
         if (t == 0) {   // publish: next free position of the ready list
@@ -1009,7 +1087,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       for (int s = 0; s < s1; ++s) {
         const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
         ok = ok && sok;
-        if (ok) consume_p1_any(ic, s * p.cw1, ring + rg.stage * p.stage_bytes, t);
+        if (ok) consume_p1_dt<PRECISE>(ic, s * p.cw1, ring + rg.stage * p.stage_bytes, t);
         release();
       }
       if (prev >= 0) finish(prev, prevk);
@@ -1035,7 +1113,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       ptx::tc_fence_after();
       if (ok)
         epi_tile_any(ic, B->desc[rg.stage][2], ring + rg.stage * p.stage_bytes,
-                     tmem + 128 + oslot_cols * rg.stage, set, q4, lane);
+                     tmem + obase + oslot_cols * rg.stage, set, q4, lane);
       release();
     }
   }
@@ -1044,15 +1122,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, kSmallTmemCols);
 }
 
-int small_blocks_per_sm(int smem_bytes) {
-  if (cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem_bytes) != cudaSuccess) {
+int small_blocks_per_sm(int smem_bytes, bool precise) {
+  auto kern = precise ? ns_small_kernel<true> : ns_small_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ns_small_kernel, kSmallThreads,
-                                                    smem_bytes) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kSmallThreads, smem_bytes) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1061,8 +1140,9 @@ int small_blocks_per_sm(int smem_bytes) {
 
 cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s) {
   if (p.items <= 0 || grid <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(ns_small_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+  auto kern = p.precise ? ns_small_kernel<true> : ns_small_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -1076,7 +1156,7 @@ cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, ns_small_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -93,7 +93,10 @@ def test_ns_config_errors(lib):
     assert _step(lib, [_grp()], cfg=binding.make_config(steps=-1)) == E_INV
     assert _step(lib, [_grp()], cfg=binding.make_config(steps=65)) == E_INV
     assert _step(lib, [_grp()], cfg=binding.make_config(eps=-1.0)) == E_INV
-    assert _step(lib, [_grp()], cfg=binding.make_config(precision=1)) == E_UNS
+    # the high-precision mode covers core shapes with min(M, N) <= 64 only
+    assert _step(lib, [_grp(M=128, N=256)], cfg=binding.make_config(precision=1)) == E_UNS
+    assert _step(lib, [_grp(M=4, N=8), _grp(W=0x300000, G=0x400000, M_=0x500000, M=65, N=65)],
+                 cfg=binding.make_config(precision=1)) == E_UNS
     assert _step(lib, [_grp()], cfg=binding.make_config(precision=5)) == E_INV
     bad = binding.make_config(steps=2, coeffs=[[1, 2, 3], [float("nan"), 0, 0]])
     assert _step(lib, [_grp()], cfg=bad) == E_INV

@@ -144,3 +144,48 @@ def test_small_repeat_bitwise_across_counter_ring():
     ref = R.ns_batched_ref(_np(x.cpu()))
     for i in range(5):
         assert _rel(_np(outs[0])[i], ref[i]) <= NS_TOL
+
+
+HP_TOL = 1e-3   # NS tolerance of the high-precision mode
+
+
+@pytest.mark.parametrize("shape", SHAPES + [(2, 64, 256), (4, 40, 3000)])
+def test_precise_ns_parity(shape):
+    """MUON_NS_TF32: X0 as bf16 hi + lo, fp32 Gram space; relative error per
+    matrix within 1e-3 of the float64 oracle."""
+    x = torch.randn(shape, generator=torch.Generator().manual_seed(sum(shape) + 1))
+    X = x.cuda()
+    out = torch.empty_like(X)
+    binding.muon_ns_batched_ex(X, binding.make_config(precision=binding.NS_TF32), out)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    ref = R.ns_batched_ref(_np(x))
+    got = _np(out)
+    errs = [_rel(got[i], ref[i]) for i in range(shape[0])]
+    print(shape, "max rel err", max(errs))
+    assert max(errs) <= HP_TOL, (shape, errs)
+    assert binding.muon_last_launch_count() == 1
+
+
+@pytest.mark.parametrize("shape", [(4, 24, 3000), (3, 3000, 24), (2, 64, 1000), (74, 24, 10240)])
+def test_precise_step_parity(shape):
+    g = synth.random_group(shape, torch.bfloat16, torch.float32, "cuda", 33, 1e-3, 1e-3)
+    host = {k: _np(g[k]) for k in ("W", "G", "Mom")}
+    binding.muon_step_grouped([g], mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0,
+                              ns_cfg=binding.make_config(precision=binding.NS_TF32))
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    k = min(shape[0], 6)
+    w2, m2, _ = R.muon_step_ref(host["W"][:k], host["G"][:k], host["Mom"][:k])
+    assert _rel(_np(g["Mom"])[:k], m2) <= MOM_TOL
+    w = _np(g["W"])
+    for i in range(k):
+        err = np.linalg.norm(w[i] - w2[i]) / np.linalg.norm(w2[i] - host["W"][i])
+        assert err <= HP_TOL, (shape, i, err)
+
+
+def test_precise_rejects_large_core_shapes():
+    x = torch.randn((2, 128, 300), device="cuda")
+    out = torch.empty_like(x)
+    with pytest.raises(binding.MuonError):
+        binding.muon_ns_batched_ex(x, binding.make_config(precision=binding.NS_TF32), out)
