@@ -8,8 +8,9 @@ One step = momentum -> Newton-Schulz (5 steps) -> decoupled-decay update over
 the whole workload, through the C ABI (libmuon).  ``value`` is the achieved
 nominal TFLOP/s (sum over matrices of 5*(4 m^2 n + 2 m^3), m <= n) divided by
 the device time of a step, inputs resident in HBM; ``e2e`` is the same metric
-with the step's inputs copied from pinned host memory and its results (W',
-Mom') copied back inside the timed region.  Between timed steps a 512 MiB
+through the host-memory entry point (muon_step_grouped_host): W, G and Mom
+start in pinned host memory and W', Mom' end there, the library's chunked
+copy-in / step / copy-out pipeline inside the timed region.  Between timed steps a 512 MiB
 buffer is written to flush the 129 MB L2 (outside the timed events).
 
 ``--impl reference`` times the float64 CPU oracle (the deliberately slow
@@ -380,23 +381,22 @@ def _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, 
 
 
 def _end_to_end(args, groups, step, stream, flush, world, dev):
+    """The step through the host-memory entry point: W, G and Mom start and
+    end in pinned host memory; the library's copy-in, step and copy-out (the
+    chunked pipeline of muon_step_grouped_host) are all inside the timed
+    region."""
     import torch
-    host_in = [{k: g[k].to("cpu").pin_memory() for k in ("W", "G", "Mom")} for g in groups]
-    host_out = [{k: torch.empty_like(h[k]).pin_memory() for k in ("W", "Mom")} for h in host_in]
-    h2d = sum(h[k].numel() * h[k].element_size() for h in host_in for k in h)
-    d2h = sum(h[k].numel() * h[k].element_size() for h in host_out for k in h)
+    from newton_schulz_gb300 import binding
+    host = [{k: g[k].to("cpu").pin_memory() for k in ("W", "G", "Mom")} for g in groups]
+    harr = binding.make_groups(host)
+    h2d = sum(h[k].numel() * h[k].element_size() for h in host for k in ("W", "G", "Mom"))
+    d2h = sum(h[k].numel() * h[k].element_size() for h in host for k in ("W", "Mom"))
     e2e_ms = []
     for i in range(args.warmup + max(3, args.steps // 2)):
         flush.fill_(float(i))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for g, h in zip(groups, host_in):
-            for k in ("W", "G", "Mom"):
-                g[k].copy_(h[k], non_blocking=True)
-        step()
-        for g, h in zip(groups, host_out):
-            for k in ("W", "Mom"):
-                h[k].copy_(g[k], non_blocking=True)
+        binding.muon_step_grouped_host(harr, stream=stream, **HP)
         b.record(stream)
         torch.cuda.synchronize()
         if i >= args.warmup:

@@ -165,6 +165,24 @@ muon_status_t muon_step_grouped_ex(const muon_group_t *groups, int n_groups, flo
                                    int nesterov, float lr, float wd, int scale_rule,
                                    const muon_ns_config_t *ns, cudaStream_t stream);
 
+/* One Muon step over parameters whose W, G and Mom are in HOST memory (an
+ * optimizer whose state lives in the Grace CPU's memory).  Same semantics,
+ * arguments and errors as muon_step_grouped_ex, with host pointers; pinned
+ * (page-locked) memory lets the copies run asynchronously and overlap.  The
+ * library cuts the matrices into chunks (about 1/8 of the bytes, at least
+ * 48 MB; MUON_HOST_CHUNKS overrides the 8) and moves
+ * each through one of three device slots it owns: copy-in, the step, and
+ * copy-out of W' and Mom' run on three internal streams so the two copy
+ * directions and the kernels overlap.  All of it is ordered after the work
+ * already on `stream`, and `stream` waits for the last copy-out, so the host
+ * arrays hold the result once `stream` has been synchronised; they must stay
+ * alive (and untouched) until then.  Ownership: the caller owns the host
+ * arrays; the library owns the device slots (freed by
+ * muon_release_workspace). */
+muon_status_t muon_step_grouped_host(const muon_group_t *groups, int n_groups, float mu,
+                                     int nesterov, float lr, float wd, int scale_rule,
+                                     const muon_ns_config_t *ns, cudaStream_t stream);
+
 /* Read and clear the current device's status word (MUON_OK, MUON_ERR_TIMEOUT
  * or MUON_ERR_NONFINITE; the first bit set wins in that order of severity).
  * The caller synchronises `stream` first; this call synchronises it again. */

@@ -26,7 +26,7 @@ PROFILE_KINDS = ("prep", "gram", "poly", "apply", "update", "fused_small")
 
 EXPORTED = (
     "muon_ns_default_config", "muon_ns_batched", "muon_ns_batched_ex", "muon_step_grouped",
-    "muon_step_grouped_ex", "muon_query_status", "muon_status_string",
+    "muon_step_grouped_ex", "muon_step_grouped_host", "muon_query_status", "muon_status_string",
     "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
     "muon_profile_read",
 )
@@ -75,6 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_step_grouped_ex.argtypes = [ctypes.POINTER(Group), ctypes.c_int, f32, ctypes.c_int,
                                          f32, f32, ctypes.c_int, ctypes.POINTER(NsConfig), vp]
     lib.muon_step_grouped_ex.restype = i32
+    lib.muon_step_grouped_host.argtypes = lib.muon_step_grouped_ex.argtypes
+    lib.muon_step_grouped_host.restype = i32
     lib.muon_query_status.argtypes = [vp]
     lib.muon_query_status.restype = i32
     lib.muon_status_string.argtypes = [i32]
@@ -194,6 +196,19 @@ def muon_step_grouped(groups, mu: float = 0.95, nesterov: bool = True, lr: float
 
 
 muon_step_grouped_ex = muon_step_grouped
+
+
+def muon_step_grouped_host(groups, mu: float = 0.95, nesterov: bool = True, lr: float = 0.02,
+                           wd: float = 0.01, scale_rule: int = SCALE_SQRT_MAX1_R_OVER_C,
+                           ns_cfg=None, stream=None) -> None:
+    """One Muon step over groups of HOST (ideally pinned) [B,M,N] tensors; the
+    library stages them through device memory.  Synchronise `stream` before
+    reading the results."""
+    arr, n = groups if isinstance(groups, tuple) else make_groups(groups)
+    code = load().muon_step_grouped_host(arr, n, mu, int(nesterov), lr, wd, scale_rule,
+                                         ctypes.byref(ns_cfg) if ns_cfg is not None else None,
+                                         _stream_ptr(stream))
+    check(code, "muon_step_grouped_host")
 
 
 def muon_query_status(stream=None) -> int:

@@ -59,6 +59,19 @@ struct ProfRec {
 
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// Host-resident steps (muon_step_grouped_host): per (device, caller stream),
+// the copy-in, compute and copy-out streams, slot events and the device
+// slots the chunks are staged through.
+constexpr int kHostSlots = 3;
+struct HostPipe {
+  cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[kHostSlots] = {}, ev_comp[kHostSlots] = {},
+              ev_free[kHostSlots] = {};
+  void* slot = nullptr;   // kHostSlots x slot_bytes
+  size_t slot_bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, HostPipe> g_host;
 std::map<int, DevState> g_dev;
 bool g_prof = false;
 std::vector<ProfRec> g_prof_recs;
@@ -874,6 +887,225 @@ muon_status_t ns_impl(void* X, int dtype, int64_t B, int64_t M, int64_t N,
   return run({q}, false, 0.f, 0, 0.f, 0.f, MUON_SCALE_ONE, ns, stream);
 }
 
+// ---- host-resident state ------------------------------------------------------------
+// One Muon step over parameters whose W, G and Mom live in host memory.  The
+// matrices are cut into chunks (about 1/8 of the bytes, at least 48 MB); chunk i moves
+// through device slot i % 3: copy-in on one stream, the step on a second,
+// copy-out (W', Mom') on a third, so that the two copy directions and the
+// kernels overlap.  Everything is ordered after the work already on
+// `stream`, and `stream` waits for the last copy-out: the call is
+// asynchronous on `stream` like the device entry points.
+muon_status_t host_pipe(cudaStream_t stream, size_t slot_bytes, HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  HostPipe& h = g_host[{dev, stream}];
+  if (!h.s_in) {
+    for (cudaStream_t* st : {&h.s_in, &h.s_comp, &h.s_out})
+      if (cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) != cudaSuccess) return MUON_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&h.ev_start, cudaEventDisableTiming) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    for (int i = 0; i < kHostSlots; ++i)
+      for (cudaEvent_t* e : {&h.ev_in[i], &h.ev_comp[i], &h.ev_free[i]})
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return MUON_ERR_CUDA;
+  }
+  if (h.slot_bytes < slot_bytes) {
+    // earlier calls may still use the old slots
+    for (cudaStream_t st : {h.s_in, h.s_comp, h.s_out})
+      if (cudaStreamSynchronize(st) != cudaSuccess) return MUON_ERR_CUDA;
+    if (h.slot) cudaFree(h.slot);
+    h.slot = nullptr;
+    h.slot_bytes = 0;
+    const size_t want = align_up(slot_bytes, size_t(1) << 21);
+    if (cudaMalloc(&h.slot, want * kHostSlots) != cudaSuccess) {
+      cudaGetLastError();
+      h.slot = nullptr;
+      return MUON_ERR_OUT_OF_MEMORY;
+    }
+    h.slot_bytes = want;
+  }
+  *out = &h;
+  return MUON_OK;
+}
+
+muon_status_t host_step_impl(const muon_group_t* groups, int n_groups, float mu, int nesterov,
+                             float lr, float wd, int scale_rule, const muon_ns_config_t* nscfg,
+                             cudaStream_t stream) {
+  if (n_groups < 0 || (n_groups > 0 && !groups)) return MUON_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(mu) || !std::isfinite(lr) || !std::isfinite(wd))
+    return MUON_ERR_INVALID_ARGUMENT;
+  if (scale_rule < 0 || scale_rule > MUON_SCALE_ONE) return MUON_ERR_INVALID_ARGUMENT;
+  NsCfg ns;
+  muon_status_t st = check_ns_cfg(nscfg, &ns);
+  if (st != MUON_OK) return st;
+  // validation and alias rules of the device entry point, on host ranges
+  std::vector<std::pair<uintptr_t, uintptr_t>> written, all;
+  struct Unit {
+    int g;
+    size_t bytes;   // W + G + Mom of one matrix
+  };
+  std::vector<Unit> units;
+  size_t total = 0;
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_group_t& g = groups[i];
+    if (g.B < 0 || g.M < 0 || g.N < 0) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.w_dtype != MUON_F32 && g.w_dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.g_dtype != MUON_F32 && g.g_dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.B == 0 || g.M == 0 || g.N == 0) continue;
+    if (!g.W || !g.G || !g.Mom) return MUON_ERR_INVALID_ARGUMENT;
+    if (!aligned(g.W, esize(g.w_dtype)) || !aligned(g.G, esize(g.g_dtype)) || !aligned(g.Mom, 4))
+      return MUON_ERR_INVALID_ARGUMENT;
+    if (g.M > (1LL << 30) || g.N > (1LL << 30) || g.B > (1LL << 30))
+      return MUON_ERR_UNSUPPORTED;
+    const size_t per = static_cast<size_t>(g.M * g.N);
+    const auto w0 = reinterpret_cast<uintptr_t>(g.W);
+    const auto g0 = reinterpret_cast<uintptr_t>(g.G);
+    const auto m0 = reinterpret_cast<uintptr_t>(g.Mom);
+    const uintptr_t wl = g.B * per * esize(g.w_dtype), gl = g.B * per * esize(g.g_dtype),
+                    ml = g.B * per * 4;
+    written.push_back({w0, w0 + wl});
+    written.push_back({m0, m0 + ml});
+    for (auto& x : std::vector<std::pair<uintptr_t, uintptr_t>>{{w0, w0 + wl}, {m0, m0 + ml}})
+      if (g0 < x.second && x.first < g0 + gl) return MUON_ERR_ALIAS;
+    all.push_back({g0, g0 + gl});
+    if (ns.precise && !small_shape(std::min(g.M, g.N))) return MUON_ERR_UNSUPPORTED;
+    const size_t ub = per * (esize(g.w_dtype) + esize(g.g_dtype) + 4);
+    for (int64_t b = 0; b < g.B; ++b) units.push_back({i, ub});
+    total += g.B * ub;
+  }
+  if (ranges_overlap(written)) return MUON_ERR_ALIAS;
+  for (auto& gr : all)
+    for (auto& w : written)
+      if (gr.first < w.second && w.first < gr.second) return MUON_ERR_ALIAS;
+  if (units.empty()) {
+    t_last_launches = 0;
+    return MUON_OK;
+  }
+  // chunks: consecutive matrices, about total / 8 bytes each (at least 8 MB,
+  // at least one matrix); a segment is a run of one group's matrices
+  struct Seg {
+    int g;
+    int64_t b0, cnt;
+  };
+  std::vector<std::vector<Seg>> chunks;
+  // at most 8 chunks, none below 48 MB: each chunk costs its launches (tens of
+  // microseconds on the small-m path), the pipeline's fill and drain cost one
+  // chunk's copy-in and copy-out (measured on 74 x [24, 10240]: 2 chunks
+  // 1.47 ms, 4 chunks 1.33 ms, 8 chunks 1.40 ms, 16 chunks 2.73 ms)
+  const size_t nchunk = std::max<size_t>(env_size("MUON_HOST_CHUNKS", 8), 1);
+  const size_t target = std::max<size_t>(total / nchunk, size_t(48) << 20);
+  {
+    std::vector<Seg> cur;
+    size_t cur_bytes = 0;
+    int64_t next_b = 0;
+    int prev_g = -1;
+    for (const Unit& u : units) {
+      if (u.g != prev_g) next_b = 0;
+      if (!cur.empty() && cur_bytes + u.bytes > target) {
+        chunks.push_back(cur);
+        cur.clear();
+        cur_bytes = 0;
+      }
+      if (!cur.empty() && cur.back().g == u.g && cur.back().b0 + cur.back().cnt == next_b)
+        ++cur.back().cnt;
+      else
+        cur.push_back({u.g, next_b, 1});
+      cur_bytes += u.bytes;
+      ++next_b;
+      prev_g = u.g;
+    }
+    if (!cur.empty()) chunks.push_back(cur);
+  }
+  // slot layout of a chunk: per segment W, G, Mom, each 256-byte aligned
+  auto seg_bytes = [&](const Seg& sg, size_t* ow, size_t* og, size_t* om, size_t off) {
+    const muon_group_t& g = groups[sg.g];
+    const size_t e = static_cast<size_t>(sg.cnt * g.M * g.N);
+    *ow = off;
+    *og = align_up(*ow + e * esize(g.w_dtype), 256);
+    *om = align_up(*og + e * esize(g.g_dtype), 256);
+    return align_up(*om + e * 4, 256);
+  };
+  size_t slot_need = 256;
+  for (auto& ch : chunks) {
+    size_t off = 0, a, b, c;
+    for (auto& sg : ch) off = seg_bytes(sg, &a, &b, &c, off);
+    slot_need = std::max(slot_need, off);
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  HostPipe* hp = nullptr;
+  st = host_pipe(stream, slot_need, &hp);
+  if (st != MUON_OK) return st;
+  if (cudaEventRecord(hp->ev_start, stream) != cudaSuccess) return MUON_ERR_CUDA;
+  for (cudaStream_t x : {hp->s_in, hp->s_comp, hp->s_out})
+    if (cudaStreamWaitEvent(x, hp->ev_start, 0) != cudaSuccess) return MUON_ERR_CUDA;
+  int launches = 0;
+  for (size_t ci = 0; ci < chunks.size(); ++ci) {
+    const int k = static_cast<int>(ci % kHostSlots);
+    char* base = static_cast<char*>(hp->slot) + k * hp->slot_bytes;
+    if (ci >= static_cast<size_t>(kHostSlots) &&
+        cudaStreamWaitEvent(hp->s_in, hp->ev_free[k], 0) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    std::vector<Req> reqs;
+    size_t off = 0;
+    for (const Seg& sg : chunks[ci]) {
+      const muon_group_t& g = groups[sg.g];
+      size_t ow, og, om;
+      off = seg_bytes(sg, &ow, &og, &om, off);
+      const size_t per = static_cast<size_t>(g.M * g.N);
+      const size_t e = sg.cnt * per;
+      const size_t h0 = static_cast<size_t>(sg.b0) * per;
+      if (cudaMemcpyAsync(base + ow, static_cast<const char*>(g.W) + h0 * esize(g.w_dtype),
+                          e * esize(g.w_dtype), cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+          cudaMemcpyAsync(base + og, static_cast<const char*>(g.G) + h0 * esize(g.g_dtype),
+                          e * esize(g.g_dtype), cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+          cudaMemcpyAsync(base + om, g.Mom + h0, e * 4, cudaMemcpyHostToDevice, hp->s_in) !=
+              cudaSuccess)
+        return MUON_ERR_CUDA;
+      Req q;
+      q.W = base + ow;
+      q.w_dtype = g.w_dtype;
+      q.G = base + og;
+      q.g_dtype = g.g_dtype;
+      q.Mom = reinterpret_cast<float*>(base + om);
+      q.B = sg.cnt;
+      q.r = g.M;
+      q.c = g.N;
+      q.trans = g.M > g.N;
+      q.m = std::min(g.M, g.N);
+      q.n = std::max(g.M, g.N);
+      reqs.push_back(q);
+    }
+    if (cudaEventRecord(hp->ev_in[k], hp->s_in) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->s_comp, hp->ev_in[k], 0) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    st = run(reqs, true, mu, nesterov, lr, wd, scale_rule, ns, hp->s_comp);
+    if (st != MUON_OK) return st;
+    launches += t_last_launches;
+    if (cudaEventRecord(hp->ev_comp[k], hp->s_comp) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->s_out, hp->ev_comp[k], 0) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    off = 0;
+    for (const Seg& sg : chunks[ci]) {
+      const muon_group_t& g = groups[sg.g];
+      size_t ow, og, om;
+      off = seg_bytes(sg, &ow, &og, &om, off);
+      const size_t per = static_cast<size_t>(g.M * g.N);
+      const size_t e = sg.cnt * per;
+      const size_t h0 = static_cast<size_t>(sg.b0) * per;
+      if (cudaMemcpyAsync(static_cast<char*>(g.W) + h0 * esize(g.w_dtype), base + ow,
+                          e * esize(g.w_dtype), cudaMemcpyDeviceToHost, hp->s_out) != cudaSuccess ||
+          cudaMemcpyAsync(g.Mom + h0, base + om, e * 4, cudaMemcpyDeviceToHost, hp->s_out) !=
+              cudaSuccess)
+        return MUON_ERR_CUDA;
+    }
+    if (cudaEventRecord(hp->ev_free[k], hp->s_out) != cudaSuccess) return MUON_ERR_CUDA;
+  }
+  // the copy-out stream ran last for every chunk; the caller's stream waits for it
+  const int last = static_cast<int>((chunks.size() - 1) % kHostSlots);
+  if (cudaStreamWaitEvent(stream, hp->ev_free[last], 0) != cudaSuccess) return MUON_ERR_CUDA;
+  t_last_launches = launches;
+  return MUON_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -933,6 +1165,16 @@ muon_status_t muon_step_grouped_ex(const muon_group_t* groups, int n_groups, flo
   }
 }
 
+muon_status_t muon_step_grouped_host(const muon_group_t* groups, int n_groups, float mu,
+                                     int nesterov, float lr, float wd, int scale_rule,
+                                     const muon_ns_config_t* ns, cudaStream_t stream) {
+  try {
+    return host_step_impl(groups, n_groups, mu, nesterov, lr, wd, scale_rule, ns, stream);
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
 muon_status_t muon_query_status(cudaStream_t stream) {
   try {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -983,6 +1225,21 @@ void muon_release_workspace(void) {
       }
     }
     g_ws.clear();
+    for (auto& kv : g_host) {
+      HostPipe& h = kv.second;
+      cudaSetDevice(kv.first.first);
+      for (cudaStream_t st : {h.s_in, h.s_comp, h.s_out})
+        if (st) {
+          cudaStreamSynchronize(st);
+          cudaStreamDestroy(st);
+        }
+      if (h.ev_start) cudaEventDestroy(h.ev_start);
+      for (int i = 0; i < kHostSlots; ++i)
+        for (cudaEvent_t e : {h.ev_in[i], h.ev_comp[i], h.ev_free[i]})
+          if (e) cudaEventDestroy(e);
+      if (h.slot) cudaFree(h.slot);
+    }
+    g_host.clear();
     cudaSetDevice(cur);
   } catch (...) {
   }

@@ -118,3 +118,20 @@ def test_ns_argument_errors(lib):
     assert lib.muon_ns_batched_ex(0x1000, 3, 1, 3, 4, None, None, None) == E_INV
     # out overlapping X
     assert lib.muon_ns_batched_ex(0x1000, 0, 1, 3, 4, None, 0x1008, None) == E_ALIAS
+
+
+def test_host_step_argument_errors(lib):
+    def host(groups, **kw):
+        arr = (binding.Group * max(1, len(groups)))(*groups)
+        cfg = kw.get("cfg")
+        return lib.muon_step_grouped_host(arr, len(groups), 0.95, 1, kw.get("lr", 0.02), 0.01,
+                                          kw.get("rule", 0),
+                                          ctypes.byref(cfg) if cfg is not None else None, None)
+    assert lib.muon_step_grouped_host(None, 1, 0.95, 1, 0.02, 0.01, 0, None, None) == E_INV
+    assert host([_grp(W=0)]) == E_INV
+    assert host([_grp(wdt=3)]) == E_INV
+    assert host([_grp()], rule=7) == E_INV
+    assert host([_grp()], lr=float("nan")) == E_INV
+    assert host([_grp(W=0x1000, M_=0x1040)]) == E_ALIAS
+    assert host([_grp(M=128, N=256)], cfg=binding.make_config(precision=1)) == E_UNS
+    assert host([_grp(B=0, W=0, G=0, M_=0)]) == 0
