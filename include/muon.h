@@ -74,11 +74,13 @@ typedef enum muon_scale_rule_t {
 typedef enum muon_ns_precision_t {
   MUON_NS_BF16 = 0, /* bf16 operands, fp32 accumulation, bf16 iterates ([HP] 6.6) */
   MUON_NS_TF32 = 1  /* high-precision NS (tolerance 1e-3, tighter than TF32 needs):
-                     * X0 carried as two bf16 operands hi + lo, the iteration in
-                     * fp32 Gram space (DMuon-2 C.3); measured error ~1e-5.
-                     * Core shapes with min(rows, cols) <= 64 only; any other
-                     * shape in the call returns MUON_ERR_UNSUPPORTED and
-                     * nothing is enqueued. */
+                     * every bf16 operand becomes a pair hi + lo (about 16
+                     * significant bits).  Small core shapes (min(rows, cols)
+                     * <= 64): X0 as hi + lo, the iteration in fp32 Gram space
+                     * (DMuon-2 C.3).  Larger ones: each product runs over the
+                     * three K segments hi*hi, hi*lo, lo*hi (three times the
+                     * tensor work) and every intermediate is stored as
+                     * hi + lo.  Measured NS error ~1e-5. */
 } muon_ns_precision_t;
 
 /* Newton-Schulz configuration ([HP] 2.3: steps, coefficients, epsilon are

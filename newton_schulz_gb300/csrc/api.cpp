@@ -130,6 +130,7 @@ struct NsGroupP {
   int ksplit = 1, kb_per_split = 1, num_kb_gram = 1;
   int64_t tri = 1, prep_tiles = 1;
   size_t off_Xt0, off_Xt1, off_A, off_B, off_inv, off_ssq, off_part;
+  size_t off_lo = 0;           // high-precision mode: Xt0, Xt1, A, B lo halves from here
   size_t ctr_prep, ctr_tile;   // element offsets in the counter buffer
 };
 
@@ -140,7 +141,7 @@ struct ChunkP {
   size_t ctrs = 0;             // counters used (elements)
 };
 
-void layout_chunk(ChunkP& ch, int sms) {
+void layout_chunk(ChunkP& ch, int sms, bool precise) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -178,6 +179,12 @@ void layout_chunk(ChunkP& ch, int sms) {
     g.off_ssq = take(static_cast<size_t>(g.cnt * g.prep_tiles) * 4);
     g.off_part = take(g.ksplit > 1 ? static_cast<size_t>(g.cnt * g.tri * g.ksplit) * bm * bn * 4
                                    : 16);
+    if (precise) {   // lo halves, laid out like the hi ones: Xt0, Xt1, A, B
+      g.off_lo = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
+      take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
+      take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+      take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+    }
     g.ctr_prep = ctr;
     ctr += static_cast<size_t>(g.cnt);
     g.ctr_tile = ctr;
@@ -257,7 +264,7 @@ size_t small_ws_bytes(const SmallParams& sp) {
          static_cast<size_t>(sp.total_mats) * sp.qbytes;
 }
 
-std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms) {
+std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms, bool precise) {
   const int64_t cap = static_cast<int64_t>(env_size("MUON_WS_CAP", size_t(1) << 29));
   std::vector<int> order;
   for (int i = 0; i < static_cast<int>(reqs.size()); ++i)
@@ -315,7 +322,7 @@ std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms) {
     }
   }
   close();
-  for (auto& ch : chunks) layout_chunk(ch, sms);
+  for (auto& ch : chunks) layout_chunk(ch, sms, precise);
   return chunks;
 }
 
@@ -497,11 +504,6 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // NS-only: reqs[i].G is the input, reqs[i].W the output (dtype w_dtype).
 muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int nesterov, float lr,
                   float wd, int scale_rule, const NsCfg& ns, cudaStream_t stream) {
-  // the high-precision NS mode exists on the small-m path only: refuse the
-  // call before anything is planned or enqueued
-  if (ns.precise)
-    for (const Req& q : reqs)
-      if (q.B > 0 && q.m > 0 && !small_shape(q.m)) return MUON_ERR_UNSUPPORTED;
   DevState* dev = nullptr;
   muon_status_t st = dev_state(&dev);
   if (st != MUON_OK) return st;
@@ -589,7 +591,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       }
     }
   }
-  std::vector<ChunkP> plan = make_plan(large, dev->sms);
+  std::vector<ChunkP> plan = make_plan(large, dev->sms, ns.precise);
   size_t need = 0, need_ctr = 0, max_mats = 0;
   for (const SmallParams& sp : smalls) {
     need = std::max(need, small_ws_bytes(sp));
@@ -649,6 +651,11 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         auto* Xt = reinterpret_cast<__nv_bfloat16*>(ws + g.off_Xt0) + s.idx0 * g.n * g.m_pad;
         ps.direct = q.trans ? Xt : nullptr;
         ps.transp = q.trans ? nullptr : Xt;
+        if (ns.precise) {
+          auto* Xl = reinterpret_cast<__nv_bfloat16*>(ws + g.off_lo) + s.idx0 * g.n * g.m_pad;
+          ps.direct_lo = q.trans ? Xl : nullptr;
+          ps.transp_lo = q.trans ? nullptr : Xl;
+        }
         ps.pitch_d = ps.pitch_t = g.m_pad;
         ps.mstride_d = ps.mstride_t = g.n * g.m_pad;
         ps.ssq_part = reinterpret_cast<float*>(ws + g.off_ssq) + s.idx0 * g.prep_tiles;
@@ -697,6 +704,15 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       d.kb_per_split = g.kb_per_split;
       d.num_kb_gram = g.num_kb_gram;
       d.tri = g.tri;
+      if (ns.precise) {
+        const size_t xb = align_up(static_cast<size_t>(g.cnt * g.n * g.m_pad) * 2, 1024);
+        const size_t ab = align_up(static_cast<size_t>(g.cnt * g.m * g.m_pad) * 2, 1024);
+        char* lo = ws + g.off_lo;
+        d.Xt_lo[0] = reinterpret_cast<__nv_bfloat16*>(lo);
+        d.Xt_lo[1] = reinterpret_cast<__nv_bfloat16*>(lo + xb);
+        d.A_lo = reinterpret_cast<__nv_bfloat16*>(lo + 2 * xb);
+        d.B_lo = reinterpret_cast<__nv_bfloat16*>(lo + 2 * xb + ab);
+      }
       if (!ns_group_maps(d)) return MUON_ERR_CUDA;
     }
     // ---- NS iterations -----------------------------------------------------------
@@ -714,6 +730,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           min_kb = std::min(min_kb, G.kb_per_split);
         }
         gp.deep = gemm_deep(phase, min_kb);
+        gp.prec = ns.precise ? 1 : 0;
         if (const char* d = std::getenv("MUON_GEMM_DEEP")) gp.deep = d[0] == '1';   // tuning override
         if (tiles >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         gp.n_groups = static_cast<int>(ch.groups.size());
@@ -749,6 +766,11 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         // O = Xt in the stored layout when rows > cols, else its transpose
         fs.O = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
                s.idx0 * g.n * g.m_pad;
+        if (ns.precise)
+          fs.O_lo = reinterpret_cast<__nv_bfloat16*>(
+                        ws + g.off_lo +
+                        (fin ? align_up(static_cast<size_t>(g.cnt * g.n * g.m_pad) * 2, 1024) : 0)) +
+                    s.idx0 * g.n * g.m_pad;
         fs.o_trans = q.trans ? 0 : 1;
         fs.pitch_o = g.m_pad;
         fs.mstride_o = g.n * g.m_pad;
@@ -967,7 +989,6 @@ muon_status_t host_step_impl(const muon_group_t* groups, int n_groups, float mu,
     for (auto& x : std::vector<std::pair<uintptr_t, uintptr_t>>{{w0, w0 + wl}, {m0, m0 + ml}})
       if (g0 < x.second && x.first < g0 + gl) return MUON_ERR_ALIAS;
     all.push_back({g0, g0 + gl});
-    if (ns.precise && !small_shape(std::min(g.M, g.N))) return MUON_ERR_UNSUPPORTED;
     const size_t ub = per * (esize(g.w_dtype) + esize(g.g_dtype) + 4);
     for (int64_t b = 0; b < g.B; ++b) units.push_back({i, ub});
     total += g.B * ub;

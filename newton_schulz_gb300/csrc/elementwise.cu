@@ -54,6 +54,14 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* d) {
   return u;
 }
 
+// lo = bf16(d - bf16(d)): the second half of a split bf16 pair
+__device__ __forceinline__ uint4 pack8_bf16_lo(const float* d) {
+  float r[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) r[j] = d[j] - __bfloat162float(__float2bfloat16_rn(d[j]));
+  return pack8_bf16(r);
+}
+
 template <typename Slice>
 __device__ __forceinline__ int find_slice(const Slice* s, int n, int blk) {
   int i = 0;
@@ -139,9 +147,11 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
       for (int j = 0; j < 8; ++j)
         if (j >= nvalid) d[j] = 0.f;
       // [r][c] copy: the padded workspace row always has room for 8 elements.
-      if (s.direct)
-        *reinterpret_cast<uint4*>(s.direct + (int64_t)mat * s.mstride_d + gr * s.pitch_d + gc) =
-            pack8_bf16(d);
+      if (s.direct) {
+        const int64_t o = (int64_t)mat * s.mstride_d + gr * s.pitch_d + gc;
+        *reinterpret_cast<uint4*>(s.direct + o) = pack8_bf16(d);
+        if (s.direct_lo) *reinterpret_cast<uint4*>(s.direct_lo + o) = pack8_bf16_lo(d);
+      }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) sD[lr][lc + j] = d[j];
@@ -158,8 +168,9 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = sD[lrr + j][lcc];
-      *reinterpret_cast<uint4*>(s.transp + (int64_t)mat * s.mstride_t + gcc * s.pitch_t + grr) =
-          pack8_bf16(v);
+      const int64_t o = (int64_t)mat * s.mstride_t + gcc * s.pitch_t + grr;
+      *reinterpret_cast<uint4*>(s.transp + o) = pack8_bf16(v);
+      if (s.transp_lo) *reinterpret_cast<uint4*>(s.transp_lo + o) = pack8_bf16_lo(v);
     }
   }
 
@@ -216,10 +227,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
 // K6
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinParams p) {
-  // o_trans tiles: the O tile [kFinTRows][kFinTCols], transposed from Xt on
-  // the way in; the odd word pitch (66 bf16) keeps both the scattered writes
-  // and the row reads free of bank conflicts
-  __shared__ __align__(16) __nv_bfloat16 sO[kFinTRows][kFinTCols + 2];
+  // o_trans tiles: the O tile [kFinTRows][kFinTCols] (fp32: hi + lo in the
+  // high-precision mode), transposed from Xt on the way in; the odd pitch
+  // (65 words) keeps the scattered writes free of bank conflicts
+  __shared__ __align__(16) float sO[kFinTRows][kFinTCols + 1];
   const int si = find_slice(p.s, p.n_slices, blockIdx.x);
   const FinSlice& s = p.s[si];
   const int local = blockIdx.x - s.tile_base;
@@ -236,38 +247,47 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     {
       const int lc = threadIdx.x >> 2, q = threadIdx.x & 3;
       const int64_t xr = c0 + lc, xc = r0 + 8 * q;
-      uint4 u = make_uint4(0, 0, 0, 0);
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = 0.f;
       if (xr < s.c) {
-        const __nv_bfloat16* src = s.O + (int64_t)mat * s.mstride_o + xr * s.pitch_o + xc;
+        const int64_t o = (int64_t)mat * s.mstride_o + xr * s.pitch_o + xc;
         if (xc + 8 <= s.r) {
-          u = *reinterpret_cast<const uint4*>(src);
+          load8_bf16(s.O + o, f);
+          if (s.O_lo) {
+            float l[8];
+            load8_bf16(s.O_lo + o, l);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] += l[j];
+          }
         } else {
-          __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&u);
           for (int j = 0; j < 8; ++j)
-            if (xc + j < s.r) h[j] = src[j];
+            if (xc + j < s.r) f[j] = bf16_to_f(s.O[o + j]) + (s.O_lo ? bf16_to_f(s.O_lo[o + j]) : 0.f);
         }
       }
-      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sO[8 * q + j][lc] = h[j];
+      for (int j = 0; j < 8; ++j) sO[8 * q + j][lc] = f[j];
     }
     __syncthreads();
     const int lr = threadIdx.x >> 3, lc0 = (threadIdx.x & 7) * 8;
     gr = r0 + lr;
     gc = c0 + lc0;
-    const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(&sO[lr][lc0]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(src[j]);
-      o[2 * j] = f.x;
-      o[2 * j + 1] = f.y;
-    }
+    for (int j = 0; j < 8; ++j) o[j] = sO[lr][lc0 + j];
   } else {
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     gr = (int64_t)ti * kFinRows + ty;
     gc = (int64_t)tj * kFinCols + tx * 8;
-    if (gr < s.r && gc < s.c)
-      load8_bf16(s.O + (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc, o);
+    if (gr < s.r && gc < s.c) {
+      const int64_t oo = (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc;
+      load8_bf16(s.O + oo, o);
+      if (s.O_lo) {
+        float l[8];
+        load8_bf16(s.O_lo + oo, l);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] += l[j];
+      }
+    }
   }
   if (gr >= s.r || gc >= s.c) return;
   const int nvalid = (int)min((int64_t)8, s.c - gc);

@@ -27,6 +27,8 @@ struct PrepSlice {
   float* Mom;             // [count][r][c] fp32 (step mode), else null
   __nv_bfloat16* direct;  // workspace Xt in [r][c] layout (rows > cols), else null
   __nv_bfloat16* transp;  // workspace Xt in [c][r] layout (rows <= cols), else null
+  __nv_bfloat16* direct_lo;   // high-precision mode: lo = bf16(D - hi) beside each, else null
+  __nv_bfloat16* transp_lo;
   float* ssq_part;        // [count][tiles] per-tile partial sum of squares
   float* inv;             // [count] 1/(||D||_F + eps)
   unsigned* cnt;          // [count] arrival counters (left at zero)
@@ -59,6 +61,7 @@ constexpr int kFinTRows = 32, kFinTCols = 64;   // tile when O is read transpose
 struct FinSlice {
   void* W;                     // step: weights [count][r][c]; ns: output
   const __nv_bfloat16* O;      // NS result (workspace Xt): [r][c], or [c][r] when o_trans
+  const __nv_bfloat16* O_lo;   // high-precision mode: its lo half (same layout), else null
   const float* inv;            // [count] extra factor when steps == 0, else null
   int64_t r, c, pitch_o, mstride_o;
   int count;
@@ -86,6 +89,8 @@ struct alignas(128) GemmGroup {
   CUtensorMap mapB;       // operand B: K-major box 64 x 256; gram: as mapA
   CUtensorMap mapC;       // output, box 64 x 128 (TMA store): gram A, poly B, apply Xt_new
   CUtensorMap mapD;       // gram / poly: the output's transposed boxes, box 64 x 64
+  // high-precision mode: the lo halves of mapA, mapB, mapC, mapD
+  CUtensorMap mapAlo, mapBlo, mapClo, mapDlo;
   const float* inv;              // first iteration scale (per matrix) or null
   float* partial;                // gram split-K partials
   unsigned* tile_cnt;            // gram split-K arrival counters
@@ -106,6 +111,7 @@ struct GemmParams {
   float alpha;             // shift: X' = (a - alpha) X + (b A + c A^2 + alpha I) X
   int first;              // 1: operands are unnormalised, apply inv scale
   int deep;               // 1: 4-stage ring, one staging box per epilogue set
+  int prec;               // 1: hi + lo operands, three K segments per product
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -123,6 +129,11 @@ struct NsGroupDev {
   int ksplit = 1, kb_per_split = 1, num_kb_gram = 1;
   int64_t tri = 1;
   CUtensorMap map_gram[2], map_xt[2], map_ap, map_aq, map_a64, map_bp, map_bq, map_b64;
+  // high-precision mode: lo halves of Xt, A and B (null otherwise) and their maps
+  __nv_bfloat16* Xt_lo[2] = {nullptr, nullptr};
+  __nv_bfloat16* A_lo = nullptr;
+  __nv_bfloat16* B_lo = nullptr;
+  CUtensorMap lo_gram[2], lo_xt[2], lo_ap, lo_aq, lo_a64, lo_bp, lo_bq, lo_b64;
 };
 
 // Tiled bf16/f32 tensor map of a [dims[2]][dims[1]][dims[0]] tensor with

@@ -155,7 +155,11 @@ __device__ __forceinline__ void cvt_bf16x32(const uint4 (&u)[4], float* v) {
 
 }  // namespace
 
-template <int EPI, bool DEEP>
+// PREC: the high-precision mode.  Every operand is a pair of bf16 tensors
+// (hi, lo) and each product runs over three K segments, hi*hi, hi*lo and
+// lo*hi, into one fp32 accumulator; the epilogue reads hi + lo and writes the
+// result again as hi = bf16(v), lo = bf16(v - hi).  Shallow layout only.
+template <int EPI, bool DEEP, bool PREC>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -194,6 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       ptx::prefetch_tmap(&p.g[g].mapB);
       ptx::prefetch_tmap(&p.g[g].mapC);
       if (EPI != kEpiApply) ptx::prefetch_tmap(&p.g[g].mapD);
+      if (PREC) {
+        ptx::prefetch_tmap(&p.g[g].mapAlo);
+        ptx::prefetch_tmap(&p.g[g].mapBlo);
+        ptx::prefetch_tmap(&p.g[g].mapClo);
+        if (EPI != kEpiApply) ptx::prefetch_tmap(&p.g[g].mapDlo);
+      }
     }
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
@@ -205,32 +215,36 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------------------
     if (lane == 0) {
+      constexpr int NSEG = PREC ? 3 : 1;   // K segments: (hi, hi), (hi, lo), (lo, hi)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool stop = false;
       for (int tile = blockIdx.x; tile < p.total_tiles && !stop; tile += gridDim.x) {
         const TileInfo t = decode<EPI>(p, tile);
         const GemmGroup& G = p.g[t.gi];
-        for (int i = 0; i < t.nkb; ++i) {
+        for (int i = 0; i < t.nkb * NSEG; ++i) {
           if (!wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, p.timeout_ns, true)) {
             stop = true;
             break;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          const int kx = (t.kb0 + i) * BK;
+          const int seg = PREC ? i / t.nkb : 0;
+          const int kx = (t.kb0 + i - seg * t.nkb) * BK;
+          const CUtensorMap* ma = (PREC && seg == 2) ? &G.mapAlo : &G.mapA;
+          const CUtensorMap* mb = (PREC && seg == 1) ? &G.mapBlo : &G.mapB;
           if (EPI == kEpiGram) {
             // MN-major chunks of Xt: 64 columns (m) x 64 rows (n, the K dim) each
 #pragma unroll
             for (int h = 0; h < BM / 64; ++h)
-              ptx::tma_load_3d(sA + stage * kABytes + h * kChunkBytes, &G.mapA, &full[stage],
+              ptx::tma_load_3d(sA + stage * kABytes + h * kChunkBytes, ma, &full[stage],
                                t.row_tile * BM + 64 * h, kx, t.mat);
 #pragma unroll
             for (int h = 0; h < BN / 64; ++h)
-              ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, &G.mapB, &full[stage],
+              ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
                                t.col_tile * BN + 64 * h, kx, t.mat);
           } else {
-            ptx::tma_load_3d(sA + stage * kABytes, &G.mapA, &full[stage], kx, t.row_tile * BM, t.mat);
-            ptx::tma_load_3d(sB + stage * kBBytes, &G.mapB, &full[stage], kx, t.col_tile * BN, t.mat);
+            ptx::tma_load_3d(sA + stage * kABytes, ma, &full[stage], kx, t.row_tile * BM, t.mat);
+            ptx::tma_load_3d(sB + stage * kBBytes, mb, &full[stage], kx, t.col_tile * BN, t.mat);
           }
           ++issued;
           if (++stage == kStages) {
@@ -264,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem + buf * BN;
-        for (int i = 0; i < t.nkb; ++i) {
+        for (int i = 0; i < t.nkb * (PREC ? 3 : 1); ++i) {
           if (!wait_bounded(&full[stage], phase, abort_flag, p.status, p.timeout_ns, true)) {
             stop = true;
             break;
@@ -316,12 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       if (EPI == kEpiApply && leader && !xpend && !*abort_flag) {
         xpend = true;
         ptx::bulk_wait_read<0>();
-        constexpr int nh = DEEP ? 1 : 2;    // halves staged now
-        ptx::mbar_arrive_expect_tx(&xfull[set], nh * kBoxBytes);
+        if (PREC) {
+          // the first half's hi and lo boxes
+          ptx::mbar_arrive_expect_tx(&xfull[set], 2 * kBoxBytes);
+          ptx::tma_load_3d(stg, &G.mapA, &xfull[set], col0 + cbase, row0, t.mat);
+          ptx::tma_load_3d(stg + kBoxBytes, &G.mapAlo, &xfull[set], col0 + cbase, row0, t.mat);
+        } else {
+          constexpr int nh = DEEP ? 1 : 2;    // halves staged now
+          ptx::mbar_arrive_expect_tx(&xfull[set], nh * kBoxBytes);
 #pragma unroll
-        for (int h = 0; h < nh; ++h)
-          ptx::tma_load_3d(stg + h * kBoxBytes, &G.mapA, &xfull[set], col0 + cbase + 64 * h, row0,
-                           t.mat);
+          for (int h = 0; h < nh; ++h)
+            ptx::tma_load_3d(stg + h * kBoxBytes, &G.mapA, &xfull[set], col0 + cbase + 64 * h,
+                             row0, t.mat);
+        }
       }
       wait_bounded(&tfull[buf], (acc >> 1) & 1, abort_flag, p.status, p.timeout_ns, false);
       // One decision for all epilogue warps (they share named barriers): one
@@ -338,7 +359,69 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         ptx::mbar_arrive(&tempty[buf]);
         break;
       }
-      if (EPI == kEpiApply) {
+      if (EPI == kEpiApply && PREC) {
+        const float s = p.first ? G.inv[t.mat] : 1.f;
+        for (int h = 0; h < 2; ++h) {
+          // box 0: hi, box 1: lo of this half (64 columns)
+          if (h == 1 && leader && !xpend && !*abort_flag) {
+            xpend = true;
+            ptx::bulk_wait_read<0>();
+            ptx::mbar_arrive_expect_tx(&xfull[set], 2 * kBoxBytes);
+            ptx::tma_load_3d(stg, &G.mapA, &xfull[set], col0 + cbase + 64, row0, t.mat);
+            ptx::tma_load_3d(stg + kBoxBytes, &G.mapAlo, &xfull[set], col0 + cbase + 64, row0, t.mat);
+          }
+          const bool xok = wait_bounded(&xfull[set], xphase, abort_flag, p.status, p.timeout_ns, false);
+          if (xok) {
+            xphase ^= 1u;
+            xpend = false;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c0 = cbase + 64 * h + 32 * cc;
+              uint32_t r[32];
+              ptx::tmem_ld_32x32b_x32(taddr + c0, r);
+              ptx::tmem_ld_wait();
+              uint32_t off[4];
+              uint4 xh[4], xl[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                off[q] = ptx::sw128_offset(row, (cc * 4 + q) * 16);
+                xh[q] = *reinterpret_cast<const uint4*>(stg + off[q]);
+                xl[q] = *reinterpret_cast<const uint4*>(stg + kBoxBytes + off[q]);
+              }
+              float x[32], xlo[32];
+              cvt_bf16x32(xh, x);
+              cvt_bf16x32(xl, xlo);
+              __align__(16) __nv_bfloat16 hv[32], lv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float v = s * fmaf(p.a, x[j] + xlo[j], __uint_as_float(r[j]));
+                hv[j] = __float2bfloat16_rn(v);
+                lv[j] = __float2bfloat16_rn(v - __bfloat162float(hv[j]));
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                *reinterpret_cast<uint4*>(stg + off[q]) = *reinterpret_cast<const uint4*>(hv + 8 * q);
+                *reinterpret_cast<uint4*>(stg + kBoxBytes + off[q]) =
+                    *reinterpret_cast<const uint4*>(lv + 8 * q);
+              }
+            }
+          }
+          if (h == 1) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[buf]);
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::named_bar(2 + set, 128);
+          if (leader && xok) {
+            const int x = col0 + cbase + 64 * h;
+            if (x < G.m && row0 < G.n) {
+              ptx::tma_store_3d(&G.mapC, stg, x, row0, t.mat);
+              ptx::tma_store_3d(&G.mapClo, stg + kBoxBytes, x, row0, t.mat);
+            }
+            ptx::bulk_commit();
+          }
+        }
+      } else if (EPI == kEpiApply) {
         const float s = p.first ? G.inv[t.mat] : 1.f;
         for (int h = 0; h < 2; ++h) {
           uint8_t* box = stg + (DEEP ? 0 : h * kBoxBytes);
@@ -442,8 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         // element of the m x m result is written exactly once.
         const float scale = (EPI == kEpiGram && p.first) ? G.inv[t.mat] * G.inv[t.mat] : 1.f;
         const bool mirror = row0 + BM <= col0;
-        uint8_t* sd = stg;                                // direct box: 128 rows x 64 columns
-        uint8_t* sm = stg + (DEEP ? 0 : kBoxBytes);      // transposed boxes: 2 x (64 x 64)
+        // direct box: 128 rows x 64 columns (PREC: hi in sd, lo in sdl); the
+        // transposed boxes 2 x (64 x 64) share the direct boxes' space when
+        // the set has one box (DEEP) or needs both for hi and lo (PREC)
+        constexpr bool kAliasMirror = DEEP || PREC;
+        uint8_t* sd = stg;
+        uint8_t* sdl = stg + kBoxBytes;
+        uint8_t* sm = stg + (kAliasMirror ? 0 : kBoxBytes);
         for (int h = 0; h < 2; ++h) {
           const int c_h = cbase + 64 * h;   // accumulator column of this half
           const int gc_h = col0 + c_h;
@@ -452,8 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             ptx::bulk_wait_read<0>();       // the previous stores have read the boxes
             if (EPI == kEpiPoly && !xpend && !*abort_flag) {
               xpend = true;
-              ptx::mbar_arrive_expect_tx(&xfull[set], kBoxBytes);
+              ptx::mbar_arrive_expect_tx(&xfull[set], (PREC ? 2 : 1) * kBoxBytes);
               ptx::tma_load_3d(sd, &G.mapA, &xfull[set], gc_h, row0, t.mat);   // A tile
+              if (PREC) ptx::tma_load_3d(sdl, &G.mapAlo, &xfull[set], gc_h, row0, t.mat);
             }
           }
           ptx::named_bar(2 + set, 128);
@@ -466,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             }
           }
           uint4 keep[2][4];   // this row's 64 results (bf16), for the transposed copy
+          uint4 keepl[PREC ? 2 : 1][4];   // PREC: their lo parts
           if (xok) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -502,6 +592,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                 for (int q = 0; q < 4; ++q) av4[q] = *reinterpret_cast<const uint4*>(sd + off[q]);
                 float av[32];
                 cvt_bf16x32(av4, av);
+                if (PREC) {
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) av4[q] = *reinterpret_cast<const uint4*>(sdl + off[q]);
+                  float al[32];
+                  cvt_bf16x32(av4, al);
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) av[j] += al[j];
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                   v[j] = fmaf(p.b, av[j], p.c * v[j]) + (gr == gc0 + j ? p.alpha : 0.f);
@@ -517,17 +615,28 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                 keep[cc][q] = *reinterpret_cast<const uint4*>(hv + 8 * q);
                 *reinterpret_cast<uint4*>(sd + off[q]) = keep[cc][q];
               }
+              if constexpr (PREC) {
+                __align__(16) __nv_bfloat16 lv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) lv[j] = __float2bfloat16_rn(v[j] - __bfloat162float(hv[j]));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  keepl[cc][q] = *reinterpret_cast<const uint4*>(lv + 8 * q);
+                  *reinterpret_cast<uint4*>(sdl + off[q]) = keepl[cc][q];
+                }
+              }
             }
           }
           ptx::fence_proxy_async_smem();
           ptx::named_bar(2 + set, 128);
           if (leader && xok) {
             ptx::tma_store_3d(&G.mapC, sd, gc_h, row0, t.mat);
+            if (PREC) ptx::tma_store_3d(&G.mapClo, sdl, gc_h, row0, t.mat);
             ptx::bulk_commit();
           }
           if (mirror) {
-            if (DEEP) {
-              // one box per set: the direct store must have read it first
+            if (kAliasMirror) {
+              // the direct stores must have read the boxes first
               if (leader) ptx::bulk_wait_read<0>();
               ptx::named_bar(2 + set, 128);
             }
@@ -541,6 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                   *reinterpret_cast<__nv_bfloat16*>(tbox + ptx::sw128_offset(cc * 32 + j, tb)) = hv[j];
+                if constexpr (PREC) {
+                  const __nv_bfloat16* lv = reinterpret_cast<const __nv_bfloat16*>(keepl[cc]);
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    *reinterpret_cast<__nv_bfloat16*>(tbox + kBoxBytes + ptx::sw128_offset(cc * 32 + j, tb)) =
+                        lv[j];
+                }
               }
             }
             ptx::fence_proxy_async_smem();
@@ -548,8 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             if (leader && xok) {
 #pragma unroll
               for (int b = 0; b < 2; ++b)
-                if (row0 + 64 * b < G.m)
+                if (row0 + 64 * b < G.m) {
                   ptx::tma_store_3d(&G.mapD, sm + b * (kBoxBytes / 2), row0 + 64 * b, gc_h, t.mat);
+                  if (PREC)
+                    ptx::tma_store_3d(&G.mapDlo, sm + kBoxBytes + b * (kBoxBytes / 2), row0 + 64 * b,
+                                      gc_h, t.mat);
+                }
               ptx::bulk_commit();
             }
           }
@@ -588,13 +708,13 @@ int gemm_sym_tiles(int m) {
   return t;
 }
 
-template <int EPI, bool DEEP>
+template <int EPI, bool DEEP, bool PREC>
 static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<EPI, DEEP>,
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<EPI, DEEP, PREC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Layout<DEEP>::smem);
   if (e != cudaSuccess) return e;
-  ns_gemm_kernel<EPI, DEEP><<<grid, kThreads, Layout<DEEP>::smem, s>>>(p);
+  ns_gemm_kernel<EPI, DEEP, PREC><<<grid, kThreads, Layout<DEEP>::smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -609,13 +729,21 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s) {
   }
   const int grid = p.total_tiles < sms ? p.total_tiles : sms;
   const bool deep = p.deep != 0;
+  if (p.prec) {   // the high-precision mode runs on the shallow layout
+    switch (epi) {
+      case kEpiGram: return launch_one<kEpiGram, false, true>(p, grid, s);
+      case kEpiPoly: return launch_one<kEpiPoly, false, true>(p, grid, s);
+      case kEpiApply: return launch_one<kEpiApply, false, true>(p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (epi) {
-    case kEpiGram: return deep ? launch_one<kEpiGram, true>(p, grid, s)
-                               : launch_one<kEpiGram, false>(p, grid, s);
-    case kEpiPoly: return deep ? launch_one<kEpiPoly, true>(p, grid, s)
-                               : launch_one<kEpiPoly, false>(p, grid, s);
-    case kEpiApply: return deep ? launch_one<kEpiApply, true>(p, grid, s)
-                                : launch_one<kEpiApply, false>(p, grid, s);
+    case kEpiGram: return deep ? launch_one<kEpiGram, true, false>(p, grid, s)
+                               : launch_one<kEpiGram, false, false>(p, grid, s);
+    case kEpiPoly: return deep ? launch_one<kEpiPoly, true, false>(p, grid, s)
+                               : launch_one<kEpiPoly, false, false>(p, grid, s);
+    case kEpiApply: return deep ? launch_one<kEpiApply, true, false>(p, grid, s)
+                                : launch_one<kEpiApply, false, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

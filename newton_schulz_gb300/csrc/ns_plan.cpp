@@ -78,6 +78,18 @@ bool ns_group_maps(NsGroupDev& g) {
        make_ns_map(&g.map_bp, g.B, g.m, g.m, g.cnt, g.m_pad, as, bm) &&
        make_ns_map(&g.map_bq, g.B, g.m, g.m, g.cnt, g.m_pad, as, bn) &&
        make_ns_map(&g.map_b64, g.B, g.m, g.m, g.cnt, g.m_pad, as, 64);
+  if (g.A_lo) {   // the same boxes on the lo halves
+    for (int b = 0; b < 2; ++b) {
+      ok = ok && make_ns_map(&g.lo_gram[b], g.Xt_lo[b], g.m, g.n, g.cnt, g.m_pad, xs, 64);
+      ok = ok && make_ns_map(&g.lo_xt[b], g.Xt_lo[b], g.m, g.n, g.cnt, g.m_pad, xs, bm);
+    }
+    ok = ok && make_ns_map(&g.lo_ap, g.A_lo, g.m, g.m, g.cnt, g.m_pad, as, bm) &&
+         make_ns_map(&g.lo_aq, g.A_lo, g.m, g.m, g.cnt, g.m_pad, as, bn) &&
+         make_ns_map(&g.lo_a64, g.A_lo, g.m, g.m, g.cnt, g.m_pad, as, 64) &&
+         make_ns_map(&g.lo_bp, g.B_lo, g.m, g.m, g.cnt, g.m_pad, as, bm) &&
+         make_ns_map(&g.lo_bq, g.B_lo, g.m, g.m, g.cnt, g.m_pad, as, bn) &&
+         make_ns_map(&g.lo_b64, g.B_lo, g.m, g.m, g.cnt, g.m_pad, as, 64);
+  }
   return ok;
 }
 
@@ -93,6 +105,11 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.mapB = g.map_gram[it & 1];
     G.mapC = g.map_ap;
     G.mapD = g.map_a64;
+    if (g.A_lo) {
+      G.mapAlo = G.mapBlo = g.lo_gram[it & 1];
+      G.mapClo = g.lo_ap;
+      G.mapDlo = g.lo_a64;
+    }
     G.partial = g.partial;
     G.tile_cnt = g.tile_cnt;
     G.nt = static_cast<int>(cdiv64(g.m, bn));
@@ -106,6 +123,12 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.mapB = g.map_aq;
     G.mapC = g.map_bp;
     G.mapD = g.map_b64;
+    if (g.A_lo) {
+      G.mapAlo = g.lo_ap;
+      G.mapBlo = g.lo_aq;
+      G.mapClo = g.lo_bp;
+      G.mapDlo = g.lo_b64;
+    }
     G.nt = static_cast<int>(cdiv64(g.m, bn));
     G.mt = static_cast<int>(cdiv64(g.m, bm));
     G.ksplit = 1;
@@ -116,6 +139,11 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.mapA = g.map_xt[it & 1];
     G.mapB = g.map_bq;
     G.mapC = g.map_xt[(it + 1) & 1];
+    if (g.A_lo) {
+      G.mapAlo = g.lo_xt[it & 1];
+      G.mapBlo = g.lo_bq;
+      G.mapClo = g.lo_xt[(it + 1) & 1];
+    }
     G.nt = static_cast<int>(cdiv64(g.m, bn));
     G.mt = static_cast<int>(cdiv64(g.n, bm));
     G.ksplit = 1;

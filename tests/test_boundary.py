@@ -93,10 +93,6 @@ def test_ns_config_errors(lib):
     assert _step(lib, [_grp()], cfg=binding.make_config(steps=-1)) == E_INV
     assert _step(lib, [_grp()], cfg=binding.make_config(steps=65)) == E_INV
     assert _step(lib, [_grp()], cfg=binding.make_config(eps=-1.0)) == E_INV
-    # the high-precision mode covers core shapes with min(M, N) <= 64 only
-    assert _step(lib, [_grp(M=128, N=256)], cfg=binding.make_config(precision=1)) == E_UNS
-    assert _step(lib, [_grp(M=4, N=8), _grp(W=0x300000, G=0x400000, M_=0x500000, M=65, N=65)],
-                 cfg=binding.make_config(precision=1)) == E_UNS
     assert _step(lib, [_grp()], cfg=binding.make_config(precision=5)) == E_INV
     bad = binding.make_config(steps=2, coeffs=[[1, 2, 3], [float("nan"), 0, 0]])
     assert _step(lib, [_grp()], cfg=bad) == E_INV
@@ -133,5 +129,4 @@ def test_host_step_argument_errors(lib):
     assert host([_grp()], rule=7) == E_INV
     assert host([_grp()], lr=float("nan")) == E_INV
     assert host([_grp(W=0x1000, M_=0x1040)]) == E_ALIAS
-    assert host([_grp(M=128, N=256)], cfg=binding.make_config(precision=1)) == E_UNS
     assert host([_grp(B=0, W=0, G=0, M_=0)]) == 0

@@ -184,8 +184,35 @@ def test_precise_step_parity(shape):
         assert err <= HP_TOL, (shape, i, err)
 
 
-def test_precise_rejects_large_core_shapes():
-    x = torch.randn((2, 128, 300), device="cuda")
-    out = torch.empty_like(x)
-    with pytest.raises(binding.MuonError):
-        binding.muon_ns_batched_ex(x, binding.make_config(precision=binding.NS_TF32), out)
+@pytest.mark.parametrize("shape,generic", [((2, 128, 300), False), ((1, 300, 200), False),
+                                           ((2, 200, 333), False), ((3, 24, 2000), True),
+                                           ((1, 520, 700), False)])
+def test_precise_gemm_path_parity(shape, generic):
+    """The high-precision mode on the grouped GEMM path (hi + lo operands,
+    three K segments per product), including a small shape forced there."""
+    if generic:
+        os.environ["MUON_SMALL_PATH"] = "0"
+    x = torch.randn(shape, generator=torch.Generator().manual_seed(sum(shape) + 5))
+    X = x.cuda()
+    out = torch.empty_like(X)
+    binding.muon_ns_batched_ex(X, binding.make_config(precision=binding.NS_TF32), out)
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    ref = R.ns_batched_ref(_np(x))
+    errs = [_rel(_np(out)[i], ref[i]) for i in range(shape[0])]
+    print(shape, "GEMM path max rel err", max(errs))
+    assert max(errs) <= HP_TOL, (shape, errs)
+
+
+def test_precise_gemm_step_parity():
+    g = synth.random_group((2, 300, 520), torch.bfloat16, torch.float32, "cuda", 35, 1e-3, 1e-3)
+    host = {k: _np(g[k]) for k in ("W", "G", "Mom")}
+    binding.muon_step_grouped([g], ns_cfg=binding.make_config(precision=binding.NS_TF32))
+    torch.cuda.synchronize()
+    assert binding.muon_query_status() == 0
+    w2, m2, _ = R.muon_step_ref(host["W"], host["G"], host["Mom"])
+    assert _rel(_np(g["Mom"]), m2) <= MOM_TOL
+    w = _np(g["W"])
+    for i in range(2):
+        err = np.linalg.norm(w[i] - w2[i]) / np.linalg.norm(w2[i] - host["W"][i])
+        assert err <= HP_TOL, (i, err)
