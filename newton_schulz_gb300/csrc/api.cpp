@@ -233,7 +233,7 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   sp->gs_lowmem = (precise && sp->mp == 64) ? 1 : 0;
   const size_t gs =
       align_up(static_cast<size_t>(sp->gs_lowmem ? 3 : 5) * sp->mp * sp->mp * 4 + 64, 16);
-  const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) + gs + 512 + 1024;
+  const size_t fixed = 2 * static_cast<size_t>(sp->qbytes) + gs + (kSmallCons / 32) * 512 + 512 + 1024;
   if (fixed >= static_cast<size_t>(kSmallSmemLimit)) return false;
   const int tcol = static_cast<int>(rup(sp->nmm, 32));
   // TMEM: two Gram accumulators in [0, 2 gcols), one O slot (2 tcol columns) per stage
@@ -252,7 +252,8 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   sp->off_ring = 0;
   sp->off_q = sp->stages * sp->stage_bytes;
   sp->off_gs = sp->off_q + 2 * sp->qbytes;
-  sp->off_bar = static_cast<int>(align_up(sp->off_gs + gs, 16));
+  sp->off_epi = static_cast<int>(align_up(sp->off_gs + gs, 16));
+  sp->off_bar = sp->off_epi + (kSmallCons / 32) * 512;
   sp->smem_bytes = sp->off_bar + 512 + 1024;
   return sp->smem_bytes <= kSmallSmemLimit;
 }

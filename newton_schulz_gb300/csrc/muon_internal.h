@@ -211,7 +211,7 @@ struct SmallParams {
   unsigned long long timeout_ns;
   int cap;                      // matrices per arrive slot
   // shared-memory carve-up (bytes from the 1024-aligned base)
-  int off_q, off_ring, stage_bytes, off_gs, off_bar;
+  int off_q, off_ring, stage_bytes, off_gs, off_epi, off_bar;   // off_epi: 512 B per consumer warp
   int smem_bytes;
 };
 

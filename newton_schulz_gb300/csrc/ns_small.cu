@@ -634,7 +634,7 @@ __device__ __forceinline__ void w_st(WT* p, int64_t i, float v) {
 // instruction instead of one scalar store per element).
 template <typename WT, bool STEP>
 __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, uint32_t oslot,
-                                         int set, int q4, int lane) {
+                                         int set, int q4, int lane, float* scr) {
   const int m = c.m, nmm = c.nmm;
   const float decay = c.decay, stepk = c.stepk;
   WT* ws = reinterpret_cast<WT*>(st);
@@ -660,17 +660,17 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
         v[j] = STEP ? fmaf(decay, w[j], -stepk * o) : o;
       }
       if (vec) {
-        // rows q0..q0+3 x the warp's 32 columns: back into the stage, then lane
-        // l stores row q0 + l / 8, columns 4 (l % 8) .. + 3 of the warp
+        // rows q0..q0+3 x the warp's 32 columns through the warp's scratch
+        // (not the stage, which TMA refills), then lane l stores row
+        // q0 + l / 8, columns 4 (l % 8) .. + 3 of the warp
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (q0 + j < m) reinterpret_cast<float*>(ws)[(q0 + j) * 128 + col] = v[j];
+        for (int j = 0; j < 4; ++j) scr[j * 32 + lane] = v[j];
         __syncwarp();
-        const int rr = q0 + (lane >> 3), cc = 32 * q4 + 4 * (lane & 7);
-        if (rr < m) {
-          const float4 x = *reinterpret_cast<const float4*>(reinterpret_cast<float*>(ws) + rr * 128 + cc);
-          __stcs(reinterpret_cast<float4*>(reinterpret_cast<float*>(wg) + static_cast<int64_t>(rr) * c.n +
-                                           c.col0 + c0 + cc), x);
+        const int rr = lane >> 3, cc = 4 * (lane & 7);
+        if (q0 + rr < m) {
+          const float4 x = *reinterpret_cast<const float4*>(scr + rr * 32 + cc);
+          __stcs(reinterpret_cast<float4*>(reinterpret_cast<float*>(wg) + static_cast<int64_t>(q0 + rr) * c.n +
+                                           c.col0 + c0 + 32 * q4 + cc), x);
         }
         __syncwarp();
       } else if (gj < c.n) {
@@ -703,13 +703,13 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
 }
 
 __device__ void epi_tile_any(const ItemCfg& c, int c0, uint8_t* st, uint32_t oslot, int set,
-                             int q4, int lane) {
+                             int q4, int lane, float* scr) {
   if (c.wdt == 0) {
-    if (c.step) epi_tile<float, true>(c, c0, st, oslot, set, q4, lane);
-    else epi_tile<float, false>(c, c0, st, oslot, set, q4, lane);
+    if (c.step) epi_tile<float, true>(c, c0, st, oslot, set, q4, lane, scr);
+    else epi_tile<float, false>(c, c0, st, oslot, set, q4, lane, scr);
   } else {
-    if (c.step) epi_tile<__nv_bfloat16, true>(c, c0, st, oslot, set, q4, lane);
-    else epi_tile<__nv_bfloat16, false>(c, c0, st, oslot, set, q4, lane);
+    if (c.step) epi_tile<__nv_bfloat16, true>(c, c0, st, oslot, set, q4, lane, scr);
+    else epi_tile<__nv_bfloat16, false>(c, c0, st, oslot, set, q4, lane, scr);
   }
 }
 
@@ -1054,13 +1054,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         cons_sync();
       }
     };
-    auto release = [&]() {   // this warp is done with the current stage
-      ptx::fence_proxy_async_smem();
+    // this warp is done with the current stage; `wrote`: it wrote the stage
+    // (the first phase's X0 tile), which the tensor core then reads through
+    // the async proxy; the second phase only reads it
+    auto release = [&](bool wrote) {
+      if (wrote) ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&B->cons_done[rg.stage]);
       rg.next(NS);
     };
+    float* escr = reinterpret_cast<float*>(sm + p.off_epi) + (warp - 2) * 128;
     int prev = -1, prevk = 0, k = 0;
     // ---- first phase ----
     for (;; ++k) {
@@ -1080,7 +1084,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       if (item < 0) {   // end of the first phase
         mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
-        release();
+        release(false);
         break;
       }
       const ItemCfg ic = item_cfg(p, item);
@@ -1088,7 +1092,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         const bool sok = mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx);
         ok = ok && sok;
         if (ok) consume_p1_dt<PRECISE>(ic, s * p.cw1, ring + rg.stage * p.stage_bytes, t);
-        release();
+        release(true);
       }
       if (prev >= 0) finish(prev, prevk);
       prev = item;
@@ -1113,8 +1117,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       ptx::tc_fence_after();
       if (ok)
         epi_tile_any(ic, B->desc[rg.stage][2], ring + rg.stage * p.stage_bytes,
-                     tmem + obase + oslot_cols * rg.stage, set, q4, lane);
-      release();
+                     tmem + obase + oslot_cols * rg.stage, set, q4, lane, escr);
+      release(false);
     }
   }
   ptx::tc_fence_before();
