@@ -208,8 +208,8 @@ bool small_shape(int64_t m) {
 // A stage holds the data tile(s) of its phase (G + Mom: m x cw1, or W:
 // m x 128, for the widest dtypes in the launch), then an X0 tile of 128
 // columns at x_off and a 2 KB zero gap.  Items are up to 2048 columns (the
-// X0 image of an item streams through the stages), shrinking while the
-// launch would leave SMs without an item.
+// X0 image of an item streams through the stages), shrinking (to no fewer
+// than 1024) while the launch would leave SMs without an item.
 bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, bool step,
                 bool precise, SmallParams* sp) {
   sp->m = static_cast<int>(m);
@@ -243,7 +243,16 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   if (sp->stages < 2) return false;
   int64_t wb = std::min<int64_t>(2048, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);
-  while (wb > 128 && mats * cdiv(n, wb) < 2 * static_cast<int64_t>(sms)) wb -= 128;
+  {
+    // Items shrink (down to 1024 columns) while the launch has fewer items
+    // than SMs.  Each item adds a partial Gram that the matrix's Gram-space
+    // job sums serially, so narrower items cost more than they spread: on
+    // [24, 10240] matrices a 128-column floor with two items per SM took
+    // 208 / 137 / 86 us for 5 / 9 / 19 matrices, this rule 56 / 55 / 58 us.
+    const int64_t minwb = static_cast<int64_t>(env_size("MUON_SMALL_MINWB", 1024));
+    const int64_t per_sm = static_cast<int64_t>(env_size("MUON_SMALL_ITEMS_PER_SM", 1));
+    while (wb > minwb && mats * cdiv(n, wb) < per_sm * static_cast<int64_t>(sms)) wb -= 128;
+  }
   sp->wb = static_cast<int>(wb);
   sp->nb = static_cast<int>(cdiv(n, wb));
   sp->total_mats = static_cast<int>(mats);
@@ -912,7 +921,7 @@ muon_status_t ns_impl(void* X, int dtype, int64_t B, int64_t M, int64_t N,
 
 // ---- host-resident state ------------------------------------------------------------
 // One Muon step over parameters whose W, G and Mom live in host memory.  The
-// matrices are cut into chunks (about 1/8 of the bytes, at least 48 MB); chunk i moves
+// matrices are cut into up to 8 chunks of at least 40 MB; chunk i moves
 // through device slot i % 3: copy-in on one stream, the step on a second,
 // copy-out (W', Mom') on a third, so that the two copy directions and the
 // kernels overlap.  Everything is ordered after the work already on
@@ -1009,29 +1018,40 @@ muon_status_t host_step_impl(const muon_group_t* groups, int n_groups, float mu,
     int64_t b0, cnt;
   };
   std::vector<std::vector<Seg>> chunks;
-  // at most 8 chunks, none below 48 MB: each chunk costs its launches (tens of
-  // microseconds on the small-m path), the pipeline's fill and drain cost one
-  // chunk's copy-in and copy-out (measured on 74 x [24, 10240]: 2 chunks
-  // 1.47 ms, 4 chunks 1.33 ms, 8 chunks 1.40 ms, 16 chunks 2.73 ms)
-  const size_t nchunk = std::max<size_t>(env_size("MUON_HOST_CHUNKS", 8), 1);
-  const size_t target = std::max<size_t>(total / nchunk, size_t(48) << 20);
+  // K chunks, K = total / 40 MB clamped to [1, 8] (MUON_HOST_CHUNKS overrides
+  // the 8): each chunk costs its launches (tens of microseconds on the small-m
+  // path).  The pipeline fills with the first chunk's copy-in and drains with
+  // the last one's copy-out, so those two are half the size of the others
+  // (weights 1, 2, ..., 2, 1).  A chunk closes once the bytes so far reach
+  // its cumulative boundary; every chunk holds at least one matrix.
+  const size_t kmax = std::max<size_t>(env_size("MUON_HOST_CHUNKS", 8), 1);
+  const size_t K = std::min(kmax, std::max<size_t>(total / (size_t(40) << 20), 1));
+  std::vector<double> bound(K);
+  {
+    const double wsum = K == 1 ? 1.0 : static_cast<double>(2 * (K - 1));
+    double acc = 0.0;
+    for (size_t i = 0; i < K; ++i) {
+      acc += (K == 1) ? 1.0 : ((i == 0 || i == K - 1) ? 1.0 : 2.0);
+      bound[i] = acc / wsum * static_cast<double>(total);
+    }
+  }
   {
     std::vector<Seg> cur;
-    size_t cur_bytes = 0;
+    size_t done = 0;
     int64_t next_b = 0;
     int prev_g = -1;
     for (const Unit& u : units) {
       if (u.g != prev_g) next_b = 0;
-      if (!cur.empty() && cur_bytes + u.bytes > target) {
+      if (!cur.empty() && chunks.size() + 1 < K &&
+          static_cast<double>(done) >= bound[chunks.size()] - 0.5 * u.bytes) {
         chunks.push_back(cur);
         cur.clear();
-        cur_bytes = 0;
       }
       if (!cur.empty() && cur.back().g == u.g && cur.back().b0 + cur.back().cnt == next_b)
         ++cur.back().cnt;
       else
         cur.push_back({u.g, next_b, 1});
-      cur_bytes += u.bytes;
+      done += u.bytes;
       ++next_b;
       prev_g = u.g;
     }
