@@ -208,8 +208,8 @@ bool small_shape(int64_t m) {
 // A stage holds the data tile(s) of its phase (G + Mom: m x cw1, or W:
 // m x 128, for the widest dtypes in the launch), then an X0 tile of 128
 // columns at x_off and a 2 KB zero gap.  Items are up to 2048 columns (the
-// X0 image of an item streams through the stages), shrinking (to no fewer
-// than 1024) while the launch would leave SMs without an item.
+// X0 image of an item streams through the stages), shrinking while the
+// launch would leave SMs without an item and a matrix keeps at most 10.
 bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, bool step,
                 bool precise, SmallParams* sp) {
   sp->m = static_cast<int>(m);
@@ -244,14 +244,16 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   int64_t wb = std::min<int64_t>(2048, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);
   {
-    // Items shrink (down to 1024 columns) while the launch has fewer items
-    // than SMs.  Each item adds a partial Gram that the matrix's Gram-space
-    // job sums serially, so narrower items cost more than they spread: on
-    // [24, 10240] matrices a 128-column floor with two items per SM took
-    // 208 / 137 / 86 us for 5 / 9 / 19 matrices, this rule 56 / 55 / 58 us.
-    const int64_t minwb = static_cast<int64_t>(env_size("MUON_SMALL_MINWB", 1024));
-    const int64_t per_sm = static_cast<int64_t>(env_size("MUON_SMALL_ITEMS_PER_SM", 1));
-    while (wb > minwb && mats * cdiv(n, wb) < per_sm * static_cast<int64_t>(sms)) wb -= 128;
+    // Items shrink while the launch has fewer items than SMs, as long as a
+    // matrix keeps at most 10 of them: each item adds a partial Gram that the
+    // matrix's Gram-space job sums serially.  On [24, 10240] matrices,
+    // 128-column items with two per SM took 208 / 137 / 86 us for 5 / 9 / 19
+    // matrices, this rule 57 / 58 / 60 us; small n still splits (4 x [64, 256]
+    // runs on 128-column items).
+    const int64_t max_nb = static_cast<int64_t>(env_size("MUON_SMALL_MAX_ITEMS", 10));
+    while (wb > 128 && mats * cdiv(n, wb) < static_cast<int64_t>(sms) &&
+           cdiv(n, wb - 128) <= max_nb)
+      wb -= 128;
   }
   sp->wb = static_cast<int>(wb);
   sp->nb = static_cast<int>(cdiv(n, wb));
