@@ -627,9 +627,9 @@ __device__ __forceinline__ void w_st(WT* p, int64_t i, float v) {
 
 // 128-column tile at item column c0: O = D[:, q] + D[:, nmm + q] (X0 Q_hi^T +
 // X0 Q_lo^T) from the TMEM slot, W' = decay W - stepk O (W from the stage) or
-// O, to global memory.  Warp (set, q4) owns lanes 32 q4.. (the columns) and
-// the 4-row blocks of O with index = set (mod sets), so all sets carry the
-// same number of rows.  Row-major tiles are written back into the stage first and
+// O, to global memory.  The tile belongs to one set of four warps (the sets
+// take alternate stages); warp q4 of the set owns lanes 32 q4.. (the
+// columns) and every row.  Row-major tiles are written back into the stage first and
 // leave as 4-column vectors (one 128-bit store per lane and 4 rows per warp
 // instruction instead of one scalar store per element).
 template <typename WT, bool STEP>
@@ -645,7 +645,7 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
   if (!c.trans) {
     const int64_t gjw = c.col0 + c0 + 32 * q4;    // first global column of this warp
     const bool vec = c.wvec && sizeof(WT) == 4 && gjw + 32 <= c.n;
-    for (int q0 = 4 * set; q0 < m; q0 += 4 * kSets) {
+    for (int q0 = 0; q0 < m; q0 += 4) {
       uint32_t rh[4], rl[4];
       ptx::tmem_ld_32x32b_x4(oslot + q0 + lq, rh);
       ptx::tmem_ld_32x32b_x4(oslot + nmm + q0 + lq, rl);
@@ -682,7 +682,7 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
   } else {
     const bool live = gj < c.n;
     WT* wrow = wg + gj * m;
-    for (int cq = 16 * set; cq < nmm; cq += 16 * kSets) {
+    for (int cq = 0; cq < nmm; cq += 16) {
       uint32_t rh[16], rl[16];
       ptx::tmem_ld_32x32b_x16(oslot + cq + lq, rh);
       ptx::tmem_ld_32x32b_x16(oslot + nmm + cq + lq, rl);
@@ -1100,13 +1100,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
     if (prev >= 0) finish(prev, prevk);
     // ---- second phase: every stage until the end token ----
+    // The two sets of four warps take alternate stages, so each tile's fixed
+    // costs (waits, fences, the stage hand-back) are paid by half of the
+    // warps while the other half works on the next tile; the other set hands
+    // the stage back at once.
     const int q4 = warp & 3, set = cw >> 2;
     int cur = -1;
     ItemCfg ic{};
-    while (ok) {
+    for (unsigned seq = 0; ok; ++seq) {
       if (!mwait_warp(&B->ring_full[rg.stage], rg.phase, ctx)) break;
       const int kind = B->desc[rg.stage][0];
       if (kind == kStageEnd) break;
+      if (static_cast<int>(seq % kSets) != set) {
+        release(false);
+        continue;
+      }
       const int item = B->desc[rg.stage][1];
       if (item != cur) {
         cur = item;
