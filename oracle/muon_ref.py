@@ -27,7 +27,7 @@ Sources (web pages on the Muon / Newton-Schulz method):
 * DMuon architecture page, section 1: the same quintic written as
   alpha*X + beta*X X^T X + gamma*X (X^T X)^2.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * Nesterov form: D = G + mu*M_t with M_t = mu*M_{t-1} + G (no dampening,
   because the momentum formula prints none).
