@@ -278,6 +278,8 @@ def main():
                     help="skip the host-buffer end-to-end pass (large workloads)")
     ap.add_argument("--layers", type=int, default=None,
                     help="c4 only: number of Llama layers (default 32; a small profiling case)")
+    ap.add_argument("--adamw", action="store_true",
+                    help="time the AdamW kernel on the Llama-3-8B non-matrix parameters instead")
     ap.add_argument("--experts", type=int, default=None,
                     help="c3 only: experts per weight (default 128; a small profiling case)")
     ap.add_argument("--scale-down", type=int, default=1,
@@ -299,6 +301,11 @@ def main():
     import torch
     from newton_schulz_gb300 import binding, synth
 
+    if args.adamw:
+        torch.cuda.set_device(local)
+        binding.load()
+        _adamw_bench(args, local)
+        return
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -334,6 +341,57 @@ def main():
     line = _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,
                   launches_per_step)
     _finish(line, world, rank)
+
+
+def _adamw_bench(args, local):
+    """AdamW over the parameters Muon does not take in Llama-3-8B shapes: the
+    embedding and the output head (128256 x 4096 each) and the 65 RMSNorm
+    gains (4096): fp32 parameters and moments, bf16 gradients, synthetic
+    values.  Algorithmic bytes per element: p r/w 8 + g 2 + m r/w 8 + v r/w 8."""
+    import torch
+    from newton_schulz_gb300 import binding
+    dev = torch.device("cuda", local)
+    sizes = [128256 * 4096, 128256 * 4096] + [4096] * 65
+    gen = torch.Generator(device=dev).manual_seed(7)
+    ts = []
+    for n in sizes:
+        ts.append({"param": torch.randn(n, device=dev, generator=gen) * 0.02,
+                   "grad": (torch.randn(n, device=dev, generator=gen) * 1e-3).to(torch.bfloat16),
+                   "exp_avg": torch.zeros(n, device=dev), "exp_avg_sq": torch.zeros(n, device=dev)})
+    elems = sum(sizes)
+    bytes_step = elems * 26
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for i in range(args.warmup):
+        binding.muon_adamw_grouped(ts, step=i + 1)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.muon_adamw_grouped(ts, step=args.warmup + i + 1)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    clocks = sampler.stop()
+    t = statistics.median(ms)
+    gbs = bytes_step / (t * 1e-3) / 1e9
+    peaks = _peaks()
+    print(json.dumps({
+        "metric": "AdamW step over the non-matrix parameters (GB/s of algorithmic traffic)",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "Llama-3-8B non-matrix parameters: 2 x [128256 x 4096] + 65 x [4096]",
+                   "elements": elems, "l2": "512 MiB L2 flush between timed steps (outside events)"},
+        "gpu_launches": args.steps * binding.muon_last_launch_count(),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes": bytes_step, "kernel": "adamw",
+                     "peak_source": peaks["source"]},
+        "clocks": clocks}))
 
 
 def _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,

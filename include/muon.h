@@ -186,6 +186,40 @@ muon_status_t muon_step_grouped_host(const muon_group_t *groups, int n_groups, f
                                      int nesterov, float lr, float wd, int scale_rule,
                                      const muon_ns_config_t *ns, cudaStream_t stream);
 
+/* ---- AdamW for the parameters Muon does not take --------------------------
+ * HyperParallel-FSDP section 6.3 chains Muon with AdamW: one-dimensional and
+ * scalar parameters (norm gains, biases; DMuon-2 section 2.1 adds the
+ * embeddings and the output head) are updated element-wise by AdamW, with
+ * decoupled weight decay.  A caller runs muon_step_grouped on the matrices
+ * and muon_adamw_grouped on the rest, on the same stream. */
+typedef struct muon_adamw_group_t {
+  void *param;          /* device, f32 or bf16, updated in place */
+  int32_t p_dtype;      /* muon_dtype_t */
+  const void *grad;     /* device, f32 or bf16, read only */
+  int32_t g_dtype;      /* muon_dtype_t */
+  float *exp_avg;       /* device fp32 first moment, updated in place */
+  float *exp_avg_sq;    /* device fp32 second moment, updated in place */
+  int64_t numel;        /* elements (any shape, contiguous) */
+} muon_adamw_group_t;
+
+typedef struct muon_adamw_config_t {
+  float lr, beta1, beta2, eps, weight_decay;
+  int64_t step;         /* the step being taken, counting from 1 (bias correction) */
+} muon_adamw_config_t;
+
+/* One AdamW step over every tensor of `groups`, in one kernel launch per 64
+ * tensors: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+ * p = p (1 - lr wd) - lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps), fp32
+ * arithmetic, the new p rounded to nearest in its dtype.  Errors: NULL
+ * groups with n_groups > 0, NULL cfg, NULL or misaligned pointers, unknown
+ * dtypes, numel < 0, step < 1, beta outside [0, 1), negative eps or
+ * non-finite hyperparameters -> MUON_ERR_INVALID_ARGUMENT; a written range
+ * (param, exp_avg, exp_avg_sq) overlapping another written range or a grad
+ * -> MUON_ERR_ALIAS; nothing is enqueued on error.  numel = 0 tensors are
+ * skipped. */
+muon_status_t muon_adamw_grouped(const muon_adamw_group_t *groups, int n_groups,
+                                 const muon_adamw_config_t *cfg, cudaStream_t stream);
+
 /* Read and clear the current device's status word (MUON_OK, MUON_ERR_TIMEOUT
  * or MUON_ERR_NONFINITE; the first bit set wins in that order of severity).
  * The caller synchronises `stream` first; this call synchronises it again. */
@@ -205,8 +239,8 @@ int muon_last_launch_count(void);
  * stream is synchronised) adds the elapsed milliseconds per kernel kind into
  * ms[0..n) and launch counts into launches[0..n) and resets the record.
  * Kinds: 0 prep (momentum/norm/cast/transpose), 1 Gram, 2 polynomial,
- * 3 apply, 4 update/copy-back, 5 fused small-m step.  Returns the number of
- * kinds (6). */
+ * 3 apply, 4 update/copy-back, 5 fused small-m step, 6 AdamW.  Returns the
+ * number of kinds (7). */
 int muon_profile_enable(int enable);
 int muon_profile_read(double *ms, int64_t *launches, int n);
 

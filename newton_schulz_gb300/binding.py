@@ -22,13 +22,13 @@ STATUS_NAMES = {
 MUON_F32, MUON_BF16 = 0, 1
 SCALE_SQRT_MAX1_R_OVER_C, SCALE_RMS_0P2_SQRT_MAXDIM, SCALE_ONE = 0, 1, 2
 NS_BF16, NS_TF32 = 0, 1
-PROFILE_KINDS = ("prep", "gram", "poly", "apply", "update", "fused_small")
+PROFILE_KINDS = ("prep", "gram", "poly", "apply", "update", "fused_small", "adamw")
 
 EXPORTED = (
     "muon_ns_default_config", "muon_ns_batched", "muon_ns_batched_ex", "muon_step_grouped",
     "muon_step_grouped_ex", "muon_step_grouped_host", "muon_query_status", "muon_status_string",
     "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
-    "muon_profile_read",
+    "muon_profile_read", "muon_adamw_grouped",
 )
 
 
@@ -49,6 +49,19 @@ class Group(ctypes.Structure):
                 ("G", ctypes.c_void_p), ("g_dtype", ctypes.c_int32),
                 ("Mom", ctypes.c_void_p),
                 ("B", ctypes.c_int64), ("M", ctypes.c_int64), ("N", ctypes.c_int64)]
+
+
+class AdamwGroup(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("p_dtype", ctypes.c_int32),
+                ("grad", ctypes.c_void_p), ("g_dtype", ctypes.c_int32),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("numel", ctypes.c_int64)]
+
+
+class AdamwConfig(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("step", ctypes.c_int64)]
 
 
 _lib = None
@@ -75,6 +88,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_step_grouped_ex.argtypes = [ctypes.POINTER(Group), ctypes.c_int, f32, ctypes.c_int,
                                          f32, f32, ctypes.c_int, ctypes.POINTER(NsConfig), vp]
     lib.muon_step_grouped_ex.restype = i32
+    lib.muon_adamw_grouped.argtypes = [ctypes.POINTER(AdamwGroup), ctypes.c_int,
+                                       ctypes.POINTER(AdamwConfig), vp]
+    lib.muon_adamw_grouped.restype = i32
     lib.muon_step_grouped_host.argtypes = lib.muon_step_grouped_ex.argtypes
     lib.muon_step_grouped_host.restype = i32
     lib.muon_query_status.argtypes = [vp]
@@ -238,3 +254,19 @@ def muon_profile_read():
     cnt = (ctypes.c_int64 * n)()
     load().muon_profile_read(ms, cnt, n)
     return {k: (ms[i], cnt[i]) for i, k in enumerate(PROFILE_KINDS)}
+
+
+def muon_adamw_grouped(groups, step: int, lr: float = 1e-3, betas=(0.9, 0.999),
+                       eps: float = 1e-8, weight_decay: float = 0.01, stream=None) -> None:
+    """One AdamW step over [{"param", "grad", "exp_avg", "exp_avg_sq"}] of
+    contiguous CUDA tensors (any shape; fp32 state)."""
+    groups = list(groups)
+    arr = (AdamwGroup * max(1, len(groups)))()
+    for i, g in enumerate(groups):
+        p, gr, m, v = g["param"], g["grad"], g["exp_avg"], g["exp_avg_sq"]
+        _check_contig(p, gr, m, v)
+        arr[i] = AdamwGroup(p.data_ptr(), _dtype_code(p), gr.data_ptr(), _dtype_code(gr),
+                            m.data_ptr(), v.data_ptr(), p.numel())
+    cfg = AdamwConfig(lr, betas[0], betas[1], eps, weight_decay, step)
+    check(load().muon_adamw_grouped(arr, len(groups), ctypes.byref(cfg), _stream_ptr(stream)),
+          "muon_adamw_grouped")

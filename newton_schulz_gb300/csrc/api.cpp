@@ -1150,6 +1150,91 @@ muon_status_t host_step_impl(const muon_group_t* groups, int n_groups, float mu,
   return MUON_OK;
 }
 
+// ---- AdamW for the non-matrix parameters ----------------------------------------------
+muon_status_t adamw_impl(const muon_adamw_group_t* groups, int n_groups,
+                         const muon_adamw_config_t* cfg, cudaStream_t stream) {
+  if (n_groups < 0 || (n_groups > 0 && !groups) || !cfg) return MUON_ERR_INVALID_ARGUMENT;
+  const float hp[5] = {cfg->lr, cfg->beta1, cfg->beta2, cfg->eps, cfg->weight_decay};
+  for (float x : hp)
+    if (!std::isfinite(x)) return MUON_ERR_INVALID_ARGUMENT;
+  if (cfg->beta1 < 0.f || cfg->beta1 >= 1.f || cfg->beta2 < 0.f || cfg->beta2 >= 1.f ||
+      cfg->eps < 0.f || cfg->step < 1)
+    return MUON_ERR_INVALID_ARGUMENT;
+  std::vector<std::pair<uintptr_t, uintptr_t>> written, read;
+  std::vector<int> live;
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_adamw_group_t& g = groups[i];
+    if (g.numel < 0) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.p_dtype != MUON_F32 && g.p_dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.g_dtype != MUON_F32 && g.g_dtype != MUON_BF16) return MUON_ERR_INVALID_ARGUMENT;
+    if (g.numel == 0) continue;
+    if (!g.param || !g.grad || !g.exp_avg || !g.exp_avg_sq) return MUON_ERR_INVALID_ARGUMENT;
+    if (!aligned(g.param, esize(g.p_dtype)) || !aligned(g.grad, esize(g.g_dtype)) ||
+        !aligned(g.exp_avg, 4) || !aligned(g.exp_avg_sq, 4))
+      return MUON_ERR_INVALID_ARGUMENT;
+    if (g.numel > (int64_t(1) << 40)) return MUON_ERR_UNSUPPORTED;
+    const auto pp = reinterpret_cast<uintptr_t>(g.param);
+    const auto mp = reinterpret_cast<uintptr_t>(g.exp_avg);
+    const auto vp = reinterpret_cast<uintptr_t>(g.exp_avg_sq);
+    const auto gp = reinterpret_cast<uintptr_t>(g.grad);
+    written.push_back({pp, pp + g.numel * esize(g.p_dtype)});
+    written.push_back({mp, mp + g.numel * 4});
+    written.push_back({vp, vp + g.numel * 4});
+    read.push_back({gp, gp + g.numel * esize(g.g_dtype)});
+    live.push_back(i);
+  }
+  if (ranges_overlap(written)) return MUON_ERR_ALIAS;
+  for (auto& r : read)
+    for (auto& w : written)
+      if (r.first < w.second && w.first < r.second) return MUON_ERR_ALIAS;
+  if (live.empty()) {
+    t_last_launches = 0;
+    return MUON_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* dev = nullptr;
+  muon_status_t st = dev_state(&dev);
+  if (st != MUON_OK) return st;
+  // bias corrections in double: 1 - beta^t for large t is close to 1
+  const double bc1 = 1.0 - std::pow(static_cast<double>(cfg->beta1), static_cast<double>(cfg->step));
+  const double bc2 = 1.0 - std::pow(static_cast<double>(cfg->beta2), static_cast<double>(cfg->step));
+  Launcher L{stream};
+  for (size_t b = 0; b < live.size(); b += kMaxSlices) {
+    AdamwParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    int64_t units = 0;
+    const size_t e = std::min(live.size(), b + kMaxSlices);
+    for (size_t k = b; k < e; ++k) {
+      const muon_adamw_group_t& g = groups[live[k]];
+      AdamwSlice& sl = ap.s[k - b];
+      sl.p = g.param;
+      sl.g = g.grad;
+      sl.m = g.exp_avg;
+      sl.v = g.exp_avg_sq;
+      sl.numel = g.numel;
+      sl.unit_base = units;
+      sl.p_dtype = g.p_dtype;
+      sl.g_dtype = g.g_dtype;
+      sl.vec = aligned(g.param, 16) && aligned(g.grad, 16) && aligned(g.exp_avg, 16) &&
+               aligned(g.exp_avg_sq, 16);
+      units += cdiv(g.numel, 8);
+    }
+    ap.n_slices = static_cast<int>(e - b);
+    ap.total_units = units;
+    ap.lr = cfg->lr;
+    ap.beta1 = cfg->beta1;
+    ap.beta2 = cfg->beta2;
+    ap.eps = cfg->eps;
+    ap.wd = cfg->weight_decay;
+    ap.step_size = static_cast<float>(static_cast<double>(cfg->lr) / bc1);
+    ap.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+    st = L.run(6, [&] { return launch_adamw(ap, dev->sms, stream); });
+    if (st != MUON_OK) return st;
+  }
+  t_last_launches = L.count;
+  return MUON_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1214,6 +1299,15 @@ muon_status_t muon_step_grouped_host(const muon_group_t* groups, int n_groups, f
                                      const muon_ns_config_t* ns, cudaStream_t stream) {
   try {
     return host_step_impl(groups, n_groups, mu, nesterov, lr, wd, scale_rule, ns, stream);
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
+muon_status_t muon_adamw_grouped(const muon_adamw_group_t* groups, int n_groups,
+                                 const muon_adamw_config_t* cfg, cudaStream_t stream) {
+  try {
+    return adamw_impl(groups, n_groups, cfg, stream);
   } catch (...) {
     return MUON_ERR_OUT_OF_MEMORY;
   }
@@ -1294,7 +1388,7 @@ int muon_last_launch_count(void) { return t_last_launches; }
 int muon_profile_enable(int enable) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_prof = enable != 0;
-  return 6;
+  return 7;
 }
 
 int muon_profile_read(double* ms, int64_t* launches, int n) {
@@ -1312,7 +1406,7 @@ int muon_profile_read(double* ms, int64_t* launches, int n) {
     cudaEventDestroy(r.e1);
   }
   g_prof_recs.clear();
-  return 6;
+  return 7;
 }
 
 }  // extern "C"

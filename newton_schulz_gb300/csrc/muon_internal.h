@@ -215,10 +215,32 @@ struct SmallParams {
   int smem_bytes;
 };
 
+// ---- AdamW for the non-matrix parameters ------------------------------------------
+struct AdamwSlice {
+  void* p;                 // parameter (f32 or bf16), updated in place
+  const void* g;           // gradient (f32 or bf16)
+  float* m;                // first moment (fp32), updated in place
+  float* v;                // second moment (fp32), updated in place
+  int64_t numel;
+  int64_t unit_base;       // first 8-element unit of this tensor in the launch
+  int p_dtype, g_dtype;    // 0 f32, 1 bf16
+  int vec;                 // 1: all four pointers 16-byte aligned
+};
+
+struct AdamwParams {
+  AdamwSlice s[kMaxSlices];
+  int n_slices;
+  int64_t total_units;
+  float lr, beta1, beta2, eps, wd;
+  float step_size;         // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;      // 1 / sqrt(1 - beta2^t)
+};
+
 // ---- launchers (return cudaGetLastError()) ----------------------------------
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
 cudaError_t launch_finish(const FinParams& p, cudaStream_t s);
 cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s);
+cudaError_t launch_adamw(const AdamwParams& p, int sms, cudaStream_t s);
 int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage

@@ -130,3 +130,27 @@ def test_host_step_argument_errors(lib):
     assert host([_grp()], lr=float("nan")) == E_INV
     assert host([_grp(W=0x1000, M_=0x1040)]) == E_ALIAS
     assert host([_grp(B=0, W=0, G=0, M_=0)]) == 0
+
+
+def test_adamw_argument_errors(lib):
+    def grp(p=0x1000, g=0x100000, m=0x200000, v=0x300000, n=16, pdt=0, gdt=0):
+        return binding.AdamwGroup(p, pdt, g, gdt, m, v, n)
+
+    def call(groups, **kw):
+        cfg = binding.AdamwConfig(kw.get("lr", 1e-3), kw.get("b1", 0.9), kw.get("b2", 0.999),
+                                  kw.get("eps", 1e-8), kw.get("wd", 0.01), kw.get("step", 1))
+        arr = (binding.AdamwGroup * max(1, len(groups)))(*groups)
+        return lib.muon_adamw_grouped(arr, len(groups), ctypes.byref(cfg), None)
+    assert lib.muon_adamw_grouped(None, 1, None, None) == E_INV
+    assert call([grp()], step=0) == E_INV
+    assert call([grp()], b1=1.0) == E_INV
+    assert call([grp()], b2=-0.1) == E_INV
+    assert call([grp()], eps=-1.0) == E_INV
+    assert call([grp()], lr=float("nan")) == E_INV
+    assert call([grp(p=0)]) == E_INV
+    assert call([grp(pdt=4)]) == E_INV
+    assert call([grp(n=-1)]) == E_INV
+    assert call([grp(p=0x1002)]) == E_INV            # misaligned f32
+    assert call([grp(m=0x1020)]) == E_ALIAS          # exp_avg inside param
+    assert call([grp(g=0x1010)]) == E_ALIAS          # grad inside param
+    assert call([grp(p=0, g=0, m=0, v=0, n=0)]) == 0  # empty tensors are skipped
