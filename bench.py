@@ -280,6 +280,8 @@ def main():
                     help="c4 only: number of Llama layers (default 32; a small profiling case)")
     ap.add_argument("--adamw", action="store_true",
                     help="time the AdamW kernel on the Llama-3-8B non-matrix parameters instead")
+    ap.add_argument("--owners", type=int, default=0,
+                    help="report the owner-assignment balance of the Llama-3-8B matrices for N ranks")
     ap.add_argument("--experts", type=int, default=None,
                     help="c3 only: experts per weight (default 128; a small profiling case)")
     ap.add_argument("--scale-down", type=int, default=1,
@@ -305,6 +307,11 @@ def main():
         torch.cuda.set_device(local)
         binding.load()
         _adamw_bench(args, local)
+        return
+    if args.owners:
+        torch.cuda.set_device(local)
+        binding.load()
+        _owners_report(args.owners)
         return
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -341,6 +348,54 @@ def main():
     line = _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,
                   launches_per_step)
     _finish(line, world, rank)
+
+
+def _owners_report(n_ranks):
+    """Owner assignment across n_ranks with NS times measured per shape on
+    this GPU (one assignment unit per matrix, byte cap eps = 0.1): the busiest
+    rank's NS time over the mean, for LPT on the measured times, LPT on
+    element counts, and round-robin in parameter order.  Two workloads: the
+    224 Llama-3-8B matrices (32 layers x q, k, v, o, gate, up, down; layer
+    spreading) and the 22 matrices of the large sweep."""
+    from newton_schulz_gb300 import binding
+    llama = [(4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096),
+             (14336, 4096), (14336, 4096), (4096, 14336)]
+    sweep = [(8192, 28672)] * 8 + [(8192, 8192)] * 8 + [(16384, 16384)] * 4 + [(8192, 8192)] * 2
+    distinct = sorted(set(llama) | set(sweep))
+    ms = dict(zip(distinct, binding.muon_ns_cost_table(distinct, reps=3)))
+
+    def report(units, layers):
+        cost = [ms[s] for s in units]
+        elems = [s[0] * s[1] for s in units]
+        nbytes = [e * 10 for e in elems]          # bf16 W, bf16 G, fp32 Mom
+
+        def ratio(owner):
+            t = [0.0] * n_ranks
+            for o, c in zip(owner, cost):
+                t[o] += c
+            return max(t) / (sum(t) / n_ranks)
+        def bytes_ratio(owner):
+            b = [0.0] * n_ranks
+            for o, x in zip(owner, nbytes):
+                b[o] += x
+            return max(b) / (sum(b) / n_ranks)
+        lpt = binding.muon_assign_owners(cost, n_ranks, nbytes, elems, layers, 0.1)
+        free = binding.muon_assign_owners(cost, n_ranks, nbytes, elems, layers, 1e9)
+        by_elems = binding.muon_assign_owners([float(e) for e in elems], n_ranks, nbytes, elems,
+                                              layers, 0.1)
+        rr = [i % n_ranks for i in range(len(units))]
+        return {"lpt_measured": ratio(lpt), "lpt_measured_bytes": bytes_ratio(lpt),
+                "lpt_no_byte_cap": ratio(free), "lpt_no_byte_cap_bytes": bytes_ratio(free),
+                "lpt_element_count": ratio(by_elems), "round_robin": ratio(rr)}
+    lu = [s for _ in range(32) for s in llama]
+    rl = report(lu, [i // 7 for i in range(len(lu))])
+    rs = report(sweep, [-1] * len(sweep))
+    print(json.dumps({
+        "metric": "owner assignment: busiest rank NS time / mean", "unit": "ratio",
+        "n_ranks": n_ranks, "value": rs["lpt_measured"], "higher_is_better": False,
+        "config": {"workload": "large sweep (22 matrices) and Llama-3-8B (224)", "eps": 0.1},
+        "ms_per_matrix": {f"{r}x{c}": v for (r, c), v in ms.items()},
+        "sweep": rs, "llama": rl}))
 
 
 def _adamw_bench(args, local):

@@ -220,6 +220,39 @@ typedef struct muon_adamw_config_t {
 muon_status_t muon_adamw_grouped(const muon_adamw_group_t *groups, int n_groups,
                                  const muon_adamw_config_t *cfg, cudaStream_t stream);
 
+/* ---- owner assignment across data-parallel ranks ---------------------------
+ * DMuon-2 section 3.3 and Appendix B: each assignment unit (the Muon matrices
+ * of one wrapping unit) goes whole to one owner rank, which runs its NS and
+ * update.  The NS time of a unit is measured per matrix shape. */
+
+/* Measured NS time per matrix, in milliseconds, of each core shape
+ * shapes[2i], shapes[2i+1] (rows, cols): the median of `reps` (>= 1) timed
+ * runs of muon_ns_batched_ex (bf16, configuration `cfg`, NULL = defaults)
+ * on a batch of the shape (as many matrices as fit 256 MB, 1 to 64),
+ * divided by the batch size.  Runs on `stream` and blocks the host until it
+ * is done; allocates and frees its own device buffers.  Errors: NULL or
+ * non-positive shapes, n < 0, reps < 1 -> MUON_ERR_INVALID_ARGUMENT. */
+muon_status_t muon_ns_cost_table(const int64_t *shapes, int n, const muon_ns_config_t *cfg,
+                                 int reps, double *ms_per_matrix, cudaStream_t stream);
+
+typedef struct muon_unit_t {
+  double cost;          /* NS time of the unit (sum over its matrices), any unit */
+  int64_t bytes;        /* bytes the owner holds for it (parameters and state) */
+  int64_t elems;        /* elements, the first tie-break */
+  int32_t layer;        /* units of one layer go to different ranks; < 0: none */
+} muon_unit_t;
+
+/* Greedy Longest-Processing-Time assignment (host only, deterministic):
+ * units in decreasing cost (ties: more elements, then input order), each to
+ * the rank with the smallest accumulated cost among the ranks not yet used
+ * in its layer (all ranks once the layer has used them all) whose bytes stay
+ * within (1 + eps) times the average after receiving it; if none stays
+ * within, to the candidate with the fewest bytes.  owner_out[i] in
+ * [0, n_ranks).  Errors: n_units < 0, n_ranks < 1, NULL arrays, negative or
+ * non-finite eps, cost or bytes -> MUON_ERR_INVALID_ARGUMENT. */
+muon_status_t muon_assign_owners(const muon_unit_t *units, int n_units, int n_ranks, double eps,
+                                 int32_t *owner_out);
+
 /* Read and clear the current device's status word (MUON_OK, MUON_ERR_TIMEOUT
  * or MUON_ERR_NONFINITE; the first bit set wins in that order of severity).
  * The caller synchronises `stream` first; this call synchronises it again. */

@@ -28,7 +28,7 @@ EXPORTED = (
     "muon_ns_default_config", "muon_ns_batched", "muon_ns_batched_ex", "muon_step_grouped",
     "muon_step_grouped_ex", "muon_step_grouped_host", "muon_query_status", "muon_status_string",
     "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
-    "muon_profile_read", "muon_adamw_grouped",
+    "muon_profile_read", "muon_adamw_grouped", "muon_ns_cost_table", "muon_assign_owners",
 )
 
 
@@ -64,6 +64,11 @@ class AdamwConfig(ctypes.Structure):
                 ("step", ctypes.c_int64)]
 
 
+class Unit(ctypes.Structure):
+    _fields_ = [("cost", ctypes.c_double), ("bytes", ctypes.c_int64), ("elems", ctypes.c_int64),
+                ("layer", ctypes.c_int32)]
+
+
 _lib = None
 
 
@@ -91,6 +96,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_adamw_grouped.argtypes = [ctypes.POINTER(AdamwGroup), ctypes.c_int,
                                        ctypes.POINTER(AdamwConfig), vp]
     lib.muon_adamw_grouped.restype = i32
+    lib.muon_ns_cost_table.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                       ctypes.POINTER(NsConfig), ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_double), vp]
+    lib.muon_ns_cost_table.restype = i32
+    lib.muon_assign_owners.argtypes = [ctypes.POINTER(Unit), ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_double, ctypes.POINTER(ctypes.c_int32)]
+    lib.muon_assign_owners.restype = i32
     lib.muon_step_grouped_host.argtypes = lib.muon_step_grouped_ex.argtypes
     lib.muon_step_grouped_host.restype = i32
     lib.muon_query_status.argtypes = [vp]
@@ -270,3 +282,29 @@ def muon_adamw_grouped(groups, step: int, lr: float = 1e-3, betas=(0.9, 0.999),
     cfg = AdamwConfig(lr, betas[0], betas[1], eps, weight_decay, step)
     check(load().muon_adamw_grouped(arr, len(groups), ctypes.byref(cfg), _stream_ptr(stream)),
           "muon_adamw_grouped")
+
+
+def muon_ns_cost_table(shapes, cfg=None, reps: int = 5, stream=None):
+    """Measured NS milliseconds per matrix for each (rows, cols) in `shapes`."""
+    shapes = [(int(r), int(c)) for r, c in shapes]
+    n = len(shapes)
+    flat = (ctypes.c_int64 * max(1, 2 * n))(*[v for rc in shapes for v in rc])
+    out = (ctypes.c_double * max(1, n))()
+    check(load().muon_ns_cost_table(flat, n, ctypes.byref(cfg) if cfg is not None else None,
+                                    reps, out, _stream_ptr(stream)), "muon_ns_cost_table")
+    return [out[i] for i in range(n)]
+
+
+def muon_assign_owners(costs, n_ranks: int, nbytes=None, elems=None, layers=None,
+                       eps: float = 0.1):
+    """Owner rank of each assignment unit (greedy LPT with a byte cap and
+    layer spreading); host only."""
+    n = len(costs)
+    nbytes = nbytes if nbytes is not None else [0] * n
+    elems = elems if elems is not None else [0] * n
+    layers = layers if layers is not None else [-1] * n
+    arr = (Unit * max(1, n))(*[Unit(float(costs[i]), int(nbytes[i]), int(elems[i]), int(layers[i]))
+                               for i in range(n)])
+    out = (ctypes.c_int32 * max(1, n))()
+    check(load().muon_assign_owners(arr, n, n_ranks, eps, out), "muon_assign_owners")
+    return [out[i] for i in range(n)]

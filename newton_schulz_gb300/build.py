@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmuon.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cpp", "ns_plan.cpp", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "noalloc.cu", "adamw.cu"]
+SOURCES = ["api.cpp", "ns_plan.cpp", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "noalloc.cu", "adamw.cu", "owners.cpp"]
 HEADERS = ["muon_internal.h", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -1313,6 +1313,71 @@ muon_status_t muon_adamw_grouped(const muon_adamw_group_t* groups, int n_groups,
   }
 }
 
+muon_status_t muon_ns_cost_table(const int64_t* shapes, int n, const muon_ns_config_t* cfg,
+                                 int reps, double* ms_per_matrix, cudaStream_t stream) {
+  try {
+    if (n < 0 || reps < 1 || (n > 0 && (!shapes || !ms_per_matrix)))
+      return MUON_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < n; ++i)
+      if (shapes[2 * i] <= 0 || shapes[2 * i + 1] <= 0 || shapes[2 * i] > (1LL << 30) ||
+          shapes[2 * i + 1] > (1LL << 30))
+        return MUON_ERR_INVALID_ARGUMENT;
+    if (n == 0) return MUON_OK;
+    void* buf = nullptr;
+    size_t have = 0;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    muon_status_t st = MUON_OK;
+    for (int i = 0; i < n && st == MUON_OK; ++i) {
+      const int64_t r = shapes[2 * i], c = shapes[2 * i + 1];
+      const size_t per = static_cast<size_t>(r * c) * 2;
+      const int64_t B = std::min<int64_t>(64, std::max<int64_t>(1, (size_t(256) << 20) / per));
+      const size_t need = per * B;
+      if (need > have) {
+        if (buf) cudaFree(buf);
+        buf = nullptr;
+        if (cudaMalloc(&buf, need) != cudaSuccess) {
+          cudaGetLastError();
+          st = MUON_ERR_OUT_OF_MEMORY;
+          break;
+        }
+        have = need;
+      }
+      // a fixed, finite bf16 pattern (0x3c3c = 0.0115 in every element)
+      if (cudaMemsetAsync(buf, 0x3c, need, stream) != cudaSuccess) {
+        st = MUON_ERR_CUDA;
+        break;
+      }
+      std::vector<float> t;
+      for (int k = 0; k <= reps && st == MUON_OK; ++k) {   // run 0 warms up
+        cudaEventRecord(e0, stream);
+        st = ns_impl(buf, MUON_BF16, B, r, c, cfg, nullptr, stream);
+        cudaEventRecord(e1, stream);
+        if (st == MUON_OK && cudaEventSynchronize(e1) != cudaSuccess) st = MUON_ERR_CUDA;
+        float ms = 0.f;
+        if (st == MUON_OK && k > 0) {
+          cudaEventElapsedTime(&ms, e0, e1);
+          t.push_back(ms);
+        }
+      }
+      if (st == MUON_OK) {
+        std::sort(t.begin(), t.end());
+        ms_per_matrix[i] = static_cast<double>(t[t.size() / 2]) / static_cast<double>(B);
+      }
+    }
+    if (buf) {
+      cudaStreamSynchronize(stream);
+      cudaFree(buf);
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return st;
+  } catch (...) {
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+}
+
 muon_status_t muon_query_status(cudaStream_t stream) {
   try {
     std::lock_guard<std::mutex> lock(g_mu);
