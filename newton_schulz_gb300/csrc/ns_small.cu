@@ -224,32 +224,47 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
   // form the products, the others only take part in the barriers
   const bool blk = t < 256;
   const int i0 = TI * ((t & 255) >> 4), j0 = TJ * (t & 15);
-  // R_0 (unnormalised) = sum of the item partials in block order; up to 8
-  // partial loads of an element are in flight together; the padding is zero
-  // partial block q (item q / nblk, stacked block q % nblk) at
-  // part + (mat nb + q / nblk) pstride + (q % nblk) m^2
+  // R_0 (unnormalised) = sum of the item partials in block order.  The
+  // m x m elements are dealt to the threads four at a time and the partial
+  // loads of the four go out together, eight partials at a time (32 loads in
+  // flight per thread: the sum is bound by L2 latency, not bandwidth).
+  // Partial block q (item q / nblk, stacked block q % nblk) is at
+  // part + (mat nb + q / nblk) pstride + (q % nblk) m^2.
   const float* part = p.part + static_cast<size_t>(mat) * p.nb * p.pstride;
   const int nblk = p.nblk;                 // 1 or 2: q / nblk and q % nblk as shift and mask
   const int bsh = nblk - 1;                // (a division by a run-time divisor here costs
   const int nq = p.nb * nblk;              // the job about 15 us at m = 24)
-  for (int e = t; e < MM; e += kT) {
-    const int i = e / LD, j = e - i * LD;
-    float acc = 0.f;
-    if (i < m && j < m) {
-      const int src = i * m + j;
-      for (int b0 = 0; b0 < nq; b0 += 8) {
-        float v[8];
+  const int mm = m * m;
+  for (int e = t; e < MM; e += kT) R[e] = 0.f;   // padding rows and columns stay zero
+  cons_sync();
+  for (int base = 0; base < mm; base += 4 * kT) {
+    int src[4];
+    float acc[4];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int q = b0 + b;
-          v[b] = q < nq ? __ldcg(part + static_cast<size_t>(q >> bsh) * p.pstride + (q & bsh) * m * m + src)
-                        : 0.f;
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc += v[b];
-      }
+    for (int u = 0; u < 4; ++u) {
+      src[u] = base + u * kT + t;
+      acc[u] = 0.f;
     }
-    R[e] = acc;
+    for (int b0 = 0; b0 < nq; b0 += 8) {
+      float v[4][8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int q = b0 + b;
+        const float* pq = part + static_cast<size_t>(q >> bsh) * p.pstride + (q & bsh) * mm;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u][b] = (q < nq && src[u] < mm) ? __ldcg(pq + src[u]) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[u] += v[u][b];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (src[u] < mm) {
+        const int i = src[u] / m, j = src[u] - (src[u] / m) * m;
+        R[i * LD + j] = acc[u];
+      }
   }
   cons_sync();
   if (t < 32) {   // trace(X0 X0^T) = ||X0||_F^2, fp32, fixed reduction order
