@@ -216,3 +216,35 @@ def test_precise_gemm_step_parity():
     for i in range(2):
         err = np.linalg.norm(w[i] - w2[i]) / np.linalg.norm(w2[i] - host["W"][i])
         assert err <= HP_TOL, (i, err)
+
+
+@pytest.mark.parametrize("generic", [False, True])
+def test_precise_steps_zero_and_table(generic):
+    """The high-precision mode with steps = 0 (O = X0 / ||X0||) and with a
+    per-step coefficient table, on both paths."""
+    if generic:
+        os.environ["MUON_SMALL_PATH"] = "0"
+    x = torch.randn((2, 40, 700), generator=torch.Generator().manual_seed(17))
+    X = x.cuda()
+    for steps, table, tol in ((0, None, 1e-5), (3, [(3.0, -3.2, 1.2), (2.5, -2.0, 0.6), (1.9, -1.2, 0.3)], HP_TOL)):
+        out = torch.empty_like(X)
+        binding.muon_ns_batched_ex(X, binding.make_config(steps=steps, coeffs=table,
+                                                          precision=binding.NS_TF32), out)
+        torch.cuda.synchronize()
+        assert binding.muon_query_status() == 0
+        ref = R.ns_batched_ref(_np(x), steps=steps, coeffs=table)
+        for i in range(2):
+            assert _rel(_np(out)[i], ref[i]) <= tol, (generic, steps, _rel(_np(out)[i], ref[i]))
+
+
+def test_precise_host_step():
+    g = synth.random_group((6, 24, 4096), torch.bfloat16, torch.float32, "cpu", 37, 1e-3, 1e-3)
+    host = {k: g[k].pin_memory() for k in ("W", "G", "Mom")}
+    h0 = {k: _np(v) for k, v in host.items()}
+    binding.muon_step_grouped_host([host], ns_cfg=binding.make_config(precision=binding.NS_TF32))
+    torch.cuda.current_stream().synchronize()
+    w2, m2, _ = R.muon_step_ref(h0["W"], h0["G"], h0["Mom"])
+    w = _np(host["W"])
+    for i in range(6):
+        err = np.linalg.norm(w[i] - w2[i]) / np.linalg.norm(w2[i] - h0["W"][i])
+        assert err <= HP_TOL, (i, err)
