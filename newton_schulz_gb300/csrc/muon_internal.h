@@ -195,6 +195,7 @@ struct SmallParams {
   int gcols;         // TMEM columns per Gram accumulator (64, or 128 for precise m > 32);
                      // the O slots start at column 2 gcols
   int gs_lowmem;     // Gram-space job in three LD x LD buffers instead of five
+  int p2_tiles;      // second phase: 128-column tiles per claim (a part of an item)
   int steps;
   float coef[kMaxSteps][3];
   int step_mode, nesterov;

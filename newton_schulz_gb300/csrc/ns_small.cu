@@ -899,20 +899,29 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       if (!ok) break;
     }
     if (ok) ok = put(kStageP1End, -1, 0, 0);
-    // Second phase: items are claimed in the order matrices were published
-    // (position j of the ready list, block blk), so no CTA waits for a late
-    // matrix while published work remains.
+    // Second phase: work is claimed in the order matrices were published
+    // (position j of the ready list, block blk, part sub of the block), so no
+    // CTA waits for a late matrix while published work remains.  A claim is
+    // a part of an item's tiles (p2_tiles of them), so the last matrices'
+    // work spreads over more CTAs at the end of the launch.
+    const int tpc = p.p2_tiles;                       // tiles per claim
+    const int parts = (tiles + tpc - 1) / tpc;        // claims per item
     for (int k = 0; ok; ++k) {
       const int b = k & 1;
-      int item = -1;
+      int item = -1, t0 = 0;
       if (lane == 0) {
         const unsigned next = atomicAdd(lctr + 1, 1u);
-        const int j = static_cast<int>(next / static_cast<unsigned>(p.nb));
+        const unsigned per = static_cast<unsigned>(p.nb * parts);
+        const int j = static_cast<int>(next / per);
         if (j < p.total_mats) {
           const int mat = wait_ready_pos(p.ready_list, j, p.epoch, ctx);
-          if (mat >= 0) item = mat * p.nb + static_cast<int>(next - j * p.nb);
+          const int rem = static_cast<int>(next - j * per);
+          if (mat >= 0) {
+            item = mat * p.nb + rem / parts;
+            t0 = (rem % parts) * tpc;
+          }
         }
-        // Q buffer b is free once the MMAs of item k-2 are done
+        // Q buffer b is free once the MMAs of claim k-2 are done
         if (item >= 0 && !mwait(&B->q_free[b], ((k >> 1) & 1) ^ 1u, ctx)) item = -1;
         if (item >= 0) {
           ptx::fence_proxy_async_global();
@@ -923,9 +932,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         }
       }
       item = __shfl_sync(0xffffffffu, item, 0);
+      t0 = __shfl_sync(0xffffffffu, t0, 0);
       if (item < 0) break;
-      for (int t = 0; t < tiles && ok; ++t)
-        ok = put(kStageP2, item, 128 * t, (t == 0 ? kFirst : 0) | (t == tiles - 1 ? kLast : 0));
+      const int t1 = min(tiles, t0 + tpc);
+      for (int t = t0; t < t1 && ok; ++t)
+        ok = put(kStageP2, item, 128 * t, (t == t0 ? kFirst : 0) | (t == t1 - 1 ? kLast : 0));
     }
     put(kStageEnd, -1, 0, 0);
   } else if (warp == 1) {
