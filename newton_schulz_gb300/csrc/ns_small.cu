@@ -152,15 +152,17 @@ __device__ __forceinline__ float ld_elem(const void* base, int dtype, int64_t e)
 // dimension LD, entries outside m x m zero).  LD is 32 (m <= 32, 2 x 2
 // blocks) or 64 (4 x 4 blocks), so the k loop is fully unrolled with no
 // bounds; the k-sum runs in index order, so every CTA forms the same bits.
+// C block = A B over k < K (K a multiple of 4, at most LD: the rows and
+// columns past m are zero, so the sum may stop at m rounded up to 4).
 template <int TI, int TJ, int LD>
 __device__ __forceinline__ void mm_block(const float* A, const float* B, int i0, int j0,
-                                         float (&acc)[TI][TJ]) {
+                                         float (&acc)[TI][TJ], int K) {
 #pragma unroll
   for (int r = 0; r < TI; ++r)
 #pragma unroll
     for (int c = 0; c < TJ; ++c) acc[r][c] = 0.f;
-#pragma unroll
-  for (int k = 0; k < LD; k += 4) {
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
     float a[TI][4], b[4][TJ];
 #pragma unroll
     for (int r = 0; r < TI; ++r) {
@@ -223,6 +225,7 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
   // the 16 x 16 blocks of TI x TJ cover LD x LD: consumer threads 0..255
   // form the products, the others only take part in the barriers
   const bool blk = t < 256;
+  const int K4 = (m + 3) & ~3;   // product length: m rounded up to 4
   const int i0 = TI * ((t & 255) >> 4), j0 = TJ * (t & 15);
   // R_0 (unnormalised) = sum of the item partials in block order.  The
   // m x m elements are dealt to the threads four at a time and the partial
@@ -286,7 +289,7 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
     const bool more = k + 1 < p.steps;
     {   // T = R^2 (in registers), P = aI + bR + cR^2 (zero outside m x m)
       float acc[TI][TJ], pv[TI][TJ];
-      if (blk) mm_block<TI, TJ, LD>(R, R, i0, j0, acc);
+      if (blk) mm_block<TI, TJ, LD>(R, R, i0, j0, acc, K4);
 #pragma unroll
       for (int r = 0; r < TI; ++r)
 #pragma unroll
@@ -306,23 +309,23 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
         // whole kernel follows its largest callee)
         float acc[TI][TJ];
         if (more) {
-          if (blk) mm_block<TI, TJ, LD>(P, R, i0, j0, acc);   // T = P R
+          if (blk) mm_block<TI, TJ, LD>(P, R, i0, j0, acc, K4);   // T = P R
           cons_sync();   // every thread has read R
           if (blk) st_block<TI, TJ, LD>(T, i0, j0, acc);
         }
         if (k > 0) {
-          if (blk) mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);   // Q' = P Q
+          if (blk) mm_block<TI, TJ, LD>(P, Q, i0, j0, acc, K4);   // Q' = P Q
           cons_sync();   // every thread has read Q
           if (blk) st_block<TI, TJ, LD>(Qn, i0, j0, acc);
         }
       } else {
         float acc[TI][TJ];
         if (blk && more) {
-          mm_block<TI, TJ, LD>(P, R, i0, j0, acc);     // T = P R
+          mm_block<TI, TJ, LD>(P, R, i0, j0, acc, K4);     // T = P R
           st_block<TI, TJ, LD>(T, i0, j0, acc);
         }
         if (blk && k > 0) {
-          mm_block<TI, TJ, LD>(P, Q, i0, j0, acc);     // Q' = P Q
+          mm_block<TI, TJ, LD>(P, Q, i0, j0, acc, K4);     // Q' = P Q
           st_block<TI, TJ, LD>(Qn, i0, j0, acc);
         }
       }
@@ -335,7 +338,7 @@ __device__ __noinline__ void gram_space(const SmallParams& p, int mat, float* gs
     }
     if (more) {
       float acc[TI][TJ];
-      if (blk) mm_block<TI, TJ, LD>(T, P, i0, j0, acc);          // R <- (P R) P
+      if (blk) mm_block<TI, TJ, LD>(T, P, i0, j0, acc, K4);          // R <- (P R) P
       if (LOWMEM) cons_sync();
       if (blk) st_block<TI, TJ, LD>(R, i0, j0, acc);
       cons_sync();
