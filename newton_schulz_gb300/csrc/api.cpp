@@ -207,7 +207,7 @@ bool small_shape(int64_t m) {
 // memory holds a ring of stages, two Q images and the Gram-space matrices.
 // A stage holds the data tile(s) of its phase (G + Mom: m x cw1, or W:
 // m x 128, for the widest dtypes in the launch), then an X0 tile of 128
-// columns at x_off and a 2 KB zero gap.  Items are up to 2048 columns (the
+// columns at x_off and a 2 KB zero gap.  Items are up to 2560 columns (the
 // X0 image of an item streams through the stages), shrinking while the
 // launch would leave SMs without an item and a matrix keeps at most 10.
 bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, bool step,
@@ -241,7 +241,12 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   sp->stages = static_cast<int>(std::min<size_t>((kSmallSmemLimit - fixed) / sp->stage_bytes,
                                                  std::min(kSmallMaxStages, ocols / (2 * tcol))));
   if (sp->stages < 2) return false;
-  int64_t wb = std::min<int64_t>(2048, rup(n, 128));
+  // items of at most 2560 columns (MUON_SMALL_ITEM_COLS; on 74 x [24, 10240]
+  // items of 1280 / 2048 / 2560 / 3456 columns took 0.099 / 0.093 / 0.091 /
+  // 0.096 ms)
+  const int64_t cap =
+      std::max<int64_t>(128, static_cast<int64_t>(env_size("MUON_SMALL_ITEM_COLS", 2560)));
+  int64_t wb = std::min<int64_t>(cap, rup(n, 128));
   wb = rup(cdiv(n, cdiv(n, wb)), 128);
   {
     // Items shrink while the launch has fewer items than SMs, as long as a

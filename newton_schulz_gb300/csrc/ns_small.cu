@@ -24,8 +24,8 @@
 // stage's 128-byte-swizzled X0 tile and to the matrix's X0 image in the
 // workspace; the MMA warp accumulates the item's Gram X0_blk X0_blk^T (fp32,
 // TMEM, two 64-column chunks stacked as one 2m-row operand) stage by stage.
-// The item's Gram is read back one item later, so its MMAs overlap the next
-// item's streaming.  The CTA whose item arrives last for a matrix sums the
+// The item's Gram is read back one stage into the next item, so its last
+// MMAs overlap that stage.  The CTA whose item arrives last for a matrix sums the
 // partials in block order, normalises by the trace (= ||X0||_F^2), runs the
 // Gram-space steps and publishes Q.
 // Phase 2, per item: wait for the matrix's Q, bulk-load Q (hi rows, then lo
@@ -154,6 +154,9 @@ __device__ __forceinline__ float ld_elem(const void* base, int dtype, int64_t e)
 // bounds; the k-sum runs in index order, so every CTA forms the same bits.
 // C block = A B over k < K (K a multiple of 4, at most LD: the rows and
 // columns past m are zero, so the sum may stop at m rounded up to 4).
+// A block wholly outside the leading K x K (rows of A or columns of B past
+// m, which are zero) is zero exactly and loads nothing: the products are
+// bound by shared-memory wavefronts, so the threads of such blocks sit out.
 template <int TI, int TJ, int LD>
 __device__ __forceinline__ void mm_block(const float* A, const float* B, int i0, int j0,
                                          float (&acc)[TI][TJ], int K) {
@@ -161,6 +164,7 @@ __device__ __forceinline__ void mm_block(const float* A, const float* B, int i0,
   for (int r = 0; r < TI; ++r)
 #pragma unroll
     for (int c = 0; c < TJ; ++c) acc[r][c] = 0.f;
+  if (i0 >= K || j0 >= K) return;
 #pragma unroll 2
   for (int k = 0; k < K; k += 4) {
     float a[TI][4], b[4][TJ];
@@ -821,6 +825,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 
   if (warp == 0) {
     // ======================= producer (loads) =======================
+    // the descriptors of the tensor maps this launch uses, fetched ahead of
+    // the first loads
+    if (lane < p.n_slices) {
+      const SmallSlice& S = p.s[lane];
+      if (S.gbulk) {
+        ptx::prefetch_tmap(&p.tm[lane][0]);
+        if (p.step_mode) ptx::prefetch_tmap(&p.tm[lane][1]);
+      }
+      if (p.step_mode && S.wbulk) ptx::prefetch_tmap(&p.tm[lane][2]);
+    }
     Ring rg;
     bool ok = true;
     // Hands the next stage to the other roles once its previous use is done
@@ -1024,9 +1038,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const int cw = warp - 2;
     bool ok = true;
     Ring rg;
-    // Deferred end of a first-phase item: partial Gram (both stacked blocks)
-    // to the workspace, arrival, and the Gram-space step if it completed its
-    // matrix.
+    // Deferred end of a first-phase item (taken after the first stage of the
+    // next item, or at the end of the phase): partial Gram (both stacked
+    // blocks) to the workspace, arrival, and the Gram-space step if it
+    // completed its matrix.
     auto finish = [&](int item, int k) {
       const int g = k & 1;
       const int mat = item / p.nb;
@@ -1122,8 +1137,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         ok = ok && sok;
         if (ok) consume_p1_dt<PRECISE>(ic, s * p.cw1, ring + rg.stage * p.stage_bytes, t);
         release(true);
+        // the previous item ends one stage into this one (its last MMAs
+        // have run meanwhile): its matrix must not wait for this item
+        if (s == 0 && prev >= 0) {
+          finish(prev, prevk);
+          prev = -1;
+        }
       }
-      if (prev >= 0) finish(prev, prevk);
       prev = item;
       prevk = k;
     }
