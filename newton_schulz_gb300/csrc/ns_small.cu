@@ -735,12 +735,6 @@ __device__ void epi_tile_any(const ItemCfg& c, int c0, uint8_t* st, uint32_t osl
   }
 }
 
-// TMA coordinates of the tile at X column gj0.
-__device__ __forceinline__ void tile_xy(const SmallSlice& S, int64_t gj0, int& x, int& y) {
-  x = S.trans ? 0 : static_cast<int>(gj0);
-  y = S.trans ? static_cast<int>(gj0) : 0;
-}
-
 struct ItemRef {
   int si;          // slice
   int mat;         // matrix within the launch
@@ -835,61 +829,91 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       if (p.step_mode && S.wbulk) ptx::prefetch_tmap(&p.tm[lane][2]);
     }
+    // Launch constants in registers, and per item (first phase) or per claim
+    // (second phase) one load plan: reading the parameter block's slice
+    // fields on every stage cost the producer about 0.2 us per stage, and
+    // in the second phase the producer sets the pace.
+    const int stage_bytes = p.stage_bytes, cw1 = p.cw1, x_off = p.x_off;
+    const int xbytes = p.xbytes, nb = p.nb, n_items = p.items, total_mats = p.total_mats;
+    const int qbytes = p.qbytes, off_q = p.off_q;
+    const bool step_mode = p.step_mode != 0;
+    uint8_t* const ximg = p.ximg;
+    const uint8_t* const qimg = p.qimg;
+    const unsigned long long* const ready_list = p.ready_list;
+    const unsigned epoch = p.epoch;
+    struct LoadPlan {
+      int item = -1;
+      int z = 0, trans = 0;        // matrix within its slice; stored transposed
+      int64_t col0 = 0;            // first X column of the item
+      bool bulk = false;           // the data tile(s) by TMA (else element-wise)
+      uint32_t tx = 0;             // bytes the stage's asynchronous copies deliver
+      uint32_t mom_off = 0;        // Mom tile inside the stage (first phase)
+      const CUtensorMap* tm = nullptr;   // G (then Mom) map, or the W map
+      const uint8_t* img = nullptr;      // the item's X0 image (second phase)
+    };
+    auto make_plan = [&](int kind, int item) {
+      LoadPlan L;
+      L.item = item;
+      const ItemRef ir = item_ref(p, item);
+      const SmallSlice& S = p.s[ir.si];
+      L.z = ir.mat - S.mat_base;
+      L.trans = S.trans;
+      L.col0 = ir.col0;
+      if (kind == kStageP1) {
+        L.bulk = S.gbulk != 0;
+        L.tm = &p.tm[ir.si][0];
+        L.mom_off = mom_off(p, S);
+        if (L.bulk) L.tx = static_cast<uint32_t>(m * cw1 * ((S.g_dtype == 0 ? 4 : 2) + (step_mode ? 4 : 0)));
+      } else {
+        L.bulk = step_mode && S.wbulk;
+        L.tm = &p.tm[ir.si][2];
+        L.img = ximg + static_cast<size_t>(item) * xbytes;
+        L.tx = static_cast<uint32_t>(2 * xs * chunk_bytes);
+        if (L.bulk) L.tx += static_cast<uint32_t>(m * 128 * (S.w_dtype == 0 ? 4 : 2));
+      }
+      return L;
+    };
     Ring rg;
     bool ok = true;
     // Hands the next stage to the other roles once its previous use is done
-    // (consumers and MMA issuer): descriptor, then the tile(s).
-    auto put = [&](int kind, int item, int c0, int flags) -> bool {
+    // (consumers and MMA issuer): descriptor, then the tile(s).  Element-wise
+    // copies (slices whose rows are not TMA-legal) go through the slice.
+    auto put = [&](int kind, const LoadPlan& L, int c0, int flags) -> bool {
       if (!mwait_warp(&B->cons_done[rg.stage], rg.phase ^ 1u, ctx)) return false;
       if (!mwait_warp(&B->mma_done[rg.stage], rg.phase ^ 1u, ctx)) return false;
-      uint8_t* st = ring + rg.stage * p.stage_bytes;
+      uint8_t* st = ring + rg.stage * stage_bytes;
       uint64_t* full = &B->ring_full[rg.stage];
-      uint32_t tx = 0;
-      ItemRef ir{};
-      bool tma = false;
-      if (item >= 0) {
-        ir = item_ref(p, item);
+      const bool data = kind == kStageP1 || kind == kStageP2;
+      if (data && !L.bulk && (kind == kStageP1 || step_mode)) {
+        const ItemRef ir = item_ref(p, L.item);
         const SmallSlice& S = p.s[ir.si];
         const int64_t gj0 = ir.col0 + c0;
         if (kind == kStageP1) {
-          if (S.gbulk) {
-            tma = true;
-            tx = static_cast<uint32_t>(m * p.cw1 * ((S.g_dtype == 0 ? 4 : 2) + (p.step_mode ? 4 : 0)));
-          } else {
-            copy_tile_in(p, S, S.g_dtype, S.G, ir.moff, gj0, p.cw1, st, lane);
-            if (p.step_mode) copy_tile_in(p, S, 0, S.Mom, ir.moff, gj0, p.cw1, st + mom_off(p, S), lane);
-          }
-        } else {   // second phase: W tile (step mode) and the X0 tile from the image
-          tx = static_cast<uint32_t>(2 * xs * chunk_bytes);
-          if (p.step_mode) {
-            if (S.wbulk) {
-              tma = true;
-              tx += static_cast<uint32_t>(m * 128 * (S.w_dtype == 0 ? 4 : 2));
-            } else {
-              copy_tile_in(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
-            }
-          }
+          copy_tile_in(p, S, S.g_dtype, S.G, ir.moff, gj0, cw1, st, lane);
+          if (step_mode) copy_tile_in(p, S, 0, S.Mom, ir.moff, gj0, cw1, st + L.mom_off, lane);
+        } else {
+          copy_tile_in(p, S, S.w_dtype, S.W, ir.moff, gj0, 128, st, lane);
         }
       }
       __syncwarp();
       if (lane == 0) {
         B->desc[rg.stage][0] = kind;
-        B->desc[rg.stage][1] = item;
+        B->desc[rg.stage][1] = data ? L.item : -1;
         B->desc[rg.stage][2] = c0;
         B->desc[rg.stage][3] = flags;
-        if (tx) {
-          const SmallSlice& S = p.s[ir.si];
-          const int z = ir.mat - S.mat_base;
-          int x, y;
-          tile_xy(S, ir.col0 + c0, x, y);
-          ptx::mbar_arrive_expect_tx(full, tx);
+        if (data && L.tx) {
+          // TMA coordinates of the tile at X column gj0 (X columns are the
+          // stored rows of a transposed matrix)
+          const int64_t gj0 = L.col0 + c0;
+          const int x = L.trans ? 0 : static_cast<int>(gj0);
+          const int y = L.trans ? static_cast<int>(gj0) : 0;
+          ptx::mbar_arrive_expect_tx(full, L.tx);
           if (kind == kStageP1) {
-            ptx::tma_load_3d(st, &p.tm[ir.si][0], full, x, y, z);
-            if (p.step_mode) ptx::tma_load_3d(st + mom_off(p, S), &p.tm[ir.si][1], full, x, y, z);
+            ptx::tma_load_3d(st, L.tm, full, x, y, L.z);
+            if (step_mode) ptx::tma_load_3d(st + L.mom_off, L.tm + 1, full, x, y, L.z);
           } else {
-            if (tma) ptx::tma_load_3d(st, &p.tm[ir.si][2], full, x, y, z);
-            ptx::bulk_load(st + p.x_off,
-                           p.ximg + static_cast<size_t>(item) * p.xbytes + (c0 / 64) * xs * chunk_bytes,
+            if (L.bulk) ptx::tma_load_3d(st, L.tm, full, x, y, L.z);
+            ptx::bulk_load(st + x_off, L.img + (c0 / 64) * xs * chunk_bytes,
                            static_cast<uint32_t>(2 * xs * chunk_bytes), full);
           }
         } else {
@@ -900,6 +924,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       rg.next(NS);
       return true;
     };
+    const LoadPlan none;
     // First phase: items are claimed in increasing order from a launch-wide
     // counter, so a CTA that spends time on a Gram-space step simply takes
     // fewer items.
@@ -907,15 +932,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       int item = -1;
       if (lane == 0) {
         const unsigned c = atomicAdd(lctr + 2, 1u);
-        if (c < static_cast<unsigned>(p.items)) item = static_cast<int>(c);
+        if (c < static_cast<unsigned>(n_items)) item = static_cast<int>(c);
       }
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item < 0) break;
+      const LoadPlan L = make_plan(kStageP1, item);
       for (int s = 0; s < s1 && ok; ++s)
-        ok = put(kStageP1, item, s * p.cw1, (s == 0 ? kFirst : 0) | (s == s1 - 1 ? kLast : 0));
+        ok = put(kStageP1, L, s * cw1, (s == 0 ? kFirst : 0) | (s == s1 - 1 ? kLast : 0));
       if (!ok) break;
     }
-    if (ok) ok = put(kStageP1End, -1, 0, 0);
+    if (ok) ok = put(kStageP1End, none, 0, 0);
     // Second phase: work is claimed in the order matrices were published
     // (position j of the ready list, block blk, part sub of the block), so no
     // CTA waits for a late matrix while published work remains.  A claim is
@@ -923,18 +949,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     // work spreads over more CTAs at the end of the launch.
     const int tpc = p.p2_tiles;                       // tiles per claim
     const int parts = (tiles + tpc - 1) / tpc;        // claims per item
+    const unsigned per = static_cast<unsigned>(nb * parts);
     for (int k = 0; ok; ++k) {
       const int b = k & 1;
       int item = -1, t0 = 0;
       if (lane == 0) {
         const unsigned next = atomicAdd(lctr + 1, 1u);
-        const unsigned per = static_cast<unsigned>(p.nb * parts);
         const int j = static_cast<int>(next / per);
-        if (j < p.total_mats) {
-          const int mat = wait_ready_pos(p.ready_list, j, p.epoch, ctx);
+        if (j < total_mats) {
+          const int mat = wait_ready_pos(ready_list, j, epoch, ctx);
           const int rem = static_cast<int>(next - j * per);
           if (mat >= 0) {
-            item = mat * p.nb + rem / parts;
+            item = mat * nb + rem / parts;
             t0 = (rem % parts) * tpc;
           }
         }
@@ -942,20 +968,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         if (item >= 0 && !mwait(&B->q_free[b], ((k >> 1) & 1) ^ 1u, ctx)) item = -1;
         if (item >= 0) {
           ptx::fence_proxy_async_global();
-          ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(p.qbytes));
-          ptx::bulk_load(sm + p.off_q + b * p.qbytes,
-                         p.qimg + static_cast<size_t>(item / p.nb) * p.qbytes,
-                         static_cast<uint32_t>(p.qbytes), &B->q_full[b]);
+          ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(qbytes));
+          ptx::bulk_load(sm + off_q + b * qbytes, qimg + static_cast<size_t>(item / nb) * qbytes,
+                         static_cast<uint32_t>(qbytes), &B->q_full[b]);
         }
       }
       item = __shfl_sync(0xffffffffu, item, 0);
       t0 = __shfl_sync(0xffffffffu, t0, 0);
       if (item < 0) break;
+      const LoadPlan L = make_plan(kStageP2, item);
       const int t1 = min(tiles, t0 + tpc);
       for (int t = t0; t < t1 && ok; ++t)
-        ok = put(kStageP2, item, 128 * t, (t == t0 ? kFirst : 0) | (t == t1 - 1 ? kLast : 0));
+        ok = put(kStageP2, L, 128 * t, (t == t0 ? kFirst : 0) | (t == t1 - 1 ? kLast : 0));
     }
-    put(kStageEnd, -1, 0, 0);
+    put(kStageEnd, none, 0, 0);
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, ngram);
