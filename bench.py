@@ -53,7 +53,7 @@ def _peaks():
 # (kernel kind, workload), valid only while the kernel's sources hash to the
 # recorded value; otherwise the roofline reports traffic = null.
 TRAFFIC = {
-    ("fused_small", "c2"): {"bytes": 195.124224e6 + 124.621568e6, "src_hash": "53883cf3f35d17e1",
+    ("fused_small", "c2"): {"bytes": 195.644160e6 + 124.335872e6, "src_hash": "c0175907812ed96d",
                             "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h"),
                             "profile": "profiles/ns_small_c2_74x24x10240.md"},
 }
