@@ -280,6 +280,9 @@ def main():
                     help="c4 only: number of Llama layers (default 32; a small profiling case)")
     ap.add_argument("--adamw", action="store_true",
                     help="time the AdamW kernel on the Llama-3-8B non-matrix parameters instead")
+    ap.add_argument("--adamw-rows", type=int, default=128256,
+                    help="rows of the embedding and output head in the AdamW workload "
+                         "(a smaller value gives a case small enough for a full profiler capture)")
     ap.add_argument("--owners", type=int, default=0,
                     help="report the owner-assignment balance of the Llama-3-8B matrices for N ranks")
     ap.add_argument("--experts", type=int, default=None,
@@ -406,7 +409,8 @@ def _adamw_bench(args, local):
     import torch
     from newton_schulz_gb300 import binding
     dev = torch.device("cuda", local)
-    sizes = [128256 * 4096, 128256 * 4096] + [4096] * 65
+    rows = args.adamw_rows
+    sizes = [rows * 4096, rows * 4096] + [4096] * 65
     gen = torch.Generator(device=dev).manual_seed(7)
     ts = []
     for n in sizes:
@@ -439,7 +443,7 @@ def _adamw_bench(args, local):
         "metric": "AdamW step over the non-matrix parameters (GB/s of algorithmic traffic)",
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "Llama-3-8B non-matrix parameters: 2 x [128256 x 4096] + 65 x [4096]",
+        "config": {"workload": f"Llama-3-8B non-matrix parameters: 2 x [{rows} x 4096] + 65 x [4096]",
                    "elements": elems, "l2": "512 MiB L2 flush between timed steps (outside events)"},
         "gpu_launches": args.steps * binding.muon_last_launch_count(),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
