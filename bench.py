@@ -280,6 +280,8 @@ def main():
                     help="c4 only: number of Llama layers (default 32; a small profiling case)")
     ap.add_argument("--adamw", action="store_true",
                     help="time the AdamW kernel on the Llama-3-8B non-matrix parameters instead")
+    ap.add_argument("--no-ns-only", action="store_true",
+                    help="skip the NS-only measurement (muon_ns_batched_ex on the same gradients)")
     ap.add_argument("--adamw-rows", type=int, default=128256,
                     help="rows of the embedding and output head in the AdamW workload "
                          "(a smaller value gives a case small enough for a full profiler capture)")
@@ -490,11 +492,54 @@ def _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, 
     if not args.no_e2e:
         e2e = _end_to_end(args, groups, step, stream, flush, world, dev)
 
+    # ---- NS alone: muon_ns_batched_ex over the same gradients --------------------------
+    ns_only = None
+    if not args.no_ns_only:
+        ns_only = _ns_only(args, groups, stream, flush, flops, world, dev)
+
     st = binding.muon_query_status()
     if st != 0:
         raise SystemExit(f"device status {binding.muon_status_string(st)} after timing")
-    return _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
+    line = _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
                    launches_per_step)
+    line["ns_only"] = ns_only
+    return line
+
+
+def _ns_only(args, groups, stream, flush, flops, world, dev):
+    """Newton-Schulz alone through muon_ns_batched_ex (fp32 or bf16 input, bf16
+    output): the step's gradients, same-shape tensors stacked into one
+    [B, M, N] batch per shape outside the timed region, one call per shape,
+    timed like the step.  Not counted in gpu_launches (its own region)."""
+    import torch
+    from newton_schulz_gb300 import binding
+    by_shape = {}
+    for g in groups:
+        x = g["G"] if g["G"].dim() == 3 else g["G"].unsqueeze(0)
+        by_shape.setdefault((tuple(x.shape[1:]), x.dtype), []).append(x)
+    xs = [torch.cat(v, 0).contiguous() for v in by_shape.values()]
+    outs = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for x in xs]
+    ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for x, o in zip(xs, outs):
+            binding.muon_ns_batched_ex(x, out=o, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(a.elapsed_time(b))
+    t = statistics.median(ms)
+    del xs, outs
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return {"ms_per_step": t, "value": world * flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "calls_per_step": len(by_shape),
+            "what": "muon_ns_batched_ex on the step's gradients, one call per shape"}
 
 
 def _end_to_end(args, groups, step, stream, flush, world, dev):
