@@ -172,7 +172,7 @@ muon_status_t muon_step_grouped_ex(const muon_group_t *groups, int n_groups, flo
  * arguments and errors as muon_step_grouped_ex, with host pointers; pinned
  * (page-locked) memory lets the copies run asynchronously and overlap.  The
  * library cuts the matrices into up to 8 chunks (MUON_HOST_CHUNKS overrides
- * the 8) of at least 40 MB, the first and last half the size of the others
+ * the 8) of at least 20 MB, the first and last half the size of the others
  * (the pipeline's fill and drain), and moves
  * each through one of three device slots it owns: copy-in, the step, and
  * copy-out of W' and Mom' run on three internal streams so the two copy
