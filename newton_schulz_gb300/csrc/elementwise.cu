@@ -62,11 +62,23 @@ __device__ __forceinline__ uint4 pack8_bf16_lo(const float* d) {
   return pack8_bf16(r);
 }
 
+// The slice that block `blk` belongs to: the last one whose first block is
+// at or before it.  The launch's first-block table is read into shared memory
+// by the block's threads in parallel (indexed reads of the parameter block
+// are generic loads; a scan would chain one per slice), then searched there.
+// Every thread of the block must call it (it holds a barrier).
 template <typename Slice>
 __device__ __forceinline__ int find_slice(const Slice* s, int n, int blk) {
-  int i = 0;
-  while (i + 1 < n && blk >= s[i + 1].tile_base) ++i;
-  return i;
+  __shared__ int base[kMaxSlices];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) base[i] = s[i].tile_base;
+  __syncthreads();
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= blk) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 }  // namespace
