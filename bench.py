@@ -1,17 +1,36 @@
 #!/usr/bin/env python3
 """Muon-step benchmark: ms per step and achieved TFLOP/s on one GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2|c1|c3|c4|c5]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1|c2|c3|c4|c5]
                     [--impl ours|reference]
 
 One step = momentum -> Newton-Schulz (5 steps) -> decoupled-decay update over
-the whole workload, through the C ABI (libmuon).  ``value`` is the achieved
-nominal TFLOP/s (sum over matrices of 5*(4 m^2 n + 2 m^3), m <= n) divided by
-the device time of a step, inputs resident in HBM; ``e2e`` is the same metric
-through the host-memory entry point (muon_step_grouped_host): W, G and Mom
-start in pinned host memory and W', Mom' end there, the library's chunked
-copy-in / step / copy-out pipeline inside the timed region.  Between timed steps a 512 MiB
-buffer is written to flush the 129 MB L2 (outside the timed events).
+the whole workload, through the C ABI (libmuon).  With no --config the run
+times all five workloads and prints ONE JSON line: its headline is the large
+compute-bound sweep (c5: 8 x [8192,28672], 10 x [8192,8192], 4 x
+[16384,16384], the largest single-GPU workload), timed over exactly K steps
+after W warm-up steps; the other four sit under ``per_config`` with the same
+fields (the Llama-3-8B-shaped c4 over min(K, 10) steps after 3 warm-ups, the
+others over K after W).  ``--config`` times one workload alone.
+
+Per workload:
+* ``value`` -- nominal TFLOP/s: sum over matrices of 5 (4 m^2 n + 2 m^3)
+  (m <= n) over the device time of a step, inputs resident in HBM;
+* ``alg`` -- the same time against the algorithmic flops of the symmetric
+  products, 5 (m (m+1) n + m^2 (m+1) + 2 m^2 n), and that rate as a fraction
+  of the measured dense bf16 peak (sustained when the timed region lasts
+  more than a second, else burst);
+* ``roofline`` -- the dominant kernel's achieved rate (algorithmic bytes or
+  flops per launch over its CUDA-event time) against the measured peak;
+* ``e2e`` -- the same metric through the host-memory entry point
+  (muon_step_grouped_host): W, G and Mom start in pinned host memory and W',
+  Mom' end there, the library's chunked copy-in / step / copy-out pipeline
+  inside the timed region;
+* ``cpu_baseline`` -- the float64 oracle on the host cores on a bounded
+  sample of the workload's own matrices, extrapolated to the whole workload
+  (per core shape, by nominal flops) where the sample is not all of it.
+Between timed steps a 512 MiB buffer is written to flush the 129 MB L2
+(outside the timed events).
 
 ``--impl reference`` times the float64 CPU oracle (the deliberately slow
 reference) on a bounded sample of the same workload.
@@ -33,6 +52,8 @@ sys.path.insert(0, ROOT)
 METRIC = "Muon step ms & achieved TFLOP/s vs GB300 bf16 peak (per config, 1 GPU)"
 HP = dict(mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
 STEPS_NS = 5
+HEADLINE = "c5"
+OTHERS = ("c1", "c2", "c3", "c4")
 
 
 def _peaks():
@@ -49,13 +70,12 @@ def _peaks():
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# one ncu capture of the dominant kernel (summaries in profiles/), keyed by
-# (kernel kind, workload), valid only while the kernel's sources hash to the
-# recorded value; otherwise the roofline reports traffic = null.
+# one ncu capture of the dominant kernel, keyed by (kernel kind, workload),
+# valid only while the kernel's sources hash to the recorded value; otherwise
+# the roofline reports traffic = null.
 TRAFFIC = {
     ("fused_small", "c2"): {"bytes": 195.644160e6 + 124.335872e6, "src_hash": "c0175907812ed96d",
-                            "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h"),
-                            "profile": "profiles/ns_small_c2_74x24x10240.md"},
+                            "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h")},
 }
 
 
@@ -80,11 +100,23 @@ def _shapes(groups):
     return out
 
 
+def ns_flops(r, c, steps=STEPS_NS):
+    """Nominal flops of NS on one [r, c] matrix: steps (4 m^2 n + 2 m^3)."""
+    m, n = min(r, c), max(r, c)
+    return steps * (4 * m * m * n + 2 * m ** 3)
+
+
 def nominal_flops(shapes, steps=STEPS_NS):
+    return sum(b * ns_flops(r, c, steps) for b, r, c, _, _ in shapes)
+
+
+def alg_flops(shapes, steps=STEPS_NS):
+    """Algorithmic flops with the symmetric products formed once:
+    steps (m (m+1) n + m^2 (m+1) + 2 m^2 n) per matrix."""
     f = 0
     for b, r, c, _, _ in shapes:
         m, n = min(r, c), max(r, c)
-        f += b * steps * (4 * m * m * n + 2 * m ** 3)
+        f += b * steps * (m * (m + 1) * n + m * m * (m + 1) + 2 * m * m * n)
     return f
 
 
@@ -171,170 +203,174 @@ def _dist_env():
     return world, rank, local
 
 
-def run_reference(args, world, rank):
-    """The float64 oracle on the host cores, on a bounded sample per step."""
-    import numpy as np
+# ---- workloads -------------------------------------------------------------------------
+def make_workload(name, dev, args):
+    from newton_schulz_gb300 import synth
+    if name == "c4" and args.layers:
+        return synth.config_c4(dev, layers=args.layers)
+    if name == "c5" and args.scale_down > 1:
+        return synth.config_c5(dev, scale_down=args.scale_down)
+    if name == "c3" and args.experts:
+        return synth.config_c3(dev, experts=args.experts)
+    return synth.CONFIGS[name](dev)
+
+
+def workload_name(name, args):
+    from newton_schulz_gb300 import synth
+    s = synth.WORKLOAD_NAMES[name]
+    if name == "c4" and args.layers:
+        s += f" [{args.layers} layers]"
+    if name == "c3" and args.experts:
+        s += f" [{args.experts} experts]"
+    if name == "c5" and args.scale_down > 1:
+        s += f" [dims / {args.scale_down}]"
+    return s
+
+
+# ---- float64 oracle baseline ---------------------------------------------------------
+# Which matrices of each workload the oracle times inside the bench (its own
+# matrices, copied to the host before the first step): all of the two small
+# workloads, 8 experts of each MoE weight, one matrix per core shape of the
+# Llama-3-8B shapes, and one [8192, 8192] matrix of the large sweep (one
+# 16384^2 matrix alone is ~1.3e14 flops, minutes on the host cores).  The
+# other matrices of a workload are extrapolated: the measured time of their
+# core shape, or, for core shapes not timed, their nominal flops at the
+# sample's rate.
+def oracle_sample_index(name, groups):
+    if name in ("c1", "c2"):
+        return [(gi, b) for gi, g in enumerate(groups) for b in range(g["W"].shape[0])]
+    if name == "c3":
+        return [(gi, b) for gi in range(len(groups)) for b in range(0, groups[gi]["W"].shape[0], 16)]
+    if name == "c4":
+        pick, seen = [], set()
+        for gi, g in enumerate(groups):
+            r, c = g["W"].shape[-2:]
+            core = (min(r, c), max(r, c))
+            if core not in seen:
+                seen.add(core)
+                pick.append((gi, 0))
+        return pick
+    # c5: one matrix of the second group ([8192, 8192] at full size)
+    return [(1, 0)]
+
+
+def oracle_samples(name, groups):
+    idx = oracle_sample_index(name, groups)
+    out = []
+    for gi, b in idx:
+        g = groups[gi]
+        out.append({k: (g[k][b] if g[k].dim() == 3 else g[k]).detach().double().cpu().numpy()
+                    for k in ("W", "G", "Mom")})
+    return out
+
+
+def cpu_baseline(name, samples, shapes):
+    """Oracle seconds on the sample, per core shape, extrapolated to the
+    workload's ms per step and nominal TFLOP/s."""
+    from oracle import muon_ref as R
+    cores = len(os.sched_getaffinity(0))
+    per_core = {}
+    done_flops, t_total = 0, 0.0
+    for x in samples:
+        r, c = x["W"].shape
+        t0 = time.perf_counter()
+        R.muon_step_ref(x["W"], x["G"], x["Mom"], **HP)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        done_flops += ns_flops(r, c)
+        per_core.setdefault((min(r, c), max(r, c)), []).append(dt)
+    rate = done_flops / t_total                  # flop/s of the oracle on the sample
+    total_mats = sum(b for b, _, _, _, _ in shapes)
+    ms, timed_mats = 0.0, 0
+    for b, r, c, _, _ in shapes:
+        core = (min(r, c), max(r, c))
+        if core in per_core:
+            ms += b * statistics.mean(per_core[core]) * 1e3
+            timed_mats += b
+        else:
+            ms += b * ns_flops(r, c) / rate * 1e3
+    flops = nominal_flops(shapes)
+    extrapolated = len(samples) < total_mats
+    desc = ", ".join(f"{len(v)} x {k[0]}x{k[1]}" for k, v in per_core.items())
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "extrapolated": extrapolated, "ms_per_step": ms,
+            "sample": (f"{len(samples)} of {total_mats} matrices ({desc}), "
+                       f"{t_total:.1f} s of float64 NumPy"
+                       + ("; the rest extrapolated per core shape (untimed core shapes by "
+                          "nominal flops at the sample's rate)" if extrapolated else ""))}
+
+
+# ---- reference arm -------------------------------------------------------------------------
+def _sample_groups_cpu(config):
+    """CPU stand-ins with the workload's shapes and value distributions (the
+    workload's own values come from the GPU's generator)."""
     import torch
     from newton_schulz_gb300 import synth
-    from oracle import muon_ref as R
+    if config in ("c1", "c2"):
+        return synth.CONFIGS[config]("cpu")
+    if config == "c3":
+        return [synth.random_group((1, r, c), torch.bfloat16, torch.float32, "cpu", r, 1e-3)
+                for r, c in ((2048, 768), (768, 2048))]
+    if config == "c4":
+        return [synth.random_group((1, 4096, 4096), torch.bfloat16, torch.bfloat16, "cpu", 4,
+                                   1e-3)]
+    return [synth.random_group((1, 8192, 8192), torch.bfloat16, torch.float32, "cpu", 5, 1.0)]
 
+
+def run_reference(args, world, rank):
+    """The float64 oracle on the host cores, on a bounded sample per step:
+    c1 whole; c2 8 of its 74 matrices; c3 one expert of each weight; c4 one
+    [4096, 4096] matrix; c5 one [8192, 8192] matrix with one of its five NS
+    iterations (a whole matrix is ~30 s there).  The rate is the sample's
+    nominal flops over its time."""
+    from oracle import muon_ref as R
     if rank != 0:
         return
+    name = args.config or HEADLINE
     cores = len(os.sched_getaffinity(0))
-    # bounded sample: a few matrices of each group of the workload
-    groups = synth.CONFIGS[args.config]("cpu") if args.config in ("c1", "c2") else None
-    if groups is None:
-        groups = _sample_groups_cpu(args.config)
-    shapes = _shapes(groups)
+    groups = _sample_groups_cpu(name)
+    ns_steps = 1 if name == "c5" else STEPS_NS
+    keep = 8 if name == "c2" else None
     sample = []
-    budget = {"c1": 5, "c2": 8, "c3": 2, "c4": 1, "c5": 1}[args.config]
-    for g, (b, r, c, _, _) in zip(groups, shapes):
-        k = min(b, budget)
+    for g in groups:
+        k = g["W"].shape[0] if keep is None else min(keep, g["W"].shape[0])
         sample.append({k2: g[k2][:k].double().numpy() for k2 in ("W", "G", "Mom")})
-    s_shapes = [(x["W"].shape[0], x["W"].shape[1], x["W"].shape[2], 4, 4) for x in sample]
-    flops = nominal_flops(s_shapes)
+    flops = sum(x["W"].shape[0] * ns_flops(x["W"].shape[1], x["W"].shape[2], ns_steps)
+                for x in sample)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         for x in sample:
-            R.muon_step_ref(x["W"], x["G"], x["Mom"], **HP)
+            R.muon_step_ref(x["W"], x["G"], x["Mom"], steps=ns_steps, **HP)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
     t = statistics.median(times)
     tf = flops / t / 1e12
-    sample_desc = "; ".join(f"{x['W'].shape[0]}x[{x['W'].shape[1]},{x['W'].shape[2]}]"
-                            for x in sample)
+    desc = "; ".join(f"{x['W'].shape[0]}x[{x['W'].shape[1]},{x['W'].shape[2]}]" for x in sample)
+    if ns_steps != STEPS_NS:
+        desc += f" with {ns_steps} of the {STEPS_NS} NS iterations"
     line = {
         "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": synth.WORKLOAD_NAMES[args.config], "sample": sample_desc},
+        "config": {"workload": workload_name(name, args), "config": name, "sample": desc},
         "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": sample_desc},
+                         "sample": desc},
         "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def _sample_groups_cpu(config):
-    """Small CPU stand-ins with the workload's shapes (for the oracle only)."""
+# ---- measurement of one workload ------------------------------------------------------
+def measure(name, steps, warmup, args, world, dev, local, with_cpu):
     import torch
-    from newton_schulz_gb300 import synth
-    if config == "c3":
-        out = []
-        for r, c in ((2048, 768), (768, 2048)):
-            out.append(synth.random_group((2, r, c), torch.bfloat16, torch.float32, "cpu", r, 1e-3))
-        return out
-    if config == "c4":
-        return [synth.random_group((1, r, c), torch.bfloat16, torch.bfloat16, "cpu", i, 1e-3)
-                for i, (r, c) in enumerate(((4096, 4096), (1024, 4096), (14336, 4096)))]
-    return [synth.random_group((1, 8192, 8192), torch.bfloat16, torch.float32, "cpu", 5, 1.0)]
-
-
-def cpu_baseline_sample(config, budget_s=12.0):
-    """Oracle seconds per step on a bounded sample, scaled to the whole workload."""
-    import torch
-    from newton_schulz_gb300 import synth
-    from oracle import muon_ref as R
-    cores = len(os.sched_getaffinity(0))
-    if config in ("c1", "c2"):
-        groups = synth.CONFIGS[config]("cpu")
-    else:
-        groups = _sample_groups_cpu(config)
-    done_flops, t_total, n_mats, desc = 0, 0.0, 0, []
-    for g in groups:
-        b = g["W"].shape[0] if g["W"].dim() == 3 else 1
-        for i in range(b):
-            x = {k: g[k][i].double().numpy() for k in ("W", "G", "Mom")}
-            t0 = time.perf_counter()
-            R.muon_step_ref(x["W"], x["G"], x["Mom"], **HP)
-            t_total += time.perf_counter() - t0
-            r, c = x["W"].shape
-            m, n = min(r, c), max(r, c)
-            done_flops += STEPS_NS * (4 * m * m * n + 2 * m ** 3)
-            n_mats += 1
-            if t_total > budget_s:
-                break
-        desc.append(f"{g['W'].shape}")
-        if t_total > budget_s:
-            break
-    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"{n_mats} matrices of {config} ({t_total:.1f} s, float64 NumPy)"}
-
-
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true",
-                    help="skip the host-buffer end-to-end pass (large workloads)")
-    ap.add_argument("--layers", type=int, default=None,
-                    help="c4 only: number of Llama layers (default 32; a small profiling case)")
-    ap.add_argument("--adamw", action="store_true",
-                    help="time the AdamW kernel on the Llama-3-8B non-matrix parameters instead")
-    ap.add_argument("--no-ns-only", action="store_true",
-                    help="skip the NS-only measurement (muon_ns_batched_ex on the same gradients)")
-    ap.add_argument("--adamw-rows", type=int, default=128256,
-                    help="rows of the embedding and output head in the AdamW workload "
-                         "(a smaller value gives a case small enough for a full profiler capture)")
-    ap.add_argument("--owners", type=int, default=0,
-                    help="report the owner-assignment balance of the Llama-3-8B matrices for N ranks")
-    ap.add_argument("--experts", type=int, default=None,
-                    help="c3 only: experts per weight (default 128; a small profiling case)")
-    ap.add_argument("--scale-down", type=int, default=1,
-                    help="c5 only: divide every dimension (a small profiling case)")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    world, rank, local = _dist_env()
-
-    if args.impl == "reference":
-        if world > 1:
-            import torch.distributed as dist
-            dist.init_process_group("gloo")
-        run_reference(args, world, rank)
-        if world > 1:
-            dist.destroy_process_group()
-        return
-
-    import torch
-    from newton_schulz_gb300 import binding, synth
-
-    if args.adamw:
-        torch.cuda.set_device(local)
-        binding.load()
-        _adamw_bench(args, local)
-        return
-    if args.owners:
-        torch.cuda.set_device(local)
-        binding.load()
-        _owners_report(args.owners)
-        return
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    binding.load()
-
-    if args.config == "c4" and args.layers:
-        groups = synth.config_c4(dev, layers=args.layers)
-    elif args.config == "c5" and args.scale_down > 1:
-        groups = synth.config_c5(dev, scale_down=args.scale_down)
-    elif args.config == "c3" and args.experts:
-        groups = synth.config_c3(dev, experts=args.experts)
-    else:
-        groups = synth.CONFIGS[args.config](dev)
+    from newton_schulz_gb300 import binding
+    groups = make_workload(name, dev, args)
+    samples = oracle_samples(name, groups) if with_cpu else None
     shapes = _shapes(groups)
-    flops = nominal_flops(shapes)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     arr = binding.make_groups(groups)
@@ -342,19 +378,198 @@ def main():
     def step():
         binding.muon_step_grouped(arr, stream=stream, **HP)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     st = binding.muon_query_status()
     if st != 0:
-        raise SystemExit(f"device status {binding.muon_status_string(st)} after warm-up")
+        raise SystemExit(f"{name}: device status {binding.muon_status_string(st)} after warm-up")
     launches_per_step = binding.muon_last_launch_count()
 
-    line = _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,
-                  launches_per_step)
-    _finish(line, world, rank)
+    # ---- device-resident timed region ------------------------------------------------
+    sampler = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    binding.muon_profile_enable(True)
+    binding.muon_profile_read()      # reset
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    prof = binding.muon_profile_read()
+    binding.muon_profile_enable(False)
+    clocks = sampler.stop()
+    t_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+
+    e2e = None if args.no_e2e else _end_to_end(groups, stream, flush, steps, warmup, world, dev)
+    ns_only = None if args.no_ns_only else _ns_only(groups, stream, flush, steps, warmup, world,
+                                                   dev, nominal_flops(shapes))
+    st = binding.muon_query_status()
+    if st != 0:
+        raise SystemExit(f"{name}: device status {binding.muon_status_string(st)} after timing")
+    line = _report(name, args, steps, warmup, world, shapes, t_ms, e2e, prof, clocks,
+                   launches_per_step)
+    line["ns_only"] = ns_only
+    del groups, arr, flush
+    torch.cuda.empty_cache()
+    if samples is not None:
+        line["cpu_baseline"] = cpu_baseline(name, samples, shapes)
+    return line
 
 
+def _ns_only(groups, stream, flush, steps, warmup, world, dev, flops):
+    """Newton-Schulz alone through muon_ns_batched_ex (fp32 or bf16 input, bf16
+    output): the step's gradients, same-shape tensors stacked into one
+    [B, M, N] batch per shape outside the timed region, one call per shape,
+    timed like the step.  Not counted in gpu_launches (its own region)."""
+    import torch
+    from newton_schulz_gb300 import binding
+    by_shape = {}
+    for g in groups:
+        x = g["G"] if g["G"].dim() == 3 else g["G"].unsqueeze(0)
+        by_shape.setdefault((tuple(x.shape[1:]), x.dtype), []).append(x)
+    xs = [torch.cat(v, 0).contiguous() for v in by_shape.values()]
+    outs = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for x in xs]
+    ms = []
+    for i in range(warmup + steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for x, o in zip(xs, outs):
+            binding.muon_ns_batched_ex(x, out=o, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            ms.append(a.elapsed_time(b))
+    t = statistics.median(ms)
+    del xs, outs
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return {"ms_per_step": t, "value": world * flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "calls_per_step": len(by_shape),
+            "what": "muon_ns_batched_ex on the step's gradients, one call per shape"}
+
+
+def _end_to_end(groups, stream, flush, steps, warmup, world, dev):
+    """The step through the host-memory entry point: W, G and Mom start and
+    end in pinned host memory; the library's copy-in, step and copy-out (the
+    chunked pipeline of muon_step_grouped_host) are all inside the timed
+    region."""
+    import torch
+    from newton_schulz_gb300 import binding
+    host = []
+    for g in groups:
+        h = {}
+        for k in ("W", "G", "Mom"):
+            h[k] = torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True)
+            h[k].copy_(g[k])
+        host.append(h)
+    harr = binding.make_groups(host)
+    h2d = sum(h[k].numel() * h[k].element_size() for h in host for k in ("W", "G", "Mom"))
+    d2h = sum(h[k].numel() * h[k].element_size() for h in host for k in ("W", "Mom"))
+    e2e_ms = []
+    for i in range(warmup + max(3, steps // 2)):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.muon_step_grouped_host(harr, stream=stream, **HP)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_t = statistics.median(e2e_ms)
+    del host, harr
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_t], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_t = float(t.item())
+    return {"ms": e2e_t, "h2d": h2d, "d2h": d2h, "steps": max(3, steps // 2)}
+
+
+def _report(name, args, steps, warmup, world, shapes, t_ms, e2e, prof, clocks,
+            launches_per_step):
+    peaks = _peaks()
+    flops = nominal_flops(shapes)
+    # a timed region of seconds runs under the power cap like the sustained
+    # GEMM measurement; shorter ones compare with the burst figure
+    sustained = t_ms * steps > 1000.0
+    tpeak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    peak_kind = "sustained" if sustained else "burst"
+    # ---- roofline of the dominant kernel ------------------------------------------------
+    kinds = {k: (ms / max(1, n), n) for k, (ms, n) in prof.items() if n}
+    per_step_ms = {k: prof[k][0] / steps for k in prof}
+    dom = max(per_step_ms, key=per_step_ms.get)
+    avg_ms, n_launch = kinds[dom]
+    byt = algorithmic_bytes(shapes)
+    fl = gemm_flops_per_kind(shapes)
+    launches_kind = n_launch / steps
+    if dom in ("prep", "update", "fused_small"):
+        per_launch = byt[dom] / launches_kind
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(dom, name),
+                "algorithmic_bytes": per_launch, "kernel": dom, "peak_source": peaks["source"]}
+    else:
+        per_launch = fl[dom] / launches_kind
+        achieved = per_launch / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": achieved / tpeak,
+                "traffic": _traffic(dom, name), "algorithmic_flops": per_launch,
+                "kernel": dom, "peak_source": peaks["source"], "peak_kind": peak_kind}
+    per_kind = {}
+    for k, (avg, n) in kinds.items():
+        lk = n / steps
+        if k in byt:
+            a = byt[k] / lk / (avg * 1e-3) / 1e9
+            per_kind[k] = {"avg_ms": avg, "GB/s": round(a, 1),
+                           "frac": round(a / peaks["hbm_gbs"], 4)}
+        elif k in fl:
+            a = fl[k] / lk / (avg * 1e-3) / 1e12
+            per_kind[k] = {"avg_ms": avg, "TFLOP/s": round(a, 1), "frac": round(a / tpeak, 4)}
+    fa = alg_flops(shapes)
+    alg = world * fa / (t_ms * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": world * flops / (t_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": t_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_name(name, args), "config": name,
+                   "matrices": sum(s[0] for s in shapes), "nominal_gflop_per_step": flops / 1e9,
+                   "alg_gflop_per_step": fa / 1e9,
+                   "l2": "512 MiB L2 flush between timed steps (outside events)",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "alg": {"value": alg, "unit": "TFLOP/s", "peak": tpeak, "peak_kind": peak_kind,
+                "frac": alg / (world * tpeak),
+                "what": "algorithmic flops (symmetric products once) over the step time"},
+        "e2e": None if e2e is None else {
+            "value": world * flops / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": e2e["ms"], "steps": e2e["steps"],
+            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": launches_per_step * steps,
+        "launches_per_step": launches_per_step,
+        "kernel_ms_per_step": {k: round(v, 5) for k, v in per_step_ms.items()},
+        "roofline": roof,
+        "kernels": per_kind,
+        "clocks": clocks,
+    }
+
+
+# ---- extra reports -------------------------------------------------------------------------
 def _owners_report(n_ranks):
     """Owner assignment across n_ranks with NS times measured per shape on
     this GPU (one assignment unit per matrix, byte cap eps = 0.1): the busiest
@@ -379,6 +594,7 @@ def _owners_report(n_ranks):
             for o, c in zip(owner, cost):
                 t[o] += c
             return max(t) / (sum(t) / n_ranks)
+
         def bytes_ratio(owner):
             b = [0.0] * n_ranks
             for o, x in zip(owner, nbytes):
@@ -455,200 +671,76 @@ def _adamw_bench(args, local):
         "clocks": clocks}))
 
 
-def _timed(args, world, rank, local, dev, groups, shapes, flops, stream, flush, step,
-           launches_per_step):
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=None, choices=["c1", "c2", "c3", "c4", "c5"],
+                    help="time one workload alone (default: all five, the large sweep as "
+                         "the headline)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-ns-only", action="store_true",
+                    help="skip the NS-only measurement (muon_ns_batched_ex on the same gradients)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="c4 only: number of Llama layers (default 32; a small profiling case)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="c3 only: experts per weight (default 128; a small profiling case)")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="c5 only: divide every dimension (a small profiling case)")
+    ap.add_argument("--adamw", action="store_true",
+                    help="time the AdamW kernel on the Llama-3-8B non-matrix parameters instead")
+    ap.add_argument("--adamw-rows", type=int, default=128256,
+                    help="rows of the embedding and output head in the AdamW workload "
+                         "(a smaller value gives a case small enough for a full profiler capture)")
+    ap.add_argument("--owners", type=int, default=0,
+                    help="report the owner-assignment balance of the Llama-3-8B matrices for N ranks")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = _dist_env()
+
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, world, rank)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     import torch
     from newton_schulz_gb300 import binding
+
+    torch.cuda.set_device(local)
+    binding.load()
+    if args.adamw:
+        _adamw_bench(args, local)
+        return
+    if args.owners:
+        _owners_report(args.owners)
+        return
+    dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
-    # ---- device-resident timed region ------------------------------------------------
-    sampler = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    binding.muon_profile_enable(True)
-    binding.muon_profile_read()      # reset
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    prof = binding.muon_profile_read()
-    binding.muon_profile_enable(False)
-    clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    t_ms = statistics.median(step_ms)
-    if world > 1:
-        t = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
-
-    # ---- end to end: pinned host inputs in, results out, through the C ABI ------------
-    e2e = None
-    if not args.no_e2e:
-        e2e = _end_to_end(args, groups, step, stream, flush, world, dev)
-
-    # ---- NS alone: muon_ns_batched_ex over the same gradients --------------------------
-    ns_only = None
-    if not args.no_ns_only:
-        ns_only = _ns_only(args, groups, stream, flush, flops, world, dev)
-
-    st = binding.muon_query_status()
-    if st != 0:
-        raise SystemExit(f"device status {binding.muon_status_string(st)} after timing")
-    line = _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
-                   launches_per_step)
-    line["ns_only"] = ns_only
-    return line
-
-
-def _ns_only(args, groups, stream, flush, flops, world, dev):
-    """Newton-Schulz alone through muon_ns_batched_ex (fp32 or bf16 input, bf16
-    output): the step's gradients, same-shape tensors stacked into one
-    [B, M, N] batch per shape outside the timed region, one call per shape,
-    timed like the step.  Not counted in gpu_launches (its own region)."""
-    import torch
-    from newton_schulz_gb300 import binding
-    by_shape = {}
-    for g in groups:
-        x = g["G"] if g["G"].dim() == 3 else g["G"].unsqueeze(0)
-        by_shape.setdefault((tuple(x.shape[1:]), x.dtype), []).append(x)
-    xs = [torch.cat(v, 0).contiguous() for v in by_shape.values()]
-    outs = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for x in xs]
-    ms = []
-    for i in range(args.warmup + args.steps):
-        flush.fill_(float(i))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for x, o in zip(xs, outs):
-            binding.muon_ns_batched_ex(x, out=o, stream=stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            ms.append(a.elapsed_time(b))
-    t = statistics.median(ms)
-    del xs, outs
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
-    return {"ms_per_step": t, "value": world * flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "calls_per_step": len(by_shape),
-            "what": "muon_ns_batched_ex on the step's gradients, one call per shape"}
-
-
-def _end_to_end(args, groups, step, stream, flush, world, dev):
-    """The step through the host-memory entry point: W, G and Mom start and
-    end in pinned host memory; the library's copy-in, step and copy-out (the
-    chunked pipeline of muon_step_grouped_host) are all inside the timed
-    region."""
-    import torch
-    from newton_schulz_gb300 import binding
-    host = [{k: g[k].to("cpu").pin_memory() for k in ("W", "G", "Mom")} for g in groups]
-    harr = binding.make_groups(host)
-    h2d = sum(h[k].numel() * h[k].element_size() for h in host for k in ("W", "G", "Mom"))
-    d2h = sum(h[k].numel() * h[k].element_size() for h in host for k in ("W", "Mom"))
-    e2e_ms = []
-    for i in range(args.warmup + max(3, args.steps // 2)):
-        flush.fill_(float(i))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        binding.muon_step_grouped_host(harr, stream=stream, **HP)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(a.elapsed_time(b))
-    e2e_t = statistics.median(e2e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_t], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
-    return {"ms": e2e_t, "h2d": h2d, "d2h": d2h}
-
-
-def _report(args, world, rank, groups, shapes, flops, t_ms, e2e, prof, clocks,
-            launches_per_step):
-    from newton_schulz_gb300 import synth
-    # ---- roofline of the dominant kernel ------------------------------------------------
-    peaks = _peaks()
-    kinds = {k: (ms / max(1, n), n) for k, (ms, n) in prof.items() if n}
-    per_step_ms = {k: prof[k][0] / args.steps for k in prof}
-    dom = max(per_step_ms, key=per_step_ms.get)
-    avg_ms, n_launch = kinds[dom]
-    byt = algorithmic_bytes(shapes)
-    fl = gemm_flops_per_kind(shapes)
-    launches_kind = n_launch / args.steps
-    if dom in ("prep", "update", "fused_small"):
-        per_launch = byt[dom] / launches_kind
-        achieved = per_launch / (avg_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(dom, args.config),
-                "algorithmic_bytes": per_launch, "kernel": dom, "peak_source": peaks["source"]}
+        dist.init_process_group("nccl", device_id=dev)
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if args.config is None and world == 1:
+        per = {}
+        for name in OTHERS:
+            k, w = (min(args.steps, 10), 3) if name == "c4" else (args.steps, args.warmup)
+            per[name] = measure(name, k, w, args, world, dev, local, with_cpu)
+        line = measure(HEADLINE, args.steps, args.warmup, args, world, dev, local, with_cpu)
+        line["per_config"] = per
     else:
-        # a timed region of seconds runs under the power cap like the
-        # sustained GEMM measurement; shorter ones compare with the burst
-        sustained = t_ms * args.steps > 1000.0
-        tpeak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        per_launch = fl[dom] / launches_kind
-        achieved = per_launch / (avg_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak,
-                "unit": "TFLOP/s", "frac": achieved / tpeak,
-                "traffic": _traffic(dom, args.config), "algorithmic_flops": per_launch,
-                "kernel": dom, "peak_source": peaks["source"],
-                "peak_kind": "sustained" if sustained else "burst"}
-
-    per_kind = {}
-    for k, (avg, n) in kinds.items():
-        lk = n / args.steps
-        if k in byt:
-            a = byt[k] / lk / (avg * 1e-3) / 1e9
-            per_kind[k] = {"avg_ms": avg, "GB/s": round(a, 1), "frac": round(a / peaks["hbm_gbs"], 4)}
-        else:
-            a = fl[k] / lk / (avg * 1e-3) / 1e12
-            per_kind[k] = {"avg_ms": avg, "TFLOP/s": round(a, 1),
-                           "frac": round(a / roof["peak"] if roof["bound"] == "tensor"
-                                         else a / peaks["bf16_tflops"], 4)}
-    value = world * flops / (t_ms * 1e-3) / 1e12
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": synth.WORKLOAD_NAMES[args.config] + (
-                       f" [{args.layers} layers]" if args.config == "c4" and args.layers else "") + (
-                       f" [{args.experts} experts]" if args.config == "c3" and args.experts else "") + (
-                       f" [dims / {args.scale_down}]" if args.config == "c5" and args.scale_down > 1
-                       else ""), "config": args.config,
-                   "matrices": sum(s[0] for s in shapes), "nominal_gflop_per_step": flops / 1e9,
-                   "l2": "512 MiB L2 flush between timed steps (outside events)",
-                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
-        "e2e": None if e2e is None else {
-            "value": world * flops / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "ms_per_step": e2e["ms"], "h2d_bytes_per_step": e2e["h2d"],
-            "d2h_bytes_per_step": e2e["d2h"]},
-        "gpu_launches": launches_per_step * args.steps,
-        "launches_per_step": launches_per_step,
-        "kernel_ms_per_step": {k: round(v, 5) for k, v in per_step_ms.items()},
-        "roofline": roof,
-        "kernels": per_kind,
-        "clocks": clocks,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(args.config)
-    return line
-
-
-def _finish(line, world, rank):
+        line = measure(args.config or HEADLINE, args.steps, args.warmup, args, world, dev, local,
+                       with_cpu)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
-        import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
 

@@ -149,16 +149,25 @@ muon_status_t muon_step_grouped(const muon_group_t *groups, int n_groups, float 
  * workspace in one fixed 64 MiB device array inside the library, so it calls
  * no cudaMalloc, cudaFree or allocating library routine.  Every GPU that
  * loads the library holds those 64 MiB until the process exits.
- *   Same arguments and result as muon_ns_batched (bf16 X [B,M,N], in place,
- *   eps = 1e-7).  A problem whose workspace does not fit in the array
- *   (roughly 3*B*M*N + 2*B*min(M,N)^2 bf16 values plus split-K partials) is
- *   rejected with MUON_ERR_UNSUPPORTED before anything is enqueued.
+ *   Same arguments as muon_ns_batched (bf16 X [B,M,N], in place, eps = 1e-7);
+ *   the result agrees with muon_ns_batched within the bf16 NS tolerance
+ *   (every shape runs on the grouped GEMM path here, so not bit for bit).
+ *   Workspace, with m = min(M,N), n = max(M,N), m8 = m rounded up to 8:
+ *   two bf16 copies of the iterate (2*B*n*m8 values), the bf16 Gram and
+ *   polynomial matrices (2*B*m*m8 values), a few fp32 words per matrix and,
+ *   when few 128 x 256 tiles of the Gram would leave SMs idle, fp32 split-K
+ *   partials of 128*256 values per tile and split.  A problem that does not
+ *   fit in the 64 MiB is rejected with MUON_ERR_UNSUPPORTED before anything
+ *   is enqueued (e.g. [2, 1024, 1024] fits; [8, 1024, 1024] does not).
  *   The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
- *   All calls share the one array: calls that can overlap on the GPU (other
- *   streams, other host threads) race and must be serialised by the caller.
- *   Device-side conditions (a non-finite norm) are not reported through
- *   muon_query_status for this entry point. */
+ *   that device current and clears its status word; make that first call
+ *   before any stream capture.
+ *   All calls share the one array, which keeps the last call's contents:
+ *   calls that can overlap on the GPU (other streams, other host threads)
+ *   race and must be serialised by the caller.
+ *   Device-side conditions (a non-finite norm, a bounded wait that gave up)
+ *   go to a status word inside the array; muon_query_status reads and clears
+ *   it together with the allocating entry points' word, allocating nothing. */
 muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, int steps,
                                       float a, float b, float c, cudaStream_t stream);
 
@@ -257,6 +266,24 @@ muon_status_t muon_assign_owners(const muon_unit_t *units, int n_units, int n_ra
  * or MUON_ERR_NONFINITE; the first bit set wins in that order of severity).
  * The caller synchronises `stream` first; this call synchronises it again. */
 muon_status_t muon_query_status(cudaStream_t stream);
+
+/* Testing hook for the failure path of the device-side waits (no counterpart
+ * on the pages).  Every wait in the library's kernels is bounded by
+ * MUON_WAIT_TIMEOUT_MS (default 2000 ms); when one runs out, the kernel sets
+ * MUON_ERR_TIMEOUT in the status word, waits (bounded) for its own copies and
+ * MMAs in flight, frees its tensor memory and returns, so the CUDA context
+ * stays usable.  This call makes the NEXT launch of one kind stall on a wait
+ * that nothing satisfies, so that path can be tested without a GPU fault:
+ *   what = 1  the next grouped-GEMM launch (matrices with min(M,N) > 64, or
+ *             the allocation-free entry point): one CTA never arms one
+ *             pipeline stage, and its MMA issuer's wait on it runs out;
+ *   what = 2  the next small-m launch (min(M,N) <= 64): the launch's last
+ *             matrix is never published, and the waits for it run out;
+ *   what = 0  cancels a pending request.
+ * The stalled call's outputs are undefined; muon_query_status then returns
+ * MUON_ERR_TIMEOUT and re-zeroes the workspace counters, and later calls are
+ * unaffected.  Returns MUON_ERR_INVALID_ARGUMENT for any other value. */
+muon_status_t muon_debug_inject_stall(int what);
 
 /* Static, human-readable name of a status code. */
 const char *muon_status_string(muon_status_t status);

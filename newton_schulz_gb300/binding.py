@@ -29,7 +29,9 @@ EXPORTED = (
     "muon_step_grouped_ex", "muon_step_grouped_host", "muon_query_status", "muon_status_string",
     "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
     "muon_profile_read", "muon_adamw_grouped", "muon_ns_cost_table", "muon_assign_owners",
+    "muon_ns_batched_noalloc", "muon_debug_inject_stall",
 )
+INJECT_NONE, INJECT_GEMM, INJECT_SMALL = 0, 1, 2
 
 
 class MuonError(RuntimeError):
@@ -105,6 +107,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_assign_owners.restype = i32
     lib.muon_step_grouped_host.argtypes = lib.muon_step_grouped_ex.argtypes
     lib.muon_step_grouped_host.restype = i32
+    lib.muon_ns_batched_noalloc.argtypes = [vp, i64, i64, i64, ctypes.c_int, f32, f32, f32, vp]
+    lib.muon_ns_batched_noalloc.restype = i32
+    lib.muon_debug_inject_stall.argtypes = [ctypes.c_int]
+    lib.muon_debug_inject_stall.restype = i32
     lib.muon_query_status.argtypes = [vp]
     lib.muon_query_status.restype = i32
     lib.muon_status_string.argtypes = [i32]
@@ -184,6 +190,16 @@ def muon_ns_batched(X, steps: int = 5, a: float = 3.4445, b: float = -4.7750,
           "muon_ns_batched")
 
 
+def muon_ns_batched_noalloc(X, steps: int = 5, a: float = 3.4445, b: float = -4.7750,
+                            c: float = 2.0315, stream=None) -> None:
+    """As muon_ns_batched, with the library's fixed workspace array (the call
+    allocates no device memory)."""
+    _check_contig(X)
+    B, M, N = _shape3(X)
+    check(load().muon_ns_batched_noalloc(X.data_ptr(), B, M, N, steps, a, b, c,
+                                         _stream_ptr(stream)), "muon_ns_batched_noalloc")
+
+
 def muon_ns_batched_ex(X, cfg=None, out=None, stream=None) -> None:
     _check_contig(X)
     B, M, N = _shape3(X)
@@ -241,6 +257,12 @@ def muon_step_grouped_host(groups, mu: float = 0.95, nesterov: bool = True, lr: 
 
 def muon_query_status(stream=None) -> int:
     return load().muon_query_status(_stream_ptr(stream))
+
+
+def muon_debug_inject_stall(what: int) -> None:
+    """Testing hook: the next launch of kind `what` (INJECT_GEMM or
+    INJECT_SMALL) stalls on a wait nothing satisfies until its bound runs out."""
+    check(load().muon_debug_inject_stall(int(what)), "muon_debug_inject_stall")
 
 
 def muon_status_string(code: int) -> str:

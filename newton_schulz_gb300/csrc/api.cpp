@@ -10,6 +10,7 @@
 // memory-safe batch cap; MUON_WS_CAP overrides); one workspace, sized for the
 // largest chunk, is allocated once per (device, stream) and reused.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -73,6 +74,7 @@ struct HostPipe {
 };
 std::map<std::pair<int, cudaStream_t>, HostPipe> g_host;
 std::map<int, DevState> g_dev;
+std::atomic<int> g_inject{0};   // muon_debug_inject_stall: one pending request
 bool g_prof = false;
 std::vector<ProfRec> g_prof_recs;
 thread_local int t_last_launches = 0;
@@ -608,6 +610,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         sp.eps = ns.eps;
         sp.status = dev->status;
         sp.timeout_ns = timeout_ns0;
+        sp.inject = take_injected_stall(kInjectSmall);
       }
     }
   }
@@ -766,6 +769,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         gp.first = it == 0 ? 1 : 0;
         gp.status = dev->status;
         gp.timeout_ns = timeout_ns;
+        gp.inject = take_injected_stall(kInjectGemm);
         st = L.run(1 + phase, [&] { return launch_gemm(phase, gp, stream); });
         if (st != MUON_OK) return st;
       }
@@ -931,7 +935,8 @@ muon_status_t ns_impl(void* X, int dtype, int64_t B, int64_t M, int64_t N,
 
 // ---- host-resident state ------------------------------------------------------------
 // One Muon step over parameters whose W, G and Mom live in host memory.  The
-// matrices are cut into up to 8 chunks of at least 40 MB; chunk i moves
+// matrices are cut into up to 8 chunks of at least 20 MB (the first and last
+// half the size of the others: weights 1, 2, ..., 2, 1); chunk i moves
 // through device slot i % 3: copy-in on one stream, the step on a second,
 // copy-out (W', Mom') on a third, so that the two copy directions and the
 // kernels overlap.  Everything is ordered after the work already on
@@ -1247,6 +1252,13 @@ muon_status_t adamw_impl(const muon_adamw_group_t* groups, int n_groups,
 
 }  // namespace
 
+namespace muon {
+int take_injected_stall(int kind) {
+  int want = kind;
+  return g_inject.compare_exchange_strong(want, 0) ? 1 : 0;
+}
+}  // namespace muon
+
 extern "C" {
 
 muon_status_t muon_ns_default_config(muon_ns_config_t* cfg) {
@@ -1391,15 +1403,24 @@ muon_status_t muon_ns_cost_table(const int64_t* shapes, int n, const muon_ns_con
 muon_status_t muon_query_status(cudaStream_t stream) {
   try {
     std::lock_guard<std::mutex> lock(g_mu);
-    DevState* dev = nullptr;
-    muon_status_t st = dev_state(&dev);
-    if (st != MUON_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+    // Two words may hold device-detected conditions: the one of the
+    // allocating entry points (it exists once any of them ran here) and the
+    // allocation-free entry point's, inside its fixed array.  Reading them
+    // allocates nothing.
     unsigned v = 0;
-    if (cudaMemcpy(&v, dev->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
-      return MUON_ERR_CUDA;
+    auto it = g_dev.find(dev);
+    unsigned* words[2] = {it != g_dev.end() ? it->second.status : nullptr, noalloc_status_word(dev)};
+    for (unsigned* w : words) {
+      if (!w) continue;
+      unsigned x = 0;
+      if (cudaMemcpy(&x, w, sizeof(x), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+      if (x && cudaMemset(w, 0, sizeof(x)) != cudaSuccess) return MUON_ERR_CUDA;
+      v |= x;
+    }
     if (v) {
-      if (cudaMemset(dev->status, 0, sizeof(v)) != cudaSuccess) return MUON_ERR_CUDA;
       for (auto& kv : g_ws) kv.second.dirty = true;
     }
     if (v & kDevTimeout) return MUON_ERR_TIMEOUT;
@@ -1459,6 +1480,12 @@ void muon_release_workspace(void) {
 }
 
 int muon_last_launch_count(void) { return t_last_launches; }
+
+muon_status_t muon_debug_inject_stall(int what) {
+  if (what != 0 && what != kInjectGemm && what != kInjectSmall) return MUON_ERR_INVALID_ARGUMENT;
+  g_inject.store(what);
+  return MUON_OK;
+}
 
 int muon_profile_enable(int enable) {
   std::lock_guard<std::mutex> lock(g_mu);

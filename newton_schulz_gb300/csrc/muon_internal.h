@@ -112,6 +112,8 @@ struct GemmParams {
   int first;              // 1: operands are unnormalised, apply inv scale
   int deep;               // 1: 4-stage ring, one staging box per epilogue set
   int prec;               // 1: hi + lo operands, three K segments per product
+  int inject;             // testing hook: CTA 0 arms its first ring stage and issues no
+                          // copy for it, so the wait on it runs out (then the status bit)
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -208,6 +210,8 @@ struct SmallParams {
   unsigned* ctr;                // [kSmallCtrSlots][4]: per launch (slot epoch % slots)
                                 // ready-list length, claimed second- and first-phase items
   unsigned epoch;               // this launch's tag, never 0
+  int inject;                   // testing hook: the last matrix is never published, so
+                                // the waits for it run out (then the status bit)
   unsigned* status;
   unsigned long long timeout_ns;
   int cap;                      // matrices per arrive slot
@@ -255,6 +259,16 @@ inline int gemm_deep(int phase, int min_kblocks) {
   return (phase != kEpiPoly || min_kblocks >= 32) ? 1 : 0;
 }
 cudaError_t launch_small(const SmallParams& p, int grid, cudaStream_t s);
+
+// ---- failure-path testing hook (muon_debug_inject_stall) -------------------------
+constexpr int kInjectGemm = 1;    // the next grouped-GEMM launch stalls one ring stage
+constexpr int kInjectSmall = 2;   // the next small-m launch withholds one matrix
+// 1 (and the request is cleared) when a stall of `kind` was requested, else 0.
+int take_injected_stall(int kind);
+
+// Device address of the allocation-free entry point's status word on device
+// `dev`, or null before that entry point's first call there (noalloc.cu).
+unsigned* noalloc_status_word(int dev);
 int small_blocks_per_sm(int smem_bytes, bool precise);   // resident CTAs per SM, 0 on failure
 
 }  // namespace muon

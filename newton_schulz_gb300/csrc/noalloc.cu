@@ -13,6 +13,13 @@
 // The host cannot use g_scratch's name as a device address; its address is
 // taken once per device with cudaGetSymbolAddress (with that device current)
 // on the first call made on that device.
+//
+// The array starts with a status word (device-detected conditions: a
+// non-finite norm, a bounded wait that gave up).  It is cleared by the first
+// call on a device and by muon_query_status, which reads it; every other
+// call leaves it alone, so a condition stays visible until it is read.
+// Behind it come the per-call counters (cleared by every call) and the data
+// buffers of the grouped GEMM path.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
@@ -36,6 +43,7 @@ __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 std::mutex g_mu;
 char* g_base[kMaxDevices];
 int g_sms[kMaxDevices];
+bool g_status_clean[kMaxDevices];   // the first call on the device cleared the status word
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -66,6 +74,14 @@ muon_status_t scratch_base(char** base, int* sms) {
 
 }  // namespace
 
+namespace muon {
+unsigned* noalloc_status_word(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_status_clean[dev] ? reinterpret_cast<unsigned*>(g_base[dev]) : nullptr;
+}
+}  // namespace muon
+
 extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, int64_t N,
                                                  int steps, float a, float b, float c,
                                                  cudaStream_t stream) {
@@ -84,7 +100,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   const int num_kb = static_cast<int>(cdiv(n, bk));
   const int64_t prep_tiles = cdiv(m, kPrepTile) * cdiv(n, kPrepTile);
 
-  // Layout: [status | counters] (cleared every call) then the data buffers.
+  // Layout: status word, counters (cleared every call), data buffers.
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -94,7 +110,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   const size_t o_status = take(sizeof(unsigned));
   const size_t o_cnt = take(static_cast<size_t>(B) * 4);
   const size_t o_tcnt = take(static_cast<size_t>(B * tri) * 4);
-  const size_t zero_bytes = off;
+  const size_t zero_end = off;
   off = align_up(off, 1024);
   const size_t o_Xt0 = take(static_cast<size_t>(B * n * m_pad) * 2);
   const size_t o_Xt1 = take(static_cast<size_t>(B * n * m_pad) * 2);
@@ -102,7 +118,11 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   const size_t o_B = take(static_cast<size_t>(B * m * m_pad) * 2);
   const size_t o_inv = take(static_cast<size_t>(B) * 4);
   const size_t o_ssq = take(static_cast<size_t>(B * prep_tiles) * 4);
-  // split-K heuristic of the allocating path, so both give the same bits
+  // The split-K rule of the allocating path's grouped GEMMs (its cap
+  // included).  The results agree with muon_ns_batched within the NS
+  // tolerance, not bit for bit: that call also cuts large batches into
+  // chunks and sends core shapes with min(M, N) <= 64 to its Gram-space
+  // kernel, while this one runs every shape on the grouped GEMM path.
   char* base = nullptr;
   int sms = 0;
   muon_status_t st = scratch_base(&base, &sms);
@@ -112,6 +132,14 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   if (gram_tiles < target && num_kb >= 8) {
     ks = static_cast<int>(std::min<int64_t>(cdiv(target, gram_tiles), num_kb / 4));
     ks = ks < 1 ? 1 : ks;
+  }
+  {
+    int cap = 64;
+    if (const char* v = std::getenv("MUON_MAX_KSPLIT")) {
+      const long x = std::strtol(v, nullptr, 10);
+      if (x > 0) cap = static_cast<int>(std::min<long>(x, 1 << 20));
+    }
+    ks = std::min(ks, cap);
   }
   const int kb_per_split = static_cast<int>(cdiv(num_kb, ks));
   const int ksplit = static_cast<int>(cdiv(num_kb, kb_per_split));
@@ -143,8 +171,16 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
   g.num_kb_gram = num_kb;
   g.tri = tri;
 
-  // The array keeps the previous call's contents: clear status and counters.
-  if (cudaMemsetAsync(base, 0, zero_bytes, stream) != cudaSuccess) return MUON_ERR_CUDA;
+  // The array keeps the previous call's contents: clear the counters (and,
+  // on the device's first call, the status word as well).
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    const size_t from = g_status_clean[dev] ? o_cnt : o_status;
+    if (cudaMemsetAsync(base + from, 0, zero_end - from, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    g_status_clean[dev] = true;
+  }
 
   if (!ns_group_maps(g)) return MUON_ERR_CUDA;
 
@@ -203,6 +239,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
       gp.deep = gemm_deep(phase, G.kb_per_split);
       gp.status = status;
       gp.timeout_ns = timeout_ns;
+      gp.inject = take_injected_stall(kInjectGemm);
       if (launch_gemm(phase, gp, stream) != cudaSuccess) return MUON_ERR_CUDA;
     }
   }

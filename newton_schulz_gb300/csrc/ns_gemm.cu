@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   uint64_t* tfull = empty + kStages;      // [2] accumulator ready
   uint64_t* tempty = tfull + 2;           // [2] accumulator drained
   uint64_t* xfull = tempty + 2;           // [2] apply: staged Xt tile of epilogue set s landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 2);
+  uint64_t* mma_drain = xfull + 2;        // the MMA issuer's last MMAs have completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);   // [2] per-tile decision
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       ptx::mbar_init(&tempty[b], kEpiThreads);
       ptx::mbar_init(&xfull[b], 1);
     }
+    ptx::mbar_init(mma_drain, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     for (int g = 0; g < p.n_groups; ++g) {
@@ -227,12 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             stop = true;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
           const int seg = PREC ? i / t.nkb : 0;
           const int kx = (t.kb0 + i - seg * t.nkb) * BK;
           const CUtensorMap* ma = (PREC && seg == 2) ? &G.mapAlo : &G.mapA;
           const CUtensorMap* mb = (PREC && seg == 1) ? &G.mapBlo : &G.mapB;
-          if (EPI == kEpiGram) {
+          if (p.inject && blockIdx.x == 0 && issued == 0) {
+            // testing hook: this stage is never armed and no copy is issued
+            // for it, so the MMA issuer's wait on it runs out
+          } else if (EPI == kEpiGram) {
+            ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
             // MN-major chunks of Xt: 64 columns (m) x 64 rows (n, the K dim) each
 #pragma unroll
             for (int h = 0; h < BM / 64; ++h)
@@ -243,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
               ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
                                t.col_tile * BN + 64 * h, kx, t.mat);
           } else {
+            ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
             ptx::tma_load_3d(sA + stage * kABytes, ma, &full[stage], kx, t.row_tile * BM, t.mat);
             ptx::tma_load_3d(sB + stage * kBBytes, mb, &full[stage], kx, t.col_tile * BN, t.mat);
           }
@@ -306,6 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         }
         ptx::umma_commit(&tfull[buf]);   // accumulator complete (or abandoned)
       }
+      // no MMA may still run when TMEM is freed (after an abort nobody
+      // waits for the last accumulator)
+      ptx::umma_commit(mma_drain);
+      wait_bounded(mma_drain, 0, abort_flag, p.status, p.timeout_ns, false);
     }
     __syncwarp();
   } else {

@@ -53,6 +53,7 @@ constexpr uint32_t kConsBar = 1;   // named barrier of the consumer warps
 struct SmallBars {
   uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], mma_done[kSmallMaxStages];
   uint64_t gram_full[2], q_full[2], q_free[2];
+  uint64_t mma_fin;    // the MMA issuer's last MMAs have completed
   uint32_t tslot;
   int last;
   int abort;
@@ -84,6 +85,23 @@ __device__ bool mwait(uint64_t* bar, uint32_t parity, const Ctx& c) {
         *ab = 1;
         return false;
       }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: at the end of a role, for copies
+// or MMAs still in flight (they finish whatever else happened).  A timeout
+// only sets the status bit.
+__device__ void mwait_drain(uint64_t* bar, uint32_t parity, const Ctx& c) {
+  const uint32_t addr = ptx::smem_u32(bar);
+  if (ptx::mbar_try_wait(addr, parity)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ptx::mbar_try_wait(addr, parity)) return;
+    if ((it & 63u) == 0 && ptx::globaltimer() - t0 > c.timeout_ns) {
+      atomicOr(c.status, kDevTimeout);
+      return;
     }
   }
 }
@@ -802,6 +820,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       ptx::mbar_init(&B->q_full[i], 1);
       ptx::mbar_init(&B->q_free[i], 1);
     }
+    ptx::mbar_init(&B->mma_fin, 1);
     B->last = 0;
     B->abort = 0;
     ptx::fence_mbar_init();
@@ -875,6 +894,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     };
     Ring rg;
     bool ok = true;
+    int nput = 0;                 // stages handed out (stage j % NS, parity (j / NS) & 1)
+    int qk_last[2] = {-1, -1};    // lane 0: last claim whose Q image went to buffer b
     // Hands the next stage to the other roles once its previous use is done
     // (consumers and MMA issuer): descriptor, then the tile(s).  Element-wise
     // copies (slices whose rows are not TMA-legal) go through the slice.
@@ -922,6 +943,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
       __syncwarp();
       rg.next(NS);
+      ++nput;
       return true;
     };
     const LoadPlan none;
@@ -971,6 +993,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(qbytes));
           ptx::bulk_load(sm + off_q + b * qbytes, qimg + static_cast<size_t>(item / nb) * qbytes,
                          static_cast<uint32_t>(qbytes), &B->q_full[b]);
+          qk_last[b] = k;
         }
       }
       item = __shfl_sync(0xffffffffu, item, 0);
@@ -982,6 +1005,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         ok = put(kStageP2, L, 128 * t, (t == t0 ? kFirst : 0) | (t == t1 - 1 ? kLast : 0));
     }
     put(kStageEnd, none, 0, 0);
+    // No copy may still target this CTA's shared memory at exit, also after
+    // an abort: the last (up to) NS stages handed out and the last Q image
+    // of each buffer have landed.
+    if (lane == 0) {
+      for (int j = nput > NS ? nput - NS : 0; j < nput; ++j)
+        mwait_drain(&B->ring_full[j % NS], static_cast<uint32_t>(j / NS) & 1u, ctx);
+      for (int b = 0; b < 2; ++b)
+        if (qk_last[b] >= 0) mwait_drain(&B->q_full[b], static_cast<uint32_t>(qk_last[b] >> 1) & 1u, ctx);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     const uint32_t idesc_gram = ptx::idesc_bf16_f32(128, ngram);
@@ -1056,6 +1089,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         }
         rg.next(NS);
       }
+      // no MMA may still run when TMEM is freed (after an abort nobody
+      // waits for the last ones)
+      ptx::umma_commit(&B->mma_fin);
+      mwait_drain(&B->mma_fin, 0, ctx);
     }
     __syncwarp();
   } else {
@@ -1115,7 +1152,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         else gram_space<4, 4, 64, false>(p, mat, gs, t);
         __threadfence();
         cons_sync();
-        if (t == 0) {   // publish: next free position of the ready list
+        // publish: next free position of the ready list (the testing hook
+        // withholds the launch's last matrix, so the waits for it run out)
+        if (t == 0 && !(p.inject && mat == p.total_mats - 1)) {
           const unsigned pos = atomicAdd(lctr, 1u);
           if (pos < static_cast<unsigned>(p.total_mats))
             st_release_u64(p.ready_list + pos, (static_cast<unsigned long long>(p.epoch) << 32) |

@@ -152,13 +152,20 @@ def config_c5(device, seed: int = 5, scale_down: int = 1) -> List[dict]:
         W = _randn((b, r, c), device, seed * 1000 + 10 * gi + 2, 0.02)
         out.append(_group(W, G, torch.zeros((b, r, c), dtype=torch.float32, device=device),
                           f"c5_{b}x{r}x{c}"))
-    r = d(8192)
+    out.append(config_c5_lowrank(device, seed, scale_down))
+    return out
+
+
+def config_c5_lowrank(device, seed: int = 5, scale_down: int = 1) -> dict:
+    """The large sweep's last group alone: 2 low-rank-plus-noise gradients
+    [8192, 8192] (same values as in ``config_c5``), fp32 weights."""
+    torch = _torch()
+    r = 8192 // scale_down
     lr_g = torch.stack([lowrank_plus_noise(r, r, max(1, 64 // scale_down), device,
                                            seed * 1000 + 100 + 10 * i) for i in range(2)])
     W = _randn((2, r, r), device, seed * 1000 + 99, 0.02)
-    out.append(_group(W, lr_g.to(torch.bfloat16),
-                      torch.zeros((2, r, r), dtype=torch.float32, device=device), "c5_lowrank"))
-    return out
+    return _group(W, lr_g.to(torch.bfloat16),
+                  torch.zeros((2, r, r), dtype=torch.float32, device=device), "c5_lowrank")
 
 
 CONFIGS = {"c1": config_c1, "c2": config_c2, "c3": config_c3, "c4": config_c4, "c5": config_c5}

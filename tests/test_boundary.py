@@ -154,3 +154,13 @@ def test_adamw_argument_errors(lib):
     assert call([grp(m=0x1020)]) == E_ALIAS          # exp_avg inside param
     assert call([grp(g=0x1010)]) == E_ALIAS          # grad inside param
     assert call([grp(p=0, g=0, m=0, v=0, n=0)]) == 0  # empty tensors are skipped
+
+
+def test_debug_inject_stall_arguments(lib):
+    """The failure-path testing hook takes 0 (cancel), 1 (GEMM) or 2 (small-m)
+    and only records the request (nothing is launched by it)."""
+    assert lib.muon_debug_inject_stall(3) == 1
+    assert lib.muon_debug_inject_stall(-1) == 1
+    assert lib.muon_debug_inject_stall(1) == 0
+    assert lib.muon_debug_inject_stall(2) == 0
+    assert lib.muon_debug_inject_stall(0) == 0
