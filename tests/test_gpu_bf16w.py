@@ -7,9 +7,15 @@ decoupled decay, W' = (1 - lr wd) W - lr s O, fp32 arithmetic, one
 round-to-nearest-even to W's dtype):
 
 1. against the float64 oracle: every element of the GPU's bf16 W' lies within
-   one bf16 ulp of RNE(W'_oracle), and the fraction of elements that differ at
-   all is reported (NS is a bf16 approximation, so a few percent of the
-   elements sit close enough to a rounding boundary to land one ulp away);
+   one bf16 ulp of RNE(W'_oracle) wherever that ulp is at least the error NS
+   itself leaves in the element.  The fp32 rerun (2.) gives that error per
+   element, delta = |W'_fp32 - W'_oracle| (lr s times the NS error, ~1e-6);
+   the check covers every element with |W'_oracle| >= 2^8 max(delta), whose
+   bf16 spacing (>= |W'| 2^-8) is then at least max(delta).  Closer to zero
+   the bf16 values are spaced more finely than the NS error, so RNE of two
+   values a few 1e-6 apart can be many ulps apart (even of opposite sign);
+   there the fp32 check below applies.  The fraction of elements covered and
+   the fraction that differ from RNE(W'_oracle) at all are printed;
 2. against the same step with the weights widened to fp32 (checked against
    the oracle at 1e-2 * ||dW|| like every fp32 case): the bf16 W' equals
    RNE(W'_fp32) bit for bit.  A lost decay factor, a second rounding or a
@@ -25,7 +31,6 @@ from oracle import muon_ref as R
 pytestmark = pytest.mark.gpu
 HP = dict(mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
 MOM_TOL, DW_TOL = 1e-6, 1e-2
-MISMATCH_MAX = 0.25   # far above the measured few percent; catches systematic errors
 
 
 @pytest.fixture(autouse=True)
@@ -59,21 +64,26 @@ def check_bf16_weights(w0, g, mom0, w_gpu_bf16, w_f32_rerun, label=""):
     values); w_gpu_bf16: the GPU's bf16 W' (torch, any device);
     w_f32_rerun: the GPU's fp32 W' of the same step from w0 widened to fp32."""
     w2, _, _ = R.muon_step_ref(w0, g, mom0, **HP)
-    ref = rne_bf16(w2)
-    got = _np(w_gpu_bf16)
-    d = np.abs(bf16_ordinal(got) - bf16_ordinal(ref))
-    mismatch = float(np.mean(d != 0))
-    print(f"bf16 W' {label}: max ulp distance {int(d.max())}, mismatch fraction {mismatch:.4f}")
-    assert d.max() <= 1, (label, int(d.max()))
-    assert mismatch <= MISMATCH_MAX, (label, mismatch)
-    # the fp32 rerun meets the fp32 weight tolerance ...
     wf = _np(w_f32_rerun)
+    # the fp32 rerun meets the fp32 weight tolerance ...
     for i in range(w2.shape[0]):
         err = np.linalg.norm(wf[i] - w2[i]) / np.linalg.norm(w2[i] - w0[i])
         assert err <= DW_TOL, (label, i, err)
-    # ... and the bf16 branch rounds exactly that fp32 result once, to nearest even
+    # ... the bf16 branch rounds exactly that fp32 result once, to nearest even ...
     exp = w_f32_rerun.detach().cpu().to(torch.bfloat16)
     assert torch.equal(w_gpu_bf16.detach().cpu(), exp), label
+    # ... and lands within one ulp of RNE(W'_oracle) wherever that ulp is at
+    # least the NS error left in the element
+    delta = float(np.abs(wf - w2).max())
+    covered = np.abs(w2) >= 256.0 * delta
+    d = np.abs(bf16_ordinal(_np(w_gpu_bf16)) - bf16_ordinal(rne_bf16(w2)))
+    mismatch = float(np.mean(d != 0))
+    print(f"bf16 W' {label}: max NS error per element {delta:.2e}; 1-ulp check on "
+          f"{covered.mean():.3f} of the elements, max distance there "
+          f"{int(d[covered].max()) if covered.any() else 0}; differ from RNE(oracle): "
+          f"{mismatch:.4f} overall, {float(np.mean(d[covered] != 0)) if covered.any() else 0:.4f} covered")
+    assert covered.mean() >= 0.25, (label, covered.mean())
+    assert d[covered].max() <= 1, (label, int(d[covered].max()))
     return mismatch
 
 
