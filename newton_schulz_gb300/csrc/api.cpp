@@ -11,6 +11,7 @@
 // largest chunk, is allocated once per (device, stream) and reused.
 #include <algorithm>
 #include <atomic>
+#include <cstdint>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -746,11 +747,24 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         std::memset(&gp, 0, sizeof(gp));
         int64_t tiles = 0;
         int min_kb = 1 << 30;
+        bool split = false;
+        int64_t min_m = INT64_MAX;
         for (size_t k = 0; k < ch.groups.size(); ++k) {
           GemmGroup& G = gp.g[k];
           ns_fill_group(G, dg[k], phase, it, static_cast<int>(tiles));
           tiles += static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
           min_kb = std::min(min_kb, G.kb_per_split);
+          split = split || G.ksplit > 1;
+          min_m = std::min(min_m, dg[k].m);
+        }
+        // CTA pairs sharing the B tile (bf16 products without split-K, large shapes)
+        if (!ns.precise && !split && gemm_use_pair(tiles, dev->sms, min_m)) {
+          gp.pair = 1;
+          tiles = 0;
+          for (size_t k = 0; k < ch.groups.size(); ++k) {
+            ns_fill_group(gp.g[k], dg[k], phase, it, static_cast<int>(tiles), true);
+            tiles += static_cast<int64_t>(gp.g[k].tiles_per_mat) * dg[k].cnt;
+          }
         }
         gp.deep = gemm_deep(phase, min_kb);
         gp.prec = ns.precise ? 1 : 0;

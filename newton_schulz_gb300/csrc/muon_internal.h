@@ -114,6 +114,8 @@ struct GemmParams {
   int prec;               // 1: hi + lo operands, three K segments per product
   int inject;             // testing hook: CTA 0 arms its first ring stage and issues no
                           // copy for it, so the wait on it runs out (then the status bit)
+  int pair;               // 1: clusters of two CTAs share the B tile (tiles count pair
+                          // tiles; mapB holds 128-row boxes for K-major B; no split-K)
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -147,7 +149,9 @@ bool make_ns_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows
                  int64_t pitch, int64_t mstride, int box_rows);
 bool ns_group_maps(NsGroupDev& g);
 // Fill the launch descriptor of group g for `phase` (Epi) of NS step `it`.
-void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base);
+// pair: the launch runs in CTA pairs (see GemmParams::pair).
+void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base,
+                   bool pair = false);
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
@@ -250,6 +254,10 @@ int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage
 int gemm_sym_tiles(int m);   // tiles of a symmetric m x m product (holding some col >= row)
+int gemm_sym_pair_tiles(int m);   // the same tiles taken in pairs of row tiles
+// Whether a launch with `tiles` (unpaired) tiles, whose smallest core-shape
+// side is min_m, runs in CTA pairs (MUON_GEMM_PAIR=0 / 1 overrides).
+bool gemm_use_pair(int64_t tiles, int sms, int64_t min_m);
 // Ring depth of a launch (GemmParams::deep): the Gram and the apply always
 // take the 4-stage ring (their epilogues need one staging box per set); the
 // polynomial, whose mirrored output wants two boxes per set in flight, only

@@ -104,8 +104,10 @@ __device__ __forceinline__ int sym_rows(int j, int ntr) {
   return r < ntr ? r : ntr;
 }
 
-template <int EPI>
-__device__ __forceinline__ TileInfo decode(const GemmParams& p, int tile) {
+// PAIR: `tile` numbers pair tiles (two row tiles sharing a column tile, one
+// per CTA of the pair); crank picks this CTA's row tile.
+template <int EPI, bool PAIR>
+__device__ __forceinline__ TileInfo decode(const GemmParams& p, int tile, int crank) {
   TileInfo t;
   int gi = 0;
   while (gi + 1 < p.n_groups && tile >= p.g[gi + 1].tile_base) ++gi;
@@ -119,18 +121,19 @@ __device__ __forceinline__ TileInfo decode(const GemmParams& p, int tile) {
   if (EPI == kEpiApply) {
     t.row_tile = r / G.nt;
     t.col_tile = r - t.row_tile * G.nt;
+    if (PAIR) t.row_tile = 2 * t.row_tile + crank;
   } else {
     int idx = r / G.ksplit;
     t.ksp = r - idx * G.ksplit;
     t.sym_idx = idx;
     int j = 0;
     for (;;) {
-      const int c = sym_rows(j, G.mt);
+      const int c = PAIR ? (sym_rows(j, G.mt) + 1) / 2 : sym_rows(j, G.mt);
       if (idx < c) break;
       idx -= c;
       ++j;
     }
-    t.row_tile = idx;
+    t.row_tile = PAIR ? 2 * idx + crank : idx;
     t.col_tile = j;
   }
   t.kb0 = t.ksp * G.kb_per_split;
@@ -159,7 +162,17 @@ __device__ __forceinline__ void cvt_bf16x32(const uint4 (&u)[4], float* v) {
 // (hi, lo) and each product runs over three K segments, hi*hi, hi*lo and
 // lo*hi, into one fp32 accumulator; the epilogue reads hi + lo and writes the
 // result again as hi = bf16(v), lo = bf16(v - hi).  Shallow layout only.
-template <int EPI, bool DEEP, bool PREC>
+//
+// PAIR: CTAs run in clusters of two on two row tiles that share a column tile
+// (a 256 x 256 output block).  Each CTA loads its own 128-row A tile and one
+// half of the common 256-row B tile, which TMA multicasts into the same
+// stage of both CTAs, so every CTA reads 32 KB instead of 48 KB per K block
+// from L2.  Each CTA still issues its own M = 128 MMAs into its own TMEM; a
+// stage is refilled once the MMAs of BOTH CTAs are done with it (each MMA
+// issuer's commit arrives on both CTAs' empty barrier, count 2).  The pair
+// passes a cluster barrier after initialising its mbarriers and before
+// exiting, so no copy or arrival ever targets a CTA that is not running.
+template <int EPI, bool DEEP, bool PREC, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -181,11 +194,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int crank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], PAIR ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
@@ -211,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
+  if (PAIR) ptx::cluster_sync();   // both CTAs' mbarriers are initialised
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -221,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.total_tiles && !stop; tile += gridDim.x) {
-        const TileInfo t = decode<EPI>(p, tile);
+      for (int tile = tile0; tile < p.total_tiles && !stop; tile += tstep) {
+        const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
         const GemmGroup& G = p.g[t.gi];
         for (int i = 0; i < t.nkb * NSEG; ++i) {
           if (!wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, p.timeout_ns, true)) {
@@ -243,14 +260,26 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             for (int h = 0; h < BM / 64; ++h)
               ptx::tma_load_3d(sA + stage * kABytes + h * kChunkBytes, ma, &full[stage],
                                t.row_tile * BM + 64 * h, kx, t.mat);
+            if (PAIR) {
+              // this CTA's half of the B chunks, into both CTAs of the pair
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h)
-              ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
-                               t.col_tile * BN + 64 * h, kx, t.mat);
+              for (int h = 2 * crank; h < 2 * crank + 2; ++h)
+                ptx::tma_load_3d_mc(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
+                                    t.col_tile * BN + 64 * h, kx, t.mat, 0x3);
+            } else {
+#pragma unroll
+              for (int h = 0; h < BN / 64; ++h)
+                ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
+                                 t.col_tile * BN + 64 * h, kx, t.mat);
+            }
           } else {
             ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
             ptx::tma_load_3d(sA + stage * kABytes, ma, &full[stage], kx, t.row_tile * BM, t.mat);
-            ptx::tma_load_3d(sB + stage * kBBytes, mb, &full[stage], kx, t.col_tile * BN, t.mat);
+            if (PAIR)   // B rows [BN/2 crank, BN/2 crank + BN/2) of the tile (128-row box)
+              ptx::tma_load_3d_mc(sB + stage * kBBytes + crank * (kBBytes / 2), mb, &full[stage], kx,
+                                  t.col_tile * BN + crank * (BN / 2), t.mat, 0x3);
+            else
+              ptx::tma_load_3d(sB + stage * kBBytes, mb, &full[stage], kx, t.col_tile * BN, t.mat);
           }
           ++issued;
           if (++stage == kStages) {
@@ -274,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       int stage = 0, acc = 0;
       uint32_t phase = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.total_tiles && !stop; tile += gridDim.x, ++acc) {
-        const TileInfo t = decode<EPI>(p, tile);
+      for (int tile = tile0; tile < p.total_tiles && !stop; tile += tstep, ++acc) {
+        const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
         const int buf = acc & 1;
         if (!wait_bounded(&tempty[buf], ((acc >> 1) & 1) ^ 1, abort_flag, p.status, p.timeout_ns,
                           true)) {
@@ -304,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                                     : ptx::sdesc_kmajor_sw128(b0 + k * UMMA_K * 2);
             ptx::umma_bf16(d, da, db, idesc, (i > 0 || k > 0) ? 1u : 0u);
           }
-          ptx::umma_commit(&empty[stage]);
+          if (PAIR) ptx::umma_commit_mc(&empty[stage], 0x3);   // both CTAs' stage
+          else ptx::umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -329,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     uint32_t xphase = 0;
     bool xpend = false;   // leader: a staged-tile load is in flight and not yet waited for
     int acc = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++acc) {
-      const TileInfo t = decode<EPI>(p, tile);
+    for (int tile = tile0; tile < p.total_tiles; tile += tstep, ++acc) {
+      const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
       const GemmGroup& G = p.g[t.gi];
       const int buf = acc & 1;
       const int row0 = t.row_tile * BM, col0 = t.col_tile * BN;
@@ -640,8 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           ptx::fence_proxy_async_smem();
           ptx::named_bar(2 + set, 128);
           if (leader && xok) {
-            ptx::tma_store_3d(&G.mapC, sd, gc_h, row0, t.mat);
-            if (PREC) ptx::tma_store_3d(&G.mapClo, sdl, gc_h, row0, t.mat);
+            if (row0 < G.m) {   // a pair's second row tile may lie past the matrix
+              ptx::tma_store_3d(&G.mapC, sd, gc_h, row0, t.mat);
+              if (PREC) ptx::tma_store_3d(&G.mapClo, sdl, gc_h, row0, t.mat);
+            }
             ptx::bulk_commit();
           }
           if (mirror) {
@@ -701,12 +733,25 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 
   ptx::tc_fence_before();
   __syncthreads();
+  // the peer's copies into this CTA and its arrivals on this CTA's barriers
+  // are all done once it has drained and reached this barrier
+  if (PAIR) ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 int gemm_block_n() { return BN; }
 int gemm_block_m() { return BM; }
 int gemm_block_k() { return BK; }
+
+int gemm_sym_pair_tiles(int m) {
+  const int ntr = (m + BM - 1) / BM, ntc = (m + BN - 1) / BN;
+  int t = 0;
+  for (int j = 0; j < ntc; ++j) {
+    const int r = (BN * j + BN - 1) / BM + 1;
+    t += ((r < ntr ? r : ntr) + 1) / 2;
+  }
+  return t;
+}
 
 int gemm_sym_tiles(int m) {
   const int ntr = (m + BM - 1) / BM, ntc = (m + BN - 1) / BN;
@@ -720,11 +765,47 @@ int gemm_sym_tiles(int m) {
 
 template <int EPI, bool DEEP, bool PREC>
 static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<EPI, DEEP, PREC>,
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<EPI, DEEP, PREC, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Layout<DEEP>::smem);
   if (e != cudaSuccess) return e;
-  ns_gemm_kernel<EPI, DEEP, PREC><<<grid, kThreads, Layout<DEEP>::smem, s>>>(p);
+  ns_gemm_kernel<EPI, DEEP, PREC, false><<<grid, kThreads, Layout<DEEP>::smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Paired launch: clusters of two CTAs, as many clusters as can be resident
+// at once (the occupancy API's count for this kernel), at most one per pair
+// tile.
+template <int EPI, bool DEEP>
+static cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
+  auto kern = ns_gemm_kernel<EPI, DEEP, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout<DEEP>::smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Layout<DEEP>::smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;   // per template instance
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_clusters = n;
+  }
+  const int clusters = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -739,11 +820,19 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s) {
   }
   const int grid = p.total_tiles < sms ? p.total_tiles : sms;
   const bool deep = p.deep != 0;
-  if (p.prec) {   // the high-precision mode runs on the shallow layout
+  if (p.prec) {   // the high-precision mode runs on the shallow layout, unpaired
     switch (epi) {
       case kEpiGram: return launch_one<kEpiGram, false, true>(p, grid, s);
       case kEpiPoly: return launch_one<kEpiPoly, false, true>(p, grid, s);
       case kEpiApply: return launch_one<kEpiApply, false, true>(p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.pair) {
+    switch (epi) {
+      case kEpiGram: return deep ? launch_pair<kEpiGram, true>(p, s) : launch_pair<kEpiGram, false>(p, s);
+      case kEpiPoly: return deep ? launch_pair<kEpiPoly, true>(p, s) : launch_pair<kEpiPoly, false>(p, s);
+      case kEpiApply: return deep ? launch_pair<kEpiApply, true>(p, s) : launch_pair<kEpiApply, false>(p, s);
       default: return cudaErrorInvalidValue;
     }
   }

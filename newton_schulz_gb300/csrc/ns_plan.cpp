@@ -7,6 +7,7 @@
 // B' = b A + c A^2 + alpha I, apply Xt' = (a - alpha) Xt + Xt B'.  The
 // iterate lives only as Xt = X^T ([n][m_pad] bf16 per matrix), ping-ponged
 // between two buffers: step `it` reads Xt[it & 1] and writes Xt[(it + 1) & 1].
+#include <cstdlib>
 #include <mutex>
 
 #include "muon_internal.h"
@@ -93,7 +94,23 @@ bool ns_group_maps(NsGroupDev& g) {
   return ok;
 }
 
-void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base) {
+bool gemm_use_pair(int64_t tiles, int sms, int64_t min_m) {
+  if (const char* v = std::getenv("MUON_GEMM_PAIR")) {
+    if (v[0] == '0') return false;
+    if (v[0] == '1') return true;
+  }
+  // Measured on one GB300, the same box back to back (ms per step, unpaired
+  // -> paired): large sweep (m = 8192, 16384; power-capped, 1500 -> 1650
+  // MHz) 520.2 -> 505.6; Llama-3-8B shapes (m <= 4096) 334.6 -> 337.4; MoE
+  // experts (m = 768, full clocks) 6.14 -> 6.25.  Pairs move a third less
+  // operand data per MMA, which buys clock under the power cap, but tie two
+  // CTAs' pipelines together: only the largest core shapes gain.  They also
+  // halve the number of work units, so a launch needs two waves of pairs.
+  return min_m >= 8192 && tiles >= 4LL * sms;
+}
+
+void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base,
+                   bool pair) {
   const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
   G.m = static_cast<int>(g.m);
   G.n = static_cast<int>(g.n);
@@ -117,10 +134,11 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.ksplit = g.ksplit;
     G.kb_per_split = g.kb_per_split;
     G.num_kb = g.num_kb_gram;
-    G.tiles_per_mat = static_cast<int>(g.tri * g.ksplit);
+    G.tiles_per_mat = pair ? gemm_sym_pair_tiles(static_cast<int>(g.m))
+                           : static_cast<int>(g.tri * g.ksplit);
   } else if (phase == kEpiPoly) {
     G.mapA = g.map_ap;      // operand rows and the epilogue's A tiles
-    G.mapB = g.map_aq;
+    G.mapB = pair ? g.map_ap : g.map_aq;   // a pair loads B in 128-row halves
     G.mapC = g.map_bp;
     G.mapD = g.map_b64;
     if (g.A_lo) {
@@ -134,10 +152,10 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.ksplit = 1;
     G.num_kb = static_cast<int>(cdiv64(g.m, bk));
     G.kb_per_split = G.num_kb;
-    G.tiles_per_mat = static_cast<int>(g.tri);
+    G.tiles_per_mat = pair ? gemm_sym_pair_tiles(static_cast<int>(g.m)) : static_cast<int>(g.tri);
   } else {
     G.mapA = g.map_xt[it & 1];
-    G.mapB = g.map_bq;
+    G.mapB = pair ? g.map_bp : g.map_bq;
     G.mapC = g.map_xt[(it + 1) & 1];
     if (g.A_lo) {
       G.mapAlo = g.lo_xt[it & 1];
@@ -149,7 +167,7 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.ksplit = 1;
     G.num_kb = static_cast<int>(cdiv64(g.m, bk));
     G.kb_per_split = G.num_kb;
-    G.tiles_per_mat = G.nt * G.mt;
+    G.tiles_per_mat = G.nt * (pair ? (G.mt + 1) / 2 : G.mt);
   }
 }
 

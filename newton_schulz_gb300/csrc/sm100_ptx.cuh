@@ -301,3 +301,32 @@ __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
 
 }  // namespace ptx
 }  // namespace muon
+
+namespace muon {
+namespace ptx {
+
+// TMA tensor load into the same shared-memory offset of every CTA of the
+// cluster named in cta_mask (this GPU's memory only); each destination CTA's
+// mbarrier at the offset of `bar` receives the complete_tx of its copy.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const void* tmap, uint64_t* bar, int x,
+                                               int y, int z, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Arrive (once) on the mbarrier at the offset of `bar` in every CTA named in
+// cta_mask when all prior tcgen05 async ops of this thread have completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+}  // namespace ptx
+}  // namespace muon
