@@ -285,6 +285,19 @@ muon_status_t muon_query_status(cudaStream_t stream);
  * unaffected.  Returns MUON_ERR_INVALID_ARGUMENT for any other value. */
 muon_status_t muon_debug_inject_stall(int what);
 
+/* Debugging aid for the workspace (no counterpart on the pages): with the
+ * environment variable MUON_WS_GUARD=1 set when a call is made, every buffer
+ * of the library's workspace is followed by a 4 KB guard band filled with a
+ * fixed byte before the kernels that use that layout, and a small kernel
+ * counts the band bytes that changed right after them.  This call
+ * synchronises `stream`, stores the count accumulated on the current device
+ * since the last read into *bad_bytes (0 when nothing wrote outside its
+ * buffers, or guard mode was never used) and clears it.  Guard mode changes
+ * neither results nor the buffers' contents; it adds the fill and check
+ * launches and 4 KB per buffer.  Errors: bad_bytes NULL ->
+ * MUON_ERR_INVALID_ARGUMENT. */
+muon_status_t muon_debug_guard_check(cudaStream_t stream, int64_t *bad_bytes);
+
 /* Static, human-readable name of a status code. */
 const char *muon_status_string(muon_status_t status);
 

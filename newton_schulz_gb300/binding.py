@@ -29,7 +29,7 @@ EXPORTED = (
     "muon_step_grouped_ex", "muon_step_grouped_host", "muon_query_status", "muon_status_string",
     "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
     "muon_profile_read", "muon_adamw_grouped", "muon_ns_cost_table", "muon_assign_owners",
-    "muon_ns_batched_noalloc", "muon_debug_inject_stall",
+    "muon_ns_batched_noalloc", "muon_debug_inject_stall", "muon_debug_guard_check",
 )
 INJECT_NONE, INJECT_GEMM, INJECT_SMALL = 0, 1, 2
 
@@ -111,6 +111,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_ns_batched_noalloc.restype = i32
     lib.muon_debug_inject_stall.argtypes = [ctypes.c_int]
     lib.muon_debug_inject_stall.restype = i32
+    lib.muon_debug_guard_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
+    lib.muon_debug_guard_check.restype = i32
     lib.muon_query_status.argtypes = [vp]
     lib.muon_query_status.restype = i32
     lib.muon_status_string.argtypes = [i32]
@@ -263,6 +265,15 @@ def muon_debug_inject_stall(what: int) -> None:
     """Testing hook: the next launch of kind `what` (INJECT_GEMM or
     INJECT_SMALL) stalls on a wait nothing satisfies until its bound runs out."""
     check(load().muon_debug_inject_stall(int(what)), "muon_debug_inject_stall")
+
+
+def muon_debug_guard_check(stream=None) -> int:
+    """Bytes found changed in the workspace guard bands since the last read
+    (calls made with MUON_WS_GUARD=1); synchronises the stream."""
+    bad = ctypes.c_int64(0)
+    check(load().muon_debug_guard_check(_stream_ptr(stream), ctypes.byref(bad)),
+          "muon_debug_guard_check")
+    return bad.value
 
 
 def muon_status_string(code: int) -> str:

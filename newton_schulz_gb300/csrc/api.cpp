@@ -52,6 +52,7 @@ struct Workspace {
 struct DevState {
   unsigned* status = nullptr;
   int sms = 0;
+  unsigned long long* guard_bad = nullptr;   // guard mode: bytes found changed in the bands
 };
 
 struct ProfRec {
@@ -109,6 +110,47 @@ muon_status_t dev_state(DevState** out) {
   return MUON_OK;
 }
 
+// ---- guard mode --------------------------------------------------------------------
+// Guard mode (MUON_WS_GUARD=1, a debugging aid): every workspace buffer is
+// followed by a band of kGuardBytes that no kernel may write; the bands are
+// filled with kGuardByte before a layout's launches and counted by
+// guard_check_kernel after them (read with muon_debug_guard_check).
+constexpr size_t kGuardBytes = 4096;
+constexpr int kGuardByte = 0xA5;
+muon_status_t guard_counter(DevState* dev) {
+  if (dev->guard_bad) return MUON_OK;
+  if (cudaMalloc(&dev->guard_bad, sizeof(unsigned long long)) != cudaSuccess) {
+    cudaGetLastError();
+    dev->guard_bad = nullptr;
+    return MUON_ERR_OUT_OF_MEMORY;
+  }
+  return cudaMemset(dev->guard_bad, 0, sizeof(unsigned long long)) == cudaSuccess ? MUON_OK
+                                                                                    : MUON_ERR_CUDA;
+}
+
+muon_status_t guard_fill(char* ws, const std::vector<size_t>& bands, size_t bytes,
+                         cudaStream_t stream) {
+  for (size_t o : bands)
+    if (cudaMemsetAsync(ws + o, kGuardByte, bytes, stream) != cudaSuccess) return MUON_ERR_CUDA;
+  return MUON_OK;
+}
+
+muon_status_t guard_check(char* ws, const std::vector<size_t>& bands, size_t bytes,
+                          DevState* dev, cudaStream_t stream) {
+  for (size_t b = 0; b < bands.size(); b += kGuardMaxBands) {
+    GuardParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.base = reinterpret_cast<const uint8_t*>(ws);
+    gp.n = static_cast<int>(std::min<size_t>(kGuardMaxBands, bands.size() - b));
+    for (int i = 0; i < gp.n; ++i) gp.off[i] = bands[b + i];
+    gp.bytes = static_cast<unsigned>(bytes);
+    gp.pattern = static_cast<unsigned>(kGuardByte);
+    gp.bad = dev->guard_bad;
+    if (launch_guard_check(gp, stream) != cudaSuccess) return MUON_ERR_CUDA;
+  }
+  return MUON_OK;
+}
+
 // ---- plan --------------------------------------------------------------------------
 struct Req {            // one user group
   void* W;
@@ -142,13 +184,18 @@ struct ChunkP {
   std::vector<NsGroupP> groups;
   size_t bytes = 0;
   size_t ctrs = 0;             // counters used (elements)
+  std::vector<size_t> guards;  // guard-band offsets (MUON_WS_GUARD)
 };
 
-void layout_chunk(ChunkP& ch, int sms, bool precise) {
+void layout_chunk(ChunkP& ch, int sms, bool precise, size_t guard) {
   size_t off = 0;
-  auto take = [&](size_t bytes) {
+  auto take = [&](size_t bytes, bool band = true) {
     size_t o = off;
     off = align_up(off + std::max<size_t>(bytes, 16), 1024);
+    if (guard && band) {
+      ch.guards.push_back(off);
+      off += guard;
+    }
     return o;
   };
   const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
@@ -182,10 +229,10 @@ void layout_chunk(ChunkP& ch, int sms, bool precise) {
     g.off_ssq = take(static_cast<size_t>(g.cnt * g.prep_tiles) * 4);
     g.off_part = take(g.ksplit > 1 ? static_cast<size_t>(g.cnt * g.tri * g.ksplit) * bm * bn * 4
                                    : 16);
-    if (precise) {   // lo halves, laid out like the hi ones: Xt0, Xt1, A, B
-      g.off_lo = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
-      take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
-      take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+    if (precise) {   // lo halves, laid out like the hi ones (one band after all four)
+      g.off_lo = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2, false);
+      take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2, false);
+      take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2, false);
       take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
     }
     g.ctr_prep = ctr;
@@ -264,9 +311,16 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
       wb -= 128;
   }
   sp->wb = static_cast<int>(wb);
-  // second-phase claims of 4 tiles (measured on 74 x [24, 10240]: whole
-  // 16-tile items 0.112 ms, 8 tiles 0.106, 4 tiles 0.103, 2 tiles 0.105)
-  sp->p2_tiles = std::max<int>(1, static_cast<int>(env_size("MUON_SMALL_P2_TILES", 4)));
+  // second-phase claims: units of 2 tiles, up to 4 units per claim while
+  // much work remains, 1 at the end (on 74 x [24, 10240] claims of a fixed
+  // 16 / 8 / 4 / 2 tiles took 0.112 / 0.106 / 0.103 / 0.105 ms: large claims
+  // spare the claim's round trips, small ones even out the end)
+  sp->p2_tiles = std::max<int>(1, static_cast<int>(env_size("MUON_SMALL_P2_TILES", 2)));
+  sp->p2_units = std::max<int>(1, static_cast<int>(env_size("MUON_SMALL_P2_UNITS", 4)));
+  {
+    const char* v = std::getenv("MUON_SMALL_TMA_STORE");
+    sp->p2_tma_store = (v && v[0] == '0') ? 0 : 1;
+  }
   sp->nb = static_cast<int>(cdiv(n, wb));
   sp->total_mats = static_cast<int>(mats);
   sp->items = static_cast<int>(mats * sp->nb);
@@ -280,14 +334,24 @@ bool small_plan(int64_t m, int64_t n, int64_t mats, int sms, int esg, int esw, b
   return sp->smem_bytes <= kSmallSmemLimit;
 }
 
-// Workspace bytes of one small-m launch: X0 images, partial Grams, Q images.
-size_t small_ws_bytes(const SmallParams& sp) {
-  return align_up(static_cast<size_t>(sp.items) * sp.xbytes, 256) +
-         align_up(static_cast<size_t>(sp.items) * sp.pstride * 4, 256) +
-         static_cast<size_t>(sp.total_mats) * sp.qbytes;
+// Workspace of one small-m launch: X0 images, partial Grams, Q images (each
+// followed by a guard band in guard mode); offsets into `off[3]`, guard-band
+// offsets into `bands[3]`; returns the bytes.
+size_t small_ws_layout(const SmallParams& sp, size_t guard, size_t* off, size_t* bands) {
+  const size_t sizes[3] = {static_cast<size_t>(sp.items) * sp.xbytes,
+                           static_cast<size_t>(sp.items) * sp.pstride * 4,
+                           static_cast<size_t>(sp.total_mats) * sp.qbytes};
+  size_t o = 0;
+  for (int i = 0; i < 3; ++i) {
+    off[i] = o;
+    o = align_up(o + sizes[i], 256);
+    bands[i] = o;
+    o += guard;
+  }
+  return o;
 }
 
-std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms, bool precise) {
+std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms, bool precise, size_t guard) {
   const int64_t cap = static_cast<int64_t>(env_size("MUON_WS_CAP", size_t(1) << 29));
   std::vector<int> order;
   for (int i = 0; i < static_cast<int>(reqs.size()); ++i)
@@ -345,7 +409,7 @@ std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms, bool precis
     }
   }
   close();
-  for (auto& ch : chunks) layout_chunk(ch, sms, precise);
+  for (auto& ch : chunks) layout_chunk(ch, sms, precise, guard);
   return chunks;
 }
 
@@ -615,10 +679,12 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       }
     }
   }
-  std::vector<ChunkP> plan = make_plan(large, dev->sms, ns.precise);
+  const size_t guard = env_size("MUON_WS_GUARD", 0) ? kGuardBytes : 0;
+  std::vector<ChunkP> plan = make_plan(large, dev->sms, ns.precise, guard);
   size_t need = 0, need_ctr = 0, max_mats = 0;
   for (const SmallParams& sp : smalls) {
-    need = std::max(need, small_ws_bytes(sp));
+    size_t off[3], bands[3];
+    need = std::max(need, small_ws_layout(sp, guard, off, bands));
     max_mats = std::max(max_mats, static_cast<size_t>(sp.total_mats));
   }
   for (auto& ch : plan) {
@@ -633,14 +699,21 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
   unsigned* ctr = nullptr;
   st = get_workspace(stream, need, need_ctr, &ws, &ctr);
   if (st != MUON_OK) return st;
+  if (guard) {
+    st = guard_counter(dev);
+    if (st != MUON_OK) return st;
+  }
   for (SmallParams& sp : smalls) {
     // the launches run in stream order, so each reuses the same workspace
-    char* w = ws;
-    sp.ximg = reinterpret_cast<uint8_t*>(w);
-    w += align_up(static_cast<size_t>(sp.items) * sp.xbytes, 256);
-    sp.part = reinterpret_cast<float*>(w);
-    w += align_up(static_cast<size_t>(sp.items) * sp.pstride * 4, 256);
-    sp.qimg = reinterpret_cast<uint8_t*>(w);
+    size_t off[3], bands[3];
+    small_ws_layout(sp, guard, off, bands);
+    sp.ximg = reinterpret_cast<uint8_t*>(ws + off[0]);
+    sp.part = reinterpret_cast<float*>(ws + off[1]);
+    sp.qimg = reinterpret_cast<uint8_t*>(ws + off[2]);
+    if (guard) {
+      st = guard_fill(ws, std::vector<size_t>(bands, bands + 3), guard, stream);
+      if (st != MUON_OK) return st;
+    }
     st = get_epoch_ctrs(stream, max_mats, &sp.arrive, &sp.ready_list, &sp.ctr, &sp.epoch, &sp.cap);
     if (st != MUON_OK) return st;
     // one CTA per SM (all resident: the launch is cooperative)
@@ -648,6 +721,10 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     const int grid = static_cast<int>(std::min<int64_t>(sp.items, dev->sms));
     st = L0.run(5, [&] { return launch_small(sp, grid, stream); });
     if (st != MUON_OK) return st;
+    if (guard) {
+      st = guard_check(ws, std::vector<size_t>(bands, bands + 3), guard, dev, stream);
+      if (st != MUON_OK) return st;
+    }
   }
   if (plan.empty()) {
     t_last_launches = L0.count;
@@ -658,6 +735,10 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
 
   Launcher L{stream};
   for (const ChunkP& ch : plan) {
+    if (guard) {
+      st = guard_fill(ws, ch.guards, guard, stream);
+      if (st != MUON_OK) return st;
+    }
     // ---- K1 -------------------------------------------------------------------
     {
       PrepParams pp;
@@ -832,6 +913,10 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       fp.lr = lr;
       fp.wd = wd;
       st = L.run(4, [&] { return launch_finish(fp, stream); });
+      if (st != MUON_OK) return st;
+    }
+    if (guard) {
+      st = guard_check(ws, ch.guards, guard, dev, stream);
       if (st != MUON_OK) return st;
     }
   }
@@ -1494,6 +1579,27 @@ void muon_release_workspace(void) {
 }
 
 int muon_last_launch_count(void) { return t_last_launches; }
+
+muon_status_t muon_debug_guard_check(cudaStream_t stream, int64_t* bad_bytes) {
+  if (!bad_bytes) return MUON_ERR_INVALID_ARGUMENT;
+  try {
+    std::lock_guard<std::mutex> lock(g_mu);
+    *bad_bytes = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+    auto it = g_dev.find(dev);
+    if (it == g_dev.end() || !it->second.guard_bad) return MUON_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+    unsigned long long v = 0;
+    if (cudaMemcpy(&v, it->second.guard_bad, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    if (v && cudaMemset(it->second.guard_bad, 0, sizeof(v)) != cudaSuccess) return MUON_ERR_CUDA;
+    *bad_bytes = static_cast<int64_t>(v);
+    return MUON_OK;
+  } catch (...) {
+    return MUON_ERR_CUDA;
+  }
+}
 
 muon_status_t muon_debug_inject_stall(int what) {
   if (what != 0 && what != kInjectGemm && what != kInjectSmall) return MUON_ERR_INVALID_ARGUMENT;

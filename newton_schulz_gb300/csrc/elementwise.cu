@@ -348,6 +348,33 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   }
 }
 
+// ---------------------------------------------------------------------------
+// Guard mode: count the bytes of each band (one block per band) that differ
+// from the fill pattern.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) guard_check_kernel(const __grid_constant__ GuardParams p) {
+  const uint4* band = reinterpret_cast<const uint4*>(p.base + p.off[blockIdx.x]);
+  const unsigned pat = p.pattern * 0x01010101u;
+  unsigned bad = 0;
+  for (unsigned i = threadIdx.x; i < p.bytes / 16; i += blockDim.x) {
+    const uint4 v = __ldcg(band + i);
+    const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const unsigned d = w[k] ^ pat;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bad += ((d >> (8 * b)) & 0xffu) ? 1u : 0u;
+    }
+  }
+  if (bad) atomicAdd(p.bad, static_cast<unsigned long long>(bad));
+}
+
+cudaError_t launch_guard_check(const GuardParams& p, cudaStream_t s) {
+  if (p.n <= 0) return cudaSuccess;
+  guard_check_kernel<<<p.n, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
   if (p.total_blocks <= 0) return cudaSuccess;
   prep_kernel<<<p.total_blocks, 256, 0, s>>>(p);

@@ -201,7 +201,9 @@ struct SmallParams {
   int gcols;         // TMEM columns per Gram accumulator (64, or 128 for precise m > 32);
                      // the O slots start at column 2 gcols
   int gs_lowmem;     // Gram-space job in three LD x LD buffers instead of five
-  int p2_tiles;      // second phase: 128-column tiles per claim (a part of an item)
+  int p2_tiles;      // second phase: 128-column tiles per claim unit (a part of an item)
+  int p2_units;      // second phase: most units per claim
+  int p2_tma_store;  // second phase: row-major TMA-legal W' written back by TMA from the stage
   int steps;
   float coef[kMaxSteps][3];
   int step_mode, nesterov;
@@ -245,11 +247,23 @@ struct AdamwParams {
   float inv_sqrt_bc2;      // 1 / sqrt(1 - beta2^t)
 };
 
+// ---- guard-band check (guard mode, a debugging aid) ------------------------------
+constexpr int kGuardMaxBands = 128;
+struct GuardParams {
+  const uint8_t* base;             // workspace
+  uint64_t off[kGuardMaxBands];    // band offsets
+  int n;                           // bands
+  unsigned bytes;                  // bytes per band (a multiple of 16)
+  unsigned pattern;                // the byte every band holds
+  unsigned long long* bad;         // += bytes found different
+};
+
 // ---- launchers (return cudaGetLastError()) ----------------------------------
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
 cudaError_t launch_finish(const FinParams& p, cudaStream_t s);
 cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s);
 cudaError_t launch_adamw(const AdamwParams& p, int sms, cudaStream_t s);
+cudaError_t launch_guard_check(const GuardParams& p, cudaStream_t s);
 int gemm_block_n();      // N tile of the NS GEMMs
 int gemm_block_m();      // M tile (TMEM lanes)
 int gemm_block_k();      // K per pipeline stage

@@ -54,12 +54,17 @@ struct SmallBars {
   uint64_t ring_full[kSmallMaxStages], cons_done[kSmallMaxStages], mma_done[kSmallMaxStages];
   uint64_t gram_full[2], q_full[2], q_free[2];
   uint64_t mma_fin;    // the MMA issuer's last MMAs have completed
+  uint64_t st_w[kSmallMaxStages];   // second phase, TMA-store epilogue: the owning
+                                    // set's 4 warps wrote the stage's W' tile
   uint32_t tslot;
   int last;
   int abort;
   int desc[kSmallMaxStages][4];      // per stage: kind, item (-1: none), first X column, flags
   int cur_item;      // first phase: the consumers' current item (-2: abort)
 };
+
+// the planner reserves 512 bytes for the control block (SmallParams::off_bar)
+static_assert(sizeof(SmallBars) <= 512, "control block larger than its reserved space");
 
 struct Ctx {
   SmallBars* B;
@@ -102,6 +107,26 @@ __device__ void mwait_drain(uint64_t* bar, uint32_t parity, const Ctx& c) {
     if ((it & 63u) == 0 && ptx::globaltimer() - t0 > c.timeout_ns) {
       atomicOr(c.status, kDevTimeout);
       return;
+    }
+  }
+}
+
+// Bounded wait for the phase a token from this thread's own arrival names
+// (the token fixes the phase, so no parity has to be tracked).
+__device__ bool mwait_token(uint64_t* bar, uint64_t tok, const Ctx& c) {
+  const uint32_t addr = ptx::smem_u32(bar);
+  if (ptx::mbar_try_wait_token(addr, tok)) return true;
+  volatile int* ab = &c.B->abort;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait_token(addr, tok)) return true;
+    if ((it & 63u) == 0) {
+      if (*ab) return false;
+      if (ptx::globaltimer() - t0 > c.timeout_ns) {
+        atomicOr(c.status, kDevTimeout);
+        *ab = 1;
+        return false;
+      }
     }
   }
 }
@@ -455,6 +480,9 @@ struct ItemCfg {
   void* W;
   int64_t col0;            // first X column of the item
   uint8_t* img;            // the item's X0 image
+  const CUtensorMap* wmap; // the slice's W tile map (TMA-legal W only)
+  int z;                   // matrix index within the slice
+  int tma_store;           // second phase: W' leaves through the stage by one TMA store
 };
 
 __device__ __forceinline__ ItemCfg item_cfg(const SmallParams& p, int item) {
@@ -486,6 +514,9 @@ __device__ __forceinline__ ItemCfg item_cfg(const SmallParams& p, int item) {
   c.W = static_cast<uint8_t*>(S.W) + moff * (S.w_dtype == 0 ? 4 : 2);
   c.col0 = static_cast<int64_t>(item - mat * p.nb) * p.wb;
   c.img = p.ximg + static_cast<size_t>(item) * p.xbytes;
+  c.wmap = &p.tm[si][2];
+  c.z = mat - S.mat_base;
+  c.tma_store = p.p2_tma_store && S.wbulk && !S.trans;
   return c;
 }
 
@@ -674,7 +705,8 @@ __device__ __forceinline__ void w_st(WT* p, int64_t i, float v) {
 // instruction instead of one scalar store per element).
 template <typename WT, bool STEP>
 __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, uint32_t oslot,
-                                         int set, int q4, int lane, float* scr) {
+                                         int set, int q4, int lane, float* scr, uint64_t* stw,
+                                         const Ctx& ctx) {
   const int m = c.m, nmm = c.nmm;
   const float decay = c.decay, stepk = c.stepk;
   WT* ws = reinterpret_cast<WT*>(st);
@@ -682,6 +714,50 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
   const int64_t gj = c.col0 + c0 + col;
   const uint32_t lq = static_cast<uint32_t>(32 * q4) << 16;
   WT* wg = static_cast<WT*>(c.W);
+  if (c.tma_store) {
+    // W' (or O) in place of W in the stage's [m][128] tile, then one TMA
+    // store of the tile (columns and rows outside the matrix are clipped);
+    // the set's leader waits until the store has read the stage before its
+    // warp hands the stage back
+    for (int q0 = 0; q0 < m; q0 += 4) {
+      uint32_t rh[4], rl[4];
+      ptx::tmem_ld_32x32b_x4(oslot + q0 + lq, rh);
+      ptx::tmem_ld_32x32b_x4(oslot + nmm + q0 + lq, rl);
+      float w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = (STEP && q0 + j < m) ? w_ld(ws, (q0 + j) * 128 + col) : 0.f;
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (q0 + j < m) {
+          const float o = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+          const float v = STEP ? fmaf(decay, w[j], -stepk * o) : o;
+          if constexpr (sizeof(WT) == 4) ws[(q0 + j) * 128 + col] = v;
+          else ws[(q0 + j) * 128 + col] = __float2bfloat16_rn(v);
+        }
+      }
+    }
+    // every writer's stores are made visible to the TMA (async proxy), each
+    // warp arrives on the stage's barrier, and the leader waits for the
+    // phase its own arrival names (bounded: a warp that gave up costs a
+    // timeout, never a hang; the stage is not reused before the leader's
+    // warp hands it back, so no arrival of a later use can complete it)
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (q4 == 0) {
+        const uint64_t tok = ptx::mbar_arrive_token(stw);
+        if (mwait_token(stw, tok, ctx)) {
+          ptx::tma_store_3d(c.wmap, ws, static_cast<int>(c.col0 + c0), 0, c.z);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read<0>();
+        }
+      } else {
+        ptx::mbar_arrive(stw);
+      }
+    }
+    return;
+  }
   if (!c.trans) {
     const int64_t gjw = c.col0 + c0 + 32 * q4;    // first global column of this warp
     const bool vec = c.wvec && sizeof(WT) == 4 && gjw + 32 <= c.n;
@@ -743,13 +819,13 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
 }
 
 __device__ void epi_tile_any(const ItemCfg& c, int c0, uint8_t* st, uint32_t oslot, int set,
-                             int q4, int lane, float* scr) {
+                             int q4, int lane, float* scr, uint64_t* stw, const Ctx& ctx) {
   if (c.wdt == 0) {
-    if (c.step) epi_tile<float, true>(c, c0, st, oslot, set, q4, lane, scr);
-    else epi_tile<float, false>(c, c0, st, oslot, set, q4, lane, scr);
+    if (c.step) epi_tile<float, true>(c, c0, st, oslot, set, q4, lane, scr, stw, ctx);
+    else epi_tile<float, false>(c, c0, st, oslot, set, q4, lane, scr, stw, ctx);
   } else {
-    if (c.step) epi_tile<__nv_bfloat16, true>(c, c0, st, oslot, set, q4, lane, scr);
-    else epi_tile<__nv_bfloat16, false>(c, c0, st, oslot, set, q4, lane, scr);
+    if (c.step) epi_tile<__nv_bfloat16, true>(c, c0, st, oslot, set, q4, lane, scr, stw, ctx);
+    else epi_tile<__nv_bfloat16, false>(c, c0, st, oslot, set, q4, lane, scr, stw, ctx);
   }
 }
 
@@ -821,6 +897,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       ptx::mbar_init(&B->q_free[i], 1);
     }
     ptx::mbar_init(&B->mma_fin, 1);
+    for (int i = 0; i < kSmallMaxStages; ++i) ptx::mbar_init(&B->st_w[i], 4);
     B->last = 0;
     B->abort = 0;
     ptx::fence_mbar_init();
@@ -965,44 +1042,63 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
     if (ok) ok = put(kStageP1End, none, 0, 0);
     // Second phase: work is claimed in the order matrices were published
-    // (position j of the ready list, block blk, part sub of the block), so no
-    // CTA waits for a late matrix while published work remains.  A claim is
-    // a part of an item's tiles (p2_tiles of them), so the last matrices'
-    // work spreads over more CTAs at the end of the launch.
-    const int tpc = p.p2_tiles;                       // tiles per claim
-    const int parts = (tiles + tpc - 1) / tpc;        // claims per item
+    // (position j of the ready list, item, unit of the item), so no CTA
+    // waits for a late matrix while published work remains.  The unit is
+    // p2_tiles tiles; a claim takes up to p2_units consecutive units, fewer
+    // as the work runs out (guided self-scheduling: the remaining units over
+    // twice the CTA count), so the claims' atomics and ready-list reads are
+    // paid once per several units while the launch ends on small claims.
+    // A claim is walked as segments (its units within one item), each with
+    // its own Q image (buffer k & 1 for segment k).
+    const int tpu = p.p2_tiles;                       // tiles per unit
+    const int parts = (tiles + tpu - 1) / tpu;        // units per item
     const unsigned per = static_cast<unsigned>(nb * parts);
-    for (int k = 0; ok; ++k) {
-      const int b = k & 1;
-      int item = -1, t0 = 0;
-      if (lane == 0) {
-        const unsigned next = atomicAdd(lctr + 1, 1u);
-        const int j = static_cast<int>(next / per);
-        if (j < total_mats) {
+    const unsigned total_units = per * static_cast<unsigned>(total_mats);
+    const unsigned max_take = static_cast<unsigned>(p.p2_units);
+    const unsigned ctas2 = 2u * gridDim.x;
+    unsigned take = max_take;
+    int k = 0;
+    while (ok) {
+      unsigned start = 0;
+      if (lane == 0) start = atomicAdd(lctr + 1, take);
+      start = __shfl_sync(0xffffffffu, start, 0);
+      if (start >= total_units) break;
+      const unsigned end = min(start + take, total_units);
+      const unsigned left = total_units - end;
+      take = max(1u, min(max_take, left / ctas2));
+      for (unsigned u = start; u < end && ok; ++k) {
+        const int j = static_cast<int>(u / per);
+        const unsigned rem = u - static_cast<unsigned>(j) * per;
+        const int it_m = static_cast<int>(rem / parts);                // item within the matrix
+        const unsigned item_end = static_cast<unsigned>(j) * per + (it_m + 1) * parts;
+        const unsigned seg_end = min(end, item_end);
+        const int t0 = static_cast<int>(rem % parts) * tpu;
+        const int t1 = min(tiles, t0 + static_cast<int>(seg_end - u) * tpu);
+        const int b = k & 1;
+        int item = -1;
+        if (lane == 0) {
           const int mat = wait_ready_pos(ready_list, j, epoch, ctx);
-          const int rem = static_cast<int>(next - j * per);
-          if (mat >= 0) {
-            item = mat * nb + rem / parts;
-            t0 = (rem % parts) * tpc;
+          if (mat >= 0) item = mat * nb + it_m;
+          // Q buffer b is free once the MMAs of segment k-2 are done
+          if (item >= 0 && !mwait(&B->q_free[b], ((k >> 1) & 1) ^ 1u, ctx)) item = -1;
+          if (item >= 0) {
+            ptx::fence_proxy_async_global();
+            ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(qbytes));
+            ptx::bulk_load(sm + off_q + b * qbytes, qimg + static_cast<size_t>(item / nb) * qbytes,
+                           static_cast<uint32_t>(qbytes), &B->q_full[b]);
+            qk_last[b] = k;
           }
         }
-        // Q buffer b is free once the MMAs of claim k-2 are done
-        if (item >= 0 && !mwait(&B->q_free[b], ((k >> 1) & 1) ^ 1u, ctx)) item = -1;
-        if (item >= 0) {
-          ptx::fence_proxy_async_global();
-          ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(qbytes));
-          ptx::bulk_load(sm + off_q + b * qbytes, qimg + static_cast<size_t>(item / nb) * qbytes,
-                         static_cast<uint32_t>(qbytes), &B->q_full[b]);
-          qk_last[b] = k;
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item < 0) {
+          ok = false;
+          break;
         }
+        const LoadPlan L = make_plan(kStageP2, item);
+        for (int t = t0; t < t1 && ok; ++t)
+          ok = put(kStageP2, L, 128 * t, (t == t0 ? kFirst : 0) | (t == t1 - 1 ? kLast : 0));
+        u = seg_end;
       }
-      item = __shfl_sync(0xffffffffu, item, 0);
-      t0 = __shfl_sync(0xffffffffu, t0, 0);
-      if (item < 0) break;
-      const LoadPlan L = make_plan(kStageP2, item);
-      const int t1 = min(tiles, t0 + tpc);
-      for (int t = t0; t < t1 && ok; ++t)
-        ok = put(kStageP2, L, 128 * t, (t == t0 ? kFirst : 0) | (t == t1 - 1 ? kLast : 0));
     }
     put(kStageEnd, none, 0, 0);
     // No copy may still target this CTA's shared memory at exit, also after
@@ -1237,11 +1333,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       const bool sok = mwait_warp(&B->mma_done[rg.stage], rg.phase, ctx);
       ok = ok && sok;
       ptx::tc_fence_after();
-      if (ok)
+      if (ok) {
         epi_tile_any(ic, B->desc[rg.stage][2], ring + rg.stage * p.stage_bytes,
-                     tmem + obase + oslot_cols * rg.stage, set, q4, lane, escr);
+                     tmem + obase + oslot_cols * rg.stage, set, q4, lane, escr,
+                     &B->st_w[rg.stage], ctx);
+      }
       release(false);
     }
+    // the set's TMA stores have written global memory before the CTA exits
+    if (q4 == 0 && lane == 0) ptx::bulk_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -330,3 +330,29 @@ __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask)
 
 }  // namespace ptx
 }  // namespace muon
+
+namespace muon {
+namespace ptx {
+
+// Arrive on an mbarrier and return the state token of the phase arrived on.
+__device__ __forceinline__ uint64_t mbar_arrive_token(uint64_t* bar) {
+  uint64_t tok;
+  asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(tok) : "r"(smem_u32(bar)) : "memory");
+  return tok;
+}
+
+// true once the phase identified by `tok` has completed
+__device__ __forceinline__ bool mbar_try_wait_token(uint32_t bar_addr, uint64_t tok) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "l"(tok)
+      : "memory");
+  return ok != 0;
+}
+
+}  // namespace ptx
+}  // namespace muon

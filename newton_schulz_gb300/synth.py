@@ -127,11 +127,20 @@ def config_c4(device, layers: int = 32, seed: int = 4,
     return out
 
 
+def _qr_q(a, device):
+    """Q factor of a tall Gaussian matrix, taken on the host in float64 (the
+    factors are r x 64; this also keeps the generator free of the GPU's
+    linear-algebra library)."""
+    torch = _torch()
+    q, _ = torch.linalg.qr(a.to("cpu", torch.float64))
+    return q.to(device, torch.float32)
+
+
 def lowrank_plus_noise(r_dim, c_dim, rank, device, seed):
     """U_r diag(s) V_r^T + N(0, 1e-3^2), s = 10**U(0,3)."""
     torch = _torch()
-    U, _ = torch.linalg.qr(_randn((r_dim, rank), device, seed + 1))
-    V, _ = torch.linalg.qr(_randn((c_dim, rank), device, seed + 2))
+    U = _qr_q(_randn((r_dim, rank), device, seed + 1), device)
+    V = _qr_q(_randn((c_dim, rank), device, seed + 2), device)
     sig_gen = np.random.default_rng(seed)
     s = torch.tensor(10.0 ** sig_gen.uniform(0.0, 3.0, size=rank), dtype=torch.float32,
                      device=device)

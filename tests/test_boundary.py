@@ -164,3 +164,7 @@ def test_debug_inject_stall_arguments(lib):
     assert lib.muon_debug_inject_stall(1) == 0
     assert lib.muon_debug_inject_stall(2) == 0
     assert lib.muon_debug_inject_stall(0) == 0
+
+
+def test_debug_guard_check_needs_an_output(lib):
+    assert lib.muon_debug_guard_check(None, None) == 1
