@@ -16,10 +16,12 @@ others over K after W).  ``--config`` times one workload alone.
 Per workload:
 * ``value`` -- nominal TFLOP/s: sum over matrices of 5 (4 m^2 n + 2 m^3)
   (m <= n) over the device time of a step, inputs resident in HBM;
-* ``alg`` -- the same time against the algorithmic flops of the symmetric
-  products, 5 (m (m+1) n + m^2 (m+1) + 2 m^2 n), and that rate as a fraction
-  of the measured dense bf16 peak (sustained when the timed region lasts
-  more than a second, else burst);
+* ``alg`` -- the same time against the algorithmic flops of the products the
+  library runs (symmetric products formed once): 5 (m (m+1) n + m^2 (m+1) +
+  2 m^2 n) per matrix in X space, m (m+1) n + 18 m^2 (m+1) + 2 m^2 n in Gram
+  space (n >= 2 m), and that rate as a fraction of the measured dense bf16
+  peak (sustained when the timed region lasts more than a second, else
+  burst);
 * ``roofline`` -- the dominant kernel's achieved rate (algorithmic bytes or
   flops per launch over its CUDA-event time) against the measured peak;
 * ``e2e`` -- the same metric through the host-memory entry point
@@ -91,12 +93,29 @@ def _traffic(kind, config):
 
 
 def _shapes(groups):
+    """(B, rows, cols, W bytes, G bytes, path) per group; path is the
+    library's choice for the shape (0 small-m, 1 X space, 2 Gram space)."""
+    from newton_schulz_gb300 import binding
     out = []
     for g in groups:
         w = g["W"]
         b, r, c = (1, *w.shape) if w.dim() == 2 else tuple(w.shape)
-        out.append((b, r, c, w.element_size(), g["G"].element_size()))
+        out.append((b, r, c, w.element_size(), g["G"].element_size(), binding.muon_ns_path(r, c)))
     return out
+
+
+def matrix_flops(r, c, path, steps=STEPS_NS):
+    """Algorithmic flops of one matrix's NS per GEMM kind, symmetric products
+    formed once.  X space (and the small-m kernel, counted the same way):
+    steps x (Gram m(m+1)n, polynomial m^2(m+1), apply 2m^2n).  Gram space:
+    the Gram once, 4 (steps - 1) + 2 symmetric m x m products (B', Q, T, R
+    per step; B' and Q only in the last), the apply 2m^2n once."""
+    m, n = min(r, c), max(r, c)
+    if path == 2:
+        nsym = 1 if steps == 1 else 4 * (steps - 1) + 2
+        return {"gram": m * (m + 1) * n, "poly": nsym * m * m * (m + 1), "apply": 2 * m * m * n}
+    return {"gram": steps * m * (m + 1) * n, "poly": steps * m * m * (m + 1),
+            "apply": steps * 2 * m * m * n}
 
 
 def ns_flops(r, c, steps=STEPS_NS):
@@ -106,17 +125,12 @@ def ns_flops(r, c, steps=STEPS_NS):
 
 
 def nominal_flops(shapes, steps=STEPS_NS):
-    return sum(b * ns_flops(r, c, steps) for b, r, c, _, _ in shapes)
+    return sum(s[0] * ns_flops(s[1], s[2], steps) for s in shapes)
 
 
 def alg_flops(shapes, steps=STEPS_NS):
-    """Algorithmic flops with the symmetric products formed once:
-    steps (m (m+1) n + m^2 (m+1) + 2 m^2 n) per matrix."""
-    f = 0
-    for b, r, c, _, _ in shapes:
-        m, n = min(r, c), max(r, c)
-        f += b * steps * (m * (m + 1) * n + m * m * (m + 1) + 2 * m * m * n)
-    return f
+    """Algorithmic flops of the computation the library runs (matrix_flops)."""
+    return sum(gemm_flops_per_kind(shapes, steps).values())
 
 
 def algorithmic_bytes(shapes):
@@ -125,7 +139,7 @@ def algorithmic_bytes(shapes):
     fused small-m kernel moves only the compulsory bytes (G read, Mom and W
     read and written)."""
     prep = upd = fused = 0
-    for b, r, c, we, ge in shapes:
+    for b, r, c, we, ge, _ in shapes:
         e = b * r * c
         prep += e * (ge + 4 + 4 + 2)
         upd += e * (we + we + 2)
@@ -135,13 +149,11 @@ def algorithmic_bytes(shapes):
 
 def gemm_flops_per_kind(shapes, steps=STEPS_NS):
     """Algorithmic (symmetry-aware) flops of one step for each GEMM kind."""
-    gram = poly = apply = 0
-    for b, r, c, _, _ in shapes:
-        m, n = min(r, c), max(r, c)
-        gram += b * steps * m * (m + 1) * n
-        poly += b * steps * m * m * (m + 1)
-        apply += b * steps * 2 * m * m * n
-    return {"gram": gram, "poly": poly, "apply": apply}
+    out = {"gram": 0, "poly": 0, "apply": 0}
+    for b, r, c, _, _, path in shapes:
+        for k, v in matrix_flops(r, c, path, steps).items():
+            out[k] += b * v
+    return out
 
 
 class ClockSampler:
@@ -279,9 +291,9 @@ def cpu_baseline(name, samples, shapes):
         done_flops += ns_flops(r, c)
         per_core.setdefault((min(r, c), max(r, c)), []).append(dt)
     rate = done_flops / t_total                  # flop/s of the oracle on the sample
-    total_mats = sum(b for b, _, _, _, _ in shapes)
+    total_mats = sum(sh[0] for sh in shapes)
     ms, timed_mats = 0.0, 0
-    for b, r, c, _, _ in shapes:
+    for b, r, c, _, _, _ in shapes:
         core = (min(r, c), max(r, c))
         if core in per_core:
             ms += b * statistics.mean(per_core[core]) * 1e3
@@ -554,7 +566,8 @@ def _report(name, args, steps, warmup, world, shapes, t_ms, e2e, prof, clocks,
                    "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
         "alg": {"value": alg, "unit": "TFLOP/s", "peak": tpeak, "peak_kind": peak_kind,
                 "frac": alg / (world * tpeak),
-                "what": "algorithmic flops (symmetric products once) over the step time"},
+                "what": "algorithmic flops of the products the library runs (symmetric "
+                        "products once; Gram space where it is used) over the step time"},
         "e2e": None if e2e is None else {
             "value": world * flops / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
             "ms_per_step": e2e["ms"], "steps": e2e["steps"],

@@ -171,6 +171,24 @@ muon_status_t muon_step_grouped(const muon_group_t *groups, int n_groups, float 
 muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, int steps,
                                       float a, float b, float c, cudaStream_t stream);
 
+/* Which implementation runs the NS of a stored [rows, cols] matrix under
+ * configuration `cfg` (NULL = defaults), with m = min(rows, cols),
+ * n = max(rows, cols), decided on the host (no GPU work):
+ *   0  the fused small-m kernel (m <= 64): Gram-space iteration in fp32
+ *      (DMuon-2 Appendix C.3), X0 applied once, fused with the update;
+ *   1  the grouped GEMM path in X space: per step the Gram X X^T, the
+ *      polynomial b A + c A^2 and the apply X' = a X + B X ([HP] 2.3 Eq. (1));
+ *   2  the grouped GEMM path in Gram space (DMuon-2 Appendix C.3), for
+ *      n >= 2 m in bf16 mode: R_0 = X0 X0^T / ||X0||^2 once, then per step
+ *      B' = b R + c R^2 + alpha I, Q <- (a - alpha) Q + Q B',
+ *      T = (a - alpha) R + R B', R <- (a - alpha) T + T B' (all symmetric
+ *      m x m products, alpha = 0.58 a), and O = Q X0 / ||X0|| once: about
+ *      (3 r + 18) m^3 instead of (15 r + 5) m^3 flops for r = n / m.
+ * The environment variables MUON_SMALL_PATH=0, MUON_GRAM_SPACE=0 / 1 and
+ * MUON_GRAM_SPACE_RATIO (default 2) change the choice.  Returns -1 for
+ * rows or cols <= 0 or an invalid cfg. */
+int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t *cfg);
+
 /* As muon_step_grouped with an explicit NS configuration (NULL = defaults). */
 muon_status_t muon_step_grouped_ex(const muon_group_t *groups, int n_groups, float mu,
                                    int nesterov, float lr, float wd, int scale_rule,

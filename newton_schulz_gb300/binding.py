@@ -30,7 +30,9 @@ EXPORTED = (
     "muon_release_workspace", "muon_last_launch_count", "muon_profile_enable",
     "muon_profile_read", "muon_adamw_grouped", "muon_ns_cost_table", "muon_assign_owners",
     "muon_ns_batched_noalloc", "muon_debug_inject_stall", "muon_debug_guard_check",
+    "muon_ns_path",
 )
+PATH_SMALL, PATH_XSPACE, PATH_GRAM_SPACE = 0, 1, 2
 INJECT_NONE, INJECT_GEMM, INJECT_SMALL = 0, 1, 2
 
 
@@ -111,6 +113,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_ns_batched_noalloc.restype = i32
     lib.muon_debug_inject_stall.argtypes = [ctypes.c_int]
     lib.muon_debug_inject_stall.restype = i32
+    lib.muon_ns_path.argtypes = [i64, i64, ctypes.POINTER(NsConfig)]
+    lib.muon_ns_path.restype = ctypes.c_int
     lib.muon_debug_guard_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
     lib.muon_debug_guard_check.restype = i32
     lib.muon_query_status.argtypes = [vp]
@@ -265,6 +269,12 @@ def muon_debug_inject_stall(what: int) -> None:
     """Testing hook: the next launch of kind `what` (INJECT_GEMM or
     INJECT_SMALL) stalls on a wait nothing satisfies until its bound runs out."""
     check(load().muon_debug_inject_stall(int(what)), "muon_debug_inject_stall")
+
+
+def muon_ns_path(rows: int, cols: int, cfg=None) -> int:
+    """0 small-m kernel, 1 grouped GEMMs in X space, 2 grouped GEMMs in Gram
+    space, for a stored [rows, cols] matrix (host-side decision)."""
+    return load().muon_ns_path(rows, cols, ctypes.byref(cfg) if cfg is not None else None)
 
 
 def muon_debug_guard_check(stream=None) -> int:

@@ -160,6 +160,7 @@ struct Req {            // one user group
   float* Mom;
   int64_t B, r, c, m, n;
   bool trans;
+  bool gs = false;      // grouped GEMM path in Gram space (see gram_space_shape)
 };
 
 struct SliceP {
@@ -176,10 +177,12 @@ struct NsGroupP {
   int64_t tri = 1, prep_tiles = 1;
   size_t off_Xt0, off_Xt1, off_A, off_B, off_inv, off_ssq, off_part;
   size_t off_lo = 0;           // high-precision mode: Xt0, Xt1, A, B lo halves from here
+  size_t off_S[5] = {0, 0, 0, 0, 0};   // Gram space: R, T, B', Q ping-pong (m x m_pad)
   size_t ctr_prep, ctr_tile;   // element offsets in the counter buffer
 };
 
 struct ChunkP {
+  bool gs = false;             // every group of the chunk runs in Gram space
   std::vector<SliceP> slices;
   std::vector<NsGroupP> groups;
   size_t bytes = 0;
@@ -223,8 +226,14 @@ void layout_chunk(ChunkP& ch, int sms, bool precise, size_t guard) {
     const size_t e2 = 2;
     g.off_Xt0 = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
     g.off_Xt1 = take(static_cast<size_t>(g.cnt * g.n * g.m_pad) * e2);
-    g.off_A = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
-    g.off_B = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+    if (ch.gs) {
+      for (int i = 0; i < 5; ++i) g.off_S[i] = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+      g.off_A = g.off_S[kGsR];   // (the X-space maps are built on these, never used)
+      g.off_B = g.off_S[kGsB];
+    } else {
+      g.off_A = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+      g.off_B = take(static_cast<size_t>(g.cnt * g.m * g.m_pad) * e2);
+    }
     g.off_inv = take(static_cast<size_t>(g.cnt) * 4);
     g.off_ssq = take(static_cast<size_t>(g.cnt * g.prep_tiles) * 4);
     g.off_part = take(g.ksplit > 1 ? static_cast<size_t>(g.cnt * g.tri * g.ksplit) * bm * bn * 4
@@ -242,6 +251,29 @@ void layout_chunk(ChunkP& ch, int sms, bool precise, size_t guard) {
   }
   ch.bytes = off;
   ch.ctrs = ctr;
+}
+
+struct NsCfg {
+  int steps;
+  std::vector<float> coeffs;   // [steps][3]
+  float eps;
+  bool precise = false;        // MUON_NS_TF32: X0 carried as bf16 hi + lo
+};
+
+// Gram-space NS on the grouped GEMM path (DMuon-2 Appendix C.3), per core
+// shape (m, n): with the symmetric m x m products on the polynomial kernel
+// a matrix costs about (3 r + 18) m^3 algorithmic flops for r = n / m
+// (Gram once, four symmetric products per step, one final apply) against
+// (15 r + 5) m^3 in X space, so it is taken from r >= 2 on (bf16 products
+// only; MUON_GRAM_SPACE=0 / 1 forbids / forces it, MUON_GRAM_SPACE_RATIO sets
+// the r from which it is used).
+bool gram_space_shape(int64_t m, int64_t n, const NsCfg& ns) {
+  if (ns.precise || ns.steps < 1) return false;
+  const char* v = std::getenv("MUON_GRAM_SPACE");
+  if (v && v[0] == '0') return false;
+  if (v && v[0] == '1') return true;
+  const double ratio = static_cast<double>(env_size("MUON_GRAM_SPACE_RATIO", 2));
+  return static_cast<double>(n) >= ratio * static_cast<double>(m);
 }
 
 // Small-m path eligibility: core shapes with m <= 64 (MUON_SMALL_PATH=0 sends
@@ -367,14 +399,19 @@ std::vector<ChunkP> make_plan(const std::vector<Req>& reqs, int sms, bool precis
   ChunkP cur;
   int64_t cur_elems = 0;
   auto close = [&] {
+    const bool gs = cur.gs;
     if (!cur.slices.empty()) chunks.push_back(std::move(cur));
     cur = ChunkP();
+    cur.gs = gs;
     cur_elems = 0;
   };
   for (int ri : order) {
     const Req& q = reqs[ri];
     const int64_t per = q.m * q.n;
     int64_t b = 0;
+    // a chunk runs either in X space or in Gram space
+    if (!cur.slices.empty() && cur.gs != q.gs) close();
+    cur.gs = q.gs;
     while (b < q.B) {
       int ng = -1;
       for (int k = 0; k < static_cast<int>(cur.groups.size()); ++k)
@@ -535,12 +572,6 @@ struct Launcher {
   }
 };
 
-struct NsCfg {
-  int steps;
-  std::vector<float> coeffs;   // [steps][3]
-  float eps;
-  bool precise = false;        // MUON_NS_TF32: X0 carried as bf16 hi + lo
-};
 
 muon_status_t check_ns_cfg(const muon_ns_config_t* cfg, NsCfg* out) {
   if (!cfg) {
@@ -611,7 +642,11 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     for (auto& kv : shapes) {
       const int64_t m = kv.first.first, n = kv.first.second;
       if (!small_shape(m)) {
-        for (int i : kv.second) large.push_back(reqs[i]);
+        const bool gs = gram_space_shape(m, n, ns);
+        for (int i : kv.second) {
+          large.push_back(reqs[i]);
+          large.back().gs = gs;
+        }
         continue;
       }
       for (size_t b = 0; b < kv.second.size(); b += kSmallMaxSlices) {
@@ -818,54 +853,107 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         d.A_lo = reinterpret_cast<__nv_bfloat16*>(lo + 2 * xb);
         d.B_lo = reinterpret_cast<__nv_bfloat16*>(lo + 2 * xb + ab);
       }
+      if (ch.gs) {
+        d.gram_space = 1;
+        for (int i = 0; i < 5; ++i) d.S[i] = reinterpret_cast<__nv_bfloat16*>(ws + g.off_S[i]);
+        if (!ns_gs_maps(d)) return MUON_ERR_CUDA;
+      }
       if (!ns_group_maps(d)) return MUON_ERR_CUDA;
     }
-    // ---- NS iterations -----------------------------------------------------------
-    for (int it = 0; it < ns.steps; ++it) {
-      const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
-      for (int phase = 0; phase < 3; ++phase) {
-        GemmParams gp;
-        std::memset(&gp, 0, sizeof(gp));
-        int64_t tiles = 0;
-        int min_kb = 1 << 30;
-        bool split = false;
-        int64_t min_m = INT64_MAX;
+    // One grouped GEMM launch of product `epi` over every group of the chunk:
+    // fill(G, group, first tile, pair) sets the groups' descriptors; CTA pairs
+    // when the launch qualifies (bf16 products, no split-K, large shapes).
+    auto gemm = [&](int epi, auto&& fill, float a, float b, float c, float alpha,
+                    int first) -> muon_status_t {
+      GemmParams gp;
+      std::memset(&gp, 0, sizeof(gp));
+      int64_t tiles = 0;
+      int min_kb = 1 << 30;
+      bool split = false;
+      int64_t min_m = INT64_MAX;
+      for (size_t k = 0; k < ch.groups.size(); ++k) {
+        GemmGroup& G = gp.g[k];
+        fill(G, dg[k], static_cast<int>(tiles), false);
+        tiles += static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
+        min_kb = std::min(min_kb, G.kb_per_split);
+        split = split || G.ksplit > 1;
+        min_m = std::min(min_m, dg[k].m);
+      }
+      if (!ns.precise && !split && gemm_use_pair(tiles, dev->sms, min_m)) {
+        gp.pair = 1;
+        tiles = 0;
         for (size_t k = 0; k < ch.groups.size(); ++k) {
-          GemmGroup& G = gp.g[k];
-          ns_fill_group(G, dg[k], phase, it, static_cast<int>(tiles));
-          tiles += static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
-          min_kb = std::min(min_kb, G.kb_per_split);
-          split = split || G.ksplit > 1;
-          min_m = std::min(min_m, dg[k].m);
+          fill(gp.g[k], dg[k], static_cast<int>(tiles), true);
+          tiles += static_cast<int64_t>(gp.g[k].tiles_per_mat) * dg[k].cnt;
         }
-        // CTA pairs sharing the B tile (bf16 products without split-K, large shapes)
-        if (!ns.precise && !split && gemm_use_pair(tiles, dev->sms, min_m)) {
-          gp.pair = 1;
-          tiles = 0;
-          for (size_t k = 0; k < ch.groups.size(); ++k) {
-            ns_fill_group(gp.g[k], dg[k], phase, it, static_cast<int>(tiles), true);
-            tiles += static_cast<int64_t>(gp.g[k].tiles_per_mat) * dg[k].cnt;
-          }
-        }
-        gp.deep = gemm_deep(phase, min_kb);
-        gp.prec = ns.precise ? 1 : 0;
-        if (const char* d = std::getenv("MUON_GEMM_DEEP")) gp.deep = d[0] == '1';   // tuning override
-        if (tiles >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
-        gp.n_groups = static_cast<int>(ch.groups.size());
-        gp.total_tiles = static_cast<int>(tiles);
-        // X' = a X + (b A + c A^2) X is evaluated as (a - alpha) X + (B + alpha I) X:
-        // identical in exact arithmetic, but the bf16 operand B + alpha I is
-        // smaller where a X and B X cancel, which lowers the rounding error.
+      }
+      gp.deep = gemm_deep(epi, min_kb);
+      gp.prec = ns.precise ? 1 : 0;
+      if (const char* d = std::getenv("MUON_GEMM_DEEP")) gp.deep = d[0] == '1';   // tuning override
+      if (tiles >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+      gp.n_groups = static_cast<int>(ch.groups.size());
+      gp.total_tiles = static_cast<int>(tiles);
+      gp.a = a;
+      gp.b = b;
+      gp.c = c;
+      gp.alpha = alpha;
+      gp.first = first;
+      gp.status = dev->status;
+      gp.timeout_ns = timeout_ns;
+      gp.inject = take_injected_stall(kInjectGemm);
+      return L.run(1 + epi, [&] { return launch_gemm(epi, gp, stream); });
+    };
+    if (ch.gs) {
+      // ---- NS in Gram space (ns_plan.cpp): R_0, then per step B'_k, Q, T, R_{k+1}
+      st = gemm(kEpiGram, [](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+                  ns_fill_gs_gram(G, d, base, pair);
+                }, 0.f, 0.f, 0.f, 0.f, 1);
+      if (st != MUON_OK) return st;
+      int q = kGsQ0;
+      for (int it = 0; it < ns.steps; ++it) {
+        const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
         const float alpha = kShiftFrac * ca;
-        gp.a = ca - alpha;
-        gp.b = cb;
-        gp.c = cc;
-        gp.alpha = alpha;
-        gp.first = it == 0 ? 1 : 0;
-        gp.status = dev->status;
-        gp.timeout_ns = timeout_ns;
-        gp.inject = take_injected_stall(kInjectGemm);
-        st = L.run(1 + phase, [&] { return launch_gemm(phase, gp, stream); });
+        const bool more = it + 1 < ns.steps;
+        auto sym = [](int a, int b, int c) {
+          return [a, b, c](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+            ns_fill_gs_sym(G, d, a, b, c, base, pair);
+          };
+        };
+        if (it > 0 || more) {   // B'_k = b R + c R^2 + alpha I
+          st = gemm(kEpiPoly, sym(kGsR, kGsR, kGsB), 0.f, cb, cc, alpha, 0);
+          if (st != MUON_OK) return st;
+        }
+        if (it == 0) {          // Q_1 = P_0 = a I + b R_0 + c R_0^2
+          st = gemm(kEpiPoly, sym(kGsR, kGsR, q), 0.f, cb, cc, ca, 0);
+        } else {                // Q_{k+1} = (a - alpha) Q_k + Q_k B'_k
+          st = gemm(kEpiPoly, sym(q, kGsB, 2 * kGsQ0 + 1 - q), 0.f, ca - alpha, 1.f, 0.f, 0);
+          q = 2 * kGsQ0 + 1 - q;
+        }
+        if (st != MUON_OK) return st;
+        if (more) {             // T = (a - alpha) R + R B'; R_{k+1} = (a - alpha) T + T B'
+          st = gemm(kEpiPoly, sym(kGsR, kGsB, kGsT), 0.f, ca - alpha, 1.f, 0.f, 0);
+          if (st != MUON_OK) return st;
+          st = gemm(kEpiPoly, sym(kGsT, kGsB, kGsR), 0.f, ca - alpha, 1.f, 0.f, 0);
+          if (st != MUON_OK) return st;
+        }
+      }
+      // O^T = Xt_0 Q / ||X0|| (Q symmetric) into Xt_1
+      st = gemm(kEpiApply, [q](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+                  ns_fill_gs_apply(G, d, q, base, pair);
+                }, 0.f, 0.f, 0.f, 0.f, 1);
+      if (st != MUON_OK) return st;
+    }
+    // ---- NS iterations (X space) -------------------------------------------------
+    for (int it = 0; !ch.gs && it < ns.steps; ++it) {
+      const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
+      // X' = a X + (b A + c A^2) X is evaluated as (a - alpha) X + (B + alpha I) X:
+      // identical in exact arithmetic, but the bf16 operand B + alpha I is
+      // smaller where a X and B X cancel, which lowers the rounding error.
+      const float alpha = kShiftFrac * ca;
+      for (int phase = 0; phase < 3; ++phase) {
+        st = gemm(phase, [phase, it](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+                    ns_fill_group(G, d, phase, it, base, pair);
+                  }, ca - alpha, cb, cc, alpha, it == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
       }
     }
@@ -881,7 +969,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         FinSlice& fs = fp.s[i];
         const int64_t per = q.r * q.c;
         fs.W = static_cast<char*>(q.W) + s.b0 * per * esize(q.w_dtype);
-        const int fin = ns.steps & 1;
+        const int fin = ch.gs ? 1 : (ns.steps & 1);   // Gram space: O^T lands in Xt_1
         // O = Xt in the stored layout when rows > cols, else its transpose
         fs.O = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
                s.idx0 * g.n * g.m_pad;
@@ -1579,6 +1667,18 @@ void muon_release_workspace(void) {
 }
 
 int muon_last_launch_count(void) { return t_last_launches; }
+
+int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t* cfg) {
+  try {
+    NsCfg ns;
+    if (rows <= 0 || cols <= 0 || check_ns_cfg(cfg, &ns) != MUON_OK) return -1;
+    const int64_t m = std::min(rows, cols), n = std::max(rows, cols);
+    if (small_shape(m)) return 0;
+    return gram_space_shape(m, n, ns) ? 2 : 1;
+  } catch (...) {
+    return -1;
+  }
+}
 
 muon_status_t muon_debug_guard_check(cudaStream_t stream, int64_t* bad_bytes) {
   if (!bad_bytes) return MUON_ERR_INVALID_ARGUMENT;

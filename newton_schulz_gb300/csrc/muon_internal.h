@@ -138,7 +138,16 @@ struct NsGroupDev {
   __nv_bfloat16* A_lo = nullptr;
   __nv_bfloat16* B_lo = nullptr;
   CUtensorMap lo_gram[2], lo_xt[2], lo_ap, lo_aq, lo_a64, lo_bp, lo_bq, lo_b64;
+  // Gram-space NS (gram_space = 1): five m x m bf16 matrices per problem,
+  // [cnt][m][m_pad] each -- R (the Gram matrix), T = R B', B' (shifted step
+  // polynomial) and Q ping-pong -- with 128-, 256- and 64-row boxes.
+  int gram_space = 0;
+  __nv_bfloat16* S[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  CUtensorMap s_p[5], s_q[5], s_64[5];
 };
+
+// Gram-space buffers of NsGroupDev::S.
+constexpr int kGsR = 0, kGsT = 1, kGsB = 2, kGsQ0 = 3;   // Q ping-pong: kGsQ0, kGsQ0 + 1
 
 // Tiled bf16/f32 tensor map of a [dims[2]][dims[1]][dims[0]] tensor with
 // byte strides strides[0] (rows) and strides[1] (matrices).
@@ -152,6 +161,16 @@ bool ns_group_maps(NsGroupDev& g);
 // pair: the launch runs in CTA pairs (see GemmParams::pair).
 void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base,
                    bool pair = false);
+// Gram-space NS (the m x m products on the polynomial kernel):
+//   the Gram R = X0 X0^T of the input Xt[0] into S[kGsR];
+bool ns_gs_maps(NsGroupDev& g);
+void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int tile_base, bool pair);
+//   C = epilogue(A B^T) on S[a], S[b] (symmetric, commuting) into S[c], with
+//   the polynomial kernel's epilogue b' S[a] + c' (A B^T) + alpha' I;
+void ns_fill_gs_sym(GemmGroup& G, const NsGroupDev& g, int a, int b, int c, int tile_base,
+                    bool pair);
+//   the apply O^T = Xt[0] S[q] (Q symmetric) into Xt[1].
+void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int tile_base, bool pair);
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64
