@@ -104,16 +104,25 @@ def _shapes(groups):
     return out
 
 
-def matrix_flops(r, c, path, steps=STEPS_NS):
+def matrix_flops(r, c, path, steps=STEPS_NS, restart=None):
     """Algorithmic flops of one matrix's NS per GEMM kind, symmetric products
     formed once.  X space (and the small-m kernel, counted the same way):
-    steps x (Gram m(m+1)n, polynomial m^2(m+1), apply 2m^2n).  Gram space:
-    the Gram once, 4 (steps - 1) + 2 symmetric m x m products (B', Q, T, R
-    per step; B' and Q only in the last), the apply 2m^2n once."""
+    steps x (Gram m(m+1)n, polynomial m^2(m+1), apply 2m^2n).  Gram space,
+    in phases of `restart` steps (the library's restart period, 0 = one
+    phase): per phase the Gram and the apply once, and 4 (p - 1) + 2
+    symmetric m x m products for a phase of p steps (B', Q, T, R per step;
+    B' and Q only in the last; Q alone in a one-step phase)."""
     m, n = min(r, c), max(r, c)
     if path == 2:
-        nsym = 1 if steps == 1 else 4 * (steps - 1) + 2
-        return {"gram": m * (m + 1) * n, "poly": nsym * m * m * (m + 1), "apply": 2 * m * m * n}
+        if restart is None:
+            from newton_schulz_gb300 import binding
+            restart = binding.muon_ns_gram_restart()
+        period = restart
+        period = period if period > 0 else steps
+        phases = [min(period, steps - k0) for k0 in range(0, steps, period)]
+        nsym = sum(1 if p == 1 else 4 * (p - 1) + 2 for p in phases)
+        return {"gram": len(phases) * m * (m + 1) * n, "poly": nsym * m * m * (m + 1),
+                "apply": len(phases) * 2 * m * m * n}
     return {"gram": steps * m * (m + 1) * n, "poly": steps * m * m * (m + 1),
             "apply": steps * 2 * m * m * n}
 

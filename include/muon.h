@@ -178,16 +178,32 @@ muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, 
  *      (DMuon-2 Appendix C.3), X0 applied once, fused with the update;
  *   1  the grouped GEMM path in X space: per step the Gram X X^T, the
  *      polynomial b A + c A^2 and the apply X' = a X + B X ([HP] 2.3 Eq. (1));
- *   2  the grouped GEMM path in Gram space (DMuon-2 Appendix C.3), for
- *      n >= 2 m in bf16 mode: R_0 = X0 X0^T / ||X0||^2 once, then per step
- *      B' = b R + c R^2 + alpha I, Q <- (a - alpha) Q + Q B',
- *      T = (a - alpha) R + R B', R <- (a - alpha) T + T B' (all symmetric
- *      m x m products, alpha = 0.58 a), and O = Q X0 / ||X0|| once: about
- *      (3 r + 18) m^3 instead of (15 r + 5) m^3 flops for r = n / m.
- * The environment variables MUON_SMALL_PATH=0, MUON_GRAM_SPACE=0 / 1 and
- * MUON_GRAM_SPACE_RATIO (default 2) change the choice.  Returns -1 for
- * rows or cols <= 0 or an invalid cfg. */
+ *   2  the grouped GEMM path in Gram space (DMuon-2 Appendix C.3), opt-in
+ *      (bf16 mode only), in phases of P steps (P from
+ *      muon_ns_gram_restart): R = X X^T of the phase's input (the first
+ *      scaled by 1 / ||X0||^2), then per step B' = b R + c R^2 + alpha I,
+ *      Q <- (a - alpha) Q + Q B' (Q = P_k = a I + b R + c R^2 at the
+ *      phase's first step), T = (a - alpha) R + R B',
+ *      R <- (a - alpha) T + T B' (m x m products with symmetric results,
+ *      alpha = 0.58 a), and X <- Q X at the phase's end.  A phase of
+ *      P >= 2 steps takes about (3 r + 4 P - 2) m^3 flops against
+ *      (3 r + 1) P m^3 in X space, r = n / m (a one-step phase costs what
+ *      an X-space step does).
+ * Path 2 is off by default: in bf16 it rounds the m x m matrices R, B', T
+ * and Q where the X space rounds A, B' and the iterate, and its update error
+ * measured 1.3-1.8x the X-space error (near the 1e-2 ||dW|| bound for
+ * m >= 4096).  MUON_GRAM_SPACE=1 selects it for n >= MUON_GRAM_SPACE_RATIO
+ * (default 2) x m, MUON_GRAM_SPACE=force for every shape of the GEMM path;
+ * MUON_SMALL_PATH=0 sends m <= 64 to the GEMM path.  Returns -1 for rows or
+ * cols <= 0 or an invalid cfg. */
 int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t *cfg);
+
+/* The restart period P of the Gram-space NS (path 2 of muon_ns_path) in NS
+ * steps: the iteration restarts from the Gram matrix of X_k = Q X every P
+ * steps (DMuon-2 Appendix C.3, "mid-way restart"), so K steps take
+ * ceil(K / P) phases.  0 means no restart (one phase).  Default 2;
+ * the environment variable MUON_GRAM_RESTART sets it.  No GPU work. */
+int muon_ns_gram_restart(void);
 
 /* As muon_step_grouped with an explicit NS configuration (NULL = defaults). */
 muon_status_t muon_step_grouped_ex(const muon_group_t *groups, int n_groups, float mu,

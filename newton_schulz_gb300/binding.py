@@ -31,6 +31,7 @@ EXPORTED = (
     "muon_profile_read", "muon_adamw_grouped", "muon_ns_cost_table", "muon_assign_owners",
     "muon_ns_batched_noalloc", "muon_debug_inject_stall", "muon_debug_guard_check",
     "muon_ns_path",
+    "muon_ns_gram_restart",
 )
 PATH_SMALL, PATH_XSPACE, PATH_GRAM_SPACE = 0, 1, 2
 INJECT_NONE, INJECT_GEMM, INJECT_SMALL = 0, 1, 2
@@ -115,6 +116,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_debug_inject_stall.restype = i32
     lib.muon_ns_path.argtypes = [i64, i64, ctypes.POINTER(NsConfig)]
     lib.muon_ns_path.restype = ctypes.c_int
+    lib.muon_ns_gram_restart.argtypes = []
+    lib.muon_ns_gram_restart.restype = ctypes.c_int
     lib.muon_debug_guard_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
     lib.muon_debug_guard_check.restype = i32
     lib.muon_query_status.argtypes = [vp]
@@ -275,6 +278,11 @@ def muon_ns_path(rows: int, cols: int, cfg=None) -> int:
     """0 small-m kernel, 1 grouped GEMMs in X space, 2 grouped GEMMs in Gram
     space, for a stored [rows, cols] matrix (host-side decision)."""
     return load().muon_ns_path(rows, cols, ctypes.byref(cfg) if cfg is not None else None)
+
+
+def muon_ns_gram_restart() -> int:
+    """Restart period (NS steps) of the Gram-space path; 0 = no restart."""
+    return load().muon_ns_gram_restart()
 
 
 def muon_debug_guard_check(stream=None) -> int:

@@ -267,11 +267,35 @@ struct NsCfg {
 // (15 r + 5) m^3 in X space, so it is taken from r >= 2 on (bf16 products
 // only; MUON_GRAM_SPACE=0 / 1 forbids / forces it, MUON_GRAM_SPACE_RATIO sets
 // the r from which it is used).
+// Gram-space restart period in NS steps (MUON_GRAM_RESTART; 0: no restart).
+int gram_restart_period_env() {
+  const char* v = std::getenv("MUON_GRAM_RESTART");
+  if (!v || !*v) return 2;
+  const long p = std::strtol(v, nullptr, 10);
+  return p < 0 ? 2 : static_cast<int>(std::min<long>(p, 1 << 20));
+}
+
+int gram_restart_period() {
+  const int p = gram_restart_period_env();
+  return p == 0 ? (1 << 30) : p;
+}
+
+int gram_phases(int steps) {
+  const int p = gram_restart_period();
+  return steps <= 0 ? 0 : (steps + p - 1) / p;
+}
+
+// Gram space is opt-in: in bf16 it rounds R, B', T and Q (m x m) where the X
+// space rounds A, B' and the iterate, and its update error measured 1.3-1.8x
+// the X-space one (about the 1e-2 ||dW|| bound for m >= 4096).
+// MUON_GRAM_SPACE=1: shapes with n >= MUON_GRAM_SPACE_RATIO (default 2) x m;
+// MUON_GRAM_SPACE=force: every shape of the GEMM path; unset or 0: none.
 bool gram_space_shape(int64_t m, int64_t n, const NsCfg& ns) {
   if (ns.precise || ns.steps < 1) return false;
   const char* v = std::getenv("MUON_GRAM_SPACE");
-  if (v && v[0] == '0') return false;
-  if (v && v[0] == '1') return true;
+  if (!v) return false;
+  if (std::strcmp(v, "force") == 0) return true;
+  if (v[0] != '1') return false;
   const double ratio = static_cast<double>(env_size("MUON_GRAM_SPACE_RATIO", 2));
   return static_cast<double>(n) >= ratio * static_cast<double>(m);
 }
@@ -901,47 +925,56 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       gp.status = dev->status;
       gp.timeout_ns = timeout_ns;
       gp.inject = take_injected_stall(kInjectGemm);
+      gp.b_mn = ch.gs && epi != kEpiGram ? 1 : 0;   // Gram space: true products A B
       return L.run(1 + epi, [&] { return launch_gemm(epi, gp, stream); });
     };
     if (ch.gs) {
-      // ---- NS in Gram space (ns_plan.cpp): R_0, then per step B'_k, Q, T, R_{k+1}
-      st = gemm(kEpiGram, [](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-                  ns_fill_gs_gram(G, d, base, pair);
-                }, 0.f, 0.f, 0.f, 0.f, 1);
-      if (st != MUON_OK) return st;
-      int q = kGsQ0;
-      for (int it = 0; it < ns.steps; ++it) {
-        const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
-        const float alpha = kShiftFrac * ca;
-        const bool more = it + 1 < ns.steps;
-        auto sym = [](int a, int b, int c) {
-          return [a, b, c](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-            ns_fill_gs_sym(G, d, a, b, c, base, pair);
-          };
+      // ---- NS in Gram space (ns_plan.cpp): per phase of `period` steps the Gram
+      // R of the iterate, then per step B'_k, Q, T, R_{k+1}; the phase ends with
+      // the apply X <- Q X (the first one also scales by 1 / ||X0||).
+      auto sym = [](int a, int b, int c) {
+        return [a, b, c](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+          ns_fill_gs_sym(G, d, a, b, c, base, pair);
         };
-        if (it > 0 || more) {   // B'_k = b R + c R^2 + alpha I
-          st = gemm(kEpiPoly, sym(kGsR, kGsR, kGsB), 0.f, cb, cc, alpha, 0);
-          if (st != MUON_OK) return st;
-        }
-        if (it == 0) {          // Q_1 = P_0 = a I + b R_0 + c R_0^2
-          st = gemm(kEpiPoly, sym(kGsR, kGsR, q), 0.f, cb, cc, ca, 0);
-        } else {                // Q_{k+1} = (a - alpha) Q_k + Q_k B'_k
-          st = gemm(kEpiPoly, sym(q, kGsB, 2 * kGsQ0 + 1 - q), 0.f, ca - alpha, 1.f, 0.f, 0);
-          q = 2 * kGsQ0 + 1 - q;
-        }
+      };
+      const int period = gram_restart_period();
+      int src = 0;   // Xt buffer holding the iterate
+      for (int k0 = 0; k0 < ns.steps; k0 += period) {
+        const int k1 = std::min(ns.steps, k0 + period);
+        st = gemm(kEpiGram, [src](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+                    ns_fill_gs_gram(G, d, src, base, pair);
+                  }, 0.f, 0.f, 0.f, 0.f, k0 == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
-        if (more) {             // T = (a - alpha) R + R B'; R_{k+1} = (a - alpha) T + T B'
-          st = gemm(kEpiPoly, sym(kGsR, kGsB, kGsT), 0.f, ca - alpha, 1.f, 0.f, 0);
+        int q = kGsQ0;
+        for (int it = k0; it < k1; ++it) {
+          const float ca = ns.coeffs[3 * it], cb = ns.coeffs[3 * it + 1], cc = ns.coeffs[3 * it + 2];
+          const float alpha = kShiftFrac * ca;
+          const bool more = it + 1 < k1;
+          if (it > k0 || more) {   // B'_k = b R + c R^2 + alpha I
+            st = gemm(kEpiPoly, sym(kGsR, kGsR, kGsB), 0.f, cb, cc, alpha, 0);
+            if (st != MUON_OK) return st;
+          }
+          if (it == k0) {          // Q = P_k = a I + b R_k + c R_k^2
+            st = gemm(kEpiPoly, sym(kGsR, kGsR, q), 0.f, cb, cc, ca, 0);
+          } else {                 // Q <- (a - alpha) Q + Q B'_k
+            st = gemm(kEpiPoly, sym(q, kGsB, 2 * kGsQ0 + 1 - q), 0.f, ca - alpha, 1.f, 0.f, 0);
+            q = 2 * kGsQ0 + 1 - q;
+          }
           if (st != MUON_OK) return st;
-          st = gemm(kEpiPoly, sym(kGsT, kGsB, kGsR), 0.f, ca - alpha, 1.f, 0.f, 0);
-          if (st != MUON_OK) return st;
+          if (more) {              // T = (a - alpha) R + R B'; R_{k+1} = (a - alpha) T + T B'
+            st = gemm(kEpiPoly, sym(kGsR, kGsB, kGsT), 0.f, ca - alpha, 1.f, 0.f, 0);
+            if (st != MUON_OK) return st;
+            st = gemm(kEpiPoly, sym(kGsT, kGsB, kGsR), 0.f, ca - alpha, 1.f, 0.f, 0);
+            if (st != MUON_OK) return st;
+          }
         }
+        // X <- Q X (the first phase: Q X0 / ||X0||) into the other Xt buffer
+        st = gemm(kEpiApply, [q, src](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
+                    ns_fill_gs_apply(G, d, q, src, base, pair);
+                  }, 0.f, 0.f, 0.f, 0.f, k0 == 0 ? 1 : 0);
+        if (st != MUON_OK) return st;
+        src ^= 1;
       }
-      // O^T = Xt_0 Q / ||X0|| (Q symmetric) into Xt_1
-      st = gemm(kEpiApply, [q](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-                  ns_fill_gs_apply(G, d, q, base, pair);
-                }, 0.f, 0.f, 0.f, 0.f, 1);
-      if (st != MUON_OK) return st;
     }
     // ---- NS iterations (X space) -------------------------------------------------
     for (int it = 0; !ch.gs && it < ns.steps; ++it) {
@@ -969,7 +1002,8 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         FinSlice& fs = fp.s[i];
         const int64_t per = q.r * q.c;
         fs.W = static_cast<char*>(q.W) + s.b0 * per * esize(q.w_dtype);
-        const int fin = ch.gs ? 1 : (ns.steps & 1);   // Gram space: O^T lands in Xt_1
+        // the Xt buffer of the result: one per step (X space) or per phase (Gram space)
+        const int fin = (ch.gs ? gram_phases(ns.steps) : ns.steps) & 1;
         // O = Xt in the stored layout when rows > cols, else its transpose
         fs.O = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
                s.idx0 * g.n * g.m_pad;
@@ -1679,6 +1713,8 @@ int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t* cfg) {
     return -1;
   }
 }
+
+int muon_ns_gram_restart(void) { return gram_restart_period_env(); }
 
 muon_status_t muon_debug_guard_check(cudaStream_t stream, int64_t* bad_bytes) {
   if (!bad_bytes) return MUON_ERR_INVALID_ARGUMENT;

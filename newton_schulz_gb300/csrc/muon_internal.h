@@ -116,6 +116,8 @@ struct GemmParams {
                           // copy for it, so the wait on it runs out (then the status bit)
   int pair;               // 1: clusters of two CTAs share the B tile (tiles count pair
                           // tiles; mapB holds 128-row boxes for K-major B; no split-K)
+  int b_mn;               // 1 (polynomial / apply): B is read MN-major from 64 x 64 boxes,
+                          // so the product is A B rather than A B^T (B not symmetric)
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -143,7 +145,7 @@ struct NsGroupDev {
   // polynomial) and Q ping-pong -- with 128-, 256- and 64-row boxes.
   int gram_space = 0;
   __nv_bfloat16* S[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
-  CUtensorMap s_p[5], s_q[5], s_64[5];
+  CUtensorMap s_p[5], s_64[5];
 };
 
 // Gram-space buffers of NsGroupDev::S.
@@ -162,15 +164,16 @@ bool ns_group_maps(NsGroupDev& g);
 void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base,
                    bool pair = false);
 // Gram-space NS (the m x m products on the polynomial kernel):
-//   the Gram R = X0 X0^T of the input Xt[0] into S[kGsR];
+//   the Gram R = X X^T of the iterate in Xt[src] into S[kGsR];
 bool ns_gs_maps(NsGroupDev& g);
-void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int tile_base, bool pair);
-//   C = epilogue(A B^T) on S[a], S[b] (symmetric, commuting) into S[c], with
-//   the polynomial kernel's epilogue b' S[a] + c' (A B^T) + alpha' I;
+void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int src, int tile_base, bool pair);
+//   C = epilogue(S[a] S[b]) into S[c] (B read MN-major, GemmParams::b_mn), with
+//   the polynomial kernel's epilogue b' S[a] + c' (S[a] S[b]) + alpha' I;
 void ns_fill_gs_sym(GemmGroup& G, const NsGroupDev& g, int a, int b, int c, int tile_base,
                     bool pair);
-//   the apply O^T = Xt[0] S[q] (Q symmetric) into Xt[1].
-void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int tile_base, bool pair);
+//   the apply Xt[src] S[q] (the iterate times Q) into Xt[src ^ 1].
+void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int src, int tile_base,
+                      bool pair);
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64

@@ -69,6 +69,8 @@ struct Layout {
   static constexpr int smem = bar_off + 256 + 1024;
 };
 constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kApplyGroup = 16;   // apply: row tiles per group of the tile order
+constexpr int kSymGroup = 8;      // Gram / polynomial: column blocks per group
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag, unsigned* status,
@@ -119,21 +121,60 @@ __device__ __forceinline__ TileInfo decode(const GemmParams& p, int tile, int cr
   t.ksp = 0;
   t.sym_idx = 0;
   if (EPI == kEpiApply) {
-    t.row_tile = r / G.nt;
-    t.col_tile = r - t.row_tile * G.nt;
-    if (PAIR) t.row_tile = 2 * t.row_tile + crank;
+    // Rows in groups of kApplyGroup row units (row tiles, or pair rows),
+    // column-major inside a group: the ~152 tiles in flight at a time share
+    // ~16 A panels and ~10 B panels (128 x K and 256 x K bf16 each), which
+    // stay in L2 even at K = 16384, instead of streaming every B panel once
+    // per row tile.
+    const int units = PAIR ? (G.mt + 1) / 2 : G.mt;
+    constexpr int kGR = PAIR ? kApplyGroup / 2 : kApplyGroup;
+    const int span = kGR * G.nt;
+    const int g = r / span;
+    const int local = r - g * span;
+    const int ge = min(kGR, units - g * kGR);
+    t.col_tile = local / ge;
+    const int ru = g * kGR + (local - t.col_tile * ge);
+    t.row_tile = PAIR ? 2 * ru + crank : ru;
   } else {
     int idx = r / G.ksplit;
     t.ksp = r - idx * G.ksplit;
     t.sym_idx = idx;
-    int j = 0;
+    // Column blocks in groups of kSymGroup; inside a group, row units (row
+    // tiles, or pair rows) outer and the group's columns inner, each tile
+    // holding some col >= row once: unit u lies in column j iff u < rows(j),
+    // rows(j) = min(units, 2j + 2) (pair rows: min(units, j + 1)), i.e. iff
+    // j >= jmin(u) = u / 2 (pair rows: u).  The tiles in flight share a few
+    // A and B panels, as in the apply's order.
+    const int units = PAIR ? (G.mt + 1) / 2 : G.mt;
+    auto rows_u = [&](int j) { return min(units, PAIR ? j + 1 : 2 * j + 2); };
+    auto jmin = [&](int u) { return PAIR ? u : u >> 1; };
+    const int ntc = G.nt;
+    int j0 = 0, j1 = 0, w = 0, full = 0;
     for (;;) {
-      const int c = PAIR ? (sym_rows(j, G.mt) + 1) / 2 : sym_rows(j, G.mt);
-      if (idx < c) break;
-      idx -= c;
-      ++j;
+      j1 = min(ntc, j0 + kSymGroup);
+      w = j1 - j0;
+      full = rows_u(j0);                 // units that hold all w columns
+      int cnt = full * w;
+      const int top = rows_u(j1 - 1);
+      for (int u = full; u < top; ++u) cnt += j1 - jmin(u);
+      if (idx < cnt || j1 >= ntc) break;
+      idx -= cnt;
+      j0 = j1;
     }
-    t.row_tile = PAIR ? 2 * idx + crank : idx;
+    int u, j;
+    if (idx < full * w) {
+      u = idx / w;
+      j = j0 + (idx - u * w);
+    } else {
+      idx -= full * w;
+      for (u = full;; ++u) {
+        const int c = j1 - jmin(u);
+        if (idx < c) break;
+        idx -= c;
+      }
+      j = jmin(u) + idx;
+    }
+    t.row_tile = PAIR ? 2 * u + crank : u;
     t.col_tile = j;
   }
   t.kb0 = t.ksp * G.kb_per_split;
@@ -275,7 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           } else {
             ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
             ptx::tma_load_3d(sA + stage * kABytes, ma, &full[stage], kx, t.row_tile * BM, t.mat);
-            if (PAIR)   // B rows [BN/2 crank, BN/2 crank + BN/2) of the tile (128-row box)
+            if (p.b_mn) {
+              // B[k][col] in MN-major chunks of 64 columns x 64 rows (K), as the Gram's B
+              for (int h = PAIR ? 2 * crank : 0; h < (PAIR ? 2 * crank + 2 : BN / 64); ++h) {
+                if (PAIR)
+                  ptx::tma_load_3d_mc(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
+                                      t.col_tile * BN + 64 * h, kx, t.mat, 0x3);
+                else
+                  ptx::tma_load_3d(sB + stage * kBBytes + h * kChunkBytes, mb, &full[stage],
+                                   t.col_tile * BN + 64 * h, kx, t.mat);
+              }
+            } else if (PAIR)   // B rows [BN/2 crank, BN/2 crank + BN/2) of the tile (128-row box)
               ptx::tma_load_3d_mc(sB + stage * kBBytes + crank * (kBBytes / 2), mb, &full[stage], kx,
                                   t.col_tile * BN + crank * (BN / 2), t.mat, 0x3);
             else
@@ -298,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     // ---- MMA issuer --------------------------------------------------------------------
     if (lane == 0) {
       // the Gram reads both operands MN-major (A and B transpose bits)
-      constexpr uint32_t idesc =
-          ptx::idesc_bf16_f32(BM, BN) | (EPI == kEpiGram ? (1u << 15) | (1u << 16) : 0u);
+      const bool b_mn = EPI == kEpiGram || p.b_mn;
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN) | (EPI == kEpiGram ? 1u << 15 : 0u) |
+                             (b_mn ? 1u << 16 : 0u);
       int stage = 0, acc = 0;
       uint32_t phase = 0;
       bool stop = false;
@@ -328,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             const uint64_t da = EPI == kEpiGram
                                     ? ptx::sdesc_mnmajor_sw128(a0 + k * 2048, kChunkBytes, 1024)
                                     : ptx::sdesc_kmajor_sw128(a0 + k * UMMA_K * 2);
-            const uint64_t db = EPI == kEpiGram
+            const uint64_t db = b_mn
                                     ? ptx::sdesc_mnmajor_sw128(b0 + k * 2048, kChunkBytes, 1024)
                                     : ptx::sdesc_kmajor_sw128(b0 + k * UMMA_K * 2);
             ptx::umma_bf16(d, da, db, idesc, (i > 0 || k > 0) ? 1u : 0u);

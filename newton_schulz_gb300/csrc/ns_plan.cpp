@@ -177,24 +177,32 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
 // matrices: B'_k = b R_k + c R_k^2 + alpha I, T = (a - alpha) R_k + R_k B'_k,
 // R_{k+1} = (a - alpha) T + T B'_k, Q_{k+1} = (a - alpha) Q_k + Q_k B'_k
 // (Q_1 = P_0 = a I + b R_0 + c R_0^2), and O = Q_K X0 / ||X0|| at the end.
-// All of R, T, B', Q are polynomials of R_0, so they are symmetric and
-// commute: every m x m product is a symmetric product on the polynomial
-// kernel (upper tiles plus mirror), whose epilogue b' A + c' (A B^T) +
-// alpha' I gives the shifted forms with b' = a - alpha, c' = 1, alpha' = 0.
+// All of R, T, B', Q are polynomials of R_0, so their products are
+// symmetric: each runs on the polynomial kernel (upper tiles plus mirror),
+// whose epilogue b' A + c' (A B) + alpha' I gives the shifted forms with
+// b' = a - alpha, c' = 1, alpha' = 0.  The B operand is read MN-major (A B,
+// not A B^T): the tiles that cross the diagonal are stored as computed, so
+// the rounded T, R and Q carry a small antisymmetric part, and products with
+// the transpose would multiply that part by about q(l) (a - b l + c l^2)
+// (~7 for the default quintic at l = 1) every step instead of damping it.
+// The iteration restarts every few steps (the section's mid-way restart):
+// X_k = Q X is formed by one apply, R is recomputed as the Gram of X_k, and Q
+// starts again from P_k.  Without it, bf16 R loses the small eigenvalues of
+// an ill-conditioned X (R squares its condition number) and Q's growing
+// range amplifies that loss.
 
 bool ns_gs_maps(NsGroupDev& g) {
-  const int bm = gemm_block_m(), bn = gemm_block_n();
+  const int bm = gemm_block_m();
   const int64_t as = g.m * g.m_pad;
   bool ok = true;
   for (int i = 0; i < 5; ++i)
     ok = ok && make_ns_map(&g.s_p[i], g.S[i], g.m, g.m, g.cnt, g.m_pad, as, bm) &&
-         make_ns_map(&g.s_q[i], g.S[i], g.m, g.m, g.cnt, g.m_pad, as, bn) &&
          make_ns_map(&g.s_64[i], g.S[i], g.m, g.m, g.cnt, g.m_pad, as, 64);
   return ok;
 }
 
-void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int tile_base, bool pair) {
-  ns_fill_group(G, g, kEpiGram, 0, tile_base, pair);
+void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int src, int tile_base, bool pair) {
+  ns_fill_group(G, g, kEpiGram, src, tile_base, pair);   // reads Xt[src]
   G.mapC = g.s_p[kGsR];
   G.mapD = g.s_64[kGsR];
 }
@@ -203,14 +211,15 @@ void ns_fill_gs_sym(GemmGroup& G, const NsGroupDev& g, int a, int b, int c, int 
                     bool pair) {
   ns_fill_group(G, g, kEpiPoly, 0, tile_base, pair);
   G.mapA = g.s_p[a];                       // operand rows and the epilogue's b' S[a] tiles
-  G.mapB = pair ? g.s_p[b] : g.s_q[b];
+  G.mapB = g.s_64[b];                      // MN-major 64 x 64 chunks (also for pairs)
   G.mapC = g.s_p[c];
   G.mapD = g.s_64[c];
 }
 
-void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int tile_base, bool pair) {
-  ns_fill_group(G, g, kEpiApply, 0, tile_base, pair);   // reads Xt[0], writes Xt[1]
-  G.mapB = pair ? g.s_p[q] : g.s_q[q];
+void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int src, int tile_base,
+                      bool pair) {
+  ns_fill_group(G, g, kEpiApply, src, tile_base, pair);   // reads Xt[src], writes Xt[src ^ 1]
+  G.mapB = g.s_64[q];                      // Xt Q, Q read MN-major
 }
 
 }  // namespace muon

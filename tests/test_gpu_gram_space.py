@@ -1,13 +1,17 @@
 """Gram-space Newton-Schulz on the grouped GEMM path (DMuon-2 Appendix C.3).
 
-For n >= 2 m the library iterates on the m x m Gram matrix:
-R_0 = X0 X0^T / ||X0||^2, per step B' = b R + c R^2 + alpha I,
-Q <- (a - alpha) Q + Q B', T = (a - alpha) R + R B', R <- (a - alpha) T + T B',
-and O = Q X0 / ||X0|| once, every m x m product a symmetric product on the
-polynomial kernel.  In exact arithmetic this is the X-space iteration; in
-bf16 it rounds R, B', T and Q instead of the iterate, so the test holds it to
-the same tolerances against the float64 oracle: NS error <= 3e-2 per matrix
-and W' within 1e-2 * ||dW||.  MUON_GRAM_SPACE=1 / 0 forces either form.
+For n >= 2 m the library iterates on the m x m Gram matrix in phases of P
+steps (the restart period, default 2): R = X X^T of the phase's input, per
+step B' = b R + c R^2 + alpha I, Q <- (a - alpha) Q + Q B',
+T = (a - alpha) R + R B', R <- (a - alpha) T + T B', and X <- Q X at the
+phase's end.  In exact arithmetic this is the X-space iteration; in bf16 it
+rounds R, B', T and Q instead of the iterate, so the test holds it to the same
+tolerances against the float64 oracle: NS error <= 3e-2 per matrix and W'
+within 1e-2 * ||dW||.  On ill-conditioned inputs, where bf16 NS in either
+form is farther from the float64 result, Gram space is held to 2.5x the
+X-space error of the same input.  Gram space is opt-in: MUON_GRAM_SPACE=1
+selects it for n >= 2 m, =force for every shape (used here), unset or 0
+for none; MUON_GRAM_RESTART sets P (0: no restart).
 """
 import numpy as np
 import pytest
@@ -28,7 +32,7 @@ def _dev(lib, cuda_ok):
 
 
 def _ns(x, gs, monkeypatch, **cfgkw):
-    monkeypatch.setenv("MUON_GRAM_SPACE", "1" if gs else "0")
+    monkeypatch.setenv("MUON_GRAM_SPACE", "force" if gs else "0")
     out = torch.empty_like(x)
     binding.muon_ns_batched_ex(x, binding.make_config(**cfgkw), out)
     torch.cuda.synchronize()
@@ -42,13 +46,23 @@ def _errs(got, x, **kw):
     return [float(np.linalg.norm(g[i] - ref[i]) / np.linalg.norm(ref[i])) for i in range(g.shape[0])]
 
 
-def test_path_choice():
+def test_path_choice(monkeypatch):
+    assert binding.muon_ns_gram_restart() == 2
+    monkeypatch.setenv("MUON_GRAM_RESTART", "0")
+    assert binding.muon_ns_gram_restart() == 0
+    monkeypatch.delenv("MUON_GRAM_RESTART")
+    monkeypatch.delenv("MUON_GRAM_SPACE", raising=False)
+    assert binding.muon_ns_path(1024, 4096) == binding.PATH_XSPACE        # opt-in
+    monkeypatch.setenv("MUON_GRAM_SPACE", "1")
     assert binding.muon_ns_path(1024, 4096) == binding.PATH_GRAM_SPACE
     assert binding.muon_ns_path(14336, 4096) == binding.PATH_GRAM_SPACE
     assert binding.muon_ns_path(4096, 4096) == binding.PATH_XSPACE
     assert binding.muon_ns_path(24, 10240) == binding.PATH_SMALL
     assert binding.muon_ns_path(1024, 4096, binding.make_config(precision=binding.NS_TF32)) == \
         binding.PATH_XSPACE
+    monkeypatch.setenv("MUON_GRAM_SPACE", "force")
+    assert binding.muon_ns_path(4096, 4096) == binding.PATH_GRAM_SPACE
+    assert binding.muon_ns_path(24, 10240) == binding.PATH_SMALL
 
 
 @pytest.mark.parametrize("shape", [
@@ -67,6 +81,37 @@ def test_gram_space_matches_oracle(shape, monkeypatch):
     assert max(eg) <= NS_TOL and max(ex) <= NS_TOL
 
 
+@pytest.mark.parametrize("period", ["0", "1", "3", "5"])
+def test_gram_space_restart_periods(period, monkeypatch):
+    """Every restart period gives the X-space result on well-conditioned
+    inputs; period 1 is one Gram, one Q = P(R) and one apply per step."""
+    monkeypatch.setenv("MUON_GRAM_RESTART", period)
+    x = torch.randn((2, 256, 1024), generator=torch.Generator().manual_seed(7)).cuda()
+    assert max(_errs(_ns(x, True, monkeypatch), x)) <= NS_TOL
+
+
+def _ill_conditioned(kind, m, n, seed):
+    """Rectangular inputs with a wide spectrum: U diag(s) V^T with
+    log-spaced s over `kind` decades, or a rank-8 signal x 10 plus noise."""
+    rng = np.random.default_rng(seed)
+    if kind == "lowrank":
+        x = rng.standard_normal((m, 8)) @ rng.standard_normal((8, n)) * 10 + rng.standard_normal((m, n))
+    else:
+        u = np.linalg.qr(rng.standard_normal((m, m)))[0]
+        v = np.linalg.qr(rng.standard_normal((n, m)))[0]
+        x = (u * np.logspace(0, -kind, m)) @ v.T
+    return torch.from_numpy(x[None]).float().cuda()
+
+
+@pytest.mark.parametrize("kind", [1, 2, 3, 5, "lowrank"])
+def test_gram_space_ill_conditioned(kind, monkeypatch):
+    x = _ill_conditioned(kind, 256, 1024, 11)
+    eg = max(_errs(_ns(x, True, monkeypatch), x))
+    ex = max(_errs(_ns(x, False, monkeypatch), x))
+    print(f"{kind}: Gram space {eg:.4f}, X space {ex:.4f}")
+    assert eg <= 2.5 * ex + 1e-3
+
+
 @pytest.mark.parametrize("steps", [1, 2, 3])
 def test_gram_space_steps_and_tables(steps, monkeypatch):
     x = torch.randn((2, 192, 800), generator=torch.Generator().manual_seed(steps)).cuda()
@@ -77,7 +122,7 @@ def test_gram_space_steps_and_tables(steps, monkeypatch):
 
 def test_gram_space_step_weights(monkeypatch):
     """One Muon step over mixed groups in Gram space, W' against the oracle."""
-    monkeypatch.setenv("MUON_GRAM_SPACE", "1")
+    monkeypatch.setenv("MUON_GRAM_SPACE", "force")
     groups = [synth.random_group((3, 256, 1024), torch.bfloat16, torch.float32, "cuda", 1, 1e-3),
               synth.random_group((2, 1536, 384), torch.float32, torch.float32, "cuda", 2, 1.0, 0.5)]
     host = [{k: g[k].double().cpu().numpy() for k in ("W", "G", "Mom")} for g in groups]
