@@ -78,6 +78,10 @@ def _peaks():
 TRAFFIC = {
     ("fused_small", "c2"): {"bytes": 201.751296e6 + 127.017984e6, "src_hash": "0fde2a6a8deff14d",
                             "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h")},
+    # large sweep: mean over the 160 apply launches of 4 steps (40 per step,
+    # every chunk and NS step), one-pass capture of the full-size workload
+    ("apply", "c5"): {"bytes": (1498461506304.0 + 143152190720.0) / 160, "src_hash": "389945b7070c7c68",
+                      "sources": ("ns_gemm.cu", "sm100_ptx.cuh", "muon_internal.h")},
 }
 
 def _traffic(kind, config):

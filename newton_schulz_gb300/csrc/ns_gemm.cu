@@ -11,7 +11,9 @@
 //                            split-K over the long side for few tiles.
 //   Poly   B' = b*A + c*A A + alpha*I   A is symmetric, so A A = A A^T:
 //                            K-major operands; the rest is fused in the
-//                            epilogue; symmetric output.
+//                            epilogue; symmetric output.  The Gram-space
+//                            products (GemmParams::b_mn) read B MN-major
+//                            and form S[a] S[b], not S[a] S[b]^T.
 //   Apply  Xt' = (a - alpha)*Xt + Xt B'   (B' symmetric), K-major operands;
 //                            the epilogue reads the Xt tile and writes the
 //                            Xt' tile through shared memory with TMA.
@@ -31,7 +33,8 @@
 //               the accumulator is waited for.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
 // tile t+1.  Tiles of all matrices of all core-shape groups of a chunk form
-// one static round-robin schedule.  Every wait is bounded; on a timeout a
+// one static round-robin schedule, ordered in column groups (decode) so that
+// the CTAs running at one time share operand panels in L2.  Every wait is bounded; on a timeout a
 // status bit is set, in-flight copies are drained, TMEM is freed and the CTA
 // returns.
 #include "muon_internal.h"
