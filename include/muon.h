@@ -58,7 +58,9 @@ typedef enum muon_status_t {
   MUON_ERR_OUT_OF_MEMORY = 4,    /* workspace allocation failed                         */
   MUON_ERR_CUDA = 5,             /* a CUDA runtime/driver call or launch failed         */
   MUON_ERR_TIMEOUT = 6,          /* device: a bounded wait gave up (status word only)   */
-  MUON_ERR_NONFINITE = 7         /* device: a matrix norm was NaN/Inf (status word only)*/
+  MUON_ERR_NONFINITE = 7,        /* device: a matrix norm was NaN/Inf (status word only)*/
+  MUON_ERR_BOUNDS = 8            /* device, MUON_DEBUG builds only: an index or TMA
+                                    coordinate check failed, the access was skipped   */
 } muon_status_t;
 
 typedef enum muon_dtype_t { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype_t;
@@ -296,10 +298,20 @@ typedef struct muon_unit_t {
 muon_status_t muon_assign_owners(const muon_unit_t *units, int n_units, int n_ranks, double eps,
                                  int32_t *owner_out);
 
-/* Read and clear the current device's status word (MUON_OK, MUON_ERR_TIMEOUT
- * or MUON_ERR_NONFINITE; the first bit set wins in that order of severity).
+/* Read and clear the current device's status word (MUON_OK, MUON_ERR_BOUNDS,
+ * MUON_ERR_TIMEOUT or MUON_ERR_NONFINITE; the first bit set wins in that
+ * order: a skipped out-of-range copy also makes its consumer's wait run out).
+ * MUON_ERR_BOUNDS comes only from a library built with -DMUON_DEBUG
+ * (newton_schulz_gb300.build --debug: libmuon_debug.so), whose kernels check
+ * every tiled TMA copy's innermost coordinate (a multiple of 16 bytes), the
+ * matrix and tile indices of every GEMM tile, the split-K partial slots and
+ * the element ranges of the streaming kernels, and skip a failing access.
  * The caller synchronises `stream` first; this call synchronises it again. */
 muon_status_t muon_query_status(cudaStream_t stream);
+
+/* 1 when the library was built with -DMUON_DEBUG (the bounds-checking build
+ * described at muon_query_status), else 0. */
+int muon_debug_build(void);
 
 /* Testing hook for the failure path of the device-side waits (no counterpart
  * on the pages).  Every wait in the library's kernels is bounded by

@@ -17,7 +17,7 @@ MUON_OK = 0
 STATUS_NAMES = {
     0: "MUON_OK", 1: "MUON_ERR_INVALID_ARGUMENT", 2: "MUON_ERR_UNSUPPORTED",
     3: "MUON_ERR_ALIAS", 4: "MUON_ERR_OUT_OF_MEMORY", 5: "MUON_ERR_CUDA",
-    6: "MUON_ERR_TIMEOUT", 7: "MUON_ERR_NONFINITE",
+    6: "MUON_ERR_TIMEOUT", 7: "MUON_ERR_NONFINITE", 8: "MUON_ERR_BOUNDS",
 }
 MUON_F32, MUON_BF16 = 0, 1
 SCALE_SQRT_MAX1_R_OVER_C, SCALE_RMS_0P2_SQRT_MAXDIM, SCALE_ONE = 0, 1, 2
@@ -32,6 +32,7 @@ EXPORTED = (
     "muon_ns_batched_noalloc", "muon_debug_inject_stall", "muon_debug_guard_check",
     "muon_ns_path",
     "muon_ns_gram_restart",
+    "muon_debug_build",
 )
 PATH_SMALL, PATH_XSPACE, PATH_GRAM_SPACE = 0, 1, 2
 INJECT_NONE, INJECT_GEMM, INJECT_SMALL = 0, 1, 2
@@ -77,11 +78,13 @@ class Unit(ctypes.Structure):
 _lib = None
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libmuon.so (raises OSError when it is missing)."""
+def load(path: str = None) -> ctypes.CDLL:
+    """Load libmuon.so, or the library MUON_LIB_PATH names (the -DMUON_DEBUG
+    build, libmuon_debug.so); raises OSError when it is missing."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("MUON_LIB_PATH") or LIB_PATH
     if not os.path.exists(path):
         raise OSError(f"{path} not found: build it with `python -m newton_schulz_gb300.build`")
     lib = ctypes.CDLL(path)
@@ -118,6 +121,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_ns_path.restype = ctypes.c_int
     lib.muon_ns_gram_restart.argtypes = []
     lib.muon_ns_gram_restart.restype = ctypes.c_int
+    lib.muon_debug_build.argtypes = []
+    lib.muon_debug_build.restype = ctypes.c_int
     lib.muon_debug_guard_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
     lib.muon_debug_guard_check.restype = i32
     lib.muon_query_status.argtypes = [vp]
@@ -283,6 +288,11 @@ def muon_ns_path(rows: int, cols: int, cfg=None) -> int:
 def muon_ns_gram_restart() -> int:
     """Restart period (NS steps) of the Gram-space path; 0 = no restart."""
     return load().muon_ns_gram_restart()
+
+
+def muon_debug_build() -> bool:
+    """True for the -DMUON_DEBUG build (libmuon_debug.so)."""
+    return bool(load().muon_debug_build())
 
 
 def muon_debug_guard_check(stream=None) -> int:

@@ -4,7 +4,12 @@ Each translation unit is compiled in parallel, then linked with the static
 CUDA runtime, so the library loads on a machine without a GPU driver (the
 driver is reached at run time through the runtime's entry-point query).
 
-    python -m newton_schulz_gb300.build [--force] [-v]
+    python -m newton_schulz_gb300.build [--force] [-v] [--debug]
+
+--debug builds libmuon_debug.so (objects in _build_debug/) with -DMUON_DEBUG:
+the kernels check their TMA coordinates, tile indices and element ranges and
+report a failed check as MUON_ERR_BOUNDS (see include/muon.h).  Load it with
+MUON_LIB_PATH=<path> in the environment of the process.
 """
 from __future__ import annotations
 
@@ -17,6 +22,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmuon.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libmuon_debug.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cpp", "ns_plan.cpp", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "noalloc.cu", "adamw.cu", "owners.cpp"]
@@ -40,17 +47,19 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    extra_flags = list(extra_flags or []) + (["-DMUON_DEBUG=1"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "muon.h")]
     objs, jobs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         objs.append(obj)
         if force or _stale(obj, [path] + hdrs):
-            cmd = [nvcc] + ARCH + NVCC_FLAGS + list(extra_flags or []) + ["-c", path, "-o", obj]
+            cmd = [nvcc] + ARCH + NVCC_FLAGS + extra_flags + ["-c", path, "-o", obj]
             if src.endswith(".cu"):
                 cmd += ["-Xptxas", "-v"] if verbose else []
             jobs.append(cmd)
@@ -62,15 +71,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    if force or jobs or _stale(LIB, objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", LIB] + objs
+    if force or jobs or _stale(lib, objs):
+        cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", lib] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-            raise RuntimeError("link of libmuon.so failed")
-    return LIB
+            raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

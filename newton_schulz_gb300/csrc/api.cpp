@@ -1031,6 +1031,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       if (blocks >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
       fp.n_slices = static_cast<int>(ch.slices.size());
       fp.total_blocks = static_cast<int>(blocks);
+      fp.status = dev->status;
       fp.step_mode = step_mode ? 1 : 0;
       fp.lr = lr;
       fp.wd = wd;
@@ -1644,6 +1645,7 @@ muon_status_t muon_query_status(cudaStream_t stream) {
     if (v) {
       for (auto& kv : g_ws) kv.second.dirty = true;
     }
+    if (v & kDevBounds) return MUON_ERR_BOUNDS;
     if (v & kDevTimeout) return MUON_ERR_TIMEOUT;
     if (v & kDevNonfinite) return MUON_ERR_NONFINITE;
     return MUON_OK;
@@ -1662,6 +1664,7 @@ const char* muon_status_string(muon_status_t s) {
     case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
     case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
     case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
+    case MUON_ERR_BOUNDS: return "MUON_ERR_BOUNDS";
     default: return "MUON_ERR_UNKNOWN";
   }
 }
@@ -1715,6 +1718,14 @@ int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t* cfg) {
 }
 
 int muon_ns_gram_restart(void) { return gram_restart_period_env(); }
+
+int muon_debug_build(void) {
+#ifdef MUON_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 muon_status_t muon_debug_guard_check(cudaStream_t stream, int64_t* bad_bytes) {
   if (!bad_bytes) return MUON_ERR_INVALID_ARGUMENT;

@@ -115,6 +115,10 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
     for (int j = 0; j < 8; ++j) d[j] = 0.f;
     int nvalid = 0;
     if (gr < s.r && gc < s.c) nvalid = (int)min((int64_t)8, s.c - gc);
+    // debug builds: the element range lies in the slice's tensors
+    if (nvalid > 0 && !dbg_ok(mat < s.count && moff + gr * s.c + gc + nvalid <= (int64_t)s.count * s.r * s.c,
+                              p.status))
+      nvalid = 0;
     if (nvalid > 0) {
       const int64_t e = moff + gr * s.c + gc;
       float g[8];
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
       for (int j = 0; j < 8; ++j)
         if (j >= nvalid) d[j] = 0.f;
       // [r][c] copy: the padded workspace row always has room for 8 elements.
-      if (s.direct) {
+      if (s.direct && dbg_ok(gc + 8 <= s.pitch_d, p.status)) {
         const int64_t o = (int64_t)mat * s.mstride_d + gr * s.pitch_d + gc;
         *reinterpret_cast<uint4*>(s.direct + o) = pack8_bf16(d);
         if (s.direct_lo) *reinterpret_cast<uint4*>(s.direct_lo + o) = pack8_bf16_lo(d);
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
     const int64_t gcc = c0 + lcc;
     const int lrr = tx * 8;
     const int64_t grr = r0 + lrr;
-    if (s.transp && gcc < s.c && grr < s.r) {
+    if (s.transp && gcc < s.c && grr < s.r && dbg_ok(grr + 8 <= s.pitch_t, p.status)) {
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = sD[lrr + j][lcc];
@@ -262,7 +266,8 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
       float f[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] = 0.f;
-      if (xr < s.c) {
+      // (the loads below touch [xc, min(xc + 8, r)) of the row)
+      if (xr < s.c && dbg_ok(mat < s.count && min(xc + 8, s.r) <= s.pitch_o, p.status)) {
         const int64_t o = (int64_t)mat * s.mstride_o + xr * s.pitch_o + xc;
         if (xc + 8 <= s.r) {
           load8_bf16(s.O + o, f);
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     gr = (int64_t)ti * kFinRows + ty;
     gc = (int64_t)tj * kFinCols + tx * 8;
-    if (gr < s.r && gc < s.c) {
+    if (gr < s.r && gc < s.c && dbg_ok(mat < s.count && gc + 8 <= s.pitch_o, p.status)) {
       const int64_t oo = (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc;
       load8_bf16(s.O + oo, o);
       if (s.O_lo) {
@@ -303,6 +308,10 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   }
   if (gr >= s.r || gc >= s.c) return;
   const int nvalid = (int)min((int64_t)8, s.c - gc);
+  // debug builds: the element range lies in the slice's W
+  if (!dbg_ok(mat < s.count && ((int64_t)mat * s.r + gr) * s.c + gc + nvalid <= (int64_t)s.count * s.r * s.c,
+              p.status))
+    return;
 
   const float os = s.inv ? s.inv[mat] : 1.f;
   const int64_t e = (int64_t)mat * s.r * s.c + gr * s.c + gc;

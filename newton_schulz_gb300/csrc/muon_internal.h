@@ -13,6 +13,23 @@ namespace muon {
 // ---- device status word bits ------------------------------------------------
 constexpr unsigned kDevTimeout = 1u;
 constexpr unsigned kDevNonfinite = 2u;
+constexpr unsigned kDevBounds = 4u;   // debug builds: an index or TMA coordinate check failed
+
+#ifdef __CUDACC__
+// Debug builds (-DMUON_DEBUG): a failed check sets kDevBounds in the status
+// word and the caller skips the access it guards (a skipped copy leaves its
+// consumer to run into a bounded wait).  In release builds it is `true`.
+__device__ __forceinline__ bool dbg_ok(bool ok, unsigned* status) {
+#ifdef MUON_DEBUG
+  if (!ok) atomicOr(status, kDevBounds);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+#endif
 
 // ---- limits ------------------------------------------------------------------
 constexpr int kMaxSlices = 64;    // user (group, batch-range) pieces per launch
@@ -78,6 +95,7 @@ struct FinParams {
   int total_blocks;
   int step_mode;
   float lr, wd;
+  unsigned* status;            // device status word (debug-build checks)
 };
 
 // ---- NS GEMM phases -----------------------------------------------------------

@@ -266,6 +266,7 @@ extern "C" muon_status_t muon_ns_batched_noalloc(void* X, int64_t B, int64_t M, 
     fs.scale = 1.f;
     fp.n_slices = 1;
     fp.total_blocks = static_cast<int>(fin_blocks);
+    fp.status = status;
     fp.step_mode = 0;
     if (launch_finish(fp, stream) != cudaSuccess) return MUON_ERR_CUDA;
   }

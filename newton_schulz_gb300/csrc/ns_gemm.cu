@@ -109,6 +109,19 @@ __device__ __forceinline__ int sym_rows(int j, int ntr) {
   return r < ntr ? r : ntr;
 }
 
+// Debug builds: the decoded tile lies in its group -- matrix index, row tile
+// (a pair's second row tile may be one past the last), column tile, split and
+// K-block range.  Every TMA coordinate derives from these as a multiple of 64
+// elements, which keeps its innermost coordinate 16-byte aligned.
+template <int EPI, bool PAIR>
+__device__ __forceinline__ bool tile_in_range(const GemmParams& p, const TileInfo& t) {
+  if (t.gi < 0 || t.gi >= p.n_groups) return false;
+  const GemmGroup& G = p.g[t.gi];
+  return t.mat >= 0 && t.mat < G.count && t.row_tile >= 0 && t.row_tile < G.mt + (PAIR ? 1 : 0) &&
+         t.col_tile >= 0 && t.col_tile < G.nt && t.kb0 >= 0 && t.nkb >= 0 &&
+         t.kb0 + t.nkb <= G.num_kb && (EPI != kEpiGram || (t.ksp >= 0 && t.ksp < G.ksplit));
+}
+
 // PAIR: `tile` numbers pair tiles (two row tiles sharing a column tile, one
 // per CTA of the pair); crank picks this CTA's row tile.
 template <int EPI, bool PAIR>
@@ -284,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       bool stop = false;
       for (int tile = tile0; tile < p.total_tiles && !stop; tile += tstep) {
         const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
+        if (!dbg_ok(tile_in_range<EPI, PAIR>(p, t), p.status)) break;   // consumers time out
         const GemmGroup& G = p.g[t.gi];
         for (int i = 0; i < t.nkb * NSEG; ++i) {
           if (!wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, p.timeout_ns, true)) {
@@ -580,8 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         }
       } else {
         const int64_t gr = (int64_t)row0 + row;
-        const bool split = G.ksplit > 1;
         const int64_t slot = (int64_t)t.mat * G.tiles_per_mat / G.ksplit + t.sym_idx;
+        // debug builds: a slot outside the partial buffer is stored directly instead
+        const bool split =
+            G.ksplit > 1 &&
+            dbg_ok(slot >= 0 && slot < (int64_t)G.count * (G.tiles_per_mat / G.ksplit) &&
+                       t.ksp >= 0 && t.ksp < G.ksplit,
+                   p.status);
         float* part = split ? G.partial + slot * G.ksplit * (int64_t)(BM * BN) : nullptr;
         if (split) {
           // partial tile -> global (valid entries only), then the last split reduces

@@ -747,7 +747,7 @@ __device__ __forceinline__ void epi_tile(const ItemCfg& c, int c0, uint8_t* st, 
     if (lane == 0) {
       if (q4 == 0) {
         const uint64_t tok = ptx::mbar_arrive_token(stw);
-        if (mwait_token(stw, tok, ctx)) {
+        if (mwait_token(stw, tok, ctx) && dbg_ok(((c.col0 + c0) & 7) == 0, ctx.status)) {
           ptx::tma_store_3d(c.wmap, ws, static_cast<int>(c.col0 + c0), 0, c.z);
           ptx::bulk_commit();
           ptx::bulk_wait_read<0>();
@@ -1006,13 +1006,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           const int x = L.trans ? 0 : static_cast<int>(gj0);
           const int y = L.trans ? static_cast<int>(gj0) : 0;
           ptx::mbar_arrive_expect_tx(full, L.tx);
-          if (kind == kStageP1) {
+          // debug builds: the innermost coordinate is a multiple of 16 bytes
+          // for both the bf16 and the fp32 tensor; the image copy is aligned
+          const uint8_t* img = L.img + (c0 / 64) * xs * chunk_bytes;
+          const uint32_t img_bytes = static_cast<uint32_t>(2 * xs * chunk_bytes);
+          if (!dbg_ok((x & 7) == 0, ctx.status)) {
+          } else if (kind == kStageP1) {
             ptx::tma_load_3d(st, L.tm, full, x, y, L.z);
             if (step_mode) ptx::tma_load_3d(st + L.mom_off, L.tm + 1, full, x, y, L.z);
-          } else {
+          } else if (dbg_ok(((reinterpret_cast<uintptr_t>(img) | img_bytes |
+                              ptx::smem_u32(st + x_off)) & 15) == 0,
+                            ctx.status)) {
             if (L.bulk) ptx::tma_load_3d(st, L.tm, full, x, y, L.z);
-            ptx::bulk_load(st + x_off, L.img + (c0 / 64) * xs * chunk_bytes,
-                           static_cast<uint32_t>(2 * xs * chunk_bytes), full);
+            ptx::bulk_load(st + x_off, img, img_bytes, full);
           }
         } else {
           ptx::mbar_arrive(full);
@@ -1084,8 +1090,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           if (item >= 0) {
             ptx::fence_proxy_async_global();
             ptx::mbar_arrive_expect_tx(&B->q_full[b], static_cast<uint32_t>(qbytes));
-            ptx::bulk_load(sm + off_q + b * qbytes, qimg + static_cast<size_t>(item / nb) * qbytes,
-                           static_cast<uint32_t>(qbytes), &B->q_full[b]);
+            const uint8_t* qsrc = qimg + static_cast<size_t>(item / nb) * qbytes;
+            if (dbg_ok(((reinterpret_cast<uintptr_t>(qsrc) | static_cast<uintptr_t>(qbytes)) & 15) == 0,
+                       ctx.status))
+              ptx::bulk_load(sm + off_q + b * qbytes, qsrc, static_cast<uint32_t>(qbytes),
+                             &B->q_full[b]);
             qk_last[b] = k;
           }
         }
