@@ -81,6 +81,13 @@ __device__ __forceinline__ int find_slice(const Slice* s, int n, int blk) {
   return lo;
 }
 
+// Column of element (r, c) of the prep kernel's 64 x 64 fp32 tile (pitch 65):
+// an XOR of bits 2..4 of c with bits 3..5 of r and of c, which leaves each of
+// the tile's access patterns -- 8-wide row writes, 8-deep column reads and
+// 16-wide row or column reads for the norm -- one wavefront per warp
+// instruction (a bijection within each row; checked exhaustively on the host).
+__device__ __forceinline__ int prep_col(int r, int c) { return c ^ ((((r >> 3) ^ (c >> 3)) & 7) << 2); }
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -170,7 +177,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sD[lr][lc + j] = d[j];
+    for (int j = 0; j < 8; ++j) sD[lr][prep_col(lr, lc + j)] = d[j];
   }
   __syncthreads();
   // [c][r] copy from the shared-memory tile.
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
     if (s.transp && gcc < s.c && grr < s.r && dbg_ok(grr + 8 <= s.pitch_t, p.status)) {
       float v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = sD[lrr + j][lcc];
+      for (int j = 0; j < 8; ++j) v[j] = sD[lrr + j][prep_col(lrr + j, lcc)];
       const int64_t o = (int64_t)mat * s.mstride_t + gcc * s.pitch_t + grr;
       *reinterpret_cast<uint4*>(s.transp + o) = pack8_bf16(v);
       if (s.transp_lo) *reinterpret_cast<uint4*>(s.transp_lo + o) = pack8_bf16_lo(v);
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
     const int xi = threadIdx.x >> 2, xj0 = (threadIdx.x & 3) * 16;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float v = s.trans ? sD[xj0 + j][xi] : sD[xi][xj0 + j];
+      const float v = s.trans ? sD[xj0 + j][prep_col(xj0 + j, xi)] : sD[xi][prep_col(xi, xj0 + j)];
       ssq = fmaf(v, v, ssq);
     }
   }

@@ -146,3 +146,17 @@ def test_gram_space_pairs_bitwise(monkeypatch):
         monkeypatch.setenv("MUON_GEMM_PAIR", pair)
         outs.append(_ns(x, True, monkeypatch))
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("shape", [(1, 4096, 14336), (1, 14336, 4096), (2, 1024, 4096)])
+def test_gram_space_full_size_llama_shapes(shape, monkeypatch):
+    """The Llama-3-8B shapes Gram space would take with MUON_GRAM_SPACE=1
+    (gate/up/down and k/v), at full size: NS error against the float64 oracle
+    within 3e-2; the X-space error of the same input printed beside it."""
+    x = torch.randn(shape, generator=torch.Generator().manual_seed(shape[1] + shape[2])).cuda()
+    monkeypatch.setenv("MUON_GRAM_SPACE", "1")
+    assert binding.muon_ns_path(shape[1], shape[2]) == binding.PATH_GRAM_SPACE
+    eg = _errs(_ns(x, True, monkeypatch), x)
+    ex = _errs(_ns(x, False, monkeypatch), x)
+    print(f"{shape}: Gram space {max(eg):.4f}, X space {max(ex):.4f}")
+    assert max(eg) <= NS_TOL
