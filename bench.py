@@ -76,11 +76,11 @@ def _peaks():
 # valid only while the kernel's sources hash to the recorded value; otherwise
 # the roofline reports traffic = null.
 TRAFFIC = {
-    ("fused_small", "c2"): {"bytes": 201.751296e6 + 127.017984e6, "src_hash": "0fde2a6a8deff14d",
+    ("fused_small", "c2"): {"bytes": 201.759744e6 + 127.020288e6, "src_hash": "e4d6633f5679ae0e",
                             "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h")},
     # large sweep: mean over the 160 apply launches of 4 steps (40 per step,
     # every chunk and NS step), one-pass capture of the full-size workload
-    ("apply", "c5"): {"bytes": (1498461506304.0 + 143152190720.0) / 160, "src_hash": "389945b7070c7c68",
+    ("apply", "c5"): {"bytes": (1498490707968.0 + 143154965504.0) / 160, "src_hash": "fd2f587338fb0111",
                       "sources": ("ns_gemm.cu", "sm100_ptx.cuh", "muon_internal.h")},
 }
 
