@@ -885,8 +885,9 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       if (!ns_group_maps(d)) return MUON_ERR_CUDA;
     }
     // One grouped GEMM launch of product `epi` over every group of the chunk:
-    // fill(G, group, first tile, pair) sets the groups' descriptors; CTA pairs
-    // when the launch qualifies (bf16 products, no split-K, large shapes).
+    // fill(G, group, first tile, mode) sets the groups' descriptors for single
+    // tiles (mode 0), CTA pairs (1) or WIDE blocks (2); pairs or WIDE blocks
+    // when the launch qualifies (bf16 products, no split-K; ns_plan.cpp).
     auto gemm = [&](int epi, auto&& fill, float a, float b, float c, float alpha,
                     int first) -> muon_status_t {
       GemmParams gp;
@@ -895,19 +896,29 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       int min_kb = 1 << 30;
       bool split = false;
       int64_t min_m = INT64_MAX;
+      double kb_sum = 0.0;
       for (size_t k = 0; k < ch.groups.size(); ++k) {
         GemmGroup& G = gp.g[k];
-        fill(G, dg[k], static_cast<int>(tiles), false);
-        tiles += static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
+        fill(G, dg[k], static_cast<int>(tiles), 0);
+        const int64_t gt = static_cast<int64_t>(G.tiles_per_mat) * dg[k].cnt;
+        tiles += gt;
+        kb_sum += static_cast<double>(gt) * G.kb_per_split;
         min_kb = std::min(min_kb, G.kb_per_split);
         split = split || G.ksplit > 1;
         min_m = std::min(min_m, dg[k].m);
       }
-      if (!ns.precise && !split && gemm_use_pair(tiles, dev->sms, min_m)) {
-        gp.pair = 1;
+      const double mean_kb = tiles > 0 ? kb_sum / static_cast<double>(tiles) : 0.0;
+      int mode = 0;
+      if (!ns.precise && !split && !ch.gs && gemm_use_wide(epi, tiles, dev->sms, min_kb, mean_kb))
+        mode = 2;
+      else if (!ns.precise && !split && gemm_use_pair(tiles, dev->sms, min_m))
+        mode = 1;
+      if (mode) {
+        gp.pair = mode == 1 ? 1 : 0;
+        gp.wide = mode == 2 ? 1 : 0;
         tiles = 0;
         for (size_t k = 0; k < ch.groups.size(); ++k) {
-          fill(gp.g[k], dg[k], static_cast<int>(tiles), true);
+          fill(gp.g[k], dg[k], static_cast<int>(tiles), mode);
           tiles += static_cast<int64_t>(gp.g[k].tiles_per_mat) * dg[k].cnt;
         }
       }
@@ -933,16 +944,16 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       // R of the iterate, then per step B'_k, Q, T, R_{k+1}; the phase ends with
       // the apply X <- Q X (the first one also scales by 1 / ||X0||).
       auto sym = [](int a, int b, int c) {
-        return [a, b, c](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-          ns_fill_gs_sym(G, d, a, b, c, base, pair);
+        return [a, b, c](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
+          ns_fill_gs_sym(G, d, a, b, c, base, mode == 1);
         };
       };
       const int period = gram_restart_period();
       int src = 0;   // Xt buffer holding the iterate
       for (int k0 = 0; k0 < ns.steps; k0 += period) {
         const int k1 = std::min(ns.steps, k0 + period);
-        st = gemm(kEpiGram, [src](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-                    ns_fill_gs_gram(G, d, src, base, pair);
+        st = gemm(kEpiGram, [src](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
+                    ns_fill_gs_gram(G, d, src, base, mode == 1);
                   }, 0.f, 0.f, 0.f, 0.f, k0 == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
         int q = kGsQ0;
@@ -969,8 +980,8 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
           }
         }
         // X <- Q X (the first phase: Q X0 / ||X0||) into the other Xt buffer
-        st = gemm(kEpiApply, [q, src](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-                    ns_fill_gs_apply(G, d, q, src, base, pair);
+        st = gemm(kEpiApply, [q, src](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
+                    ns_fill_gs_apply(G, d, q, src, base, mode == 1);
                   }, 0.f, 0.f, 0.f, 0.f, k0 == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
         src ^= 1;
@@ -984,8 +995,8 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       // smaller where a X and B X cancel, which lowers the rounding error.
       const float alpha = kShiftFrac * ca;
       for (int phase = 0; phase < 3; ++phase) {
-        st = gemm(phase, [phase, it](GemmGroup& G, const NsGroupDev& d, int base, bool pair) {
-                    ns_fill_group(G, d, phase, it, base, pair);
+        st = gemm(phase, [phase, it](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
+                    ns_fill_group(G, d, phase, it, base, mode == 1, mode == 2);
                   }, ca - alpha, cb, cc, alpha, it == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
       }

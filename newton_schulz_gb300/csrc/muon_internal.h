@@ -134,6 +134,8 @@ struct GemmParams {
                           // copy for it, so the wait on it runs out (then the status bit)
   int pair;               // 1: clusters of two CTAs share the B tile (tiles count pair
                           // tiles; mapB holds 128-row boxes for K-major B; no split-K)
+  int wide;               // 1: one CTA per 256 x 256 block, both 128-row halves (tiles count
+                          // pair tiles; maps as for single tiles; bf16, no split-K)
   int b_mn;               // 1 (polynomial / apply): B is read MN-major from 64 x 64 boxes,
                           // so the product is A B rather than A B^T (B not symmetric)
   unsigned* status;
@@ -179,8 +181,9 @@ bool make_ns_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows
 bool ns_group_maps(NsGroupDev& g);
 // Fill the launch descriptor of group g for `phase` (Epi) of NS step `it`.
 // pair: the launch runs in CTA pairs (see GemmParams::pair).
+// wide: tiles count pair tiles (GemmParams::wide), maps as for single tiles.
 void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base,
-                   bool pair = false);
+                   bool pair = false, bool wide = false);
 // Gram-space NS (the m x m products on the polynomial kernel):
 //   the Gram R = X X^T of the iterate in Xt[src] into S[kGsR];
 bool ns_gs_maps(NsGroupDev& g);
@@ -312,6 +315,10 @@ int gemm_sym_pair_tiles(int m);   // the same tiles taken in pairs of row tiles
 // Whether a launch with `tiles` (unpaired) tiles, whose smallest core-shape
 // side is min_m, runs in CTA pairs (MUON_GEMM_PAIR=0 / 1 overrides).
 bool gemm_use_pair(int64_t tiles, int sms, int64_t min_m);
+// Whether a bf16, unsplit grouped-GEMM launch of product `epi` runs WIDE:
+// tiles = single-tile count, min_kb / mean_kb = the least and the
+// tile-weighted mean number of 64-wide K blocks per tile (ns_plan.cpp).
+bool gemm_use_wide(int epi, int64_t tiles, int sms, int min_kb, double mean_kb);
 // Ring depth of a launch (GemmParams::deep): the Gram and the apply always
 // take the 4-stage ring (their epilogues need one staging box per set); the
 // polynomial, whose mirrored output wants two boxes per set in flight, only

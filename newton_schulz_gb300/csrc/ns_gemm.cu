@@ -64,11 +64,17 @@ constexpr int kBoxBytes = BM * 128;        // apply staging: 128 rows x 64 colum
 // (two boxes: both halves of the set's columns, or a tile half and its
 // transpose, in flight together); long-K launches (DEEP) take a 4-stage ring
 // and one 16 KB box per set, which the set's stores then use in turn.
-template <bool DEEP>
+//
+// WIDE launches (one CTA per 256 x 256 block, both 128-row halves) take a
+// 3-stage ring of 64 KB stages (two A tiles and the B tile) and one box per
+// set.
+template <bool DEEP, bool WIDE = false>
 struct Layout {
-  static constexpr int stages = DEEP ? 4 : 3;
-  static constexpr int set_bytes = DEEP ? kBoxBytes : 2 * kBoxBytes;
-  static constexpr int bar_off = stages * kStageBytes + 2 * set_bytes;
+  static constexpr int a_bytes = WIDE ? 2 * kABytes : kABytes;   // A tiles per stage
+  static constexpr int stage_bytes = a_bytes + kBBytes;
+  static constexpr int stages = WIDE ? 3 : (DEEP ? 4 : 3);
+  static constexpr int set_bytes = (DEEP || WIDE) ? kBoxBytes : 2 * kBoxBytes;
+  static constexpr int bar_off = stages * stage_bytes + 2 * set_bytes;
   static constexpr int smem = bar_off + 256 + 1024;
 };
 constexpr uint32_t kTmemCols = 2 * BN;
@@ -229,15 +235,28 @@ __device__ __forceinline__ void cvt_bf16x32(const uint4 (&u)[4], float* v) {
 // issuer's commit arrives on both CTAs' empty barrier, count 2).  The pair
 // passes a cluster barrier after initialising its mbarriers and before
 // exiting, so no copy or arrival ever targets a CTA that is not running.
-template <int EPI, bool DEEP, bool PREC, bool PAIR>
+//
+// WIDE: one CTA computes both 128-row halves of a 256 x 256 block (the pair
+// tiles above, without a partner).  Each stage holds the two A tiles and the
+// common B tile, and the MMA issuer runs both halves' MMAs on it, half h into
+// accumulator h: 64 KB of operands per two 128 x 256 x 64 MMA blocks instead
+// of 48 KB per one, a third less operand data into the SM per MMA.  Both
+// accumulators belong to one block, so a block's MMAs start once the
+// epilogue has drained both; the epilogue sees the halves as consecutive
+// tiles (virtual tile 2n + h).
+template <int EPI, bool DEEP, bool PREC, bool PAIR, bool WIDE = false>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(!(WIDE && (PAIR || PREC)), "WIDE runs alone, in bf16");
+  constexpr bool kPT = PAIR || WIDE;   // tiles are pair tiles
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-  using L = Layout<DEEP>;
+  using L = Layout<DEEP, WIDE>;
   constexpr int kStages = L::stages;
+  constexpr int kAB = L::a_bytes;
+  constexpr int kSB = L::stage_bytes;
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
-  uint8_t* sX = smem + kStages * kStageBytes;   // epilogue output staging
+  uint8_t* sB = smem + kStages * kAB;
+  uint8_t* sX = smem + kStages * kSB;   // epilogue output staging
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;      // [2] accumulator ready
@@ -296,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       uint32_t phase = 0;
       bool stop = false;
       for (int tile = tile0; tile < p.total_tiles && !stop; tile += tstep) {
-        const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
-        if (!dbg_ok(tile_in_range<EPI, PAIR>(p, t), p.status)) break;   // consumers time out
+        const TileInfo t = decode<EPI, kPT>(p, tile, crank);
+        if (!dbg_ok(tile_in_range<EPI, kPT>(p, t), p.status)) break;   // consumers time out
         const GemmGroup& G = p.g[t.gi];
         for (int i = 0; i < t.nkb * NSEG; ++i) {
           if (!wait_bounded(&empty[stage], phase ^ 1, abort_flag, p.status, p.timeout_ns, true)) {
@@ -312,11 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             // testing hook: this stage is never armed and no copy is issued
             // for it, so the MMA issuer's wait on it runs out
           } else if (EPI == kEpiGram) {
-            ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            // MN-major chunks of Xt: 64 columns (m) x 64 rows (n, the K dim) each
+            ptx::mbar_arrive_expect_tx(&full[stage], kSB);
+            // MN-major chunks of Xt: 64 columns (m) x 64 rows (n, the K dim)
+            // each; WIDE: both 128-row halves (half h at kABytes h)
 #pragma unroll
-            for (int h = 0; h < BM / 64; ++h)
-              ptx::tma_load_3d(sA + stage * kABytes + h * kChunkBytes, ma, &full[stage],
+            for (int h = 0; h < (WIDE ? 2 : 1) * BM / 64; ++h)
+              ptx::tma_load_3d(sA + stage * kAB + h * kChunkBytes, ma, &full[stage],
                                t.row_tile * BM + 64 * h, kx, t.mat);
             if (PAIR) {
               // this CTA's half of the B chunks, into both CTAs of the pair
@@ -331,8 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                                  t.col_tile * BN + 64 * h, kx, t.mat);
             }
           } else {
-            ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            ptx::tma_load_3d(sA + stage * kABytes, ma, &full[stage], kx, t.row_tile * BM, t.mat);
+            ptx::mbar_arrive_expect_tx(&full[stage], kSB);
+#pragma unroll
+            for (int hh = 0; hh < (WIDE ? 2 : 1); ++hh)   // WIDE: both 128-row halves
+              ptx::tma_load_3d(sA + stage * kAB + hh * kABytes, ma, &full[stage], kx,
+                               (t.row_tile + hh) * BM, t.mat);
             if (p.b_mn) {
               // B[k][col] in MN-major chunks of 64 columns x 64 rows (K), as the Gram's B
               for (int h = PAIR ? 2 * crank : 0; h < (PAIR ? 2 * crank + 2 : BN / 64); ++h) {
@@ -372,11 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       int stage = 0, acc = 0;
       uint32_t phase = 0;
       bool stop = false;
-      for (int tile = tile0; tile < p.total_tiles && !stop; tile += tstep, ++acc) {
-        const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
+      // WIDE: a block takes both accumulators (virtual tiles acc, acc + 1)
+      for (int tile = tile0; tile < p.total_tiles && !stop; tile += tstep, acc += WIDE ? 2 : 1) {
+        const TileInfo t = decode<EPI, kPT>(p, tile, crank);
         const int buf = acc & 1;
         if (!wait_bounded(&tempty[buf], ((acc >> 1) & 1) ^ 1, abort_flag, p.status, p.timeout_ns,
-                          true)) {
+                          true) ||
+            (WIDE && !wait_bounded(&tempty[1], ((acc >> 1) & 1) ^ 1, abort_flag, p.status,
+                                   p.timeout_ns, true))) {
           stop = true;
           break;
         }
@@ -388,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sA + stage * kABytes);
+          const uint32_t a0 = ptx::smem_u32(sA + stage * kAB);
           const uint32_t b0 = ptx::smem_u32(sB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -401,6 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                                     ? ptx::sdesc_mnmajor_sw128(b0 + k * 2048, kChunkBytes, 1024)
                                     : ptx::sdesc_kmajor_sw128(b0 + k * UMMA_K * 2);
             ptx::umma_bf16(d, da, db, idesc, (i > 0 || k > 0) ? 1u : 0u);
+            if (WIDE) {   // the second half's A tile, same B, into accumulator 1
+              const uint64_t da1 =
+                  EPI == kEpiGram
+                      ? ptx::sdesc_mnmajor_sw128(a0 + kABytes + k * 2048, kChunkBytes, 1024)
+                      : ptx::sdesc_kmajor_sw128(a0 + kABytes + k * UMMA_K * 2);
+              ptx::umma_bf16(tmem + BN, da1, db, idesc, (i > 0 || k > 0) ? 1u : 0u);
+            }
           }
           if (PAIR) ptx::umma_commit_mc(&empty[stage], 0x3);   // both CTAs' stage
           else ptx::umma_commit(&empty[stage]);
@@ -410,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
         }
         ptx::umma_commit(&tfull[buf]);   // accumulator complete (or abandoned)
+        if (WIDE) ptx::umma_commit(&tfull[1]);
       }
       // no MMA may still run when TMEM is freed (after an abort nobody
       // waits for the last accumulator)
@@ -428,8 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     uint32_t xphase = 0;
     bool xpend = false;   // leader: a staged-tile load is in flight and not yet waited for
     int acc = 0;
-    for (int tile = tile0; tile < p.total_tiles; tile += tstep, ++acc) {
-      const TileInfo t = decode<EPI, PAIR>(p, tile, crank);
+    // WIDE: virtual tile vt is half vt & 1 of block vt >> 1 (accumulator vt & 1)
+    for (int vt = 0;; ++vt, ++acc) {
+      const int tile = tile0 + (WIDE ? (vt >> 1) : vt) * tstep;
+      if (tile >= p.total_tiles) break;
+      const TileInfo t = decode<EPI, kPT>(p, tile, WIDE ? (vt & 1) : crank);
       const GemmGroup& G = p.g[t.gi];
       const int buf = acc & 1;
       const int row0 = t.row_tile * BM, col0 = t.col_tile * BN;
@@ -847,6 +884,17 @@ static cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// WIDE launch: one CTA per SM over the 256 x 256 blocks (pair tiles).
+template <int EPI>
+static cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s) {
+  using LW = Layout<true, true>;
+  auto kern = ns_gemm_kernel<EPI, true, false, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LW::smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, LW::smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 // Paired launch: clusters of two CTAs, as many clusters as can be resident
 // at once (the occupancy API's count for this kernel), at most one per pair
 // tile.
@@ -899,6 +947,14 @@ cudaError_t launch_gemm(int epi, const GemmParams& p, cudaStream_t s) {
       case kEpiGram: return launch_one<kEpiGram, false, true>(p, grid, s);
       case kEpiPoly: return launch_one<kEpiPoly, false, true>(p, grid, s);
       case kEpiApply: return launch_one<kEpiApply, false, true>(p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.wide) {
+    switch (epi) {
+      case kEpiGram: return launch_wide<kEpiGram>(p, grid, s);
+      case kEpiPoly: return launch_wide<kEpiPoly>(p, grid, s);
+      case kEpiApply: return launch_wide<kEpiApply>(p, grid, s);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -109,8 +109,28 @@ bool gemm_use_pair(int64_t tiles, int sms, int64_t min_m) {
   return min_m >= 8192 && tiles >= 4LL * sms;
 }
 
+bool gemm_use_wide(int epi, int64_t tiles, int sms, int min_kb, double mean_kb) {
+  if (const char* v = std::getenv("MUON_GEMM_WIDE")) {
+    if (v[0] == '0') return false;
+    if (v[0] == '1') return true;
+  }
+  // Measured on one GB300, the same box back to back (ms per launch, single
+  // tiles -> WIDE; the large sweep power-capped at 1590-1650 MHz): large
+  // sweep (K >= 8192) Gram 3.00 -> 2.76, polynomial 2.28 -> 2.14, apply
+  // 6.18 -> 5.49 (step 475 -> 432); Llama-3-8B shapes (mean K ~4000, k/v at
+  // K = 1024) Gram 1.306 -> 1.238, apply 2.477 -> 2.323, polynomial 0.571 ->
+  // 0.620; MoE experts (K = 768 / 2048) Gram 0.288 -> 0.302, polynomial
+  // 0.158 -> 0.216, apply 0.478 -> 0.549.  A block needs both accumulators,
+  // so its epilogue no longer overlaps the next block's MMAs: only long K
+  // amortises that, and the polynomial (its epilogue loads the b A term and
+  // writes the mirror too) needs the longest.
+  if (tiles < 2LL * sms) return false;
+  return epi == kEpiPoly ? min_kb >= 128 : mean_kb >= 48.0;
+}
+
 void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int tile_base,
-                   bool pair) {
+                   bool pair, bool wide) {
+  const bool pt = pair || wide;   // tiles are pair tiles
   const int bm = gemm_block_m(), bn = gemm_block_n(), bk = gemm_block_k();
   G.m = static_cast<int>(g.m);
   G.n = static_cast<int>(g.n);
@@ -134,8 +154,8 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.ksplit = g.ksplit;
     G.kb_per_split = g.kb_per_split;
     G.num_kb = g.num_kb_gram;
-    G.tiles_per_mat = pair ? gemm_sym_pair_tiles(static_cast<int>(g.m))
-                           : static_cast<int>(g.tri * g.ksplit);
+    G.tiles_per_mat = pt ? gemm_sym_pair_tiles(static_cast<int>(g.m))
+                         : static_cast<int>(g.tri * g.ksplit);
   } else if (phase == kEpiPoly) {
     G.mapA = g.map_ap;      // operand rows and the epilogue's A tiles
     G.mapB = pair ? g.map_ap : g.map_aq;   // a pair loads B in 128-row halves
@@ -152,7 +172,7 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.ksplit = 1;
     G.num_kb = static_cast<int>(cdiv64(g.m, bk));
     G.kb_per_split = G.num_kb;
-    G.tiles_per_mat = pair ? gemm_sym_pair_tiles(static_cast<int>(g.m)) : static_cast<int>(g.tri);
+    G.tiles_per_mat = pt ? gemm_sym_pair_tiles(static_cast<int>(g.m)) : static_cast<int>(g.tri);
   } else {
     G.mapA = g.map_xt[it & 1];
     G.mapB = pair ? g.map_bp : g.map_bq;
@@ -167,7 +187,7 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
     G.ksplit = 1;
     G.num_kb = static_cast<int>(cdiv64(g.m, bk));
     G.kb_per_split = G.num_kb;
-    G.tiles_per_mat = G.nt * (pair ? (G.mt + 1) / 2 : G.mt);
+    G.tiles_per_mat = G.nt * (pt ? (G.mt + 1) / 2 : G.mt);
   }
 }
 

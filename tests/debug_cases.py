@@ -17,7 +17,8 @@ sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 from newton_schulz_gb300 import binding, synth  # noqa: E402
 
 HP = dict(mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
-ENV_KEYS = ("MUON_GEMM_PAIR", "MUON_MAX_KSPLIT", "MUON_GRAM_SPACE", "MUON_SMALL_PATH")
+ENV_KEYS = ("MUON_GEMM_PAIR", "MUON_GEMM_WIDE", "MUON_MAX_KSPLIT", "MUON_GRAM_SPACE",
+            "MUON_SMALL_PATH")
 
 
 def _env(**kw):
@@ -60,7 +61,9 @@ def main(out_path):
     ns("splitk", (1, 96, 10240), 5)
     ns("generic_small", (2, 24, 2048), 6, MUON_SMALL_PATH="0")
     # CTA pairs forced, with and without split-K
-    ns("pairs", (2, 640, 2048), 7, MUON_GEMM_PAIR="1", MUON_MAX_KSPLIT="1")
+    ns("pairs", (2, 640, 2048), 7, MUON_GEMM_PAIR="1", MUON_GEMM_WIDE="0", MUON_MAX_KSPLIT="1")
+    # WIDE blocks forced (an odd number of row tiles: an empty second half)
+    ns("wide", (2, 640, 1000), 13, MUON_GEMM_WIDE="1", MUON_MAX_KSPLIT="1")
     # high-precision mode on both paths
     ns("precise_gemm", (1, 300, 700), 8, binding.make_config(precision=binding.NS_TF32))
     ns("precise_small", (2, 48, 900), 9, binding.make_config(precision=binding.NS_TF32))

@@ -36,7 +36,8 @@ def _groups(kind):
 @pytest.mark.parametrize("kind,env", [
     ("small", {}),
     ("gemm", {}),
-    ("gemm", {"MUON_GEMM_PAIR": "1", "MUON_MAX_KSPLIT": "1"}),
+    ("gemm", {"MUON_GEMM_PAIR": "1", "MUON_GEMM_WIDE": "0", "MUON_MAX_KSPLIT": "1"}),
+    ("gemm", {"MUON_GEMM_WIDE": "1", "MUON_MAX_KSPLIT": "1"}),
     ("long", {}),
     ("gemm", {"PRECISE": "1"}),
     ("small", {"PRECISE": "1"}),

@@ -23,7 +23,8 @@ HP = dict(mu=0.95, nesterov=True, lr=0.02, wd=0.01, scale_rule=0)
 
 
 @pytest.fixture(autouse=True)
-def _dev(lib, cuda_ok):
+def _dev(lib, cuda_ok, monkeypatch):
+    monkeypatch.setenv("MUON_GEMM_WIDE", "0")   # pairs, not WIDE blocks
     yield
     torch.cuda.synchronize()
 
