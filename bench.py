@@ -80,7 +80,7 @@ TRAFFIC = {
                             "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h")},
     # large sweep: mean over the 160 apply launches of 4 steps (40 per step,
     # every chunk and NS step), one-pass capture of the full-size workload
-    ("apply", "c5"): {"bytes": (1498490707968.0 + 143154965504.0) / 160, "src_hash": "fd2f587338fb0111",
+    ("apply", "c5"): {"bytes": (1290296708352.0 + 142215855360.0) / 160, "src_hash": "2342b6dd0b76ec32",
                       "sources": ("ns_gemm.cu", "sm100_ptx.cuh", "muon_internal.h")},
 }
 
