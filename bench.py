@@ -80,7 +80,7 @@ TRAFFIC = {
                             "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h")},
     # large sweep: mean over the 160 apply launches of 4 steps (40 per step,
     # every chunk and NS step), one-pass capture of the full-size workload
-    ("apply", "c5"): {"bytes": (1290296708352.0 + 142215855360.0) / 160, "src_hash": "2342b6dd0b76ec32",
+    ("apply", "c5"): {"bytes": (1290296708352.0 + 142215855360.0) / 160, "src_hash": "7559e1a68b1d8c9c",
                       "sources": ("ns_gemm.cu", "sm100_ptx.cuh", "muon_internal.h")},
 }
 

@@ -32,11 +32,13 @@
 //               mirrored copy; the polynomial's A operand is loaded before
 //               the accumulator is waited for.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
-// tile t+1.  Tiles of all matrices of all core-shape groups of a chunk form
-// one static round-robin schedule, ordered in column groups (decode) so that
-// the CTAs running at one time share operand panels in L2.  Every wait is bounded; on a timeout a
-// status bit is set, in-flight copies are drained, TMEM is freed and the CTA
-// returns.
+// tile t+1.  Long-K launches run in WIDE blocks instead: both 128-row halves
+// of a 256 x 256 block from one stage, one accumulator per half (see the
+// kernel's template parameters).  Tiles of all matrices of all core-shape
+// groups of a chunk form one static round-robin schedule, ordered in column
+// groups (decode) so that the CTAs running at one time share operand panels
+// in L2.  Every wait is bounded; on a timeout a status bit is set, in-flight
+// copies are drained, TMEM is freed and the CTA returns.
 #include "muon_internal.h"
 #include "sm100_ptx.cuh"
 
