@@ -120,7 +120,7 @@ def matrix_flops(r, c, path, steps=STEPS_NS, restart=None):
     if path == 2:
         if restart is None:
             from newton_schulz_gb300 import binding
-            restart = binding.muon_ns_gram_restart()
+            restart = binding.muon_ns_gram_restart(m)
         period = restart
         period = period if period > 0 else steps
         phases = [min(period, steps - k0) for k0 in range(0, steps, period)]

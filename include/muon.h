@@ -200,12 +200,15 @@ muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, 
  * cols <= 0 or an invalid cfg. */
 int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t *cfg);
 
-/* The restart period P of the Gram-space NS (path 2 of muon_ns_path) in NS
- * steps: the iteration restarts from the Gram matrix of X_k = Q X every P
- * steps (DMuon-2 Appendix C.3, "mid-way restart"), so K steps take
- * ceil(K / P) phases.  0 means no restart (one phase).  Default 2;
- * the environment variable MUON_GRAM_RESTART sets it.  No GPU work. */
-int muon_ns_gram_restart(void);
+/* The restart period P of the Gram-space NS (path 2 of muon_ns_path) for a
+ * core shape with small side m, in NS steps: the iteration restarts from the
+ * Gram matrix of X_k = Q X every P steps (DMuon-2 Appendix C.3, "mid-way
+ * restart"), so K steps take ceil(K / P) phases.  0 means no restart (one
+ * phase).  Default 3 for m >= 1024, else 2 (the periods with the lowest
+ * update error measured at those sizes); a launch whose core shapes differ
+ * uses the period of its smallest m.  The environment variable
+ * MUON_GRAM_RESTART sets it for every m.  -1 for m <= 0.  No GPU work. */
+int muon_ns_gram_restart(int64_t m);
 
 /* As muon_step_grouped with an explicit NS configuration (NULL = defaults). */
 muon_status_t muon_step_grouped_ex(const muon_group_t *groups, int n_groups, float mu,

@@ -119,7 +119,7 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.muon_debug_inject_stall.restype = i32
     lib.muon_ns_path.argtypes = [i64, i64, ctypes.POINTER(NsConfig)]
     lib.muon_ns_path.restype = ctypes.c_int
-    lib.muon_ns_gram_restart.argtypes = []
+    lib.muon_ns_gram_restart.argtypes = [i64]
     lib.muon_ns_gram_restart.restype = ctypes.c_int
     lib.muon_debug_build.argtypes = []
     lib.muon_debug_build.restype = ctypes.c_int
@@ -285,9 +285,10 @@ def muon_ns_path(rows: int, cols: int, cfg=None) -> int:
     return load().muon_ns_path(rows, cols, ctypes.byref(cfg) if cfg is not None else None)
 
 
-def muon_ns_gram_restart() -> int:
-    """Restart period (NS steps) of the Gram-space path; 0 = no restart."""
-    return load().muon_ns_gram_restart()
+def muon_ns_gram_restart(m: int) -> int:
+    """Restart period (NS steps) of the Gram-space path for small side m;
+    0 = no restart."""
+    return load().muon_ns_gram_restart(m)
 
 
 def muon_debug_build() -> bool:

@@ -267,37 +267,45 @@ struct NsCfg {
 // (15 r + 5) m^3 in X space, so it is taken from r >= 2 on (bf16 products
 // only; MUON_GRAM_SPACE=0 / 1 forbids / forces it, MUON_GRAM_SPACE_RATIO sets
 // the r from which it is used).
-// Gram-space restart period in NS steps (MUON_GRAM_RESTART; 0: no restart).
-int gram_restart_period_env() {
+// Gram-space restart period in NS steps for core shapes with small side m
+// (MUON_GRAM_RESTART; 0: no restart).  Default: 3 for m >= 1024, else 2.
+// Update error against the float64 oracle (one Gaussian matrix per shape,
+// GB300): m = 768: P = 2 0.0087, P = 3 0.0110; m = 1024 ... 8192: P = 3
+// 0.0062-0.0086, P = 2 0.0080-0.0121 (the 1e-2 ||dW|| bound).
+int gram_restart_period_env(int64_t m) {
   const char* v = std::getenv("MUON_GRAM_RESTART");
-  if (!v || !*v) return 2;
+  if (!v || !*v) return m >= 1024 ? 3 : 2;
   const long p = std::strtol(v, nullptr, 10);
   return p < 0 ? 2 : static_cast<int>(std::min<long>(p, 1 << 20));
 }
 
-int gram_restart_period() {
-  const int p = gram_restart_period_env();
+int gram_restart_period(int64_t m) {
+  const int p = gram_restart_period_env(m);
   return p == 0 ? (1 << 30) : p;
 }
 
-int gram_phases(int steps) {
-  const int p = gram_restart_period();
+int gram_phases(int steps, int64_t m) {
+  const int p = gram_restart_period(m);
   return steps <= 0 ? 0 : (steps + p - 1) / p;
 }
 
-// Gram space is opt-in: in bf16 it rounds R, B', T and Q (m x m) where the X
-// space rounds A, B' and the iterate, and its update error measured 1.3-1.8x
-// the X-space one (about the 1e-2 ||dW|| bound for m >= 4096).
-// MUON_GRAM_SPACE=1: shapes with n >= MUON_GRAM_SPACE_RATIO (default 2) x m;
-// MUON_GRAM_SPACE=force: every shape of the GEMM path; unset or 0: none.
+// Gram space (the default iteration of DMuon-2 Appendix C.3) for core shapes
+// with m >= 128 and n >= ratio x m (MUON_GRAM_SPACE_RATIO, default 2) in bf16
+// mode.  With the restart period of gram_restart_period_env its update error
+// measured 0.0062-0.0086 of ||dW|| against 0.0059-0.0074 in X space (the
+// bound is 1e-2) at m = 768 ... 8192 for 1-24 % less time per step; below
+// m = 128 (shapes the small-m kernel does not take, or all of them with
+// MUON_SMALL_PATH=0) its NS error reached 0.031 on a [33, 1000] matrix, so
+// those stay in X space.  MUON_GRAM_SPACE=0 turns it off, =force applies it
+// to every shape of the GEMM path.
+constexpr int64_t kGramSpaceMinM = 128;
 bool gram_space_shape(int64_t m, int64_t n, const NsCfg& ns) {
   if (ns.precise || ns.steps < 1) return false;
   const char* v = std::getenv("MUON_GRAM_SPACE");
-  if (!v) return false;
-  if (std::strcmp(v, "force") == 0) return true;
-  if (v[0] != '1') return false;
+  if (v && std::strcmp(v, "force") == 0) return true;
+  if (v && v[0] == '0') return false;
   const double ratio = static_cast<double>(env_size("MUON_GRAM_SPACE_RATIO", 2));
-  return static_cast<double>(n) >= ratio * static_cast<double>(m);
+  return m >= kGramSpaceMinM && static_cast<double>(n) >= ratio * static_cast<double>(m);
 }
 
 // Small-m path eligibility: core shapes with m <= 64 (MUON_SMALL_PATH=0 sends
@@ -909,7 +917,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       }
       const double mean_kb = tiles > 0 ? kb_sum / static_cast<double>(tiles) : 0.0;
       int mode = 0;
-      if (!ns.precise && !split && !ch.gs && gemm_use_wide(epi, tiles, dev->sms, min_kb, mean_kb))
+      if (!ns.precise && !split && gemm_use_wide(epi, tiles, dev->sms, min_kb, mean_kb))
         mode = 2;
       else if (!ns.precise && !split && gemm_use_pair(tiles, dev->sms, min_m))
         mode = 1;
@@ -945,15 +953,17 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       // the apply X <- Q X (the first one also scales by 1 / ||X0||).
       auto sym = [](int a, int b, int c) {
         return [a, b, c](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
-          ns_fill_gs_sym(G, d, a, b, c, base, mode == 1);
+          ns_fill_gs_sym(G, d, a, b, c, base, mode == 1, mode == 2);
         };
       };
-      const int period = gram_restart_period();
+      int64_t gs_min_m = INT64_MAX;   // one period per chunk: its smallest m decides
+      for (const NsGroupP& g : ch.groups) gs_min_m = std::min(gs_min_m, g.m);
+      const int period = gram_restart_period(gs_min_m);
       int src = 0;   // Xt buffer holding the iterate
       for (int k0 = 0; k0 < ns.steps; k0 += period) {
         const int k1 = std::min(ns.steps, k0 + period);
         st = gemm(kEpiGram, [src](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
-                    ns_fill_gs_gram(G, d, src, base, mode == 1);
+                    ns_fill_gs_gram(G, d, src, base, mode == 1, mode == 2);
                   }, 0.f, 0.f, 0.f, 0.f, k0 == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
         int q = kGsQ0;
@@ -981,7 +991,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         }
         // X <- Q X (the first phase: Q X0 / ||X0||) into the other Xt buffer
         st = gemm(kEpiApply, [q, src](GemmGroup& G, const NsGroupDev& d, int base, int mode) {
-                    ns_fill_gs_apply(G, d, q, src, base, mode == 1);
+                    ns_fill_gs_apply(G, d, q, src, base, mode == 1, mode == 2);
                   }, 0.f, 0.f, 0.f, 0.f, k0 == 0 ? 1 : 0);
         if (st != MUON_OK) return st;
         src ^= 1;
@@ -1003,6 +1013,8 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
     }
     // ---- K6 -------------------------------------------------------------------
     {
+      int64_t chunk_min_m = INT64_MAX;   // the Gram-space restart period's m
+      for (const NsGroupP& g : ch.groups) chunk_min_m = std::min(chunk_min_m, g.m);
       FinParams fp;
       std::memset(&fp, 0, sizeof(fp));
       int64_t blocks = 0;
@@ -1014,7 +1026,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         const int64_t per = q.r * q.c;
         fs.W = static_cast<char*>(q.W) + s.b0 * per * esize(q.w_dtype);
         // the Xt buffer of the result: one per step (X space) or per phase (Gram space)
-        const int fin = (ch.gs ? gram_phases(ns.steps) : ns.steps) & 1;
+        const int fin = (ch.gs ? gram_phases(ns.steps, chunk_min_m) : ns.steps) & 1;
         // O = Xt in the stored layout when rows > cols, else its transpose
         fs.O = reinterpret_cast<__nv_bfloat16*>(ws + (fin ? g.off_Xt1 : g.off_Xt0)) +
                s.idx0 * g.n * g.m_pad;
@@ -1728,7 +1740,7 @@ int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t* cfg) {
   }
 }
 
-int muon_ns_gram_restart(void) { return gram_restart_period_env(); }
+int muon_ns_gram_restart(int64_t m) { return m <= 0 ? -1 : gram_restart_period_env(m); }
 
 int muon_debug_build(void) {
 #ifdef MUON_DEBUG

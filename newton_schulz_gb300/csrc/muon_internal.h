@@ -187,14 +187,15 @@ void ns_fill_group(GemmGroup& G, const NsGroupDev& g, int phase, int it, int til
 // Gram-space NS (the m x m products on the polynomial kernel):
 //   the Gram R = X X^T of the iterate in Xt[src] into S[kGsR];
 bool ns_gs_maps(NsGroupDev& g);
-void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int src, int tile_base, bool pair);
+void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int src, int tile_base, bool pair,
+                     bool wide = false);
 //   C = epilogue(S[a] S[b]) into S[c] (B read MN-major, GemmParams::b_mn), with
 //   the polynomial kernel's epilogue b' S[a] + c' (S[a] S[b]) + alpha' I;
 void ns_fill_gs_sym(GemmGroup& G, const NsGroupDev& g, int a, int b, int c, int tile_base,
-                    bool pair);
+                    bool pair, bool wide = false);
 //   the apply Xt[src] S[q] (the iterate times Q) into Xt[src ^ 1].
 void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int src, int tile_base,
-                      bool pair);
+                      bool pair, bool wide = false);
 
 // ---- fused small-m path: Gram-space Newton-Schulz -------------------------------
 constexpr int kSmallMaxM = 64;             // core shapes with m <= 64

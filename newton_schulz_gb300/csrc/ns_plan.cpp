@@ -221,15 +221,16 @@ bool ns_gs_maps(NsGroupDev& g) {
   return ok;
 }
 
-void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int src, int tile_base, bool pair) {
-  ns_fill_group(G, g, kEpiGram, src, tile_base, pair);   // reads Xt[src]
+void ns_fill_gs_gram(GemmGroup& G, const NsGroupDev& g, int src, int tile_base, bool pair,
+                     bool wide) {
+  ns_fill_group(G, g, kEpiGram, src, tile_base, pair, wide);   // reads Xt[src]
   G.mapC = g.s_p[kGsR];
   G.mapD = g.s_64[kGsR];
 }
 
 void ns_fill_gs_sym(GemmGroup& G, const NsGroupDev& g, int a, int b, int c, int tile_base,
-                    bool pair) {
-  ns_fill_group(G, g, kEpiPoly, 0, tile_base, pair);
+                    bool pair, bool wide) {
+  ns_fill_group(G, g, kEpiPoly, 0, tile_base, pair, wide);
   G.mapA = g.s_p[a];                       // operand rows and the epilogue's b' S[a] tiles
   G.mapB = g.s_64[b];                      // MN-major 64 x 64 chunks (also for pairs)
   G.mapC = g.s_p[c];
@@ -237,8 +238,8 @@ void ns_fill_gs_sym(GemmGroup& G, const NsGroupDev& g, int a, int b, int c, int 
 }
 
 void ns_fill_gs_apply(GemmGroup& G, const NsGroupDev& g, int q, int src, int tile_base,
-                      bool pair) {
-  ns_fill_group(G, g, kEpiApply, src, tile_base, pair);   // reads Xt[src], writes Xt[src ^ 1]
+                      bool pair, bool wide) {
+  ns_fill_group(G, g, kEpiApply, src, tile_base, pair, wide);   // reads Xt[src], writes Xt[src ^ 1]
   G.mapB = g.s_64[q];                      // Xt Q, Q read MN-major
 }
 

@@ -1,7 +1,7 @@
 """Gram-space Newton-Schulz on the grouped GEMM path (DMuon-2 Appendix C.3).
 
 For n >= 2 m the library iterates on the m x m Gram matrix in phases of P
-steps (the restart period, default 2): R = X X^T of the phase's input, per
+steps (the restart period: 3 for m >= 1024, else 2): R = X X^T of the phase's input, per
 step B' = b R + c R^2 + alpha I, Q <- (a - alpha) Q + Q B',
 T = (a - alpha) R + R B', R <- (a - alpha) T + T B', and X <- Q X at the
 phase's end.  In exact arithmetic this is the X-space iteration; in bf16 it
@@ -9,9 +9,9 @@ rounds R, B', T and Q instead of the iterate, so the test holds it to the same
 tolerances against the float64 oracle: NS error <= 3e-2 per matrix and W'
 within 1e-2 * ||dW||.  On ill-conditioned inputs, where bf16 NS in either
 form is farther from the float64 result, Gram space is held to 2.5x the
-X-space error of the same input.  Gram space is opt-in: MUON_GRAM_SPACE=1
-selects it for n >= 2 m, =force for every shape (used here), unset or 0
-for none; MUON_GRAM_RESTART sets P (0: no restart).
+X-space error of the same input.  Gram space is the default for n >= 2 m
+(MUON_GRAM_SPACE unset or 1), =force applies it to every shape (used
+here), 0 turns it off; MUON_GRAM_RESTART sets P (0: no restart).
 """
 import numpy as np
 import pytest
@@ -47,17 +47,21 @@ def _errs(got, x, **kw):
 
 
 def test_path_choice(monkeypatch):
-    assert binding.muon_ns_gram_restart() == 2
+    assert binding.muon_ns_gram_restart(768) == 2
+    assert binding.muon_ns_gram_restart(1024) == 3
     monkeypatch.setenv("MUON_GRAM_RESTART", "0")
-    assert binding.muon_ns_gram_restart() == 0
+    assert binding.muon_ns_gram_restart(4096) == 0
     monkeypatch.delenv("MUON_GRAM_RESTART")
     monkeypatch.delenv("MUON_GRAM_SPACE", raising=False)
-    assert binding.muon_ns_path(1024, 4096) == binding.PATH_XSPACE        # opt-in
+    assert binding.muon_ns_path(1024, 4096) == binding.PATH_GRAM_SPACE    # the default
+    monkeypatch.setenv("MUON_GRAM_SPACE", "0")
+    assert binding.muon_ns_path(1024, 4096) == binding.PATH_XSPACE
     monkeypatch.setenv("MUON_GRAM_SPACE", "1")
     assert binding.muon_ns_path(1024, 4096) == binding.PATH_GRAM_SPACE
     assert binding.muon_ns_path(14336, 4096) == binding.PATH_GRAM_SPACE
     assert binding.muon_ns_path(4096, 4096) == binding.PATH_XSPACE
     assert binding.muon_ns_path(24, 10240) == binding.PATH_SMALL
+    assert binding.muon_ns_path(100, 1000) == binding.PATH_XSPACE    # m < 128
     assert binding.muon_ns_path(1024, 4096, binding.make_config(precision=binding.NS_TF32)) == \
         binding.PATH_XSPACE
     monkeypatch.setenv("MUON_GRAM_SPACE", "force")
@@ -103,9 +107,10 @@ def _ill_conditioned(kind, m, n, seed):
     return torch.from_numpy(x[None]).float().cuda()
 
 
+@pytest.mark.parametrize("m,n", [(256, 1024), (1024, 4096)])   # restart period 2, 3
 @pytest.mark.parametrize("kind", [1, 2, 3, 5, "lowrank"])
-def test_gram_space_ill_conditioned(kind, monkeypatch):
-    x = _ill_conditioned(kind, 256, 1024, 11)
+def test_gram_space_ill_conditioned(kind, m, n, monkeypatch):
+    x = _ill_conditioned(kind, m, n, 11)
     eg = max(_errs(_ns(x, True, monkeypatch), x))
     ex = max(_errs(_ns(x, False, monkeypatch), x))
     print(f"{kind}: Gram space {eg:.4f}, X space {ex:.4f}")
@@ -160,3 +165,15 @@ def test_gram_space_full_size_llama_shapes(shape, monkeypatch):
     ex = _errs(_ns(x, False, monkeypatch), x)
     print(f"{shape}: Gram space {max(eg):.4f}, X space {max(ex):.4f}")
     assert max(eg) <= NS_TOL
+
+
+def test_gram_space_wide_bitwise(monkeypatch):
+    """WIDE blocks on the Gram-space launches (forced) give the same bits."""
+    monkeypatch.setenv("MUON_MAX_KSPLIT", "1")
+    monkeypatch.setenv("MUON_GEMM_PAIR", "0")
+    x = torch.randn((2, 640, 2048), generator=torch.Generator().manual_seed(4)).cuda()
+    outs = []
+    for wide in ("0", "1"):
+        monkeypatch.setenv("MUON_GEMM_WIDE", wide)
+        outs.append(_ns(x, True, monkeypatch))
+    assert torch.equal(outs[0], outs[1])
