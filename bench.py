@@ -76,11 +76,11 @@ def _peaks():
 # valid only while the kernel's sources hash to the recorded value; otherwise
 # the roofline reports traffic = null.
 TRAFFIC = {
-    ("fused_small", "c2"): {"bytes": 201.759744e6 + 127.020288e6, "src_hash": "e4d6633f5679ae0e",
+    ("fused_small", "c2"): {"bytes": 202.21312e6 + 126.546944e6, "src_hash": "72126eaf79b769f6",
                             "sources": ("ns_small.cu", "sm100_ptx.cuh", "muon_internal.h")},
-    # large sweep: mean over the 160 apply launches of 4 steps (40 per step,
-    # every chunk and NS step), one-pass capture of the full-size workload
-    ("apply", "c5"): {"bytes": (1290296708352.0 + 142215855360.0) / 160, "src_hash": "7559e1a68b1d8c9c",
+    # large sweep: mean over the 112 apply launches of 4 steps (every chunk and
+    # phase: X-space applies and the Gram-space ones), one-pass capture
+    ("apply", "c5"): {"bytes": (1041320741376.0 + 98436361728.0) / 112, "src_hash": "573f9bb97c4b8a62",
                       "sources": ("ns_gemm.cu", "sm100_ptx.cuh", "muon_internal.h")},
 }
 
