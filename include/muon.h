@@ -180,8 +180,8 @@ muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, 
  *      (DMuon-2 Appendix C.3), X0 applied once, fused with the update;
  *   1  the grouped GEMM path in X space: per step the Gram X X^T, the
  *      polynomial b A + c A^2 and the apply X' = a X + B X ([HP] 2.3 Eq. (1));
- *   2  the grouped GEMM path in Gram space (DMuon-2 Appendix C.3), opt-in
- *      (bf16 mode only), in phases of P steps (P from
+ *   2  the grouped GEMM path in Gram space (DMuon-2 Appendix C.3), in
+ *      bf16 mode for m >= 128 and n >= 2 m, in phases of P steps (P from
  *      muon_ns_gram_restart): R = X X^T of the phase's input (the first
  *      scaled by 1 / ||X0||^2), then per step B' = b R + c R^2 + alpha I,
  *      Q <- (a - alpha) Q + Q B' (Q = P_k = a I + b R + c R^2 at the
@@ -190,14 +190,14 @@ muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, 
  *      alpha = 0.58 a), and X <- Q X at the phase's end.  A phase of
  *      P >= 2 steps takes about (3 r + 4 P - 2) m^3 flops against
  *      (3 r + 1) P m^3 in X space, r = n / m (a one-step phase costs what
- *      an X-space step does).
- * Path 2 is off by default: in bf16 it rounds the m x m matrices R, B', T
- * and Q where the X space rounds A, B' and the iterate, and its update error
- * measured 1.3-1.8x the X-space error (near the 1e-2 ||dW|| bound for
- * m >= 4096).  MUON_GRAM_SPACE=1 selects it for n >= MUON_GRAM_SPACE_RATIO
- * (default 2) x m, MUON_GRAM_SPACE=force for every shape of the GEMM path;
- * MUON_SMALL_PATH=0 sends m <= 64 to the GEMM path.  Returns -1 for rows or
- * cols <= 0 or an invalid cfg. */
+ *      an X-space step does).  It rounds the m x m matrices R, B', T and Q
+ *      to bf16 where the X space rounds A, B' and the iterate: its update
+ *      error measured 0.0062-0.0086 of ||dW|| against 0.0059-0.0074 in X
+ *      space (bound 1e-2) at m = 768 ... 8192; below m = 128 it was worse.
+ * MUON_GRAM_SPACE=0 keeps every shape in X space, =force sends every shape
+ * of the GEMM path to Gram space; MUON_GRAM_SPACE_RATIO (default 2) sets the
+ * n / m threshold; MUON_SMALL_PATH=0 sends m <= 64 to the GEMM path.
+ * Returns -1 for rows or cols <= 0 or an invalid cfg. */
 int muon_ns_path(int64_t rows, int64_t cols, const muon_ns_config_t *cfg);
 
 /* The restart period P of the Gram-space NS (path 2 of muon_ns_path) for a
