@@ -181,7 +181,7 @@ muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, 
  *   1  the grouped GEMM path in X space: per step the Gram X X^T, the
  *      polynomial b A + c A^2 and the apply X' = a X + B X ([HP] 2.3 Eq. (1));
  *   2  the grouped GEMM path in Gram space (DMuon-2 Appendix C.3), in
- *      bf16 mode for m >= 128 and n >= 2 m, in phases of P steps (P from
+ *      bf16 mode for m >= 1024 and n >= 2 m, in phases of P steps (P from
  *      muon_ns_gram_restart): R = X X^T of the phase's input (the first
  *      scaled by 1 / ||X0||^2), then per step B' = b R + c R^2 + alpha I,
  *      Q <- (a - alpha) Q + Q B' (Q = P_k = a I + b R + c R^2 at the
@@ -193,7 +193,8 @@ muon_status_t muon_ns_batched_noalloc(void *X, int64_t B, int64_t M, int64_t N, 
  *      an X-space step does).  It rounds the m x m matrices R, B', T and Q
  *      to bf16 where the X space rounds A, B' and the iterate: its update
  *      error measured 0.0062-0.0086 of ||dW|| against 0.0059-0.0074 in X
- *      space (bound 1e-2) at m = 768 ... 8192; below m = 128 it was worse.
+ *      space (bound 1e-2) at m = 1024 ... 8192; below m = 1024 it gained
+ *      little and erred more (0.0086 against 0.0072 at m = 768).
  * MUON_GRAM_SPACE=0 keeps every shape in X space, =force sends every shape
  * of the GEMM path to Gram space; MUON_GRAM_SPACE_RATIO (default 2) sets the
  * n / m threshold; MUON_SMALL_PATH=0 sends m <= 64 to the GEMM path.

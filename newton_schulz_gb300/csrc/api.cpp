@@ -290,15 +290,15 @@ int gram_phases(int steps, int64_t m) {
 }
 
 // Gram space (the default iteration of DMuon-2 Appendix C.3) for core shapes
-// with m >= 128 and n >= ratio x m (MUON_GRAM_SPACE_RATIO, default 2) in bf16
-// mode.  With the restart period of gram_restart_period_env its update error
-// measured 0.0062-0.0086 of ||dW|| against 0.0059-0.0074 in X space (the
-// bound is 1e-2) at m = 768 ... 8192 for 1-24 % less time per step; below
-// m = 128 (shapes the small-m kernel does not take, or all of them with
-// MUON_SMALL_PATH=0) its NS error reached 0.031 on a [33, 1000] matrix, so
-// those stay in X space.  MUON_GRAM_SPACE=0 turns it off, =force applies it
-// to every shape of the GEMM path.
-constexpr int64_t kGramSpaceMinM = 128;
+// with m >= 1024 and n >= ratio x m (MUON_GRAM_SPACE_RATIO, default 2) in
+// bf16 mode: there its restart period is 3 and its update error measured
+// 0.0062-0.0086 of ||dW|| against 0.0059-0.0069 in X space (the bound is
+// 1e-2) for 9-24 % less time per step.  Below m = 1024 the period-2 form
+// saved 1.3 % on the MoE experts (m = 768) at 0.0086 against 0.0072, and
+// at m = 33 its NS error reached 0.031, so those shapes stay in X space.
+// MUON_GRAM_SPACE=0 turns it off, =force applies it to every shape of the
+// GEMM path.
+constexpr int64_t kGramSpaceMinM = 1024;
 bool gram_space_shape(int64_t m, int64_t n, const NsCfg& ns) {
   if (ns.precise || ns.steps < 1) return false;
   const char* v = std::getenv("MUON_GRAM_SPACE");

@@ -9,9 +9,9 @@ rounds R, B', T and Q instead of the iterate, so the test holds it to the same
 tolerances against the float64 oracle: NS error <= 3e-2 per matrix and W'
 within 1e-2 * ||dW||.  On ill-conditioned inputs, where bf16 NS in either
 form is farther from the float64 result, Gram space is held to 2.5x the
-X-space error of the same input.  Gram space is the default for n >= 2 m
-(MUON_GRAM_SPACE unset or 1), =force applies it to every shape (used
-here), 0 turns it off; MUON_GRAM_RESTART sets P (0: no restart).
+X-space error of the same input.  Gram space is the default for m >= 1024
+and n >= 2 m (MUON_GRAM_SPACE unset or 1), =force applies it to every shape
+(used here), 0 turns it off; MUON_GRAM_RESTART sets P (0: no restart).
 """
 import numpy as np
 import pytest
@@ -61,7 +61,8 @@ def test_path_choice(monkeypatch):
     assert binding.muon_ns_path(14336, 4096) == binding.PATH_GRAM_SPACE
     assert binding.muon_ns_path(4096, 4096) == binding.PATH_XSPACE
     assert binding.muon_ns_path(24, 10240) == binding.PATH_SMALL
-    assert binding.muon_ns_path(100, 1000) == binding.PATH_XSPACE    # m < 128
+    assert binding.muon_ns_path(100, 1000) == binding.PATH_XSPACE    # m < 1024
+    assert binding.muon_ns_path(768, 2048) == binding.PATH_XSPACE
     assert binding.muon_ns_path(1024, 4096, binding.make_config(precision=binding.NS_TF32)) == \
         binding.PATH_XSPACE
     monkeypatch.setenv("MUON_GRAM_SPACE", "force")
