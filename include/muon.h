@@ -53,7 +53,7 @@ typedef struct CUstream_st *cudaStream_t;
 typedef enum muon_status_t {
   MUON_OK = 0,
   MUON_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, bad enum, misalignment */
-  MUON_ERR_UNSUPPORTED = 2,      /* valid request this build does not implement        */
+  MUON_ERR_UNSUPPORTED = 2,      /* valid request the library does not implement       */
   MUON_ERR_ALIAS = 3,            /* W, G, Mom (or X and out) ranges overlap            */
   MUON_ERR_OUT_OF_MEMORY = 4,    /* workspace allocation failed                         */
   MUON_ERR_CUDA = 5,             /* a CUDA runtime/driver call or launch failed         */

@@ -1,5 +1,5 @@
-"""Workspace guard bands (the survey's substitute for a memory sanitizer,
-which this GPU pool does not offer).
+"""Workspace guard bands: a check for out-of-bounds writes into the
+library's workspace that needs no memory sanitizer.
 
 With MUON_WS_GUARD=1 every buffer of the library's workspace is followed by a
 4 KB band filled with a fixed byte before the kernels that use that layout;
