@@ -23,20 +23,14 @@ namespace {
 
 __device__ __forceinline__ float bf16_to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-__device__ __forceinline__ void load8_f32_stream(const float* p, float* d) {
-  float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-  float4 b = __ldcs(reinterpret_cast<const float4*>(p + 4));
-  d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
-  d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
-}
-
 __device__ __forceinline__ void store8_f32(float* p, const float* d) {
   *reinterpret_cast<float4*>(p) = make_float4(d[0], d[1], d[2], d[3]);
   *reinterpret_cast<float4*>(p + 4) = make_float4(d[4], d[5], d[6], d[7]);
 }
 
-__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* d) {
-  uint4 u = *reinterpret_cast<const uint4*>(p);
+// Raw 16-byte loads are kept apart from their conversions so that a thread
+// issues all of its loads before the first conversion waits for data.
+__device__ __forceinline__ void unpack8_bf16(uint4 u, float* d) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -44,6 +38,17 @@ __device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* d) {
     d[2 * j] = f.x;
     d[2 * j + 1] = f.y;
   }
+}
+
+__device__ __forceinline__ void unpack4_f32(uint4 u, float* d) {
+  d[0] = __uint_as_float(u.x);
+  d[1] = __uint_as_float(u.y);
+  d[2] = __uint_as_float(u.z);
+  d[3] = __uint_as_float(u.w);
+}
+
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* d) {
+  unpack8_bf16(*reinterpret_cast<const uint4*>(p), d);
 }
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* d) {
@@ -93,7 +98,9 @@ __device__ __forceinline__ int prep_col(int r, int c) { return c ^ ((((r >> 3) ^
 // ---------------------------------------------------------------------------
 // K1
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepParams p) {
+// Six resident blocks per SM (at most 40 registers a thread), for the same
+// reason as the update kernel's bound.
+__global__ void __launch_bounds__(256, 6) prep_kernel(const __grid_constant__ PrepParams p) {
   // fp32 tile of D in the stored [r][c] layout (+1 pad against bank conflicts)
   __shared__ float sD[kPrepTile][kPrepTile + 1];
   __shared__ float red[8];
@@ -128,10 +135,32 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
       nvalid = 0;
     if (nvalid > 0) {
       const int64_t e = moff + gr * s.c + gc;
-      float g[8];
-      if (nvalid == 8 && s.vec) {
-        if (s.g_dtype == 0) load8_f32_stream(reinterpret_cast<const float*>(s.G) + e, g);
-        else load8_bf16(reinterpret_cast<const __nv_bfloat16*>(s.G) + e, g);
+      const bool v8 = nvalid == 8 && s.vec;
+      float g[8], m[8];
+      if (v8) {
+        // G's and Mom's raw bits first, then the conversions: a bf16 G
+        // converted next to its load would hold Mom's load back until G came
+        uint4 g0, g1 = make_uint4(0u, 0u, 0u, 0u), m0 = g1, m1 = g1;
+        if (s.g_dtype == 0) {
+          const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const float*>(s.G) + e);
+          g0 = __ldcs(g4);
+          g1 = __ldcs(g4 + 1);
+        } else {
+          g0 = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(s.G) + e);
+        }
+        if (p.step_mode) {
+          const uint4* m4 = reinterpret_cast<const uint4*>(s.Mom + e);
+          m0 = __ldcs(m4);
+          m1 = __ldcs(m4 + 1);
+        }
+        if (s.g_dtype == 0) {
+          unpack4_f32(g0, g);
+          unpack4_f32(g1, g + 4);
+        } else {
+          unpack8_bf16(g0, g);
+        }
+        unpack4_f32(m0, m);
+        unpack4_f32(m1, m + 4);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -140,22 +169,19 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
             g[j] = s.g_dtype == 0 ? reinterpret_cast<const float*>(s.G)[e + j]
                                   : bf16_to_f(reinterpret_cast<const __nv_bfloat16*>(s.G)[e + j]);
         }
-      }
-      if (p.step_mode) {
-        float m[8];
-        if (nvalid == 8 && s.vec) {
-          load8_f32_stream(s.Mom + e, m);
-        } else {
+        if (p.step_mode) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) m[j] = j < nvalid ? s.Mom[e + j] : 0.f;
         }
+      }
+      if (p.step_mode) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float mn = fmaf(p.mu, m[j], g[j]);          // M_t = mu*M_{t-1} + G
           m[j] = mn;
           d[j] = p.nesterov ? fmaf(p.mu, mn, g[j]) : mn;    // D = G + mu*M_t
         }
-        if (nvalid == 8 && s.vec) {
+        if (v8) {
           store8_f32(s.Mom + e, m);
         } else {
 #pragma unroll
@@ -249,7 +275,9 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepP
 // ---------------------------------------------------------------------------
 // K6
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ FinParams p) {
+// Eight resident blocks per SM (at most 32 registers a thread): the W and O
+// loads in flight per SM are what this kernel's rate is set by.
+__global__ void __launch_bounds__(256, 8) finish_kernel(const __grid_constant__ FinParams p) {
   // o_trans tiles: the O tile [kFinTRows][kFinTCols] (fp32: hi + lo in the
   // high-precision mode), transposed from Xt on the way in; the odd pitch
   // (65 words) keeps the scattered writes free of bank conflicts
@@ -261,7 +289,35 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
   const int mat = local / tiles;
   const int t = local - mat * tiles;
   const int ti = t / s.tiles_c, tj = t - ti * s.tiles_c;
+  // the thread's elements of W: row gr, columns [gc, gc + nvalid)
   int64_t gr, gc;
+  if (s.o_trans) {
+    gr = (int64_t)ti * kFinTRows + (threadIdx.x >> 3);
+    gc = (int64_t)tj * kFinTCols + (threadIdx.x & 7) * 8;
+  } else {
+    gr = (int64_t)ti * kFinRows + (threadIdx.x >> 5);
+    gc = (int64_t)tj * kFinCols + (threadIdx.x & 31) * 8;
+  }
+  const bool live = gr < s.r && gc < s.c;
+  const int nvalid = live ? (int)min((int64_t)8, s.c - gc) : 0;
+  const int64_t e = (int64_t)mat * s.r * s.c + gr * s.c + gc;
+  // debug builds: the element range lies in the slice's W
+  const bool w_ok =
+      live && dbg_ok(mat < s.count && e + nvalid <= (int64_t)s.count * s.r * s.c, p.status);
+  const bool vec8 = w_ok && nvalid == 8 && s.vec;
+  // A full vector of W is loaded first, as raw bits, and converted only once
+  // O is in registers: the two loads' latencies overlap instead of adding up
+  // (a conversion next to its load would make the thread wait for W there).
+  uint4 wr0 = make_uint4(0u, 0u, 0u, 0u), wr1 = wr0;
+  if (p.step_mode && vec8) {
+    if (s.w_dtype == 0) {
+      const uint4* w4 = reinterpret_cast<const uint4*>(static_cast<const float*>(s.W) + e);
+      wr0 = __ldcs(w4);
+      wr1 = __ldcs(w4 + 1);
+    } else {
+      wr0 = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(s.W) + e);
+    }
+  }
   float o[8];
   if (s.o_trans) {
     // O[gr][gc] = Xt[gc][gr]: each thread brings 8 consecutive gr of one Xt
@@ -275,18 +331,18 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
       for (int j = 0; j < 8; ++j) f[j] = 0.f;
       // (the loads below touch [xc, min(xc + 8, r)) of the row)
       if (xr < s.c && dbg_ok(mat < s.count && min(xc + 8, s.r) <= s.pitch_o, p.status)) {
-        const int64_t o = (int64_t)mat * s.mstride_o + xr * s.pitch_o + xc;
+        const int64_t oo = (int64_t)mat * s.mstride_o + xr * s.pitch_o + xc;
         if (xc + 8 <= s.r) {
-          load8_bf16(s.O + o, f);
+          load8_bf16(s.O + oo, f);
           if (s.O_lo) {
             float l[8];
-            load8_bf16(s.O_lo + o, l);
+            load8_bf16(s.O_lo + oo, l);
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] += l[j];
           }
         } else {
           for (int j = 0; j < 8; ++j)
-            if (xc + j < s.r) f[j] = bf16_to_f(s.O[o + j]) + (s.O_lo ? bf16_to_f(s.O_lo[o + j]) : 0.f);
+            if (xc + j < s.r) f[j] = bf16_to_f(s.O[oo + j]) + (s.O_lo ? bf16_to_f(s.O_lo[oo + j]) : 0.f);
         }
       }
 #pragma unroll
@@ -294,34 +350,29 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     }
     __syncthreads();
     const int lr = threadIdx.x >> 3, lc0 = (threadIdx.x & 7) * 8;
-    gr = r0 + lr;
-    gc = c0 + lc0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = sO[lr][lc0 + j];
   } else {
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    gr = (int64_t)ti * kFinRows + ty;
-    gc = (int64_t)tj * kFinCols + tx * 8;
-    if (gr < s.r && gc < s.c && dbg_ok(mat < s.count && gc + 8 <= s.pitch_o, p.status)) {
+    // both halves' raw bits first, then the conversions
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = 0.f;
+    if (live && dbg_ok(mat < s.count && gc + 8 <= s.pitch_o, p.status)) {
       const int64_t oo = (int64_t)mat * s.mstride_o + gr * s.pitch_o + gc;
-      load8_bf16(s.O + oo, o);
+      const uint4 hi = *reinterpret_cast<const uint4*>(s.O + oo);
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u);
+      if (s.O_lo) lo = *reinterpret_cast<const uint4*>(s.O_lo + oo);
+      unpack8_bf16(hi, o);
       if (s.O_lo) {
         float l[8];
-        load8_bf16(s.O_lo + oo, l);
+        unpack8_bf16(lo, l);
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] += l[j];
       }
     }
   }
-  if (gr >= s.r || gc >= s.c) return;
-  const int nvalid = (int)min((int64_t)8, s.c - gc);
-  // debug builds: the element range lies in the slice's W
-  if (!dbg_ok(mat < s.count && ((int64_t)mat * s.r + gr) * s.c + gc + nvalid <= (int64_t)s.count * s.r * s.c,
-              p.status))
-    return;
+  if (!w_ok) return;
 
   const float os = s.inv ? s.inv[mat] : 1.f;
-  const int64_t e = (int64_t)mat * s.r * s.c + gr * s.c + gc;
 
   if (p.step_mode) {
     const float decay = 1.f - p.lr * p.wd;
@@ -329,8 +380,9 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     float w[8];
     if (s.w_dtype == 0) {
       float* W = reinterpret_cast<float*>(s.W);
-      if (nvalid == 8 && s.vec) {
-        load8_f32_stream(W + e, w);
+      if (vec8) {
+        unpack4_f32(wr0, w);
+        unpack4_f32(wr1, w + 4);
 #pragma unroll
         for (int j = 0; j < 8; ++j) w[j] = fmaf(decay, w[j], -step * o[j]);
         store8_f32(W + e, w);
@@ -339,8 +391,8 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
       }
     } else {
       __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(s.W);
-      if (nvalid == 8 && s.vec) {
-        load8_bf16(W + e, w);
+      if (vec8) {
+        unpack8_bf16(wr0, w);
 #pragma unroll
         for (int j = 0; j < 8; ++j) w[j] = fmaf(decay, w[j], -step * o[j]);
         *reinterpret_cast<uint4*>(W + e) = pack8_bf16(w);
@@ -354,11 +406,11 @@ __global__ void __launch_bounds__(256) finish_kernel(const __grid_constant__ Fin
     for (int j = 0; j < 8; ++j) o[j] *= os;
     if (s.w_dtype == 0) {
       float* W = reinterpret_cast<float*>(s.W);
-      if (nvalid == 8 && s.vec) store8_f32(W + e, o);
+      if (vec8) store8_f32(W + e, o);
       else for (int j = 0; j < nvalid; ++j) W[e + j] = o[j];
     } else {
       __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(s.W);
-      if (nvalid == 8 && s.vec) *reinterpret_cast<uint4*>(W + e) = pack8_bf16(o);
+      if (vec8) *reinterpret_cast<uint4*>(W + e) = pack8_bf16(o);
       else for (int j = 0; j < nvalid; ++j) W[e + j] = __float2bfloat16_rn(o[j]);
     }
   }
