@@ -308,6 +308,18 @@ bool gram_space_shape(int64_t m, int64_t n, const NsCfg& ns) {
   return m >= kGramSpaceMinM && static_cast<double>(n) >= ratio * static_cast<double>(m);
 }
 
+// Row passes of an update launch: two when every weight it writes is bf16
+// (tiles twice as tall, 16 elements a thread), else one.  MUON_FIN_PASSES=1
+// or 2 overrides (a launch with fp32 weights still prefetches them at one
+// pass only).
+int fin_passes(const std::vector<SliceP>& slices, const std::vector<Req>& reqs) {
+  const char* v = std::getenv("MUON_FIN_PASSES");
+  if (v && (v[0] == '1' || v[0] == '2')) return v[0] - '0';
+  for (const SliceP& s : slices)
+    if (reqs[s.req].w_dtype != MUON_BF16) return 1;
+  return 2;
+}
+
 // Small-m path eligibility: core shapes with m <= 64 (MUON_SMALL_PATH=0 sends
 // every shape to the grouped GEMM path).
 bool small_shape(int64_t m) {
@@ -1017,6 +1029,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
       for (const NsGroupP& g : ch.groups) chunk_min_m = std::min(chunk_min_m, g.m);
       FinParams fp;
       std::memset(&fp, 0, sizeof(fp));
+      fp.passes = fin_passes(ch.slices, large);
       int64_t blocks = 0;
       for (size_t i = 0; i < ch.slices.size(); ++i) {
         const SliceP& s = ch.slices[i];
@@ -1044,7 +1057,7 @@ muon_status_t run(const std::vector<Req>& reqs, bool step_mode, float mu, int ne
         fs.c = q.c;
         fs.count = static_cast<int>(s.cnt);
         fs.w_dtype = q.w_dtype;
-        fs.tiles_r = static_cast<int>(cdiv(q.r, fs.o_trans ? kFinTRows : kFinRows));
+        fs.tiles_r = static_cast<int>(cdiv(q.r, fin_tile_rows(fs.o_trans, fp.passes)));
         fs.tiles_c = static_cast<int>(cdiv(q.c, fs.o_trans ? kFinTCols : kFinCols));
         fs.tile_base = static_cast<int>(blocks);
         fs.vec = (q.w_dtype == MUON_F32 ? (q.c % 4 == 0) : (q.c % 8 == 0)) && aligned(fs.W, 16);

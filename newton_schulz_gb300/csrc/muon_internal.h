@@ -74,6 +74,9 @@ struct PrepParams {
 // ---- K6: update / copy-back --------------------------------------------------
 constexpr int kFinRows = 8, kFinCols = 256;     // tile when O is stored [r][c]
 constexpr int kFinTRows = 32, kFinTCols = 64;   // tile when O is read transposed from Xt
+// Rows of one update tile: those of one row pass times the launch's passes
+// (FinParams::passes).
+constexpr int fin_tile_rows(int o_trans, int passes) { return (o_trans ? kFinTRows : kFinRows) * passes; }
 
 struct FinSlice {
   void* W;                     // step: weights [count][r][c]; ns: output
@@ -96,6 +99,7 @@ struct FinParams {
   int step_mode;
   float lr, wd;
   unsigned* status;            // device status word (debug-build checks)
+  int passes;                  // row passes per tile: 2 (every W bf16) or 1; 0 reads as 1
 };
 
 // ---- NS GEMM phases -----------------------------------------------------------
