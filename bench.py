@@ -453,10 +453,11 @@ def measure(name, steps, warmup, args, world, dev, local, with_cpu):
 
 
 def _ns_only(groups, stream, flush, steps, warmup, world, dev, flops):
-    """Newton-Schulz alone through muon_ns_batched_ex (fp32 or bf16 input, bf16
-    output): the step's gradients, same-shape tensors stacked into one
-    [B, M, N] batch per shape outside the timed region, one call per shape,
-    timed like the step.  Not counted in gpu_launches (its own region)."""
+    """Newton-Schulz alone through muon_ns_batched_ex (fp32 or bf16 input, the
+    output in the input's dtype): the step's gradients, same-shape tensors
+    stacked into one [B, M, N] batch per shape outside the timed region, one
+    call per shape, timed like the step.  Not counted in gpu_launches (its
+    own region)."""
     import torch
     from newton_schulz_gb300 import binding
     by_shape = {}
@@ -464,7 +465,7 @@ def _ns_only(groups, stream, flush, steps, warmup, world, dev, flops):
         x = g["G"] if g["G"].dim() == 3 else g["G"].unsqueeze(0)
         by_shape.setdefault((tuple(x.shape[1:]), x.dtype), []).append(x)
     xs = [torch.cat(v, 0).contiguous() for v in by_shape.values()]
-    outs = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for x in xs]
+    outs = [torch.empty_like(x) for x in xs]
     ms = []
     for i in range(warmup + steps):
         flush.fill_(float(i))

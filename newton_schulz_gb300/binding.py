@@ -215,10 +215,16 @@ def muon_ns_batched_noalloc(X, steps: int = 5, a: float = 3.4445, b: float = -4.
 
 
 def muon_ns_batched_ex(X, cfg=None, out=None, stream=None) -> None:
+    """NS of every [M,N] slice of X (f32 or bf16) into X, or into `out`,
+    which the library writes in X's dtype and shape (checked here: the C
+    entry point sees only a pointer)."""
     _check_contig(X)
     B, M, N = _shape3(X)
     if out is not None:
         _check_contig(out)
+        if out.dtype != X.dtype or tuple(out.shape) != tuple(X.shape):
+            raise ValueError(f"out must match X: {out.dtype} {tuple(out.shape)} against "
+                             f"{X.dtype} {tuple(X.shape)}")
     check(load().muon_ns_batched_ex(X.data_ptr(), _dtype_code(X), B, M, N,
                                     ctypes.byref(cfg) if cfg is not None else None,
                                     out.data_ptr() if out is not None else None,

@@ -168,3 +168,17 @@ def test_debug_inject_stall_arguments(lib):
 
 def test_debug_guard_check_needs_an_output(lib):
     assert lib.muon_debug_guard_check(None, None) == 1
+
+
+def test_binding_rejects_out_of_another_dtype_or_shape():
+    """muon_ns_batched_ex writes `out` in X's dtype and shape; the C entry point
+    sees only a pointer, so the binding refuses a mismatched `out` (fp32 data
+    into a bf16 buffer would write past its end) before the library is
+    reached (CPU tensors: nothing runs)."""
+    import torch
+    x = torch.zeros((2, 8, 16), dtype=torch.float32)
+    for out in (torch.zeros((2, 8, 16), dtype=torch.bfloat16),
+                torch.zeros((2, 16, 8), dtype=torch.float32),
+                torch.zeros((1, 8, 16), dtype=torch.float32)):
+        with pytest.raises(ValueError, match="out must match X"):
+            binding.muon_ns_batched_ex(x, binding.make_config(), out)

@@ -58,11 +58,11 @@ def test_two_passes_equal_one_pass(specs, precise, monkeypatch):
         assert torch.equal(ga["Mom"], gb["Mom"])
 
 
-@pytest.mark.parametrize("shape,dt", [((1, 130, 1001), BF), ((2, 1001, 130), F32),
-                                      ((2, 256, 1024), BF), ((1, 1024, 256), F32)])
+@pytest.mark.parametrize("shape", [(1, 130, 1001), (2, 1001, 130), (2, 256, 1024), (1, 1024, 256)])
 @pytest.mark.parametrize("steps", [0, 5])
-def test_two_passes_copy_back(shape, dt, steps, monkeypatch):
-    x = torch.randn(shape, generator=torch.Generator().manual_seed(sum(shape) + steps)).to("cuda", dt)
+def test_two_passes_copy_back(shape, steps, monkeypatch):
+    # the output has X's dtype: a bf16 X makes the copy-back a bf16-only launch
+    x = torch.randn(shape, generator=torch.Generator().manual_seed(sum(shape) + steps)).to("cuda", BF)
     outs = []
     for passes in ("1", None):
         if passes:
