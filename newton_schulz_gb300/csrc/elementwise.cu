@@ -424,8 +424,8 @@ __global__ void __launch_bounds__(256, 8) finish_kernel(const __grid_constant__ 
 // arithmetic as finish_kernel; all four 16-byte loads (W and O, both passes)
 // are issued before the first conversion.  56 registers a thread, four
 // resident blocks per SM: capped at 48 registers (five blocks) the kernel
-// spills and measured 0.64 of HBM against 0.77 uncapped, on 8 Llama-3-8B
-// layers, where the one-pass kernel is issue-bound at 0.63.
+// spills and measured 0.64 of HBM against 0.77-0.79 uncapped, on 8
+// Llama-3-8B layers, where the one-pass kernel is issue-bound at 0.63.
 __global__ void __launch_bounds__(256) finish_tall_kernel(const __grid_constant__ FinParams p) {
   __shared__ __align__(16) float sO[2 * kFinTRows][kFinTCols + 1];
   const int si = find_slice(p.s, p.n_slices, blockIdx.x);
