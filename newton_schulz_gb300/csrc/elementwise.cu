@@ -10,9 +10,11 @@
 //  finish_kernel (K6)  W <- (1 - lr*wd)*W - lr*s*O (RFC issue 204 item 6,
 //                      DMuon-2 section 2.1), or the copy-back of an NS-only call;
 //                      O is read from Xt, through a shared-memory transpose
-//                      when the stored layout is [m][n].
+//                      when the stored layout is [m][n].  finish_tall_kernel
+//                      is the same update in two row passes a thread, for
+//                      launches whose weights are all bf16.
 //
-// Both are HBM-bound streaming kernels: 16-byte vector loads and stores,
+// All are HBM-bound streaming kernels: 16-byte vector loads and stores,
 // warp-shuffle reductions, deterministic two-stage norm (per-tile partials,
 // then the last-arriving block of each matrix sums them in a fixed order).
 #include "muon_internal.h"
@@ -98,8 +100,9 @@ __device__ __forceinline__ int prep_col(int r, int c) { return c ^ ((((r >> 3) ^
 // ---------------------------------------------------------------------------
 // K1
 // ---------------------------------------------------------------------------
-// Six resident blocks per SM (at most 40 registers a thread), for the same
-// reason as the update kernel's bound.
+// Six resident blocks per SM (at most 40 registers a thread): the loads in
+// flight per SM set this kernel's rate (48 registers, five blocks, measured
+// slower).
 __global__ void __launch_bounds__(256, 6) prep_kernel(const __grid_constant__ PrepParams p) {
   // fp32 tile of D in the stored [r][c] layout (+1 pad against bank conflicts)
   __shared__ float sD[kPrepTile][kPrepTile + 1];
@@ -275,8 +278,10 @@ __global__ void __launch_bounds__(256, 6) prep_kernel(const __grid_constant__ Pr
 // ---------------------------------------------------------------------------
 // K6
 // ---------------------------------------------------------------------------
-// Eight resident blocks per SM (at most 32 registers a thread): the W and O
-// loads in flight per SM are what this kernel's rate is set by.
+// One row pass, 8 elements a thread; eight resident blocks per SM (at most
+// 32 registers a thread: the W and O loads in flight per SM set the rate on
+// fp32 weights).  On bf16 weights it is issue-bound, and launches whose
+// weights are all bf16 run finish_tall_kernel instead.
 __global__ void __launch_bounds__(256, 8) finish_kernel(const __grid_constant__ FinParams p) {
   // o_trans tiles: the O tile [kFinTRows][kFinTCols] (fp32: hi + lo in the
   // high-precision mode), transposed from Xt on the way in; the odd pitch
