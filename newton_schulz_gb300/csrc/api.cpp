@@ -308,13 +308,13 @@ bool gram_space_shape(int64_t m, int64_t n, const NsCfg& ns) {
   return m >= kGramSpaceMinM && static_cast<double>(n) >= ratio * static_cast<double>(m);
 }
 
-// Row passes of an update launch: two when every weight it writes is bf16
-// (tiles twice as tall, 16 elements a thread), else one.  MUON_FIN_PASSES=1
-// or 2 overrides (a launch with fp32 weights still prefetches them at one
-// pass only).
+// Row passes of an update launch: two (finish_tall_kernel: tiles twice as
+// tall, 16 elements a thread) when every weight it writes is bf16 -- that
+// kernel handles bf16 weights only -- else one.  MUON_FIN_PASSES=1 forces
+// one pass.
 int fin_passes(const std::vector<SliceP>& slices, const std::vector<Req>& reqs) {
   const char* v = std::getenv("MUON_FIN_PASSES");
-  if (v && (v[0] == '1' || v[0] == '2')) return v[0] - '0';
+  if (v && v[0] == '1') return 1;
   for (const SliceP& s : slices)
     if (reqs[s.req].w_dtype != MUON_BF16) return 1;
   return 2;
